@@ -1,0 +1,209 @@
+/*
+ * gdpa.h - C ABI of the GB300 (sm_103a) GDPA library.
+ *
+ * GDPA (Generalized Dot-Product Attention) is defined on the page
+ * "범용 내적 어텐션(GDPA): 실제 추천 시스템 학습 부하를 위한 커널 최적화"
+ * (aitrends.kr), summary ("핵심 요약") and first paragraph of "섹션별 상세":
+ * attention in which the softmax is replaced by an element-wise activation
+ * such as GELU or SiLU.  For every sample b of a jagged batch and every head:
+ *
+ *     O_b = act(alpha * Q_b K_b^T) V_b
+ *
+ * with no row normalisation.  The same section describes host-side
+ * precomputation of the valid tiles of a jagged batch and their zigzag
+ * assignment to SMs (gdpa_plan_create), and the ALU-only 6th-order Taylor
+ * GELU (GDPA_ACT_GELU_TAYLOR6).
+ *
+ * Conventions shared by every call:
+ *   - Offsets are int32 exclusive prefix sums of the per-sample lengths:
+ *     q_off[0] = 0, q_off[b+1] - q_off[b] = Lq_b, likewise kv_off; B samples.
+ *   - Tensors are token-major with heads interleaved, row-major, contiguous:
+ *     Q, O, dO are [q_off[B]][H][d]; K, V are [kv_off[B]][H][d];
+ *     dQ is [q_off[B]][H][d] float32; dK, dV are [kv_off[B]][H][d] float32.
+ *     Q, K, V, O, dO share one element type (gdpa_dtype).  Device pointers
+ *     must be 16-byte aligned.
+ *   - Query i of sample b is row q_off[b] + i; with the causal window W, key
+ *     j of the same sample is valid for query i iff i - W < j <= i.  Pairs
+ *     that are not valid contribute exactly zero; a row with no valid key
+ *     gets a zero output (and zero dQ).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  gdpa_fwd / gdpa_bwd only enqueue work and never synchronise.
+ *   - Every call returns a gdpa_status and never aborts.  Device-side
+ *     failures (an expired wait in a kernel) are reported by gdpa_check.
+ *   - The caller owns all tensors and streams; a plan owns its host and
+ *     device buffers and is freed by gdpa_plan_destroy.
+ */
+#ifndef GDPA_H
+#define GDPA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GDPA_OK = 0,
+    GDPA_ERR_INVALID_ARG = 1,   /* bad pointer, offsets, sizes or enum value */
+    GDPA_ERR_UNSUPPORTED = 2,   /* valid but not implemented (e.g. head dim) */
+    GDPA_ERR_CUDA = 3,          /* a CUDA runtime call failed */
+    GDPA_ERR_ALLOC = 4,         /* host or device allocation failed */
+    GDPA_ERR_TIMEOUT = 5,       /* a kernel gave up waiting on a barrier */
+    GDPA_ERR_DEVICE = 6         /* a kernel flagged an internal inconsistency */
+} gdpa_status;
+
+/* Element-wise activation applied to x = alpha * q.k (GDPA page, summary
+ * and the SFU paragraph with its Taylor code figure). */
+typedef enum {
+    GDPA_ACT_GELU_ERF = 0,      /* x * Phi(x) = x/2 (1 + erf(x / sqrt 2)) */
+    GDPA_ACT_GELU_TANH = 1,     /* x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
+    GDPA_ACT_SILU = 2,          /* x / (1 + exp(-x)) */
+    GDPA_ACT_GELU_TAYLOR6 = 3,  /* x/2 + (x^2 - x^4/6 + x^6/40) / sqrt(2 pi) */
+    GDPA_ACT_IDENTITY = 4       /* x (for tests of the linear algebra) */
+} gdpa_act;
+
+typedef enum {
+    GDPA_MASK_NONE = 0,            /* every (query, key) pair of a sample */
+    GDPA_MASK_CAUSAL_WINDOW = 1    /* i - window < j <= i */
+} gdpa_mask;
+
+/* Tile-to-SM assignment (GDPA page, zigzag scheduling paragraph and diagram). */
+typedef enum {
+    GDPA_SCHED_ZIGZAG = 0,       /* sort by cost, deal in snake order */
+    GDPA_SCHED_ROUND_ROBIN = 1   /* enumeration order, tile r to SM r % S */
+} gdpa_sched;
+
+typedef enum { GDPA_BF16 = 0, GDPA_F32 = 1 } gdpa_dtype;
+
+/* Which kernels a plan launches.  AUTO: tensor-core (tcgen05) kernels for
+ * bf16 with d in {64, 128}, CUDA-core kernels otherwise (float32 always
+ * runs on CUDA cores so that it keeps full float32 products). */
+typedef enum { GDPA_KERNEL_AUTO = 0, GDPA_KERNEL_TCGEN05 = 1, GDPA_KERNEL_SIMT = 2 } gdpa_kernel;
+
+typedef struct gdpa_plan_s* gdpa_plan;   /* opaque, owned by the library */
+
+/* Tile sizes of every plan: 128 query rows x 128 key rows. */
+#define GDPA_BLOCK_M 128
+#define GDPA_BLOCK_N 128
+
+/*
+ * Build the tile plan of a jagged batch on the host and upload it on
+ * `stream` (GDPA page: the CPU precomputes the valid tiles from the jagged
+ * lengths and assigns them to SMs in zigzag order).
+ *
+ *   q_off_host, kv_off_host  host int32 [B+1]; read only during this call.
+ *   B >= 0 samples; H >= 1 heads; d = head dim (a multiple of 4, <= 128;
+ *     the tcgen05 kernels need 64 or 128).
+ *   mask, window             window >= 1 when mask is CAUSAL_WINDOW.
+ *   sched                    dealing policy.
+ *   num_sms                  S, the number of persistent CTAs (0 = the
+ *                            current device's SM count).
+ *   max_kv_blocks_per_tile   0 = one forward tile per query tile; > 0 cuts
+ *                            longer key ranges into chunks (planning only:
+ *                            gdpa_fwd rejects such plans with UNSUPPORTED).
+ *   out                      receives the plan; *out is NULL on failure.
+ *
+ * Forward tiles: one per (sample, head, 128-row query tile), with the range
+ * of 128-row key blocks that hold a valid pair (a zero tile, kb0 = kb1 = 0,
+ * when none does); cost = number of key blocks.  Backward units: one per
+ * (sample, head, key block), with the range of query tiles that hold a valid
+ * pair; cost = number of query tiles.  Zigzag: stable sort by cost
+ * descending; the r-th tile goes to SM r % S on even rounds r / S and to
+ * S - 1 - r % S on odd rounds.
+ *
+ * Errors: INVALID_ARG for NULL pointers, negative sizes, offsets that do not
+ * start at 0 or decrease, window < 1 with the window mask; UNSUPPORTED for
+ * d > 128 or d % 4 != 0; ALLOC / CUDA for allocation or copy failures.
+ */
+gdpa_status gdpa_plan_create(const int32_t* q_off_host, const int32_t* kv_off_host, int B,
+                             int H, int d, gdpa_mask mask, int window, gdpa_sched sched,
+                             int num_sms, int max_kv_blocks_per_tile, void* stream,
+                             gdpa_plan* out);
+
+/*
+ * Same planning on the host only, with no device and no upload: num_sms must
+ * be > 0.  The plan can be exported and destroyed but not launched
+ * (gdpa_fwd / gdpa_bwd return INVALID_ARG).  Useful to inspect a plan on a
+ * machine without a GPU.
+ */
+gdpa_status gdpa_plan_create_host(const int32_t* q_off_host, const int32_t* kv_off_host, int B,
+                                  int H, int d, gdpa_mask mask, int window, gdpa_sched sched,
+                                  int num_sms, int max_kv_blocks_per_tile, gdpa_plan* out);
+
+/* Number of forward tiles, backward units and SMs (S) of a plan. */
+gdpa_status gdpa_plan_sizes(gdpa_plan plan, int64_t* n_fwd, int64_t* n_bwd, int* num_sms);
+
+/*
+ * Copy the forward tile list to host memory in queue order (SM 0's queue
+ * first).  tiles_out: int32 [cap][6] rows (b, h, m, kb0, kb1, sm);
+ * seg_start_out: int32 [S+1] first row of each SM's queue (may be NULL).
+ * Returns INVALID_ARG if cap is smaller than the tile count (*n_out still
+ * receives the count).
+ */
+gdpa_status gdpa_plan_export(gdpa_plan plan, int32_t* tiles_out, int64_t cap, int64_t* n_out,
+                             int32_t* seg_start_out);
+
+/*
+ * Same for the backward units: int32 [cap][7] rows (b, h, j, m0, m1, flags,
+ * sm); flags bit 0 = this sample's dQ is accumulated with atomic adds.
+ * *zero_dq_out (may be NULL) is 1 when gdpa_bwd clears dQ before its kernels.
+ */
+gdpa_status gdpa_plan_export_bwd(gdpa_plan plan, int32_t* units_out, int64_t cap,
+                                 int64_t* n_out, int32_t* seg_start_out, int* zero_dq_out);
+
+/* Choose the kernel family (default AUTO); INVALID_ARG for unknown values. */
+gdpa_status gdpa_plan_set_kernel(gdpa_plan plan, gdpa_kernel kernel);
+
+/* Record per-CTA start/end times (%globaltimer, ns) and SM ids on the next
+ * launches (enable != 0), readable with gdpa_sm_times. */
+gdpa_status gdpa_plan_set_timing(gdpa_plan plan, int enable);
+
+/*
+ * Forward: O = act(alpha Q K^T) V per sample and head (GDPA page, summary).
+ * q, k, v, o: device pointers, layouts above, element type `dtype`.  Every
+ * row of O is written (rows with no valid key become zero).  Enqueued on
+ * `stream`; returns INVALID_ARG / UNSUPPORTED before any launch when the
+ * arguments do not fit the plan.
+ */
+gdpa_status gdpa_fwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k,
+                     const void* v, void* o, float alpha, gdpa_act act, void* stream);
+
+/*
+ * Backward: given dO, the float32 gradients
+ *   dV_j = sum_i act(x_ij) dO_i,  dQ_i = alpha sum_j g_ij K_j,
+ *   dK_j = alpha sum_i g_ij Q_i,  g_ij = (dO_i . V_j) act'(x_ij),
+ * with x_ij = alpha q_i . k_j over valid pairs.  dq, dk, dv are device
+ * float32 buffers that this call overwrites entirely (no prior clearing
+ * needed).  Enqueued on `stream`.
+ */
+gdpa_status gdpa_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k,
+                     const void* v, const void* d_o, float* dq, float* dk, float* dv,
+                     float alpha, gdpa_act act, void* stream);
+
+/*
+ * Synchronise `stream` and report device-side failures of this plan's
+ * launches since the last check: TIMEOUT if a kernel abandoned a barrier
+ * wait (its outputs are then incomplete), DEVICE for other flagged errors,
+ * CUDA for an asynchronous CUDA error.  Clears the flags.
+ */
+gdpa_status gdpa_check(gdpa_plan plan, void* stream);
+
+/*
+ * Per-CTA timing of the last timed launch (which = 0 forward, 1 backward):
+ * start_end: uint64 [S][2] globaltimer ns; smid: int32 [S].  Synchronous.
+ * INVALID_ARG if timing was not enabled or nothing was recorded.
+ */
+gdpa_status gdpa_sm_times(gdpa_plan plan, int which, uint64_t* start_end, int32_t* smid);
+
+/* Number of kernel launches this plan has issued since creation. */
+int64_t gdpa_plan_launches(gdpa_plan plan);
+
+void gdpa_plan_destroy(gdpa_plan plan);
+
+const char* gdpa_status_str(gdpa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDPA_H */

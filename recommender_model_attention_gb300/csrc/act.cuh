@@ -1,0 +1,133 @@
+// Element-wise GDPA activations and their derivatives, as device functions.
+//
+// The GDPA page (aitrends.kr, "범용 내적 어텐션(GDPA) ...") replaces the
+// softmax by GELU, SiLU and similar functions, and replaces the tanh-based
+// GELU by an ALU-only 6th-order Taylor polynomial to avoid the SFU (the SFU
+// paragraph and its code figure):  x/2 + c2 x^2 + c4 x^4 + c6 x^6 with
+// c2 = 1/sqrt(2 pi), c4 = -c2/6, c6 = c2/40.
+//
+// Two flavours:
+//  * Precise (CUDA-core float32 path): CUDA's erff / tanhf / expf.
+//  * Fast (bf16 tensor-core path, whose P is rounded to bf16 anyway):
+//    GELU-tanh through the tanh.approx.f32 instruction, SiLU through
+//    __expf and a fast reciprocal; GELU-erf still calls erff; the Taylor
+//    polynomial is the same FMA chain in both.
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace gdpa {
+
+enum : int { kGeluErf = 0, kGeluTanh = 1, kSilu = 2, kTaylor6 = 3, kIdentity = 4 };
+
+constexpr float kRsqrt2 = 0.70710678118654752440f;     // 1/sqrt(2)
+constexpr float kRsqrt2Pi = 0.39894228040143267794f;   // 1/sqrt(2 pi)
+constexpr float kSqrt2OverPi = 0.79788456080286535588f;
+constexpr float kTanhCubic = 0.044715f;
+constexpr float kT6c2 = kRsqrt2Pi;
+constexpr float kT6c4 = -kRsqrt2Pi / 6.0f;
+constexpr float kT6c6 = kRsqrt2Pi / 40.0f;
+
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// x * (1/2 + x (c2 + x^2 (c4 + c6 x^2)))  ==  x/2 + c2 x^2 + c4 x^4 + c6 x^6
+__device__ __forceinline__ float taylor6(float x) {
+    const float x2 = x * x;
+    float t = fmaf(kT6c6, x2, kT6c4);
+    t = fmaf(t, x2, kT6c2);
+    t = fmaf(t, x, 0.5f);
+    return t * x;
+}
+
+// 1/2 + 2 c2 x + 4 c4 x^3 + 6 c6 x^5
+__device__ __forceinline__ float dtaylor6(float x) {
+    const float x2 = x * x;
+    float t = fmaf(6.0f * kT6c6, x2, 4.0f * kT6c4);
+    t = fmaf(t, x2, 2.0f * kT6c2);
+    return fmaf(t, x, 0.5f);
+}
+
+template <int ACT, bool FAST>
+__device__ __forceinline__ float act_f(float x) {
+    if constexpr (ACT == kGeluErf) {
+        return 0.5f * x * (1.0f + erff(x * kRsqrt2));
+    } else if constexpr (ACT == kGeluTanh) {
+        const float u = kSqrt2OverPi * fmaf(kTanhCubic * x, x * x, x);
+        const float t = FAST ? tanh_approx(u) : tanhf(u);
+        return 0.5f * x * (1.0f + t);
+    } else if constexpr (ACT == kSilu) {
+        if constexpr (FAST) {
+            return __fdividef(x, 1.0f + __expf(-x));
+        } else {
+            return x / (1.0f + expf(-x));
+        }
+    } else if constexpr (ACT == kTaylor6) {
+        return taylor6(x);
+    } else {
+        return x;
+    }
+}
+
+template <int ACT, bool FAST>
+__device__ __forceinline__ float dact_f(float x) {
+    if constexpr (ACT == kGeluErf) {
+        const float cdf = 0.5f * (1.0f + erff(x * kRsqrt2));
+        const float pdf = kRsqrt2Pi * (FAST ? __expf(-0.5f * x * x) : expf(-0.5f * x * x));
+        return fmaf(x, pdf, cdf);
+    } else if constexpr (ACT == kGeluTanh) {
+        const float u = kSqrt2OverPi * fmaf(kTanhCubic * x, x * x, x);
+        const float t = FAST ? tanh_approx(u) : tanhf(u);
+        const float du = kSqrt2OverPi * fmaf(3.0f * kTanhCubic, x * x, 1.0f);
+        return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * du;
+    } else if constexpr (ACT == kSilu) {
+        const float s = FAST ? __fdividef(1.0f, 1.0f + __expf(-x)) : 1.0f / (1.0f + expf(-x));
+        return s * fmaf(x, 1.0f - s, 1.0f);
+    } else if constexpr (ACT == kTaylor6) {
+        return dtaylor6(x);
+    } else {
+        return 1.0f;
+    }
+}
+
+// act and act' together (backward recompute).
+template <int ACT, bool FAST>
+__device__ __forceinline__ void act_dact_f(float x, float& a, float& da) {
+    if constexpr (ACT == kGeluErf) {
+        const float cdf = 0.5f * (1.0f + erff(x * kRsqrt2));
+        const float pdf = kRsqrt2Pi * (FAST ? __expf(-0.5f * x * x) : expf(-0.5f * x * x));
+        a = x * cdf;
+        da = fmaf(x, pdf, cdf);
+    } else if constexpr (ACT == kGeluTanh) {
+        const float u = kSqrt2OverPi * fmaf(kTanhCubic * x, x * x, x);
+        const float t = FAST ? tanh_approx(u) : tanhf(u);
+        const float du = kSqrt2OverPi * fmaf(3.0f * kTanhCubic, x * x, 1.0f);
+        a = 0.5f * x * (1.0f + t);
+        da = 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * du;
+    } else if constexpr (ACT == kSilu) {
+        const float s = FAST ? __fdividef(1.0f, 1.0f + __expf(-x)) : 1.0f / (1.0f + expf(-x));
+        a = x * s;
+        da = s * fmaf(x, 1.0f - s, 1.0f);
+    } else if constexpr (ACT == kTaylor6) {
+        a = taylor6(x);
+        da = dtaylor6(x);
+    } else {
+        a = x;
+        da = 1.0f;
+    }
+}
+
+// Runtime activation id -> template instantiation.
+#define GDPA_DISPATCH_ACT(act, ACTC, ...)                      \
+    switch (act) {                                             \
+    case kGeluErf: { constexpr int ACTC = kGeluErf; __VA_ARGS__; } break;   \
+    case kGeluTanh: { constexpr int ACTC = kGeluTanh; __VA_ARGS__; } break; \
+    case kSilu: { constexpr int ACTC = kSilu; __VA_ARGS__; } break;         \
+    case kTaylor6: { constexpr int ACTC = kTaylor6; __VA_ARGS__; } break;   \
+    default: { constexpr int ACTC = kIdentity; __VA_ARGS__; } break;        \
+    }
+
+}  // namespace gdpa

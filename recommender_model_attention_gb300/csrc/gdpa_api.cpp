@@ -1,0 +1,270 @@
+// C ABI of the GDPA library: argument checks, plan ownership, dispatch to
+// the kernel launchers, and device error reporting.
+#include <stdlib.h>
+#include <string.h>
+
+#include <new>
+
+#include "gdpa_internal.h"
+
+using gdpa::Plan;
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+template <typename T>
+gdpa_status upload(T** dst, const void* src, size_t bytes, cudaStream_t st) {
+    if (bytes == 0) return GDPA_OK;
+    if (cudaMalloc((void**)dst, bytes) != cudaSuccess) return GDPA_ERR_ALLOC;
+    if (cudaMemcpyAsync(*dst, src, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return GDPA_ERR_CUDA;
+    return GDPA_OK;
+}
+
+void free_plan(Plan* p) {
+    if (!p) return;
+    if (!p->host_only) {
+        cudaFree(p->d_fwd);
+        cudaFree(p->d_fwd_seg);
+        cudaFree(p->d_bwd);
+        cudaFree(p->d_bwd_seg);
+        cudaFree(p->d_err);
+        cudaFree(p->d_times);
+        cudaFree(p->d_smid);
+    }
+    delete p;
+}
+
+bool valid_act(int a) { return a >= GDPA_ACT_GELU_ERF && a <= GDPA_ACT_IDENTITY; }
+
+// true when this plan/dtype combination runs on the tcgen05 kernels
+bool use_tc(const Plan& p, gdpa_dtype dt) {
+    if (dt != GDPA_BF16) return false;
+    if (p.kernel == GDPA_KERNEL_SIMT) return false;
+    return p.d == 64 || p.d == 128;
+}
+
+}  // namespace
+
+extern "C" const char* gdpa_status_str(gdpa_status s) {
+    switch (s) {
+    case GDPA_OK: return "ok";
+    case GDPA_ERR_INVALID_ARG: return "invalid argument";
+    case GDPA_ERR_UNSUPPORTED: return "unsupported configuration";
+    case GDPA_ERR_CUDA: return "CUDA error";
+    case GDPA_ERR_ALLOC: return "allocation failed";
+    case GDPA_ERR_TIMEOUT: return "kernel barrier wait timed out";
+    case GDPA_ERR_DEVICE: return "kernel reported an internal error";
+    }
+    return "unknown status";
+}
+
+namespace {
+
+gdpa_status create_common(const int32_t* q_off_host, const int32_t* kv_off_host, int B, int H,
+                          int d, gdpa_mask mask, int window, gdpa_sched sched, int num_sms,
+                          int max_kv_blocks_per_tile, bool host_only, cudaStream_t s,
+                          gdpa_plan* out) {
+    if (!out) return GDPA_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!q_off_host || !kv_off_host || B < 0 || H < 1 || d < 1) return GDPA_ERR_INVALID_ARG;
+    if (mask != GDPA_MASK_NONE && mask != GDPA_MASK_CAUSAL_WINDOW) return GDPA_ERR_INVALID_ARG;
+    if (mask == GDPA_MASK_CAUSAL_WINDOW && window < 1) return GDPA_ERR_INVALID_ARG;
+    if (sched != GDPA_SCHED_ZIGZAG && sched != GDPA_SCHED_ROUND_ROBIN) return GDPA_ERR_INVALID_ARG;
+    if (num_sms < 0 || max_kv_blocks_per_tile < 0) return GDPA_ERR_INVALID_ARG;
+    if (host_only && num_sms == 0) return GDPA_ERR_INVALID_ARG;
+    if (d > 128 || d % 4 != 0) return GDPA_ERR_UNSUPPORTED;
+    if ((int64_t)H * d > (1 << 20)) return GDPA_ERR_UNSUPPORTED;
+
+    Plan* p = new (std::nothrow) Plan();
+    if (!p) return GDPA_ERR_ALLOC;
+    p->host_only = host_only;
+    if (!host_only) {
+        if (cudaGetDevice(&p->device) != cudaSuccess) {
+            delete p;
+            return GDPA_ERR_CUDA;
+        }
+        if (num_sms == 0 && cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount,
+                                                   p->device) != cudaSuccess) {
+            delete p;
+            return GDPA_ERR_CUDA;
+        }
+    }
+    p->B = B;
+    p->H = H;
+    p->d = d;
+    p->mask = mask;
+    p->window = mask == GDPA_MASK_CAUSAL_WINDOW ? window : 0;
+    p->sched = sched;
+    p->S = num_sms;
+    p->max_kvb = max_kv_blocks_per_tile;
+    gdpa_status st = gdpa::build_plan_host(*p, q_off_host, kv_off_host);
+    if (st != GDPA_OK) {
+        delete p;
+        return st;
+    }
+    if (!host_only) {
+        const size_t S1 = (size_t)p->S + 1;
+        if ((st = upload(&p->d_fwd, p->fwd_dev_host.data(),
+                         p->fwd_dev_host.size() * sizeof(gdpa::FwdTile), s)) ||
+            (st = upload(&p->d_fwd_seg, p->fwd_seg.data(), S1 * sizeof(int32_t), s)) ||
+            (st = upload(&p->d_bwd, p->bwd_dev_host.data(),
+                         p->bwd_dev_host.size() * sizeof(gdpa::BwdUnit), s)) ||
+            (st = upload(&p->d_bwd_seg, p->bwd_seg.data(), S1 * sizeof(int32_t), s))) {
+            cudaStreamSynchronize(s);
+            free_plan(p);
+            return st;
+        }
+        if (cudaMalloc((void**)&p->d_err, 4 * sizeof(int32_t)) != cudaSuccess ||
+            cudaMalloc((void**)&p->d_times, 2 * (size_t)p->S * 2 * sizeof(unsigned long long)) !=
+                cudaSuccess ||
+            cudaMalloc((void**)&p->d_smid, 2 * (size_t)p->S * sizeof(int32_t)) != cudaSuccess) {
+            cudaStreamSynchronize(s);
+            free_plan(p);
+            return GDPA_ERR_ALLOC;
+        }
+        // the synchronisation also keeps the host staging vectors alive
+        // until their asynchronous copies have finished
+        if (cudaMemsetAsync(p->d_err, 0, 4 * sizeof(int32_t), s) != cudaSuccess ||
+            cudaStreamSynchronize(s) != cudaSuccess) {
+            free_plan(p);
+            return GDPA_ERR_CUDA;
+        }
+    }
+    std::vector<gdpa::FwdTile>().swap(p->fwd_dev_host);
+    std::vector<gdpa::BwdUnit>().swap(p->bwd_dev_host);
+    *out = (gdpa_plan)p;
+    return GDPA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdpa_status gdpa_plan_create(const int32_t* q_off_host, const int32_t* kv_off_host, int B, int H,
+                             int d, gdpa_mask mask, int window, gdpa_sched sched, int num_sms,
+                             int max_kv_blocks_per_tile, void* stream, gdpa_plan* out) {
+    return create_common(q_off_host, kv_off_host, B, H, d, mask, window, sched, num_sms,
+                         max_kv_blocks_per_tile, false, (cudaStream_t)stream, out);
+}
+
+gdpa_status gdpa_plan_create_host(const int32_t* q_off_host, const int32_t* kv_off_host, int B,
+                                  int H, int d, gdpa_mask mask, int window, gdpa_sched sched,
+                                  int num_sms, int max_kv_blocks_per_tile, gdpa_plan* out) {
+    return create_common(q_off_host, kv_off_host, B, H, d, mask, window, sched, num_sms,
+                         max_kv_blocks_per_tile, true, nullptr, out);
+}
+
+gdpa_status gdpa_plan_sizes(gdpa_plan plan, int64_t* n_fwd, int64_t* n_bwd, int* num_sms) {
+    if (!plan) return GDPA_ERR_INVALID_ARG;
+    Plan* p = (Plan*)plan;
+    if (n_fwd) *n_fwd = p->n_fwd;
+    if (n_bwd) *n_bwd = p->n_bwd;
+    if (num_sms) *num_sms = p->S;
+    return GDPA_OK;
+}
+
+gdpa_status gdpa_plan_export(gdpa_plan plan, int32_t* tiles_out, int64_t cap, int64_t* n_out,
+                             int32_t* seg_start_out) {
+    if (!plan) return GDPA_ERR_INVALID_ARG;
+    Plan* p = (Plan*)plan;
+    if (n_out) *n_out = p->n_fwd;
+    if (seg_start_out) memcpy(seg_start_out, p->fwd_seg.data(), p->fwd_seg.size() * sizeof(int32_t));
+    if (cap < p->n_fwd || (p->n_fwd > 0 && !tiles_out)) return GDPA_ERR_INVALID_ARG;
+    if (p->n_fwd) memcpy(tiles_out, p->fwd_export.data(), p->fwd_export.size() * sizeof(int32_t));
+    return GDPA_OK;
+}
+
+gdpa_status gdpa_plan_export_bwd(gdpa_plan plan, int32_t* units_out, int64_t cap, int64_t* n_out,
+                                 int32_t* seg_start_out, int* zero_dq_out) {
+    if (!plan) return GDPA_ERR_INVALID_ARG;
+    Plan* p = (Plan*)plan;
+    if (n_out) *n_out = p->n_bwd;
+    if (zero_dq_out) *zero_dq_out = p->zero_dq;
+    if (seg_start_out) memcpy(seg_start_out, p->bwd_seg.data(), p->bwd_seg.size() * sizeof(int32_t));
+    if (cap < p->n_bwd || (p->n_bwd > 0 && !units_out)) return GDPA_ERR_INVALID_ARG;
+    if (p->n_bwd) memcpy(units_out, p->bwd_export.data(), p->bwd_export.size() * sizeof(int32_t));
+    return GDPA_OK;
+}
+
+gdpa_status gdpa_plan_set_kernel(gdpa_plan plan, gdpa_kernel kernel) {
+    if (!plan || kernel < GDPA_KERNEL_AUTO || kernel > GDPA_KERNEL_SIMT) return GDPA_ERR_INVALID_ARG;
+    ((Plan*)plan)->kernel = kernel;
+    return GDPA_OK;
+}
+
+gdpa_status gdpa_plan_set_timing(gdpa_plan plan, int enable) {
+    if (!plan) return GDPA_ERR_INVALID_ARG;
+    ((Plan*)plan)->timing = enable ? 1 : 0;
+    return GDPA_OK;
+}
+
+int64_t gdpa_plan_launches(gdpa_plan plan) { return plan ? ((Plan*)plan)->launches : -1; }
+
+gdpa_status gdpa_fwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k, const void* v,
+                     void* o, float alpha, gdpa_act act, void* stream) {
+    if (!plan || ((Plan*)plan)->host_only) return GDPA_ERR_INVALID_ARG;
+    Plan& p = *(Plan*)plan;
+    if (dtype != GDPA_BF16 && dtype != GDPA_F32) return GDPA_ERR_INVALID_ARG;
+    if (!valid_act(act)) return GDPA_ERR_INVALID_ARG;
+    if (p.Tq > 0 && (!q || !o)) return GDPA_ERR_INVALID_ARG;
+    if (p.Tkv > 0 && (!k || !v)) return GDPA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return GDPA_ERR_INVALID_ARG;
+    if (p.fwd_split) return GDPA_ERR_UNSUPPORTED;
+    if (p.n_fwd == 0) return GDPA_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
+    if (use_tc(p, dtype)) return gdpa::launch_tc_fwd(p, q, k, v, o, alpha, act, st);
+    return gdpa::launch_simt_fwd(p, dtype, q, k, v, o, alpha, act, st);
+}
+
+gdpa_status gdpa_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k, const void* v,
+                     const void* d_o, float* dq, float* dk, float* dv, float alpha, gdpa_act act,
+                     void* stream) {
+    if (!plan || ((Plan*)plan)->host_only) return GDPA_ERR_INVALID_ARG;
+    Plan& p = *(Plan*)plan;
+    if (dtype != GDPA_BF16 && dtype != GDPA_F32) return GDPA_ERR_INVALID_ARG;
+    if (!valid_act(act)) return GDPA_ERR_INVALID_ARG;
+    if (p.Tq > 0 && (!q || !d_o || !dq)) return GDPA_ERR_INVALID_ARG;
+    if (p.Tkv > 0 && (!k || !v || !dk || !dv)) return GDPA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) || !aligned16(dq) ||
+        !aligned16(dk) || !aligned16(dv))
+        return GDPA_ERR_INVALID_ARG;
+    if (p.fwd_split) return GDPA_ERR_UNSUPPORTED;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
+    if (use_tc(p, dtype)) return gdpa::launch_tc_bwd(p, q, k, v, d_o, dq, dk, dv, alpha, act, st);
+    return gdpa::launch_simt_bwd(p, dtype, q, k, v, d_o, dq, dk, dv, alpha, act, st);
+}
+
+gdpa_status gdpa_check(gdpa_plan plan, void* stream) {
+    if (!plan || ((Plan*)plan)->host_only) return GDPA_ERR_INVALID_ARG;
+    Plan& p = *(Plan*)plan;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return GDPA_ERR_CUDA;
+    int32_t err[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(err, p.d_err, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GDPA_ERR_CUDA;
+    if (err[0] == gdpa::kDevOk) return GDPA_OK;
+    if (cudaMemset(p.d_err, 0, sizeof(err)) != cudaSuccess) return GDPA_ERR_CUDA;
+    return err[0] == gdpa::kDevTimeout ? GDPA_ERR_TIMEOUT : GDPA_ERR_DEVICE;
+}
+
+gdpa_status gdpa_sm_times(gdpa_plan plan, int which, uint64_t* start_end, int32_t* smid) {
+    if (!plan || ((Plan*)plan)->host_only || which < 0 || which > 1 || !start_end || !smid)
+        return GDPA_ERR_INVALID_ARG;
+    Plan& p = *(Plan*)plan;
+    if (!p.timed[which]) return GDPA_ERR_INVALID_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return GDPA_ERR_CUDA;
+    if (cudaMemcpy(start_end, p.d_times + (size_t)which * p.S * 2, (size_t)p.S * 2 * sizeof(uint64_t),
+                   cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(smid, p.d_smid + (size_t)which * p.S, (size_t)p.S * sizeof(int32_t),
+                   cudaMemcpyDeviceToHost) != cudaSuccess)
+        return GDPA_ERR_CUDA;
+    return GDPA_OK;
+}
+
+void gdpa_plan_destroy(gdpa_plan plan) { free_plan((Plan*)plan); }
+
+}  // extern "C"

@@ -1,0 +1,83 @@
+// Internal declarations shared by the host planner, the ABI layer and the
+// kernel launchers of the GDPA library.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <vector>
+
+#include "gdpa.h"
+
+namespace gdpa {
+
+constexpr int kBM = GDPA_BLOCK_M;  // query rows per tile
+constexpr int kBN = GDPA_BLOCK_N;  // key rows per block
+
+// One forward tile as the kernels read it: query rows [qt0, qt0 + nq) of a
+// sample whose keys are rows [kvt0, kvt0 + lkv); key blocks [kb0, kb1) of
+// kBN rows; i0 = position of the tile's first query inside its sample.
+struct FwdTile {
+    int32_t qt0, nq, kvt0, lkv, h, kb0, kb1, i0;
+};
+static_assert(sizeof(FwdTile) == 32, "FwdTile layout");
+
+// One backward unit: key rows [kvt0, kvt0 + nkv) at position c0 inside a
+// sample whose queries are rows [qt0, qt0 + lq); query tiles [m0, m1).
+// hf = head | flags << 16 (flag bit 0: dQ by atomic add).
+struct BwdUnit {
+    int32_t kvt0, nkv, qt0, lq, hf, m0, m1, c0;
+};
+static_assert(sizeof(BwdUnit) == 32, "BwdUnit layout");
+
+constexpr int kUnitAtomicDQ = 1;
+
+// Device error word layout (int32[4]): code, where, cta, detail.
+enum DevErr : int32_t { kDevOk = 0, kDevTimeout = 1, kDevBad = 2 };
+
+struct Plan {
+    int device = 0;
+    bool host_only = false;
+    int B = 0, H = 0, d = 0, mask = 0, window = 0, sched = 0, S = 0;
+    int max_kvb = 0;
+    int kernel = GDPA_KERNEL_AUTO;
+    int timing = 0;
+    int64_t Tq = 0, Tkv = 0;
+    int zero_dq = 0;
+    int fwd_split = 0;
+    std::vector<int32_t> fwd_export;  // [n][6] b, h, m, kb0, kb1, sm
+    std::vector<int32_t> fwd_seg;     // [S + 1]
+    std::vector<int32_t> bwd_export;  // [n][7] b, h, j, m0, m1, flags, sm
+    std::vector<int32_t> bwd_seg;     // [S + 1]
+    std::vector<FwdTile> fwd_dev_host;  // kernel records in queue order
+    std::vector<BwdUnit> bwd_dev_host;
+    int64_t n_fwd = 0, n_bwd = 0;
+    int64_t max_fwd_kvb = 0;          // largest kb1 - kb0 over forward tiles
+    // device copies (owned)
+    FwdTile* d_fwd = nullptr;
+    int32_t* d_fwd_seg = nullptr;
+    BwdUnit* d_bwd = nullptr;
+    int32_t* d_bwd_seg = nullptr;
+    int32_t* d_err = nullptr;                // [4]
+    unsigned long long* d_times = nullptr;   // [2][S][2]
+    int32_t* d_smid = nullptr;               // [2][S]
+    int timed[2] = {0, 0};
+    int64_t launches = 0;
+};
+
+// Host planner (gdpa_plan.cpp): fills the host-side vectors of `p` from the
+// offsets; returns GDPA_OK or INVALID_ARG.
+gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off);
+
+// Kernel launchers.  Arguments are already validated by the ABI layer.
+gdpa_status launch_simt_fwd(Plan& p, gdpa_dtype dt, const void* q, const void* k, const void* v,
+                            void* o, float alpha, int act, cudaStream_t st);
+gdpa_status launch_simt_bwd(Plan& p, gdpa_dtype dt, const void* q, const void* k, const void* v,
+                            const void* d_o, float* dq, float* dk, float* dv, float alpha, int act,
+                            cudaStream_t st);
+gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, void* o,
+                          float alpha, int act, cudaStream_t st);
+gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, const void* d_o,
+                          float* dq, float* dk, float* dv, float alpha, int act, cudaStream_t st);
+
+}  // namespace gdpa

@@ -1,0 +1,202 @@
+// Host tile planner of the GDPA library.
+//
+// The GDPA page ("범용 내적 어텐션(GDPA): 실제 추천 시스템 학습 부하를 위한
+// 커널 최적화", aitrends.kr, "섹션별 상세", the paragraph on jagged inputs and
+// the zigzag-scheduling diagram) has the CPU compute the valid tiles of a
+// jagged batch ahead of the launch and hand them to the SMs in a zigzag
+// pattern after sorting, in place of round robin, to even out SM load.
+//
+// Rules (the page gives only the idea; these are the library's definitions):
+//  * forward tile  = (sample b, head h, query tile m); its key blocks are the
+//    hull of the valid keys of its rows (no mask: all keys; causal window W:
+//    [m*BM - W + 1, min((m+1)*BM, Lq))), clipped to [0, Lkv).  An empty hull
+//    gives a zero tile (kb0 = kb1 = 0) whose rows the kernel writes as zeros.
+//  * backward unit = (b, h, key block j); its query tiles are the hull of the
+//    queries that see a key of the block.  A sample whose query tiles are
+//    reached by more than one key block gets its dQ by atomic adds.
+//  * cost = blocks on the inner loop; zigzag = stable sort by cost,
+//    descending, then snake dealing over the S SMs; round robin = tile r to
+//    SM r % S in enumeration order.
+#include <algorithm>
+#include <numeric>
+
+#include "gdpa_internal.h"
+
+namespace gdpa {
+namespace {
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct Item {
+    int32_t f[6];  // forward: b h m kb0 kb1 -; backward: b h j m0 m1 flags
+    int64_t cost;
+};
+
+// Deal items to S queues; returns the SM of each item in dealing order.
+void deal(const std::vector<Item>& items, int S, int sched, std::vector<int64_t>& order,
+          std::vector<int32_t>& sm) {
+    const int64_t n = (int64_t)items.size();
+    order.resize(n);
+    std::iota(order.begin(), order.end(), 0);
+    if (sched == GDPA_SCHED_ZIGZAG) {
+        std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
+            return items[a].cost > items[b].cost;
+        });
+    }
+    sm.resize(n);
+    for (int64_t r = 0; r < n; ++r) {
+        int32_t pos = (int32_t)(r % S);
+        if (sched == GDPA_SCHED_ZIGZAG && ((r / S) & 1)) pos = S - 1 - pos;
+        sm[r] = pos;
+    }
+}
+
+// Group dealt items by SM (stable within an SM) and emit export rows.
+template <int W>
+void emit(const std::vector<Item>& items, int S, int sched, std::vector<int32_t>& rows,
+          std::vector<int32_t>& seg, std::vector<int64_t>& queue_order) {
+    std::vector<int64_t> order;
+    std::vector<int32_t> sm;
+    deal(items, S, sched, order, sm);
+    std::vector<int64_t> count(S + 1, 0);
+    for (int64_t r = 0; r < (int64_t)order.size(); ++r) count[sm[r] + 1]++;
+    for (int s = 0; s < S; ++s) count[s + 1] += count[s];
+    seg.assign(count.begin(), count.end());
+    queue_order.assign(order.size(), 0);
+    std::vector<int64_t> fill(count.begin(), count.end() - 1);
+    for (int64_t r = 0; r < (int64_t)order.size(); ++r) queue_order[fill[sm[r]]++] = order[r];
+    rows.assign(order.size() * W, 0);
+    for (int s = 0; s < S; ++s) {
+        for (int64_t q = count[s]; q < count[s + 1]; ++q) {
+            const Item& it = items[queue_order[q]];
+            for (int c = 0; c < W - 1; ++c) rows[q * W + c] = it.f[c];
+            rows[q * W + W - 1] = s;
+        }
+    }
+}
+
+}  // namespace
+
+gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off) {
+    const int B = p.B, H = p.H, S = p.S;
+    if (q_off[0] != 0 || kv_off[0] != 0) return GDPA_ERR_INVALID_ARG;
+    for (int b = 0; b < B; ++b)
+        if (q_off[b + 1] < q_off[b] || kv_off[b + 1] < kv_off[b]) return GDPA_ERR_INVALID_ARG;
+    p.Tq = q_off[B];
+    p.Tkv = kv_off[B];
+    const bool win = p.mask == GDPA_MASK_CAUSAL_WINDOW;
+    const int64_t W = p.window;
+
+    // forward tiles, enumerated b -> h -> m (-> chunk)
+    std::vector<Item> ft;
+    std::vector<FwdTile> ft_dev;
+    p.max_fwd_kvb = 0;
+    p.fwd_split = 0;
+    for (int b = 0; b < B; ++b) {
+        const int64_t lq = q_off[b + 1] - q_off[b], lkv = kv_off[b + 1] - kv_off[b];
+        for (int h = 0; h < H; ++h) {
+            for (int64_t m = 0; m < cdiv(lq, kBM); ++m) {
+                const int64_t r0 = m * kBM, r1 = std::min<int64_t>(r0 + kBM, lq);
+                int64_t lo = 0, hi = lkv;
+                if (win) {
+                    lo = std::max<int64_t>(0, r0 - W + 1);
+                    hi = std::min<int64_t>(lkv, r1);
+                }
+                int64_t k0 = 0, k1 = 0;
+                if (lo < hi) {
+                    k0 = lo / kBN;
+                    k1 = cdiv(hi, kBN);
+                }
+                const int64_t step = (p.max_kvb > 0 && k1 > k0) ? p.max_kvb : std::max<int64_t>(1, k1 - k0);
+                int64_t s = k0;
+                do {
+                    const int64_t e = std::min(k1, s + step);
+                    Item it{{b, h, (int32_t)m, (int32_t)s, (int32_t)e, 0}, e - s};
+                    ft.push_back(it);
+                    FwdTile t;
+                    t.qt0 = (int32_t)(q_off[b] + r0);
+                    t.nq = (int32_t)(r1 - r0);
+                    t.kvt0 = kv_off[b];
+                    t.lkv = (int32_t)lkv;
+                    t.h = h;
+                    t.kb0 = (int32_t)s;
+                    t.kb1 = (int32_t)e;
+                    t.i0 = (int32_t)r0;
+                    ft_dev.push_back(t);
+                    p.max_fwd_kvb = std::max<int64_t>(p.max_fwd_kvb, e - s);
+                    if (e - s < k1 - k0) p.fwd_split = 1;
+                    s = e;
+                } while (s < k1);
+            }
+        }
+    }
+
+    // backward units, enumerated b -> h -> j
+    std::vector<Item> bu;
+    std::vector<BwdUnit> bu_dev;
+    p.zero_dq = 0;
+    for (int b = 0; b < B; ++b) {
+        const int64_t lq = q_off[b + 1] - q_off[b], lkv = kv_off[b + 1] - kv_off[b];
+        const int64_t nkb = cdiv(lkv, kBN), nm = cdiv(lq, kBM);
+        std::vector<int64_t> m0s(nkb), m1s(nkb);
+        for (int64_t j = 0; j < nkb; ++j) {
+            const int64_t c0 = j * kBN, c1 = std::min<int64_t>(c0 + kBN, lkv);
+            int64_t lo = 0, hi = lq;
+            if (win) {
+                lo = c0;
+                hi = std::min<int64_t>(lq, c1 - 1 + W);
+            }
+            m0s[j] = lo < hi ? lo / kBM : 0;
+            m1s[j] = lo < hi ? cdiv(hi, kBM) : 0;
+        }
+        // query-tile coverage count: atomic dQ if any tile is reached twice,
+        // clearing needed if any tile is never reached
+        std::vector<int32_t> cover(nm, 0);
+        for (int64_t j = 0; j < nkb; ++j)
+            for (int64_t m = m0s[j]; m < m1s[j]; ++m) cover[m]++;
+        bool atomic = false, hole = false;
+        for (int64_t m = 0; m < nm; ++m) {
+            atomic |= cover[m] > 1;
+            hole |= cover[m] == 0;
+        }
+        if (atomic || hole) p.zero_dq = 1;
+        const int32_t flags = atomic ? kUnitAtomicDQ : 0;
+        for (int h = 0; h < H; ++h) {
+            for (int64_t j = 0; j < nkb; ++j) {
+                const int64_t c0 = j * kBN, c1 = std::min<int64_t>(c0 + kBN, lkv);
+                Item it{{b, h, (int32_t)j, (int32_t)m0s[j], (int32_t)m1s[j], flags}, m1s[j] - m0s[j]};
+                bu.push_back(it);
+                BwdUnit u;
+                u.kvt0 = (int32_t)(kv_off[b] + c0);
+                u.nkv = (int32_t)(c1 - c0);
+                u.qt0 = q_off[b];
+                u.lq = (int32_t)lq;
+                u.hf = h | (flags << 16);
+                u.m0 = (int32_t)m0s[j];
+                u.m1 = (int32_t)m1s[j];
+                u.c0 = (int32_t)c0;
+                bu_dev.push_back(u);
+            }
+        }
+    }
+
+    std::vector<int64_t> qorder;
+    emit<6>(ft, S, p.sched, p.fwd_export, p.fwd_seg, qorder);
+    p.n_fwd = (int64_t)ft.size();
+    {
+        std::vector<FwdTile> sorted(ft_dev.size());
+        for (size_t i = 0; i < qorder.size(); ++i) sorted[i] = ft_dev[qorder[i]];
+        ft_dev.swap(sorted);
+    }
+    emit<7>(bu, S, p.sched, p.bwd_export, p.bwd_seg, qorder);
+    p.n_bwd = (int64_t)bu.size();
+    std::vector<BwdUnit> bsorted(bu_dev.size());
+    for (size_t i = 0; i < qorder.size(); ++i) bsorted[i] = bu_dev[qorder[i]];
+
+    // kernel-layout records in queue order, uploaded by the ABI layer
+    p.fwd_dev_host.swap(ft_dev);
+    p.bwd_dev_host.swap(bsorted);
+    return GDPA_OK;
+}
+
+}  // namespace gdpa

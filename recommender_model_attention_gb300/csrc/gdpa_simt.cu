@@ -1,0 +1,222 @@
+// CUDA-core (SIMT) GDPA kernels: float32 arithmetic for float32 and bf16
+// inputs, walking the host plan.  They are the float32 path of the library
+// (tensor-core tf32 would round the products to a 10-bit mantissa) and the
+// path for head dims the tensor-core kernels do not take.
+//
+// One CTA of four warps per tile; one warp per row; lane c holds elements
+// c, c + 32, c + 64, c + 96 of the row (d <= 128).  Scores are warp
+// reductions.  The key loop of a row is limited to its valid keys, so no
+// masking is needed inside it.
+#include <cuda_bf16.h>
+
+#include "act.cuh"
+#include "gdpa_internal.h"
+
+namespace gdpa {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kPer = 4;  // elements per lane (d <= 128)
+
+__device__ __forceinline__ float ldf(const float* p) { return *p; }
+__device__ __forceinline__ float ldf(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void stf(float* p, float v) { *p = v; }
+__device__ __forceinline__ void stf(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <typename T>
+__device__ __forceinline__ void load_row(float (&x)[kPer], const T* p, int d, int lane) {
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) {
+        const int e = lane + 32 * c;
+        x[c] = e < d ? ldf(p + e) : 0.0f;
+    }
+}
+
+__device__ __forceinline__ float dot_row(const float (&a)[kPer], const float (&b)[kPer]) {
+    float s = 0.0f;
+#pragma unroll
+    for (int c = 0; c < kPer; ++c) s = fmaf(a[c], b[c], s);
+    return warp_sum(s);
+}
+
+// valid keys of query position i: [lo, hi)
+__device__ __forceinline__ void key_range(int i, int kb0, int kb1, int lkv, int mask, int window,
+                                          int& lo, int& hi) {
+    lo = kb0 * kBN;
+    hi = min(kb1 * kBN, lkv);
+    if (mask == GDPA_MASK_CAUSAL_WINDOW) {
+        lo = max(lo, i - window + 1);
+        hi = min(hi, i + 1);
+    }
+}
+
+template <int ACT, typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+simt_fwd_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__ Q, const T* __restrict__ K,
+                const T* __restrict__ V, T* __restrict__ O, int H, int d, float alpha, int mask,
+                int window) {
+    const FwdTile t = tiles[blockIdx.x];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)H * d;
+    for (int r = warp; r < t.nq; r += kWarps) {
+        const int64_t qrow = (int64_t)(t.qt0 + r) * row + (int64_t)t.h * d;
+        float q[kPer], o[kPer] = {0.f, 0.f, 0.f, 0.f};
+        load_row(q, Q + qrow, d, lane);
+        int lo, hi;
+        key_range(t.i0 + r, t.kb0, t.kb1, t.lkv, mask, window, lo, hi);
+        for (int j = lo; j < hi; ++j) {
+            const int64_t krow = (int64_t)(t.kvt0 + j) * row + (int64_t)t.h * d;
+            float kx[kPer], vx[kPer];
+            load_row(kx, K + krow, d, lane);
+            load_row(vx, V + krow, d, lane);
+            const float p = act_f<ACT, false>(alpha * dot_row(q, kx));
+#pragma unroll
+            for (int c = 0; c < kPer; ++c) o[c] = fmaf(p, vx[c], o[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < kPer; ++c) {
+            const int e = lane + 32 * c;
+            if (e < d) stf(O + qrow + e, o[c]);
+        }
+    }
+}
+
+// dQ_i = alpha sum_j (dO_i . V_j) act'(x_ij) K_j over the tile's rows
+template <int ACT, typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+simt_bwd_dq_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__ Q,
+                   const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
+                   float* __restrict__ dQ, int H, int d, float alpha, int mask, int window) {
+    const FwdTile t = tiles[blockIdx.x];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)H * d;
+    for (int r = warp; r < t.nq; r += kWarps) {
+        const int64_t qrow = (int64_t)(t.qt0 + r) * row + (int64_t)t.h * d;
+        float q[kPer], go[kPer], acc[kPer] = {0.f, 0.f, 0.f, 0.f};
+        load_row(q, Q + qrow, d, lane);
+        load_row(go, dO + qrow, d, lane);
+        int lo, hi;
+        key_range(t.i0 + r, t.kb0, t.kb1, t.lkv, mask, window, lo, hi);
+        for (int j = lo; j < hi; ++j) {
+            const int64_t krow = (int64_t)(t.kvt0 + j) * row + (int64_t)t.h * d;
+            float kx[kPer], vx[kPer];
+            load_row(kx, K + krow, d, lane);
+            load_row(vx, V + krow, d, lane);
+            const float x = alpha * dot_row(q, kx);
+            const float g = dot_row(go, vx) * dact_f<ACT, false>(x);
+#pragma unroll
+            for (int c = 0; c < kPer; ++c) acc[c] = fmaf(g, kx[c], acc[c]);
+        }
+#pragma unroll
+        for (int c = 0; c < kPer; ++c) {
+            const int e = lane + 32 * c;
+            if (e < d) dQ[qrow + e] = alpha * acc[c];
+        }
+    }
+}
+
+// dK_j = alpha sum_i g_ij Q_i and dV_j = sum_i act(x_ij) dO_i over the unit's keys
+template <int ACT, typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+simt_bwd_dkdv_kernel(const BwdUnit* __restrict__ units, const T* __restrict__ Q,
+                     const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
+                     float* __restrict__ dK, float* __restrict__ dV, int H, int d, float alpha,
+                     int mask, int window) {
+    const BwdUnit u = units[blockIdx.x];
+    const int h = u.hf & 0xffff;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)H * d;
+    for (int c0 = warp; c0 < u.nkv; c0 += kWarps) {
+        const int j = u.c0 + c0;
+        const int64_t krow = (int64_t)(u.kvt0 + c0) * row + (int64_t)h * d;
+        float kx[kPer], vx[kPer], ak[kPer] = {0.f, 0.f, 0.f, 0.f}, av[kPer] = {0.f, 0.f, 0.f, 0.f};
+        load_row(kx, K + krow, d, lane);
+        load_row(vx, V + krow, d, lane);
+        int lo = u.m0 * kBM, hi = min(u.m1 * kBM, u.lq);
+        if (mask == GDPA_MASK_CAUSAL_WINDOW) {
+            lo = max(lo, j);
+            hi = min(hi, j + window);
+        }
+        for (int i = lo; i < hi; ++i) {
+            const int64_t qrow = (int64_t)(u.qt0 + i) * row + (int64_t)h * d;
+            float q[kPer], go[kPer];
+            load_row(q, Q + qrow, d, lane);
+            load_row(go, dO + qrow, d, lane);
+            const float x = alpha * dot_row(q, kx);
+            float a, da;
+            act_dact_f<ACT, false>(x, a, da);
+            const float g = dot_row(go, vx) * da;
+#pragma unroll
+            for (int c = 0; c < kPer; ++c) {
+                ak[c] = fmaf(g, q[c], ak[c]);
+                av[c] = fmaf(a, go[c], av[c]);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < kPer; ++c) {
+            const int e = lane + 32 * c;
+            if (e < d) {
+                dK[krow + e] = alpha * ak[c];
+                dV[krow + e] = av[c];
+            }
+        }
+    }
+}
+
+template <typename T>
+gdpa_status fwd_impl(Plan& p, const void* q, const void* k, const void* v, void* o, float alpha,
+                     int act, cudaStream_t st) {
+    const unsigned grid = (unsigned)p.n_fwd;
+    GDPA_DISPATCH_ACT(act, A,
+        simt_fwd_kernel<A, T><<<grid, kWarps * 32, 0, st>>>(
+            p.d_fwd, (const T*)q, (const T*)k, (const T*)v, (T*)o, p.H, p.d, alpha, p.mask,
+            p.window))
+    p.launches += 1;
+    return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+template <typename T>
+gdpa_status bwd_impl(Plan& p, const void* q, const void* k, const void* v, const void* d_o,
+                     float* dq, float* dk, float* dv, float alpha, int act, cudaStream_t st) {
+    // The forward tiles (zero tiles included) cover every query row once and
+    // the backward units every key row once, so both kernels store their
+    // rows directly and nothing needs clearing first.
+    if (p.n_fwd > 0) {
+        GDPA_DISPATCH_ACT(act, A,
+            simt_bwd_dq_kernel<A, T><<<(unsigned)p.n_fwd, kWarps * 32, 0, st>>>(
+                p.d_fwd, (const T*)q, (const T*)k, (const T*)v, (const T*)d_o, dq, p.H, p.d,
+                alpha, p.mask, p.window))
+        p.launches += 1;
+    }
+    if (p.n_bwd > 0) {
+        GDPA_DISPATCH_ACT(act, A,
+            simt_bwd_dkdv_kernel<A, T><<<(unsigned)p.n_bwd, kWarps * 32, 0, st>>>(
+                p.d_bwd, (const T*)q, (const T*)k, (const T*)v, (const T*)d_o, dk, dv, p.H, p.d,
+                alpha, p.mask, p.window))
+        p.launches += 1;
+    }
+    return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+}  // namespace
+
+gdpa_status launch_simt_fwd(Plan& p, gdpa_dtype dt, const void* q, const void* k, const void* v,
+                            void* o, float alpha, int act, cudaStream_t st) {
+    if (dt == GDPA_F32) return fwd_impl<float>(p, q, k, v, o, alpha, act, st);
+    return fwd_impl<__nv_bfloat16>(p, q, k, v, o, alpha, act, st);
+}
+
+gdpa_status launch_simt_bwd(Plan& p, gdpa_dtype dt, const void* q, const void* k, const void* v,
+                            const void* d_o, float* dq, float* dk, float* dv, float alpha, int act,
+                            cudaStream_t st) {
+    if (dt == GDPA_F32) return bwd_impl<float>(p, q, k, v, d_o, dq, dk, dv, alpha, act, st);
+    return bwd_impl<__nv_bfloat16>(p, q, k, v, d_o, dq, dk, dv, alpha, act, st);
+}
+
+}  // namespace gdpa

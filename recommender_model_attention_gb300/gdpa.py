@@ -1,0 +1,255 @@
+"""Thin ctypes binding of the GDPA C ABI (``include/gdpa.h``).
+
+Argument marshalling only: every step of planning and of the forward and
+backward passes runs in the C++/CUDA library.  There is no fallback: if the
+library has not been built, every call raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libgdpa_gb300.so")
+
+ACT = {"gelu_erf": 0, "gelu_tanh": 1, "silu": 2, "gelu_taylor6": 3, "identity": 4}
+MASK = {"none": 0, "causal_window": 1}
+SCHED = {"zigzag": 0, "round_robin": 1}
+KERNEL = {"auto": 0, "tcgen05": 1, "simt": 2}
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
+          4: "allocation failed", 5: "kernel barrier wait timed out",
+          6: "kernel reported an internal error"}
+BLOCK_M = 128
+BLOCK_N = 128
+
+_lib = None
+
+
+class GdpaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__("%s: %s (status %d)" % (what, STATUS.get(status, "?"), status))
+        self.status = status
+
+
+def lib():
+    """The loaded shared library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("GDPA CUDA library missing (%s); build it with "
+                               "recommender_model_attention_gb300.build()" % LIB_PATH)
+        try:
+            import torch  # noqa: F401  (loads the CUDA runtime the library links)
+        except ImportError:
+            pass
+        L = ctypes.CDLL(LIB_PATH)
+        i32p = ctypes.POINTER(ctypes.c_int32)
+        i64p = ctypes.POINTER(ctypes.c_int64)
+        vp = ctypes.c_void_p
+        st = ctypes.c_int
+        sig = {
+            "gdpa_plan_create": [i32p, i32p, st, st, st, st, st, st, st, st, vp, ctypes.POINTER(vp)],
+            "gdpa_plan_create_host": [i32p, i32p, st, st, st, st, st, st, st, st, ctypes.POINTER(vp)],
+            "gdpa_plan_sizes": [vp, i64p, i64p, ctypes.POINTER(ctypes.c_int)],
+            "gdpa_plan_export": [vp, i32p, ctypes.c_int64, i64p, i32p],
+            "gdpa_plan_export_bwd": [vp, i32p, ctypes.c_int64, i64p, i32p, ctypes.POINTER(ctypes.c_int)],
+            "gdpa_plan_set_kernel": [vp, st],
+            "gdpa_plan_set_timing": [vp, st],
+            "gdpa_fwd": [vp, st, vp, vp, vp, vp, ctypes.c_float, st, vp],
+            "gdpa_bwd": [vp, st, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, st, vp],
+            "gdpa_check": [vp, vp],
+            "gdpa_sm_times": [vp, st, ctypes.POINTER(ctypes.c_uint64), i32p],
+        }
+        for name, args in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        L.gdpa_plan_launches.argtypes = [vp]
+        L.gdpa_plan_launches.restype = ctypes.c_int64
+        L.gdpa_plan_destroy.argtypes = [vp]
+        L.gdpa_plan_destroy.restype = None
+        L.gdpa_status_str.argtypes = [ctypes.c_int]
+        L.gdpa_status_str.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def _ok(status: int, what: str):
+    if status != 0:
+        raise GdpaError(status, what)
+
+
+def _i32(a):
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return a, a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+class Plan:
+    """A GDPA tile plan (forward tiles and backward units dealt to SMs)."""
+
+    def __init__(self, q_off, kv_off, H: int, d: int, mask: str = "none", window: int = 0,
+                 sched: str = "zigzag", num_sms: int = 0, max_kv_blocks: int = 0,
+                 stream=None, host_only: bool = False):
+        L = lib()
+        qo, qp = _i32(q_off)
+        ko, kp = _i32(kv_off)
+        if len(qo) != len(ko) or len(qo) < 1:
+            raise ValueError("offset arrays must both have B + 1 entries")
+        self.B, self.H, self.d = len(qo) - 1, int(H), int(d)
+        self.mask, self.window = mask, int(window)
+        self.Tq, self.Tkv = int(qo[-1]), int(ko[-1])
+        self.q_off, self.kv_off = qo.copy(), ko.copy()
+        h = ctypes.c_void_p()
+        if host_only:
+            _ok(L.gdpa_plan_create_host(qp, kp, self.B, self.H, self.d, MASK[mask], int(window),
+                                        SCHED[sched], int(num_sms), int(max_kv_blocks),
+                                        ctypes.byref(h)), "gdpa_plan_create_host")
+        else:
+            _ok(L.gdpa_plan_create(qp, kp, self.B, self.H, self.d, MASK[mask], int(window),
+                                   SCHED[sched], int(num_sms), int(max_kv_blocks),
+                                   _stream_ptr(stream), ctypes.byref(h)), "gdpa_plan_create")
+        self._h = h
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise RuntimeError("plan destroyed")
+        return self._h
+
+    def sizes(self):
+        nf, nb, s = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int()
+        _ok(lib().gdpa_plan_sizes(self.handle, ctypes.byref(nf), ctypes.byref(nb), ctypes.byref(s)),
+            "gdpa_plan_sizes")
+        return nf.value, nb.value, s.value
+
+    @property
+    def num_sms(self) -> int:
+        return self.sizes()[2]
+
+    def export(self):
+        """(tiles int32 [n, 6] = b, h, m, kb0, kb1, sm;  seg int32 [S + 1])."""
+        nf, _, S = self.sizes()
+        tiles = np.zeros((max(nf, 1), 6), dtype=np.int32)
+        seg = np.zeros(S + 1, dtype=np.int32)
+        n = ctypes.c_int64()
+        _ok(lib().gdpa_plan_export(self.handle, tiles.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                   nf, ctypes.byref(n),
+                                   seg.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))), "gdpa_plan_export")
+        return tiles[:n.value], seg
+
+    def export_bwd(self):
+        """(units int32 [n, 7] = b, h, j, m0, m1, flags, sm;  seg [S + 1];  zero_dq)."""
+        _, nb, S = self.sizes()
+        units = np.zeros((max(nb, 1), 7), dtype=np.int32)
+        seg = np.zeros(S + 1, dtype=np.int32)
+        n, z = ctypes.c_int64(), ctypes.c_int()
+        _ok(lib().gdpa_plan_export_bwd(self.handle, units.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                       nb, ctypes.byref(n),
+                                       seg.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                                       ctypes.byref(z)), "gdpa_plan_export_bwd")
+        return units[:n.value], seg, bool(z.value)
+
+    def set_kernel(self, kernel: str):
+        _ok(lib().gdpa_plan_set_kernel(self.handle, KERNEL[kernel]), "gdpa_plan_set_kernel")
+
+    def set_timing(self, enable: bool):
+        _ok(lib().gdpa_plan_set_timing(self.handle, 1 if enable else 0), "gdpa_plan_set_timing")
+
+    def sm_times(self, which: str = "fwd"):
+        """(start_end uint64 [S, 2] in ns, smid int32 [S]) of the last timed launch."""
+        S = self.num_sms
+        se = np.zeros((S, 2), dtype=np.uint64)
+        sm = np.zeros(S, dtype=np.int32)
+        _ok(lib().gdpa_sm_times(self.handle, 0 if which == "fwd" else 1,
+                                se.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
+                                sm.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))), "gdpa_sm_times")
+        return se, sm
+
+    def check(self, stream=None):
+        _ok(lib().gdpa_check(self.handle, _stream_ptr(stream)), "gdpa_check")
+
+    @property
+    def launches(self) -> int:
+        return int(lib().gdpa_plan_launches(self.handle))
+
+    def destroy(self):
+        if getattr(self, "_h", None) is not None:
+            lib().gdpa_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def _dtype_id(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return 0
+    if t.dtype == torch.float32:
+        return 1
+    raise TypeError("GDPA takes bfloat16 or float32 tensors, got %s" % t.dtype)
+
+
+def _check(t, rows, plan, name, dtype=None):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if tuple(t.shape) != (rows, plan.H, plan.d):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), (rows, plan.H, plan.d)))
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s" % (name, dtype))
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t.numel() else ctypes.c_void_p(0)
+
+
+def gdpa_fwd(plan: Plan, q, k, v, o=None, alpha=None, act: str = "gelu_erf", stream=None):
+    """O = act(alpha Q K^T) V per sample and head; returns O ([Tq, H, d], dtype of q)."""
+    import torch
+    _check(q, plan.Tq, plan, "q")
+    _check(k, plan.Tkv, plan, "k", q.dtype)
+    _check(v, plan.Tkv, plan, "v", q.dtype)
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, plan.Tq, plan, "o", q.dtype)
+    alpha = plan.d ** -0.5 if alpha is None else float(alpha)
+    _ok(lib().gdpa_fwd(plan.handle, _dtype_id(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                       ctypes.c_float(alpha), ACT[act], _stream_ptr(stream)), "gdpa_fwd")
+    return o
+
+
+def gdpa_bwd(plan: Plan, q, k, v, do, dq=None, dk=None, dv=None, alpha=None,
+             act: str = "gelu_erf", stream=None):
+    """(dQ, dK, dV) as float32 tensors given the upstream gradient dO."""
+    import torch
+    _check(q, plan.Tq, plan, "q")
+    _check(k, plan.Tkv, plan, "k", q.dtype)
+    _check(v, plan.Tkv, plan, "v", q.dtype)
+    _check(do, plan.Tq, plan, "do", q.dtype)
+    f32 = torch.float32
+    dq = torch.empty(q.shape, dtype=f32, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=f32, device=k.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=f32, device=v.device) if dv is None else dv
+    _check(dq, plan.Tq, plan, "dq", f32)
+    _check(dk, plan.Tkv, plan, "dk", f32)
+    _check(dv, plan.Tkv, plan, "dv", f32)
+    alpha = plan.d ** -0.5 if alpha is None else float(alpha)
+    _ok(lib().gdpa_bwd(plan.handle, _dtype_id(q), _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq),
+                       _ptr(dk), _ptr(dv), ctypes.c_float(alpha), ACT[act], _stream_ptr(stream)),
+        "gdpa_bwd")
+    return dq, dk, dv
