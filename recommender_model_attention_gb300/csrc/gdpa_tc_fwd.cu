@@ -1,9 +1,503 @@
-// tcgen05 forward kernel (placeholder until the tensor-core path lands).
-#include "gdpa_internal.h"
+// Persistent tcgen05 GDPA forward kernel (bf16 in, fp32 accumulate, bf16 out).
+//
+// GDPA ("범용 내적 어텐션(GDPA)", aitrends.kr) computes O = act(alpha Q K^T) V
+// per sample with the softmax replaced by an element-wise activation; the
+// page's design notes drop the softmax correction (no running max, row sum
+// or rescaling of O), pipeline across the outer loop for short K/V, flatten
+// the (query tile, key block) loops, and walk a host-planned tile list dealt
+// to SMs in zigzag order.  This kernel is the GB300 rendering of that:
+//
+//  * grid = one CTA per planned SM queue; CTA s walks tiles seg[s]..seg[s+1].
+//  * warp 0 (one lane): TMA producer.  Q tile [128 x d] per tile, K and V
+//    blocks [128 x d] per (tile, key block) item, through 2-stage rings.
+//  * warp 1 (one lane): tcgen05.mma issuer.  Per item: S = Q K^T into TMEM;
+//    the P V product of the previous item is issued after the next S, so the
+//    tensor core computes item i+1's scores while item i's activation runs
+//    (software pipelining across tile boundaries on one flattened loop).
+//  * warps 2-9: two activation/epilogue warpgroups taking alternate tiles,
+//    each with its own TMEM S (128 columns) and O (128 columns) accumulators.
+//    They read S with tcgen05.ld, apply alpha, the activation and the jagged /
+//    window mask (masked pairs become exactly 0 after the activation), write
+//    P as bf16 into shared memory in the 128-byte-swizzled K-major layout,
+//    and after the last key block read O from TMEM, stage it in the tile's
+//    (now consumed) Q buffer and store the valid rows with coalesced 16-byte
+//    stores.  Zero tiles (no valid key) are written as zeros directly.
+//  * O accumulates P V over key blocks with no rescaling.
+//  * Every barrier wait is bounded; a timeout sets the plan's error word and
+//    the CTA unwinds (waits for its TMA loads and MMAs, frees TMEM, returns).
+#include <cuda_bf16.h>
+
+#include "act.cuh"
+#include "tc_common.cuh"
 
 namespace gdpa {
-gdpa_status launch_tc_fwd(Plan&, const void*, const void*, const void*, void*, float, int,
-                          cudaStream_t) {
-    return GDPA_ERR_UNSUPPORTED;
+namespace {
+
+using namespace tc;
+
+constexpr int kNumWG = 2;                       // activation warpgroups
+constexpr int kThreads = 64 + 128 * kNumWG;     // producer, MMA, warpgroups
+constexpr int kHalfBytes = 128 * 128;           // 128 rows x 128 bytes (64 bf16)
+constexpr uint32_t kTmemCols = 512;
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kNQ = 2;
+    static constexpr int kNKV = 2;
+    static constexpr int kPBytes = 128 * 128 * 2;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffK = kOffQ + kNQ * kTileBytes;
+    static constexpr int kOffV = kOffK + kNKV * kTileBytes;
+    static constexpr int kOffP = kOffV + kNKV * kTileBytes;
+    static constexpr int kOffBar = kOffP + kPBytes;
+    // q_full, q_empty, k_full, v_full, kv_empty, p_full, p_free,
+    // s_full, s_free, o_full, o_free, stage (per warpgroup), mma_done
+    static constexpr int kBarQFull = 0;
+    static constexpr int kBarQEmpty = kBarQFull + kNQ;
+    static constexpr int kBarKFull = kBarQEmpty + kNQ;
+    static constexpr int kBarVFull = kBarKFull + kNKV;
+    static constexpr int kBarKVEmpty = kBarVFull + kNKV;
+    static constexpr int kBarPFull = kBarKVEmpty + kNKV;
+    static constexpr int kBarPFree = kBarPFull + 1;
+    static constexpr int kBarSFull = kBarPFree + 1;
+    static constexpr int kBarSFree = kBarSFull + kNumWG;
+    static constexpr int kBarOFull = kBarSFree + kNumWG;
+    static constexpr int kBarOFree = kBarOFull + kNumWG;
+    static constexpr int kBarStage = kBarOFree + kNumWG;
+    static constexpr int kBarMmaDone = kBarStage + kNumWG;
+    static constexpr int kNumBars = kBarMmaDone + 1;
+    static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+};
+
+struct FwdParams {
+    const FwdTile* tiles;
+    const int32_t* seg;
+    __nv_bfloat16* O;
+    int H;
+    float alpha;
+    int mask;
+    int window;
+    int32_t* err;
+    unsigned long long* times;
+    int32_t* smid;
+    int timing;
+};
+
+__device__ __forceinline__ FwdTile load_tile(const FwdTile* p) {
+    const int4* q = reinterpret_cast<const int4*>(p);
+    const int4 a = __ldg(q), b = __ldg(q + 1);
+    FwdTile t;
+    t.qt0 = a.x; t.nq = a.y; t.kvt0 = a.z; t.lkv = a.w;
+    t.h = b.x; t.kb0 = b.y; t.kb1 = b.z; t.i0 = b.w;
+    return t;
 }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int D>
+__device__ void fwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                             const FwdParams& prm, uint8_t* smem, uint64_t* bars, int seg0,
+                             int seg1, const Abort& ab) {
+    using C = FwdCfg<D>;
+    const uint64_t pol_q = policy_evict_first();
+    const uint64_t pol_kv = policy_evict_last();
+    int32_t q_armed[C::kNQ], kv_armed[C::kNKV];
+    for (int s = 0; s < C::kNQ; ++s) q_armed[s] = -1;
+    for (int s = 0; s < C::kNKV; ++s) kv_armed[s] = -1;
+    uint32_t a = 0, i = 0;
+    for (int t = seg0; t < seg1; ++t) {
+        const FwdTile tile = load_tile(prm.tiles + t);
+        if (tile.kb1 <= tile.kb0) continue;
+        const uint32_t qs = a % C::kNQ, qph = (a / C::kNQ) & 1;
+        if (!mbar_wait(&bars[C::kBarQEmpty + qs], qph ^ 1, ab, 1)) goto unwind;
+        mbar_arrive_expect_tx(&bars[C::kBarQFull + qs], C::kTileBytes);
+        q_armed[qs] = (int32_t)qph;
+#pragma unroll
+        for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_2d(tmQ, &bars[C::kBarQFull + qs],
+                        smem + C::kOffQ + qs * C::kTileBytes + hf * kHalfBytes,
+                        tile.h * D + hf * 64, tile.qt0, pol_q);
+        for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++i) {
+            const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
+            if (!mbar_wait(&bars[C::kBarKVEmpty + ks], kph ^ 1, ab, 2)) goto unwind;
+            const int y = tile.kvt0 + kb * kBN;
+            mbar_arrive_expect_tx(&bars[C::kBarKFull + ks], C::kTileBytes);
+#pragma unroll
+            for (int hf = 0; hf < C::kHalves; ++hf)
+                tma_load_2d(tmK, &bars[C::kBarKFull + ks],
+                            smem + C::kOffK + ks * C::kTileBytes + hf * kHalfBytes,
+                            tile.h * D + hf * 64, y, pol_kv);
+            mbar_arrive_expect_tx(&bars[C::kBarVFull + ks], C::kTileBytes);
+#pragma unroll
+            for (int hf = 0; hf < C::kHalves; ++hf)
+                tma_load_2d(tmV, &bars[C::kBarVFull + ks],
+                            smem + C::kOffV + ks * C::kTileBytes + hf * kHalfBytes,
+                            tile.h * D + hf * 64, y, pol_kv);
+            kv_armed[ks] = (int32_t)kph;
+        }
+        ++a;
+    }
+unwind:
+    // never leave the CTA with a TMA write still in flight
+    for (int s = 0; s < C::kNQ; ++s)
+        if (q_armed[s] >= 0) mbar_wait_teardown(&bars[C::kBarQFull + s], (uint32_t)q_armed[s]);
+    for (int s = 0; s < C::kNKV; ++s)
+        if (kv_armed[s] >= 0) {
+            mbar_wait_teardown(&bars[C::kBarKFull + s], (uint32_t)kv_armed[s]);
+            mbar_wait_teardown(&bars[C::kBarVFull + s], (uint32_t)kv_armed[s]);
+        }
+}
+
+struct PendingPV {
+    uint32_t item, wg, ks, kph, nsteps;
+    bool first, last;
+};
+
+template <int D>
+__device__ __forceinline__ bool issue_pv(const PendingPV& pd, uint8_t* smem, uint64_t* bars,
+                                         uint32_t tmem, uint32_t* o_use, const Abort& ab) {
+    using C = FwdCfg<D>;
+    if (!mbar_wait(&bars[C::kBarVFull + pd.ks], pd.kph, ab, 10)) return false;
+    if (!mbar_wait(&bars[C::kBarPFull], pd.item & 1, ab, 11)) return false;
+    if (pd.first && !mbar_wait(&bars[C::kBarOFree + pd.wg], (o_use[pd.wg] & 1) ^ 1, ab, 12))
+        return false;
+    tc_fence_after();
+    constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
+    const uint32_t d_o = tmem + pd.wg * 256 + 128;
+    const uint32_t pbase = smem_u32(smem + C::kOffP);
+    const uint32_t vbase = smem_u32(smem + C::kOffV + pd.ks * C::kTileBytes);
+    for (uint32_t k = 0; k < pd.nsteps; ++k) {
+        const uint64_t a_desc = smem_desc_sw128(pbase + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
+        const uint64_t b_desc = smem_desc_sw128(vbase + k * 2048, kHalfBytes, 1024);
+        mma_ss(d_o, a_desc, b_desc, idesc, (pd.first && k == 0) ? 0u : 1u);
+    }
+    mma_commit(&bars[C::kBarPFree]);
+    mma_commit(&bars[C::kBarKVEmpty + pd.ks]);
+    if (pd.last) {
+        mma_commit(&bars[C::kBarOFull + pd.wg]);
+        o_use[pd.wg]++;
+    }
+    return true;
+}
+
+template <int D>
+__device__ void fwd_mma(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
+                        int seg0, int seg1, const Abort& ab) {
+    using C = FwdCfg<D>;
+    uint32_t s_use[kNumWG] = {}, o_use[kNumWG] = {};
+    uint32_t a = 0, i = 0;
+    PendingPV pend{};
+    bool have_pend = false;
+    for (int t = seg0; t < seg1; ++t) {
+        const FwdTile tile = load_tile(prm.tiles + t);
+        if (tile.kb1 <= tile.kb0) continue;
+        const uint32_t wg = a % kNumWG;
+        const uint32_t qs = a % C::kNQ, qph = (a / C::kNQ) & 1;
+        if (!mbar_wait(&bars[C::kBarQFull + qs], qph, ab, 3)) goto drain;
+        for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++i) {
+            const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
+            const int nvalid = min(kBN, tile.lkv - kb * kBN);
+            const uint32_t n32 = (uint32_t)((nvalid + 31) & ~31);
+            if (!mbar_wait(&bars[C::kBarKFull + ks], kph, ab, 4)) goto drain;
+            if (!mbar_wait(&bars[C::kBarSFree + wg], (s_use[wg] & 1) ^ 1, ab, 5)) goto drain;
+            tc_fence_after();
+            const uint32_t idesc = idesc_bf16(128, n32, false, false);
+            const uint32_t qbase = smem_u32(smem + C::kOffQ + qs * C::kTileBytes);
+            const uint32_t kbase = smem_u32(smem + C::kOffK + ks * C::kTileBytes);
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
+                mma_ss(tmem + wg * 256, smem_desc_sw128(qbase + off, 16, 1024),
+                       smem_desc_sw128(kbase + off, 16, 1024), idesc, k > 0 ? 1u : 0u);
+            }
+            mma_commit(&bars[C::kBarSFull + wg]);
+            s_use[wg]++;
+            if (have_pend && !issue_pv<D>(pend, smem, bars, tmem, o_use, ab)) goto drain;
+            pend = PendingPV{i, wg, ks, kph, n32 / 16, kb == tile.kb0, kb == tile.kb1 - 1};
+            have_pend = true;
+        }
+        ++a;
+    }
+    if (have_pend) issue_pv<D>(pend, smem, bars, tmem, o_use, ab);
+drain:
+    // all MMAs issued by this thread complete before TMEM is released
+    mma_commit(&bars[C::kBarMmaDone]);
+    mbar_wait_teardown(&bars[C::kBarMmaDone], 0);
+}
+
+template <int D>
+__device__ __forceinline__ void store_zero_rows(const FwdTile& tile, const FwdParams& prm, int tid) {
+    constexpr int kChunks = D / 8;  // 16-byte chunks per row
+    const int64_t rs = (int64_t)prm.H * D;
+    for (int idx = tid; idx < tile.nq * kChunks; idx += 128) {
+        const int row = idx / kChunks, ch = idx % kChunks;
+        *reinterpret_cast<uint4*>(prm.O + (int64_t)(tile.qt0 + row) * rs + tile.h * D + ch * 8) =
+            make_uint4(0, 0, 0, 0);
+    }
+}
+
+// A wait taken by every thread of a warpgroup; warp-uniform result so that
+// the .sync.aligned tcgen05 loads after it run with whole warps.
+__device__ __forceinline__ bool wg_wait(uint64_t* bar, uint32_t parity, const Abort& ab,
+                                        int32_t where) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, where));
+}
+
+template <int D, int ACT>
+__device__ void fwd_compute(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
+                            int seg0, int seg1, const Abort& ab) {
+    using C = FwdCfg<D>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t wg = (uint32_t)(warp - 2) / 4;
+    const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;          // tile row of this thread
+    const int tid = (int)threadIdx.x - 64 - 128 * (int)wg;
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const uint32_t s_tmem = tmem + wg * 256 + lane_addr;
+    const uint32_t o_tmem = tmem + wg * 256 + 128 + lane_addr;
+    uint8_t* pbuf = smem + C::kOffP;
+    uint32_t a = 0, i = 0, s_use = 0, o_use = 0;
+    for (int t = seg0; t < seg1; ++t) {
+        const FwdTile tile = load_tile(prm.tiles + t);
+        if (tile.kb1 <= tile.kb0) {
+            if ((uint32_t)((t - seg0) % kNumWG) == wg) store_zero_rows<D>(tile, prm, tid);
+            continue;
+        }
+        if (a % kNumWG != wg) {
+            i += tile.kb1 - tile.kb0;
+            ++a;
+            continue;
+        }
+        const uint32_t qs = a % C::kNQ;
+        const bool warp_rows = quarter * 32 < tile.nq;
+        const int ipos = tile.i0 + r;
+        for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++i) {
+            const int nvalid = min(kBN, tile.lkv - kb * kBN);
+            const int nch = (nvalid + 31) >> 5;
+            if (!wg_wait(&bars[C::kBarSFull + wg], s_use & 1, ab, 6)) return;
+            s_use++;
+            tc_fence_after();
+            // S -> registers one 32-column chunk at a time, activation and
+            // mask applied straight away (keeps register pressure low)
+            uint32_t pk[4][16];
+            if (warp_rows) {
+                const int jbase = kb * kBN;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (c < nch) {
+                        uint32_t sv[32];
+                        tmem_ld32(s_tmem + c * 32, sv);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float pv[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int col = c * 32 + e + u;
+                                const int jpos = jbase + col;
+                                bool valid = col < nvalid;
+                                if (prm.mask == GDPA_MASK_CAUSAL_WINDOW)
+                                    valid = valid && jpos <= ipos && jpos > ipos - prm.window;
+                                const float x = prm.alpha * __uint_as_float(sv[e + u]);
+                                pv[u] = valid ? act_f<ACT, true>(x) : 0.0f;
+                            }
+                            pk[c][e >> 1] = pack_bf16x2(pv[0], pv[1]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars[C::kBarSFree + wg]);
+            if (!wg_wait(&bars[C::kBarPFree], (i & 1) ^ 1, ab, 7)) return;
+            if (warp_rows) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (c < nch) {
+                        uint8_t* rowp = pbuf + (c >> 1) * kHalfBytes + r * 128;
+#pragma unroll
+                        for (int u = 0; u < 4; ++u) {
+                            const int chunk = ((c & 1) * 4 + u) ^ (r & 7);
+                            *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+                                make_uint4(pk[c][4 * u], pk[c][4 * u + 1], pk[c][4 * u + 2],
+                                           pk[c][4 * u + 3]);
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[C::kBarPFull]);
+        }
+        // epilogue: O (TMEM) -> bf16 -> staging (this tile's Q buffer) -> global
+        if (!wg_wait(&bars[C::kBarOFull + wg], o_use & 1, ab, 8)) return;
+        o_use++;
+        tc_fence_after();
+        uint8_t* stage = smem + C::kOffQ + qs * C::kTileBytes;
+        constexpr int kRowBytes = D * 2;
+        if (warp_rows) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t ov[32];
+                tmem_ld32(o_tmem + c * 32, ov);
+                tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int chunk = (c * 4 + u) ^ (r & 7);
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(ov[8 * u + 0]), __uint_as_float(ov[8 * u + 1]));
+                    w.y = pack_bf16x2(__uint_as_float(ov[8 * u + 2]), __uint_as_float(ov[8 * u + 3]));
+                    w.z = pack_bf16x2(__uint_as_float(ov[8 * u + 4]), __uint_as_float(ov[8 * u + 5]));
+                    w.w = pack_bf16x2(__uint_as_float(ov[8 * u + 6]), __uint_as_float(ov[8 * u + 7]));
+                    *reinterpret_cast<uint4*>(stage + r * kRowBytes + chunk * 16) = w;
+                }
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(&bars[C::kBarOFree + wg]);
+        // the whole warpgroup's staging writes before anyone reads them back
+        mbar_arrive(&bars[C::kBarStage + wg]);
+        if (!wg_wait(&bars[C::kBarStage + wg], (o_use - 1) & 1, ab, 9)) return;
+        {
+            constexpr int kChunks = D / 8;
+            const int64_t rs = (int64_t)prm.H * D;
+            __nv_bfloat16* obase = prm.O + (int64_t)tile.qt0 * rs + tile.h * D;
+            for (int idx = tid; idx < tile.nq * kChunks; idx += 128) {
+                const int row = idx / kChunks, ch = idx % kChunks;
+                const uint4 w = *reinterpret_cast<const uint4*>(stage + row * kRowBytes +
+                                                                ((ch ^ (row & 7)) * 16));
+                *reinterpret_cast<uint4*>(obase + (int64_t)row * rs + ch * 8) = w;
+            }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[C::kBarQEmpty + qs]);
+        ++a;
+    }
+}
+
+template <int D, int ACT>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const FwdParams prm) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int seg0 = prm.seg[blockIdx.x], seg1 = prm.seg[blockIdx.x + 1];
+    uint64_t t_start = 0;
+    if (threadIdx.x == 0) {
+        t_start = globaltimer();
+        for (int s = 0; s < C::kNQ; ++s) {
+            mbar_init(&bars[C::kBarQFull + s], 1);
+            mbar_init(&bars[C::kBarQEmpty + s], 128);
+        }
+        for (int s = 0; s < C::kNKV; ++s) {
+            mbar_init(&bars[C::kBarKFull + s], 1);
+            mbar_init(&bars[C::kBarVFull + s], 1);
+            mbar_init(&bars[C::kBarKVEmpty + s], 1);
+        }
+        mbar_init(&bars[C::kBarPFull], 128);
+        mbar_init(&bars[C::kBarPFree], 1);
+        for (int w = 0; w < kNumWG; ++w) {
+            mbar_init(&bars[C::kBarSFull + w], 1);
+            mbar_init(&bars[C::kBarSFree + w], 128);
+            mbar_init(&bars[C::kBarOFull + w], 1);
+            mbar_init(&bars[C::kBarOFree + w], 128);
+            mbar_init(&bars[C::kBarStage + w], 128);
+        }
+        mbar_init(&bars[C::kBarMmaDone], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Abort ab{abort_flag, prm.err};
+
+    if (warp == 0) {
+        if (lane == 0) fwd_producer<D>(&tmQ, &tmK, &tmV, prm, smem, bars, seg0, seg1, ab);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) fwd_mma<D>(prm, smem, bars, tmem, seg0, seg1, ab);
+        __syncwarp();
+    } else {
+        fwd_compute<D, ACT>(prm, smem, bars, tmem, seg0, seg1, ab);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (threadIdx.x == 0 && prm.timing) {
+        prm.times[2 * blockIdx.x] = t_start;
+        prm.times[2 * blockIdx.x + 1] = globaltimer();
+        prm.smid[blockIdx.x] = (int32_t)smid();
+    }
+}
+
+template <int D, int ACT>
+gdpa_status launch(Plan& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                   const FwdParams& prm, cudaStream_t st) {
+    using C = FwdCfg<D>;
+    auto kern = tc_fwd_kernel<D, ACT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+        return GDPA_ERR_CUDA;
+    kern<<<p.S, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, prm);
+    p.launches += 1;
+    return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+}  // namespace
+
+gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, void* o,
+                          float alpha, int act, cudaStream_t st) {
+    if (p.d != 64 && p.d != 128) return GDPA_ERR_UNSUPPORTED;
+    if (p.Tq == 0 || p.n_fwd == 0) return GDPA_OK;
+    CUtensorMap mq, mk, mv;
+    const uint64_t row = (uint64_t)p.H * p.d;
+    const uint64_t kv_rows = p.Tkv > 0 ? (uint64_t)p.Tkv : 1;
+    const void* kp = p.Tkv > 0 ? k : q;
+    const void* vp = p.Tkv > 0 ? v : q;
+    if (!tc::make_tmap_bf16(&mq, q, (uint64_t)p.Tq, row, 128) ||
+        !tc::make_tmap_bf16(&mk, kp, kv_rows, row, 128) ||
+        !tc::make_tmap_bf16(&mv, vp, kv_rows, row, 128))
+        return GDPA_ERR_CUDA;
+    FwdParams prm;
+    prm.tiles = p.d_fwd;
+    prm.seg = p.d_fwd_seg;
+    prm.O = (__nv_bfloat16*)o;
+    prm.H = p.H;
+    prm.alpha = alpha;
+    prm.mask = p.mask;
+    prm.window = p.window;
+    prm.err = p.d_err;
+    prm.times = p.d_times;
+    prm.smid = p.d_smid;
+    prm.timing = p.timing;
+    if (p.timing) p.timed[0] = 1;
+    gdpa_status s = GDPA_OK;
+    if (p.d == 128) {
+        GDPA_DISPATCH_ACT(act, A, s = launch<128, A>(p, mq, mk, mv, prm, st))
+    } else {
+        GDPA_DISPATCH_ACT(act, A, s = launch<64, A>(p, mq, mk, mv, prm, st))
+    }
+    return s;
+}
+
 }  // namespace gdpa
