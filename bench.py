@@ -1,0 +1,391 @@
+"""GDPA benchmark: one step = forward + backward over one jagged batch.
+
+Default workload: the training step (jagged user-ad cross-attention, B=2048,
+H=8, d=128, bf16 inputs, Lq ~ Zipf(1.2) clipped to [1, 4096], Lkv ~ U[8, 128],
+GELU-erf, dO ~ N(0, 1)), inputs resident in HBM.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own batch of the same shape (different
+seed): the work shards by sample with no exchange, so scaling is weak.
+``--impl reference`` times the float64 CPU oracle on a bounded sample.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "GDPA fwd/bwd useful TFLOP/s on jagged batches; % of GB300 BF16 tensor peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def useful_pairs(q_off, kv_off, mask, window):
+    """Valid (query, key) pairs summed over samples (per head), closed form."""
+    lq = np.diff(np.asarray(q_off, dtype=np.int64))
+    lkv = np.diff(np.asarray(kv_off, dtype=np.int64))
+    if mask == "none":
+        return int(np.sum(lq * lkv))
+    # causal window on self-attention: sum_i min(i + 1, W) for i < min(Lq, Lkv)
+    n = 0
+    for a, b in zip(lq, lkv):
+        L = min(int(a), int(b))
+        W = window
+        n += W * (W + 1) // 2 + (L - W) * W if L >= W else L * (L + 1) // 2
+    return n
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(w, x, budget_s=15.0):
+    """Time the float64 oracle (forward + backward) on a prefix of the batch.
+
+    A small calibration prefix is timed first; the rest of the sample is
+    sized from it so that the whole measurement takes about ``budget_s``
+    seconds.  ``x`` holds the batch (device or host tensors); only the rows
+    of the sampled sequences are copied to the host.
+    """
+    from oracle import ref
+    ref.build()
+    q_off = np.asarray(x["q_off"], dtype=np.int64)
+    kv_off = np.asarray(x["kv_off"], dtype=np.int64)
+    backward = x.get("do") is not None
+    nb = len(q_off) - 1
+    per = np.diff(q_off) * np.diff(kv_off) * w.H * w.d * (12 if backward else 4)
+
+    def host(t, a, b):
+        return t[a:b].float().cpu().numpy()
+
+    def run(s0, s1):
+        qa, qb, ka, kb = q_off[s0], q_off[s1], kv_off[s0], kv_off[s1]
+        sq = (q_off[s0:s1 + 1] - qa).astype(np.int32)
+        skv = (kv_off[s0:s1 + 1] - ka).astype(np.int32)
+        q, k, v = host(x["q"], qa, qb), host(x["k"], ka, kb), host(x["v"], ka, kb)
+        t0 = time.perf_counter()
+        ref.fwd(sq, skv, q, k, v, w.alpha, w.act, w.mask, w.window)
+        if backward:
+            ref.bwd(sq, skv, q, k, v, host(x["do"], qa, qb), w.alpha, w.act, w.mask, w.window)
+        dt = time.perf_counter() - t0
+        flops = (12 if backward else 4) * w.d * w.H * useful_pairs(sq, skv, w.mask, w.window)
+        return flops, dt
+
+    n0 = int(min(nb, max(1, np.searchsorted(np.cumsum(per), 2e8) + 1)))
+    f0, t0 = run(0, n0)
+    rate = per[:n0].sum() / max(t0, 1e-9)
+    n1 = int(min(nb, n0 + np.searchsorted(np.cumsum(per[n0:]), rate * max(budget_s - t0, 0.0))))
+    f1, t1 = run(n0, n1) if n1 > n0 else (0, 0.0)
+    total_t = t0 + t1
+    return {"value": (f0 + f1) / total_t / 1e12, "unit": UNIT, "cores": ref.threads(),
+            "kind": "oracle",
+            "sample": "first %d of %d sequences of the same batch, %s, float64 loops "
+                      "(%.1f s)" % (n1 if n1 > n0 else n0, w.B,
+                                    "forward + backward" if backward else "forward", total_t)}
+
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from workloads import draw_lengths, make_inputs
+    lq, lkv = draw_lengths(w)
+    # a prefix of the batch with about 4e10 double flops is plenty for a
+    # bounded sample; the tensors are drawn on the host for it alone
+    per = lq * lkv * w.H * w.d * 12
+    n = int(min(w.B, np.searchsorted(np.cumsum(per), 4e10) + 1))
+    xh = make_inputs(w, device="cpu", lengths=(lq[:n], lkv[:n]))
+    budget = 20.0 / max(1, args.steps + args.warmup)
+    vals = []
+    base = None
+    for s in range(args.warmup + args.steps):
+        r = cpu_baseline(w, xh, budget_s=budget)
+        if s >= args.warmup:
+            vals.append(r["value"])
+            base = r
+    value = float(np.median(vals))
+    base["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded, same shapes as the GPU arm)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "d": w.d},
+            "cpu_baseline": base,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="training_cross_fwd_bwd")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    from workloads import get_config, make_inputs
+    w = get_config(args.workload)
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+    import torch.distributed as dist
+    import recommender_model_attention_gb300 as gd
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl")
+    gd.lib()
+    pk, pk_kind = peaks()
+
+    x = make_inputs(w, device="cuda", seed=1000 + w.index + 7919 * rank)
+    stream = torch.cuda.current_stream()
+    plan = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window)
+    f32 = torch.float32
+    o = torch.empty_like(x["q"])
+    dq = torch.empty(x["q"].shape, dtype=f32, device="cuda")
+    dk = torch.empty(x["k"].shape, dtype=f32, device="cuda")
+    dv = torch.empty(x["v"].shape, dtype=f32, device="cuda")
+    backward = x["do"] is not None
+
+    def step():
+        gd.gdpa_fwd(plan, x["q"], x["k"], x["v"], o=o, alpha=w.alpha, act=w.act)
+        if backward:
+            gd.gdpa_bwd(plan, x["q"], x["k"], x["v"], x["do"], dq, dk, dv, alpha=w.alpha,
+                        act=w.act)
+
+    Tq, Tkv = int(x["q_off"][-1]), int(x["kv_off"][-1])
+    pairs = useful_pairs(x["q_off"], x["kv_off"], w.mask, w.window)
+    fwd_flops = 4.0 * w.d * w.H * pairs
+    bwd_flops = 8.0 * w.d * w.H * pairs if backward else 0.0
+    row = w.H * w.d
+    fwd_bytes = (2 * Tq + 2 * Tkv) * row * 2
+    bwd_bytes = (2 * Tq + 2 * Tkv) * row * 2 + (Tq + 2 * Tkv) * row * 4 if backward else 0
+    input_bytes = sum(t.numel() * t.element_size() for t in (x["q"], x["k"], x["v"], x["do"])
+                      if t is not None)
+
+    for _ in range(args.warmup):
+        step()
+    plan.check()
+    torch.cuda.synchronize()
+
+    # timed region: K steps, per-phase events on the launching stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = Clocks(local)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    launches0 = plan.launches
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for s in range(args.steps):
+        ev[s][0].record(stream)
+        gd.gdpa_fwd(plan, x["q"], x["k"], x["v"], o=o, alpha=w.alpha, act=w.act)
+        ev[s][1].record(stream)
+        if backward:
+            gd.gdpa_bwd(plan, x["q"], x["k"], x["v"], x["do"], dq, dk, dv, alpha=w.alpha,
+                        act=w.act)
+        ev[s][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    launches = plan.launches - launches0
+    plan.check()
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_step = elapsed_ms / args.steps
+    fwd_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in ev]))
+    bwd_ms = float(np.mean([b.elapsed_time(c) for _, b, c in ev])) if backward else 0.0
+    value = (fwd_flops + bwd_flops) * world / (ms_step * 1e-3) / 1e12
+
+    # roofline of the dominant phase (kernel time measured live above)
+    if bwd_ms > fwd_ms:
+        dom, dom_ms, dom_bytes = "gdpa_bwd", bwd_ms, bwd_bytes
+    else:
+        dom, dom_ms, dom_bytes = "gdpa_fwd", fwd_ms, fwd_bytes
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": None,
+                "peak_kind": pk_kind}
+
+    # end to end through the public API: pinned host inputs in, results out
+    e2e = None
+    if not args.no_e2e:
+        hq = x["q"].cpu().pin_memory()
+        hk = x["k"].cpu().pin_memory()
+        hv = x["v"].cpu().pin_memory()
+        hdo = x["do"].cpu().pin_memory() if backward else None
+        ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+        hgrads = [torch.empty(t.shape, dtype=f32, pin_memory=True) for t in (dq, dk, dv)]
+        q_d, k_d, v_d = (torch.empty_like(t) for t in (x["q"], x["k"], x["v"]))
+        do_d = torch.empty_like(x["q"]) if backward else None
+
+        def e2e_step():
+            q_d.copy_(hq, non_blocking=True)
+            k_d.copy_(hk, non_blocking=True)
+            v_d.copy_(hv, non_blocking=True)
+            if backward:
+                do_d.copy_(hdo, non_blocking=True)
+            gd.gdpa_fwd(plan, q_d, k_d, v_d, o=o, alpha=w.alpha, act=w.act)
+            ho.copy_(o, non_blocking=True)
+            if backward:
+                gd.gdpa_bwd(plan, q_d, k_d, v_d, do_d, dq, dk, dv, alpha=w.alpha, act=w.act)
+                for h, d_ in zip(hgrads, (dq, dk, dv)):
+                    h.copy_(d_, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        n_e2e = max(2, min(args.steps, 5))
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / n_e2e
+        h2d = input_bytes
+        d2h = o.numel() * o.element_size() + (sum(t.numel() * 4 for t in (dq, dk, dv))
+                                              if backward else 0)
+        e2e = {"value": (fwd_flops + bwd_flops) / (e2e_ms * 1e-3) / 1e12 * world, "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e2e_ms}
+
+    # SM busy-time spread of each policy (separate, untimed launches)
+    spread = {}
+    try:
+        for pol in ("zigzag", "round_robin"):
+            pp = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window, sched=pol)
+            pp.set_timing(True)
+            gd.gdpa_fwd(pp, x["q"], x["k"], x["v"], o=o, alpha=w.alpha, act=w.act)
+            pp.check()
+            se, _ = pp.sm_times("fwd")
+            busy = (se[:, 1] - se[:, 0]).astype(np.float64)
+            spread[pol] = {"max_over_min": float(busy.max() / max(busy.min(), 1.0)),
+                           "max_minus_min_over_mean": float((busy.max() - busy.min()) / busy.mean())}
+            pp.destroy()
+    except Exception as e:  # timing is a report, not the measurement
+        spread["error"] = str(e)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, x)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded lengths and RMSNorm'd N(0,1) inputs, random dO)",
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "act": w.act,
+                       "Tq": Tq, "Tkv": Tkv, "useful_pairs": pairs,
+                       "l2": "inputs larger than L2 (%.1f GB resident)" % (input_bytes / 1e9),
+                       "parallelism": "samples sharded by rank, no exchange" if world > 1
+                       else "single GPU"},
+            "pct_of_bf16_peak": 100.0 * value / world / pk["bf16_tflops"],
+            "fwd": {"ms": fwd_ms, "tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12,
+                    "gbs": fwd_bytes / (fwd_ms * 1e-3) / 1e9},
+            "bwd": ({"ms": bwd_ms, "tflops": bwd_flops / (bwd_ms * 1e-3) / 1e12,
+                     "gbs": bwd_bytes / (bwd_ms * 1e-3) / 1e9} if backward else None),
+            "roofline": roofline,
+            "gpu_launches": int(launches),
+            "clocks": clk,
+            "e2e": e2e,
+            "sm_spread_fwd": spread,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    plan.destroy()
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

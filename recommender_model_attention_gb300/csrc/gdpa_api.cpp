@@ -45,10 +45,6 @@ bool use_tc(const Plan& p, gdpa_dtype dt) {
     return p.d == 64 || p.d == 128;
 }
 
-// the tensor-core backward is not built yet: AUTO runs it on CUDA cores
-bool use_tc_bwd(const Plan& p, gdpa_dtype dt) {
-    return use_tc(p, dt) && p.kernel == GDPA_KERNEL_TCGEN05;
-}
 
 }  // namespace
 
@@ -239,7 +235,7 @@ gdpa_status gdpa_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void
     if (p.fwd_split) return GDPA_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
-    if (use_tc_bwd(p, dtype)) return gdpa::launch_tc_bwd(p, q, k, v, d_o, dq, dk, dv, alpha, act, st);
+    if (use_tc(p, dtype)) return gdpa::launch_tc_bwd(p, q, k, v, d_o, dq, dk, dv, alpha, act, st);
     return gdpa::launch_simt_bwd(p, dtype, q, k, v, d_o, dq, dk, dv, alpha, act, st);
 }
 

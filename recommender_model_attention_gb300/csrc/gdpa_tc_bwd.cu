@@ -1,9 +1,532 @@
-// tcgen05 backward kernel (placeholder until the tensor-core path lands).
-#include "gdpa_internal.h"
+// Persistent tcgen05 GDPA backward kernel (bf16 inputs, fp32 gradients).
+//
+// With x = alpha q.k over the valid pairs of a sample, P = act(x) and
+// dS = (dO V^T) * act'(x) (the derivative of O = act(alpha Q K^T) V, the GDPA
+// of "범용 내적 어텐션(GDPA)", aitrends.kr, which has no softmax and so no
+// row-sum term):
+//     dV = P^T dO,   dK = alpha dS^T Q,   dQ = alpha dS K.
+//
+// Work unit = one 128-row key block of one (sample, head) with the range of
+// 128-row query tiles that see it (host plan, zigzag-dealt like the forward
+// tiles).  The unit's dK and dV accumulate in TMEM over its query tiles and
+// are stored once; each query tile's dQ is complete when the sample has a
+// single key block (stored directly) and is otherwise added atomically into
+// a cleared dQ.
+//
+// Roles: warp 0 TMA producer (K, V once per unit; Q and dO per query tile
+// through 2-stage rings); warp 1 tcgen05.mma issuer; warps 2-5 one
+// warpgroup that turns S and dP (TMEM) into P and dS (bf16, shared memory)
+// and drains dQ, dK, dV from TMEM.  Per query tile:
+//     S  = Q K^T   -> TMEM [0, 128)      dP = dO V^T -> TMEM [128, 256)
+//     P, dS        -> one 32 KB shared buffer, P first, then dS
+//     dV += P^T dO -> TMEM [256, 384)    dK += dS^T Q -> TMEM [384, 512)
+//     dQ  = dS K   -> TMEM [128, 256) (dP's columns, already read)
+// P^T and dS^T are the MN-major reading of the [query x key] buffer, and Q,
+// dO, K are the MN-major reading of their [row x d] tiles, so nothing is
+// transposed in memory.  Every wait is bounded (timeouts set the plan's
+// error word; the CTA unwinds, frees TMEM and returns).
+#include <cuda_bf16.h>
+
+#include "act.cuh"
+#include "tc_common.cuh"
 
 namespace gdpa {
-gdpa_status launch_tc_bwd(Plan&, const void*, const void*, const void*, const void*, float*,
-                          float*, float*, float, int, cudaStream_t) {
-    return GDPA_ERR_UNSUPPORTED;
+namespace {
+
+using namespace tc;
+
+constexpr int kThreads = 64 + 128;
+constexpr int kHalfBytes = 128 * 128;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
+
+template <int D>
+struct BwdCfg {
+    static constexpr int kHalves = D / 64;
+    static constexpr int kTileBytes = 128 * D * 2;
+    static constexpr int kOffK = 0;
+    static constexpr int kOffV = kOffK + kTileBytes;
+    static constexpr int kOffQ = kOffV + kTileBytes;          // 2 stages
+    static constexpr int kOffDO = kOffQ + 2 * kTileBytes;     // 2 stages
+    static constexpr int kOffPS = kOffDO + 2 * kTileBytes;    // P / dS / staging
+    static constexpr int kOffBar = kOffPS + 128 * 128 * 2;
+    enum {
+        kKVFull = 0, kKVEmpty, kQFull, kQFull1, kQEmpty, kQEmpty1, kDOFull, kDOFull1, kDOEmpty,
+        kDOEmpty1, kSDFull, kSFree, kDQFree, kPFull, kPVDone, kDSFull, kDQFull, kAccFull,
+        kAccFree, kStage, kMmaDone, kNumBars
+    };
+    static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
+};
+
+struct BwdParams {
+    const BwdUnit* units;
+    const int32_t* seg;
+    float* dQ;
+    float* dK;
+    float* dV;
+    int H;
+    float alpha;
+    int mask;
+    int window;
+    int32_t* err;
+    unsigned long long* times;
+    int32_t* smid;
+    int timing;
+};
+
+__device__ __forceinline__ BwdUnit load_unit(const BwdUnit* p) {
+    const int4* q = reinterpret_cast<const int4*>(p);
+    const int4 a = __ldg(q), b = __ldg(q + 1);
+    BwdUnit u;
+    u.kvt0 = a.x; u.nkv = a.y; u.qt0 = a.z; u.lq = a.w;
+    u.hf = b.x; u.m0 = b.y; u.m1 = b.z; u.c0 = b.w;
+    return u;
 }
+
+template <int D>
+__device__ void bwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                             const CUtensorMap* tmDO, const BwdParams& prm, uint8_t* smem,
+                             uint64_t* bars, int seg0, int seg1, const Abort& ab) {
+    using C = BwdCfg<D>;
+    const uint64_t pol_stream = policy_evict_first();
+    const uint64_t pol_keep = policy_evict_last();
+    int32_t kv_armed = -1, q_armed[2] = {-1, -1}, do_armed[2] = {-1, -1};
+    uint32_t nu = 0, i = 0;
+    for (int t = seg0; t < seg1; ++t) {
+        const BwdUnit u = load_unit(prm.units + t);
+        if (u.m1 <= u.m0) continue;
+        const int h = u.hf & 0xffff;
+        if (!mbar_wait(&bars[C::kKVEmpty], (nu & 1) ^ 1, ab, 21)) goto unwind;
+        mbar_arrive_expect_tx(&bars[C::kKVFull], 2 * C::kTileBytes);
+        kv_armed = (int32_t)(nu & 1);
+#pragma unroll
+        for (int hf = 0; hf < C::kHalves; ++hf) {
+            tma_load_2d(tmK, &bars[C::kKVFull], smem + C::kOffK + hf * kHalfBytes, h * D + hf * 64,
+                        u.kvt0, pol_keep);
+            tma_load_2d(tmV, &bars[C::kKVFull], smem + C::kOffV + hf * kHalfBytes, h * D + hf * 64,
+                        u.kvt0, pol_keep);
+        }
+        for (int m = u.m0; m < u.m1; ++m, ++i) {
+            const uint32_t s = i & 1, ph = (i >> 1) & 1;
+            const int y = u.qt0 + m * kBM;
+            if (!mbar_wait(&bars[C::kQEmpty + s], ph ^ 1, ab, 22)) goto unwind;
+            mbar_arrive_expect_tx(&bars[C::kQFull + s], C::kTileBytes);
+            q_armed[s] = (int32_t)ph;
+#pragma unroll
+            for (int hf = 0; hf < C::kHalves; ++hf)
+                tma_load_2d(tmQ, &bars[C::kQFull + s],
+                            smem + C::kOffQ + s * C::kTileBytes + hf * kHalfBytes, h * D + hf * 64,
+                            y, pol_stream);
+            if (!mbar_wait(&bars[C::kDOEmpty + s], ph ^ 1, ab, 23)) goto unwind;
+            mbar_arrive_expect_tx(&bars[C::kDOFull + s], C::kTileBytes);
+            do_armed[s] = (int32_t)ph;
+#pragma unroll
+            for (int hf = 0; hf < C::kHalves; ++hf)
+                tma_load_2d(tmDO, &bars[C::kDOFull + s],
+                            smem + C::kOffDO + s * C::kTileBytes + hf * kHalfBytes, h * D + hf * 64,
+                            y, pol_stream);
+        }
+        ++nu;
+    }
+unwind:
+    if (kv_armed >= 0) mbar_wait_teardown(&bars[C::kKVFull], (uint32_t)kv_armed);
+    for (int s = 0; s < 2; ++s) {
+        if (q_armed[s] >= 0) mbar_wait_teardown(&bars[C::kQFull + s], (uint32_t)q_armed[s]);
+        if (do_armed[s] >= 0) mbar_wait_teardown(&bars[C::kDOFull + s], (uint32_t)do_armed[s]);
+    }
+}
+
+template <int D>
+__device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
+                        int seg0, int seg1, const Abort& ab) {
+    using C = BwdCfg<D>;
+    const uint32_t kbase = smem_u32(smem + C::kOffK);
+    const uint32_t vbase = smem_u32(smem + C::kOffV);
+    const uint32_t psbase = smem_u32(smem + C::kOffPS);
+    constexpr uint32_t idesc_acc = idesc_bf16(128, D, true, true);   // P^T dO, dS^T Q
+    constexpr uint32_t idesc_dq = idesc_bf16(128, D, false, true);   // dS K
+    uint32_t nu = 0, i = 0;
+    for (int t = seg0; t < seg1; ++t) {
+        const BwdUnit u = load_unit(prm.units + t);
+        if (u.m1 <= u.m0) continue;
+        const uint32_t nkv32 = (uint32_t)((u.nkv + 31) & ~31);
+        const uint32_t idesc_s = idesc_bf16(128, nkv32, false, false);
+        if (!mbar_wait(&bars[C::kKVFull], nu & 1, ab, 31)) goto drain;
+        for (int m = u.m0; m < u.m1; ++m, ++i) {
+            const uint32_t s = i & 1, ph = (i >> 1) & 1;
+            const bool first = m == u.m0, last = m == u.m1 - 1;
+            const int nq = min(kBM, u.lq - m * kBM);
+            const uint32_t nq32 = (uint32_t)((nq + 31) & ~31);
+            const uint32_t qb = smem_u32(smem + C::kOffQ + s * C::kTileBytes);
+            const uint32_t dob = smem_u32(smem + C::kOffDO + s * C::kTileBytes);
+            // S = Q K^T
+            if (!mbar_wait(&bars[C::kQFull + s], ph, ab, 32)) goto drain;
+            if (!mbar_wait(&bars[C::kSFree], (i & 1) ^ 1, ab, 33)) goto drain;
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
+                mma_ss(tmem + kColS, smem_desc_sw128(qb + off, 16, 1024),
+                       smem_desc_sw128(kbase + off, 16, 1024), idesc_s, k > 0);
+            }
+            // dP = dO V^T (into the columns dQ of the previous tile used)
+            if (!mbar_wait(&bars[C::kDOFull + s], ph, ab, 34)) goto drain;
+            if (!mbar_wait(&bars[C::kDQFree], (i & 1) ^ 1, ab, 35)) goto drain;
+            tc_fence_after();
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
+                mma_ss(tmem + kColDP, smem_desc_sw128(dob + off, 16, 1024),
+                       smem_desc_sw128(vbase + off, 16, 1024), idesc_s, k > 0);
+            }
+            mma_commit(&bars[C::kSDFull]);
+            // dV += P^T dO
+            if (!mbar_wait(&bars[C::kPFull], i & 1, ab, 36)) goto drain;
+            if (first && !mbar_wait(&bars[C::kAccFree], (nu & 1) ^ 1, ab, 37)) goto drain;
+            tc_fence_after();
+            for (uint32_t k = 0; k < nq32 / 16; ++k)
+                mma_ss(tmem + kColDV, smem_desc_sw128(psbase + k * 2048, kHalfBytes, 1024),
+                       smem_desc_sw128(dob + k * 2048, kHalfBytes, 1024), idesc_acc,
+                       (first && k == 0) ? 0u : 1u);
+            mma_commit(&bars[C::kDOEmpty + s]);
+            mma_commit(&bars[C::kPVDone]);
+            // dK += dS^T Q, dQ = dS K
+            if (!mbar_wait(&bars[C::kDSFull], i & 1, ab, 38)) goto drain;
+            tc_fence_after();
+            for (uint32_t k = 0; k < nq32 / 16; ++k)
+                mma_ss(tmem + kColDK, smem_desc_sw128(psbase + k * 2048, kHalfBytes, 1024),
+                       smem_desc_sw128(qb + k * 2048, kHalfBytes, 1024), idesc_acc,
+                       (first && k == 0) ? 0u : 1u);
+            mma_commit(&bars[C::kQEmpty + s]);
+            for (uint32_t k = 0; k < nkv32 / 16; ++k)
+                mma_ss(tmem + kColDP,
+                       smem_desc_sw128(psbase + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024),
+                       smem_desc_sw128(kbase + k * 2048, kHalfBytes, 1024), idesc_dq, k > 0);
+            mma_commit(&bars[C::kDQFull]);
+            if (last) {
+                mma_commit(&bars[C::kAccFull]);
+                mma_commit(&bars[C::kKVEmpty]);
+            }
+        }
+        ++nu;
+    }
+drain:
+    mma_commit(&bars[C::kMmaDone]);
+    mbar_wait_teardown(&bars[C::kMmaDone], 0);
+}
+
+// Store a [128 x 64] fp32 block staged in shared memory (row r at r * 256
+// bytes, 16-byte chunk c at (c ^ (r & 7))) to rows [0, nrows) of `dst`
+// (row stride `rs` floats); atomically added when `atomic`.
+__device__ __forceinline__ void store_staged(const uint8_t* stage, float* dst, int64_t rs,
+                                             int nrows, bool atomic, int tid) {
+    for (int idx = tid; idx < nrows * 16; idx += 128) {
+        const int row = idx >> 4, ch = idx & 15;
+        const float4 v =
+            *reinterpret_cast<const float4*>(stage + row * 256 + ((ch ^ (row & 7)) << 4));
+        float4* p = reinterpret_cast<float4*>(dst + (int64_t)row * rs + ch * 4);
+        if (atomic)
+            atomicAdd(p, v);
+        else
+            *p = v;
+    }
+}
+
+// Drain columns [col, col + D) of this warpgroup's TMEM rows to global rows
+// via the staging buffer, 64 columns at a time, scaled by `scale`.
+template <int D>
+__device__ __forceinline__ bool drain_rows(uint32_t tmem_row, uint32_t col, uint8_t* stage,
+                                           float* dst, int64_t rs, int nrows, bool atomic,
+                                           float scale, bool warp_rows, int r, int tid,
+                                           uint64_t* stage_bar, uint32_t& st_use, const Abort& ab,
+                                           uint64_t* release_bar) {
+#pragma unroll
+    for (int hf = 0; hf < D / 64; ++hf) {
+        if (warp_rows) {
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tmem_row + col + hf * 64 + c * 32, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int chunk = (c * 8 + u) ^ (r & 7);
+                    *reinterpret_cast<float4*>(stage + r * 256 + chunk * 16) =
+                        make_float4(scale * __uint_as_float(v[4 * u]),
+                                    scale * __uint_as_float(v[4 * u + 1]),
+                                    scale * __uint_as_float(v[4 * u + 2]),
+                                    scale * __uint_as_float(v[4 * u + 3]));
+                }
+            }
+        }
+        if (hf == D / 64 - 1 && release_bar) {
+            tc_fence_before();
+            mbar_arrive(release_bar);
+        }
+        mbar_arrive(stage_bar);
+        if (!wg_wait(stage_bar, st_use & 1, ab, 41)) return false;
+        ++st_use;
+        store_staged(stage, dst + hf * 64, rs, nrows, atomic, tid);
+        mbar_arrive(stage_bar);
+        if (!wg_wait(stage_bar, st_use & 1, ab, 42)) return false;
+        ++st_use;
+    }
+    return true;
+}
+
+template <int D>
+__device__ __forceinline__ void zero_rows(float* dst, int64_t rs, int nrows, int tid) {
+    constexpr int kChunks = D / 4;
+    for (int idx = tid; idx < nrows * kChunks; idx += 128) {
+        const int row = idx / kChunks, ch = idx % kChunks;
+        *reinterpret_cast<float4*>(dst + (int64_t)row * rs + ch * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+template <int D, int ACT>
+__device__ void bwd_compute(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
+                            int seg0, int seg1, const Abort& ab) {
+    using C = BwdCfg<D>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;   // TMEM lane = row of this thread
+    const int tid = (int)threadIdx.x - 64;
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+    uint8_t* ps = smem + C::kOffPS;
+    const int64_t rs = (int64_t)prm.H * D;
+    uint32_t nu = 0, i = 0, st_use = 0;
+    for (int t = seg0; t < seg1; ++t) {
+        const BwdUnit u = load_unit(prm.units + t);
+        const int h = u.hf & 0xffff;
+        const bool atomic_dq = (u.hf >> 16) & kUnitAtomicDQ;
+        if (u.m1 <= u.m0) {
+            zero_rows<D>(prm.dK + (int64_t)u.kvt0 * rs + h * D, rs, u.nkv, tid);
+            zero_rows<D>(prm.dV + (int64_t)u.kvt0 * rs + h * D, rs, u.nkv, tid);
+            continue;
+        }
+        const int nkv32 = (u.nkv + 31) & ~31;
+        const int nch = nkv32 >> 5;
+        for (int m = u.m0; m < u.m1; ++m, ++i) {
+            const int nq = min(kBM, u.lq - m * kBM);
+            const bool warp_rows = quarter * 32 < nq;
+            const int ipos = m * kBM + r;        // query position in the sample
+            const bool row_ok = r < nq;
+            if (!wg_wait(&bars[C::kSDFull], i & 1, ab, 43)) return;
+            tc_fence_after();
+            uint32_t pp[4][16], pd[4][16];
+            if (warp_rows) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (c < nch) {
+                        uint32_t sv[32], dv[32];
+                        tmem_ld32(trow + kColS + c * 32, sv);
+                        tmem_ld32(trow + kColDP + c * 32, dv);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; e += 2) {
+                            float p2[2], d2[2];
+#pragma unroll
+                            for (int w = 0; w < 2; ++w) {
+                                const int col = c * 32 + e + w;
+                                const int jpos = u.c0 + col;
+                                bool valid = row_ok && col < u.nkv;
+                                if (prm.mask == GDPA_MASK_CAUSAL_WINDOW)
+                                    valid = valid && jpos <= ipos && jpos > ipos - prm.window;
+                                float a, da;
+                                act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + w]), a, da);
+                                p2[w] = valid ? a : 0.0f;
+                                d2[w] = valid ? __uint_as_float(dv[e + w]) * da : 0.0f;
+                            }
+                            pp[c][e >> 1] = pack_bf16x2(p2[0], p2[1]);
+                            pd[c][e >> 1] = pack_bf16x2(d2[0], d2[1]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars[C::kSFree]);
+            // P -> shared (the previous tile's dS and staging are done with:
+            // this warpgroup drained that tile's dQ after its MMAs finished)
+            if (warp_rows) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (c < nch) {
+                        uint8_t* rowp = ps + (c >> 1) * kHalfBytes + r * 128;
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const int chunk = ((c & 1) * 4 + w) ^ (r & 7);
+                            *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+                                make_uint4(pp[c][4 * w], pp[c][4 * w + 1], pp[c][4 * w + 2],
+                                           pp[c][4 * w + 3]);
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[C::kPFull]);
+            // dS -> shared once P^T dO has read P
+            if (!wg_wait(&bars[C::kPVDone], i & 1, ab, 44)) return;
+            if (warp_rows) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    if (c < nch) {
+                        uint8_t* rowp = ps + (c >> 1) * kHalfBytes + r * 128;
+#pragma unroll
+                        for (int w = 0; w < 4; ++w) {
+                            const int chunk = ((c & 1) * 4 + w) ^ (r & 7);
+                            *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+                                make_uint4(pd[c][4 * w], pd[c][4 * w + 1], pd[c][4 * w + 2],
+                                           pd[c][4 * w + 3]);
+                        }
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[C::kDSFull]);
+            // dQ tile: TMEM -> staging (the P/dS buffer, free once dQ is done) -> global
+            if (!wg_wait(&bars[C::kDQFull], i & 1, ab, 45)) return;
+            tc_fence_after();
+            float* dq = prm.dQ + (int64_t)(u.qt0 + m * kBM) * rs + h * D;
+            if (!drain_rows<D>(trow, kColDP, ps, dq, rs, nq, atomic_dq, prm.alpha, warp_rows, r,
+                               tid, &bars[C::kStage], st_use, ab, &bars[C::kDQFree]))
+                return;
+        }
+        // the unit's dK, dV rows
+        if (!wg_wait(&bars[C::kAccFull], nu & 1, ab, 46)) return;
+        tc_fence_after();
+        {
+            const bool kv_rows = quarter * 32 < u.nkv;
+            float* dv = prm.dV + (int64_t)u.kvt0 * rs + h * D;
+            float* dk = prm.dK + (int64_t)u.kvt0 * rs + h * D;
+            if (!drain_rows<D>(trow, kColDV, ps, dv, rs, u.nkv, false, 1.0f, kv_rows, r, tid,
+                               &bars[C::kStage], st_use, ab, nullptr))
+                return;
+            if (!drain_rows<D>(trow, kColDK, ps, dk, rs, u.nkv, false, prm.alpha, kv_rows, r, tid,
+                               &bars[C::kStage], st_use, ab, &bars[C::kAccFree]))
+                return;
+        }
+        ++nu;
+    }
+}
+
+template <int D, int ACT>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+              const BwdParams prm) {
+    using C = BwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int seg0 = prm.seg[blockIdx.x], seg1 = prm.seg[blockIdx.x + 1];
+    uint64_t t_start = 0;
+    if (threadIdx.x == 0) {
+        t_start = globaltimer();
+        const uint32_t counts[C::kNumBars] = {
+            1, 1,            // kv full / empty
+            1, 1, 1, 1,      // q full x2, q empty x2
+            1, 1, 1, 1,      // dO full x2, dO empty x2
+            1, 128, 128,     // sd full, s free, dq free
+            128, 1, 128, 1,  // p full, pv done, ds full, dq full
+            1, 128, 128, 1   // acc full, acc free, stage, mma done
+        };
+        for (int b = 0; b < C::kNumBars; ++b) mbar_init(&bars[b], counts[b]);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmQ);
+        tma_prefetch_desc(&tmK);
+        tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmDO);
+    }
+    if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const Abort ab{abort_flag, prm.err};
+
+    if (warp == 0) {
+        if (lane == 0) bwd_producer<D>(&tmQ, &tmK, &tmV, &tmDO, prm, smem, bars, seg0, seg1, ab);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) bwd_mma<D>(prm, smem, bars, tmem, seg0, seg1, ab);
+        __syncwarp();
+    } else {
+        bwd_compute<D, ACT>(prm, smem, bars, tmem, seg0, seg1, ab);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+    if (threadIdx.x == 0 && prm.timing) {
+        prm.times[2 * (gridDim.x + blockIdx.x)] = t_start;
+        prm.times[2 * (gridDim.x + blockIdx.x) + 1] = globaltimer();
+        prm.smid[gridDim.x + blockIdx.x] = (int32_t)smid();
+    }
+}
+
+template <int D, int ACT>
+gdpa_status launch(Plan& p, const CUtensorMap* maps, const BwdParams& prm, cudaStream_t st) {
+    using C = BwdCfg<D>;
+    auto kern = tc_bwd_kernel<D, ACT>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
+        cudaSuccess)
+        return GDPA_ERR_CUDA;
+    kern<<<p.S, kThreads, C::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], prm);
+    p.launches += 1;
+    return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+}  // namespace
+
+gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, const void* d_o,
+                          float* dq, float* dk, float* dv, float alpha, int act, cudaStream_t st) {
+    if (p.d != 64 && p.d != 128) return GDPA_ERR_UNSUPPORTED;
+    const uint64_t row = (uint64_t)p.H * p.d;
+    if (p.zero_dq && p.Tq > 0) {
+        if (cudaMemsetAsync(dq, 0, (size_t)p.Tq * row * sizeof(float), st) != cudaSuccess)
+            return GDPA_ERR_CUDA;
+    }
+    if (p.n_bwd == 0) return GDPA_OK;
+    CUtensorMap maps[4];
+    const uint64_t q_rows = p.Tq > 0 ? (uint64_t)p.Tq : 1;
+    const void* qp = p.Tq > 0 ? q : k;
+    const void* dop = p.Tq > 0 ? d_o : k;
+    if (!tc::make_tmap_bf16(&maps[0], qp, q_rows, row, 128) ||
+        !tc::make_tmap_bf16(&maps[1], k, (uint64_t)p.Tkv, row, 128) ||
+        !tc::make_tmap_bf16(&maps[2], v, (uint64_t)p.Tkv, row, 128) ||
+        !tc::make_tmap_bf16(&maps[3], dop, q_rows, row, 128))
+        return GDPA_ERR_CUDA;
+    BwdParams prm;
+    prm.units = p.d_bwd;
+    prm.seg = p.d_bwd_seg;
+    prm.dQ = dq;
+    prm.dK = dk;
+    prm.dV = dv;
+    prm.H = p.H;
+    prm.alpha = alpha;
+    prm.mask = p.mask;
+    prm.window = p.window;
+    prm.err = p.d_err;
+    prm.times = p.d_times;
+    prm.smid = p.d_smid;
+    prm.timing = p.timing;
+    if (p.timing) p.timed[1] = 1;
+    gdpa_status s = GDPA_OK;
+    if (p.d == 128) {
+        GDPA_DISPATCH_ACT(act, A, s = launch<128, A>(p, maps, prm, st))
+    } else {
+        GDPA_DISPATCH_ACT(act, A, s = launch<64, A>(p, maps, prm, st))
+    }
+    return s;
+}
+
 }  // namespace gdpa

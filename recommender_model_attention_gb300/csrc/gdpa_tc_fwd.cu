@@ -94,11 +94,6 @@ __device__ __forceinline__ FwdTile load_tile(const FwdTile* p) {
     return t;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-    return *reinterpret_cast<uint32_t*>(&v);
-}
-
 template <int D>
 __device__ void fwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                              const FwdParams& prm, uint8_t* smem, uint64_t* bars, int seg0,
@@ -239,13 +234,6 @@ __device__ __forceinline__ void store_zero_rows(const FwdTile& tile, const FwdPa
         *reinterpret_cast<uint4*>(prm.O + (int64_t)(tile.qt0 + row) * rs + tile.h * D + ch * 8) =
             make_uint4(0, 0, 0, 0);
     }
-}
-
-// A wait taken by every thread of a warpgroup; warp-uniform result so that
-// the .sync.aligned tcgen05 loads after it run with whole warps.
-__device__ __forceinline__ bool wg_wait(uint64_t* bar, uint32_t parity, const Abort& ab,
-                                        int32_t where) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, where));
 }
 
 template <int D, int ACT>

@@ -81,7 +81,7 @@ __device__ __forceinline__ void raise_error(const Abort& ab, int32_t code, int32
     *ab.flag = 1;
 }
 
-__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const Abort& ab,
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const Abort& ab,
                                             int32_t where) {
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
@@ -241,6 +241,19 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
            ((b_mn ? 1u : 0u) << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
+// A wait taken by every thread of a warp(group); warp-uniform result so
+// that the .sync.aligned tcgen05 instructions after it run with whole warps.
+__device__ __forceinline__ bool wg_wait(uint64_t* bar, uint32_t parity, const Abort& ab,
+                                        int32_t where) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, where));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
 }
 
 // ---------------------------------------------------------------- host side

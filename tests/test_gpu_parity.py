@@ -16,7 +16,7 @@ from workloads import CONFIGS, get_config, make_inputs
 pytestmark = pytest.mark.gpu
 
 ACTS = ["gelu_erf", "gelu_tanh", "silu", "gelu_taylor6", "identity"]
-BF16_KERNELS = ["simt", "tcgen05"]
+BF16_KERNELS = ["simt", "auto"]
 
 
 @pytest.fixture(scope="module")
