@@ -49,7 +49,8 @@ typedef enum {
     GDPA_ERR_CUDA = 3,          /* a CUDA runtime call failed */
     GDPA_ERR_ALLOC = 4,         /* host or device allocation failed */
     GDPA_ERR_TIMEOUT = 5,       /* a kernel gave up waiting on a barrier */
-    GDPA_ERR_DEVICE = 6         /* a kernel flagged an internal inconsistency */
+    GDPA_ERR_DEVICE = 6,        /* a kernel flagged an internal inconsistency */
+    GDPA_ERR_SCRATCH_LIMIT = 7  /* more tiles than gdpa_fwd_noalloc's static scratch holds */
 } gdpa_status;
 
 /* Element-wise activation applied to x = alpha * q.k (GDPA page, summary
@@ -199,6 +200,42 @@ gdpa_status gdpa_sm_times(gdpa_plan plan, int which, uint64_t* start_end, int32_
 int64_t gdpa_plan_launches(gdpa_plan plan);
 
 void gdpa_plan_destroy(gdpa_plan plan);
+
+/*
+ * Forward pass that allocates nothing (the GDPA page has no counterpart of
+ * this call; it exists for callers of this library).
+ *
+ * Some callers cannot call cudaMalloc: code running inside a custom device
+ * allocator or memory pool (which would recurse into itself), plugins that
+ * are handed one fixed device arena, and processes that must reserve all of
+ * their device memory up front.  They cannot create a gdpa_plan, whose tile
+ * queue and error word are cudaMalloc'd.  This call computes the same
+ * O = act(alpha Q K^T) V as gdpa_fwd with a zigzag plan over the current
+ * device's SMs, on the tensor-core kernel (bf16, d = 64 or 128), without
+ * allocating: the plan is built in static host buffers and its tile queue
+ * is uploaded into a static device array of GDPA_NOALLOC_SCRATCH_BYTES that
+ * every GPU loading the library keeps until the process exits.  The caller
+ * still owns q, k, v, o (device, layout as above) and the stream.
+ *
+ *   - Returns GDPA_ERR_SCRATCH_LIMIT, before any work, when the batch has
+ *     more than GDPA_NOALLOC_MAX_TILES forward tiles (one per sample, head
+ *     and 128-row query tile); UNSUPPORTED for other head dims; INVALID_ARG
+ *     for bad offsets or pointers.
+ *   - The first call on a device sets up that device (looks up the array's
+ *     device address, creates one event); make it before any stream capture.
+ *   - Every call shares the one array and overwrites it: calls whose work
+ *     overlaps on the GPU (e.g. on two streams) race.  Host threads are
+ *     serialised internally.  A call waits for the previous call's upload
+ *     (not its kernel) before reusing the host staging buffers.
+ *   - The kernel's barrier-timeout word lives in the array and is cleared by
+ *     every call; it is not reported (use a gdpa_plan and gdpa_check for
+ *     that).
+ */
+#define GDPA_NOALLOC_MAX_TILES 32768
+#define GDPA_NOALLOC_SCRATCH_BYTES 1056768
+gdpa_status gdpa_fwd_noalloc(const int32_t* q_off_host, const int32_t* kv_off_host, int B, int H,
+                             int d, gdpa_mask mask, int window, const void* q, const void* k,
+                             const void* v, void* o, float alpha, gdpa_act act, void* stream);
 
 const char* gdpa_status_str(gdpa_status status);
 

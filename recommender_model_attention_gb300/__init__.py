@@ -17,8 +17,10 @@ from .gdpa import (  # noqa: F401
     LIB_PATH,
     MASK,
     Plan,
+    STATUS,
     gdpa_bwd,
     gdpa_fwd,
+    gdpa_fwd_noalloc,
     lib,
 )
 

@@ -57,6 +57,7 @@ extern "C" const char* gdpa_status_str(gdpa_status s) {
     case GDPA_ERR_ALLOC: return "allocation failed";
     case GDPA_ERR_TIMEOUT: return "kernel barrier wait timed out";
     case GDPA_ERR_DEVICE: return "kernel reported an internal error";
+    case GDPA_ERR_SCRATCH_LIMIT: return "batch exceeds the static scratch of gdpa_fwd_noalloc";
     }
     return "unknown status";
 }

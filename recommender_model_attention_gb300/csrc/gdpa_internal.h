@@ -77,6 +77,12 @@ gdpa_status launch_simt_bwd(Plan& p, gdpa_dtype dt, const void* q, const void* k
                             cudaStream_t st);
 gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, void* o,
                           float alpha, int act, cudaStream_t st);
+// Forward tensor-core launch on explicit device buffers (tile queue, queue
+// starts, error word; times/smid may be NULL to skip per-CTA timing).
+gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, int32_t* err,
+                              unsigned long long* times, int32_t* smid, int H, int d, int64_t Tq,
+                              int64_t Tkv, int mask, int window, const void* q, const void* k,
+                              const void* v, void* o, float alpha, int act, cudaStream_t st);
 gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, const void* d_o,
                           float* dq, float* dk, float* dv, float alpha, int act, cudaStream_t st);
 

@@ -439,52 +439,64 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 }
 
 template <int D, int ACT>
-gdpa_status launch(Plan& p, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+gdpa_status launch(int S, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                    const FwdParams& prm, cudaStream_t st) {
     using C = FwdCfg<D>;
     auto kern = tc_fwd_kernel<D, ACT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return GDPA_ERR_CUDA;
-    kern<<<p.S, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, prm);
-    p.launches += 1;
+    kern<<<S, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, prm);
     return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
 }  // namespace
 
-gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, void* o,
-                          float alpha, int act, cudaStream_t st) {
-    if (p.d != 64 && p.d != 128) return GDPA_ERR_UNSUPPORTED;
-    if (p.Tq == 0 || p.n_fwd == 0) return GDPA_OK;
+gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, int32_t* err,
+                              unsigned long long* times, int32_t* smid, int H, int d, int64_t Tq,
+                              int64_t Tkv, int mask, int window, const void* q, const void* k,
+                              const void* v, void* o, float alpha, int act, cudaStream_t st) {
+    if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
+    if (Tq == 0) return GDPA_OK;
     CUtensorMap mq, mk, mv;
-    const uint64_t row = (uint64_t)p.H * p.d;
-    const uint64_t kv_rows = p.Tkv > 0 ? (uint64_t)p.Tkv : 1;
-    const void* kp = p.Tkv > 0 ? k : q;
-    const void* vp = p.Tkv > 0 ? v : q;
-    if (!tc::make_tmap_bf16(&mq, q, (uint64_t)p.Tq, row, 128) ||
+    const uint64_t row = (uint64_t)H * d;
+    const uint64_t kv_rows = Tkv > 0 ? (uint64_t)Tkv : 1;
+    const void* kp = Tkv > 0 ? k : q;
+    const void* vp = Tkv > 0 ? v : q;
+    if (!tc::make_tmap_bf16(&mq, q, (uint64_t)Tq, row, 128) ||
         !tc::make_tmap_bf16(&mk, kp, kv_rows, row, 128) ||
         !tc::make_tmap_bf16(&mv, vp, kv_rows, row, 128))
         return GDPA_ERR_CUDA;
     FwdParams prm;
-    prm.tiles = p.d_fwd;
-    prm.seg = p.d_fwd_seg;
+    prm.tiles = tiles;
+    prm.seg = seg;
     prm.O = (__nv_bfloat16*)o;
-    prm.H = p.H;
+    prm.H = H;
     prm.alpha = alpha;
-    prm.mask = p.mask;
-    prm.window = p.window;
-    prm.err = p.d_err;
-    prm.times = p.d_times;
-    prm.smid = p.d_smid;
-    prm.timing = p.timing;
-    if (p.timing) p.timed[0] = 1;
+    prm.mask = mask;
+    prm.window = window;
+    prm.err = err;
+    prm.times = times;
+    prm.smid = smid;
+    prm.timing = times != nullptr && smid != nullptr;
     gdpa_status s = GDPA_OK;
-    if (p.d == 128) {
-        GDPA_DISPATCH_ACT(act, A, s = launch<128, A>(p, mq, mk, mv, prm, st))
+    if (d == 128) {
+        GDPA_DISPATCH_ACT(act, A, s = launch<128, A>(S, mq, mk, mv, prm, st))
     } else {
-        GDPA_DISPATCH_ACT(act, A, s = launch<64, A>(p, mq, mk, mv, prm, st))
+        GDPA_DISPATCH_ACT(act, A, s = launch<64, A>(S, mq, mk, mv, prm, st))
     }
+    return s;
+}
+
+gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, void* o,
+                          float alpha, int act, cudaStream_t st) {
+    if (p.n_fwd == 0) return GDPA_OK;
+    if (p.timing) p.timed[0] = 1;
+    const gdpa_status s = launch_tc_fwd_raw(
+        p.d_fwd, p.d_fwd_seg, p.S, p.d_err, p.timing ? p.d_times : nullptr,
+        p.timing ? p.d_smid : nullptr, p.H, p.d, p.Tq, p.Tkv, p.mask, p.window, q, k, v, o, alpha,
+        act, st);
+    if (s == GDPA_OK) p.launches += 1;
     return s;
 }
 

@@ -21,7 +21,8 @@ SCHED = {"zigzag": 0, "round_robin": 1}
 KERNEL = {"auto": 0, "tcgen05": 1, "simt": 2}
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
           4: "allocation failed", 5: "kernel barrier wait timed out",
-          6: "kernel reported an internal error"}
+          6: "kernel reported an internal error",
+          7: "batch exceeds the static scratch of gdpa_fwd_noalloc"}
 BLOCK_M = 128
 BLOCK_N = 128
 
@@ -62,6 +63,8 @@ def lib():
             "gdpa_bwd": [vp, st, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, st, vp],
             "gdpa_check": [vp, vp],
             "gdpa_sm_times": [vp, st, ctypes.POINTER(ctypes.c_uint64), i32p],
+            "gdpa_fwd_noalloc": [i32p, i32p, st, st, st, st, st, vp, vp, vp, vp, ctypes.c_float,
+                                 st, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -253,3 +256,22 @@ def gdpa_bwd(plan: Plan, q, k, v, do, dq=None, dk=None, dv=None, alpha=None,
                        _ptr(dk), _ptr(dv), ctypes.c_float(alpha), ACT[act], _stream_ptr(stream)),
         "gdpa_bwd")
     return dq, dk, dv
+
+
+def gdpa_fwd_noalloc(q_off, kv_off, q, k, v, o, alpha=None, act: str = "gelu_erf",
+                     mask: str = "none", window: int = 0, stream=None):
+    """Forward into a caller-provided ``o`` with no allocation by the library.
+
+    For callers that cannot allocate device memory themselves (see
+    ``gdpa_fwd_noalloc`` in include/gdpa.h): bf16, d in {64, 128}, at most
+    GDPA_NOALLOC_MAX_TILES (32768) forward tiles.
+    """
+    qo, qp = _i32(q_off)
+    ko, kp = _i32(kv_off)
+    B = len(qo) - 1
+    H, d = int(q.shape[1]), int(q.shape[2])
+    alpha = d ** -0.5 if alpha is None else float(alpha)
+    _ok(lib().gdpa_fwd_noalloc(qp, kp, B, H, d, MASK[mask], int(window), _ptr(q), _ptr(k), _ptr(v),
+                               _ptr(o), ctypes.c_float(alpha), ACT[act], _stream_ptr(stream)),
+        "gdpa_fwd_noalloc")
+    return o
