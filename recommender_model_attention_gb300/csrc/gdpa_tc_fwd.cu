@@ -8,18 +8,21 @@
 // to SMs in zigzag order.  This kernel is the GB300 rendering of that:
 //
 //  * grid = one CTA per planned SM queue; CTA s walks tiles seg[s]..seg[s+1].
-//  * warp 0 (one lane): TMA producer.  Q tile [128 x d] per tile, K and V
-//    blocks [128 x d] per (tile, key block) item, through 2-stage rings.
+//  * warp 0 (one lane): TMA producer.  Q tile [128 x d] per tile through a
+//    3-stage ring, K and V blocks [128 x d] per (tile, key block) item
+//    through 2-stage rings.
 //  * warp 1 (one lane): tcgen05.mma issuer.  Per item: S = Q K^T into TMEM;
-//    the P V product of the previous item is issued after the next S, so the
-//    tensor core computes item i+1's scores while item i's activation runs
-//    (software pipelining across tile boundaries on one flattened loop).
+//    the P V product of the previous item is issued after the next item's S
+//    when the two belong to different warpgroups, so the tensor core
+//    computes item i+1's scores while item i's activation runs (software
+//    pipelining across tile boundaries on one flattened loop).
 //  * warps 2-9: two activation/epilogue warpgroups taking alternate tiles,
 //    each with its own TMEM S (128 columns) and O (128 columns) accumulators.
 //    They read S with tcgen05.ld, apply alpha, the activation and the jagged /
-//    window mask (masked pairs become exactly 0 after the activation), write
-//    P as bf16 into shared memory in the 128-byte-swizzled K-major layout,
-//    and after the last key block read O from TMEM, stage it in the tile's
+//    window mask (masked pairs become exactly 0 after the activation), and
+//    write P as packed bf16 back into the S columns they have read
+//    (tcgen05.st); P V then takes P straight from TMEM (A operand in TMEM).
+//    After the last key block they read O from TMEM, stage it in the tile's
 //    (now consumed) Q buffer and store the valid rows with coalesced 16-byte
 //    stores.  Zero tiles (no valid key) are written as zeros directly.
 //  * O accumulates P V over key blocks with no rescaling.
@@ -44,26 +47,22 @@ template <int D>
 struct FwdCfg {
     static constexpr int kHalves = D / 64;
     static constexpr int kTileBytes = 128 * D * 2;
-    static constexpr int kNQ = 2;
+    static constexpr int kNQ = 3;
     static constexpr int kNKV = 2;
-    static constexpr int kPBytes = 128 * 128 * 2;
     static constexpr int kOffQ = 0;
     static constexpr int kOffK = kOffQ + kNQ * kTileBytes;
     static constexpr int kOffV = kOffK + kNKV * kTileBytes;
-    static constexpr int kOffP = kOffV + kNKV * kTileBytes;
-    static constexpr int kOffBar = kOffP + kPBytes;
-    // q_full, q_empty, k_full, v_full, kv_empty, p_full, p_free,
-    // s_full, s_free, o_full, o_free, stage (per warpgroup), mma_done
+    static constexpr int kOffBar = kOffV + kNKV * kTileBytes;
+    // q_full, q_empty, k_full, v_full, kv_empty,
+    // s_full, p_full, o_full, o_free, stage (per warpgroup), mma_done
     static constexpr int kBarQFull = 0;
     static constexpr int kBarQEmpty = kBarQFull + kNQ;
     static constexpr int kBarKFull = kBarQEmpty + kNQ;
     static constexpr int kBarVFull = kBarKFull + kNKV;
     static constexpr int kBarKVEmpty = kBarVFull + kNKV;
-    static constexpr int kBarPFull = kBarKVEmpty + kNKV;
-    static constexpr int kBarPFree = kBarPFull + 1;
-    static constexpr int kBarSFull = kBarPFree + 1;
-    static constexpr int kBarSFree = kBarSFull + kNumWG;
-    static constexpr int kBarOFull = kBarSFree + kNumWG;
+    static constexpr int kBarSFull = kBarKVEmpty + kNKV;
+    static constexpr int kBarPFull = kBarSFull + kNumWG;
+    static constexpr int kBarOFull = kBarPFull + kNumWG;
     static constexpr int kBarOFree = kBarOFull + kNumWG;
     static constexpr int kBarStage = kBarOFree + kNumWG;
     static constexpr int kBarMmaDone = kBarStage + kNumWG;
@@ -149,29 +148,31 @@ unwind:
 }
 
 struct PendingPV {
-    uint32_t item, wg, ks, kph, nsteps;
+    uint32_t wg, ks, kph, nsteps;
     bool first, last;
 };
 
+// O[wg] (+)= P V: P from the warpgroup's S columns in TMEM, V (MN-major) from
+// shared memory.
 template <int D>
 __device__ __forceinline__ bool issue_pv(const PendingPV& pd, uint8_t* smem, uint64_t* bars,
-                                         uint32_t tmem, uint32_t* o_use, const Abort& ab) {
+                                         uint32_t tmem, uint32_t* p_use, uint32_t* o_use,
+                                         const Abort& ab) {
     using C = FwdCfg<D>;
     if (!mbar_wait(&bars[C::kBarVFull + pd.ks], pd.kph, ab, 10)) return false;
-    if (!mbar_wait(&bars[C::kBarPFull], pd.item & 1, ab, 11)) return false;
+    if (!mbar_wait(&bars[C::kBarPFull + pd.wg], p_use[pd.wg] & 1, ab, 11)) return false;
+    p_use[pd.wg]++;
     if (pd.first && !mbar_wait(&bars[C::kBarOFree + pd.wg], (o_use[pd.wg] & 1) ^ 1, ab, 12))
         return false;
     tc_fence_after();
     constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
+    const uint32_t p_tmem = tmem + pd.wg * 256;
     const uint32_t d_o = tmem + pd.wg * 256 + 128;
-    const uint32_t pbase = smem_u32(smem + C::kOffP);
     const uint32_t vbase = smem_u32(smem + C::kOffV + pd.ks * C::kTileBytes);
     for (uint32_t k = 0; k < pd.nsteps; ++k) {
-        const uint64_t a_desc = smem_desc_sw128(pbase + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024);
         const uint64_t b_desc = smem_desc_sw128(vbase + k * 2048, kHalfBytes, 1024);
-        mma_ss(d_o, a_desc, b_desc, idesc, (pd.first && k == 0) ? 0u : 1u);
+        mma_ts(d_o, p_tmem + k * 8, b_desc, idesc, (pd.first && k == 0) ? 0u : 1u);
     }
-    mma_commit(&bars[C::kBarPFree]);
     mma_commit(&bars[C::kBarKVEmpty + pd.ks]);
     if (pd.last) {
         mma_commit(&bars[C::kBarOFull + pd.wg]);
@@ -184,7 +185,7 @@ template <int D>
 __device__ void fwd_mma(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
                         int seg0, int seg1, const Abort& ab) {
     using C = FwdCfg<D>;
-    uint32_t s_use[kNumWG] = {}, o_use[kNumWG] = {};
+    uint32_t p_use[kNumWG] = {}, o_use[kNumWG] = {};
     uint32_t a = 0, i = 0;
     PendingPV pend{};
     bool have_pend = false;
@@ -198,8 +199,14 @@ __device__ void fwd_mma(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
             const int nvalid = min(kBN, tile.lkv - kb * kBN);
             const uint32_t n32 = (uint32_t)((nvalid + 31) & ~31);
+            // S[wg] holds the previous item's P when that item is this
+            // warpgroup's too: its P V goes first (the tensor pipe runs its
+            // MMAs in issue order, so the S overwrite follows the P read)
+            if (have_pend && pend.wg == wg) {
+                if (!issue_pv<D>(pend, smem, bars, tmem, p_use, o_use, ab)) goto drain;
+                have_pend = false;
+            }
             if (!mbar_wait(&bars[C::kBarKFull + ks], kph, ab, 4)) goto drain;
-            if (!mbar_wait(&bars[C::kBarSFree + wg], (s_use[wg] & 1) ^ 1, ab, 5)) goto drain;
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, n32, false, false);
             const uint32_t qbase = smem_u32(smem + C::kOffQ + qs * C::kTileBytes);
@@ -211,14 +218,13 @@ __device__ void fwd_mma(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uin
                        smem_desc_sw128(kbase + off, 16, 1024), idesc, k > 0 ? 1u : 0u);
             }
             mma_commit(&bars[C::kBarSFull + wg]);
-            s_use[wg]++;
-            if (have_pend && !issue_pv<D>(pend, smem, bars, tmem, o_use, ab)) goto drain;
-            pend = PendingPV{i, wg, ks, kph, n32 / 16, kb == tile.kb0, kb == tile.kb1 - 1};
+            if (have_pend && !issue_pv<D>(pend, smem, bars, tmem, p_use, o_use, ab)) goto drain;
+            pend = PendingPV{wg, ks, kph, n32 / 16, kb == tile.kb0, kb == tile.kb1 - 1};
             have_pend = true;
         }
         ++a;
     }
-    if (have_pend) issue_pv<D>(pend, smem, bars, tmem, o_use, ab);
+    if (have_pend) issue_pv<D>(pend, smem, bars, tmem, p_use, o_use, ab);
 drain:
     // all MMAs issued by this thread complete before TMEM is released
     mma_commit(&bars[C::kBarMmaDone]);
@@ -248,7 +254,6 @@ __device__ void fwd_compute(const FwdParams& prm, uint8_t* smem, uint64_t* bars,
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const uint32_t s_tmem = tmem + wg * 256 + lane_addr;
     const uint32_t o_tmem = tmem + wg * 256 + 128 + lane_addr;
-    uint8_t* pbuf = smem + C::kOffP;
     uint32_t a = 0, i = 0, s_use = 0, o_use = 0;
     for (int t = seg0; t < seg1; ++t) {
         const FwdTile tile = load_tile(prm.tiles + t);
@@ -270,15 +275,15 @@ __device__ void fwd_compute(const FwdParams& prm, uint8_t* smem, uint64_t* bars,
             if (!wg_wait(&bars[C::kBarSFull + wg], s_use & 1, ab, 6)) return;
             s_use++;
             tc_fence_after();
-            // S -> registers one 32-column chunk at a time, activation and
-            // mask applied straight away (keeps register pressure low)
-            uint32_t pk[4][16];
+            // S -> registers one 32-column chunk at a time; alpha, activation
+            // and mask; P (bf16 pairs) back into the chunk's first 16 columns
+            // (already read: P column 16c+k holds S columns 32c+2k, +1)
             if (warp_rows) {
                 const int jbase = kb * kBN;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     if (c < nch) {
-                        uint32_t sv[32];
+                        uint32_t sv[32], pk[16];
                         tmem_ld32(s_tmem + c * 32, sv);
                         tmem_ld_wait();
 #pragma unroll
@@ -294,31 +299,15 @@ __device__ void fwd_compute(const FwdParams& prm, uint8_t* smem, uint64_t* bars,
                                 const float x = prm.alpha * __uint_as_float(sv[e + u]);
                                 pv[u] = valid ? act_f<ACT, true>(x) : 0.0f;
                             }
-                            pk[c][e >> 1] = pack_bf16x2(pv[0], pv[1]);
+                            pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
                         }
+                        tmem_st16(s_tmem + c * 16, pk);
                     }
                 }
+                tmem_st_wait();
             }
             tc_fence_before();
-            mbar_arrive(&bars[C::kBarSFree + wg]);
-            if (!wg_wait(&bars[C::kBarPFree], (i & 1) ^ 1, ab, 7)) return;
-            if (warp_rows) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (c < nch) {
-                        uint8_t* rowp = pbuf + (c >> 1) * kHalfBytes + r * 128;
-#pragma unroll
-                        for (int u = 0; u < 4; ++u) {
-                            const int chunk = ((c & 1) * 4 + u) ^ (r & 7);
-                            *reinterpret_cast<uint4*>(rowp + chunk * 16) =
-                                make_uint4(pk[c][4 * u], pk[c][4 * u + 1], pk[c][4 * u + 2],
-                                           pk[c][4 * u + 3]);
-                        }
-                    }
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(&bars[C::kBarPFull]);
+            mbar_arrive(&bars[C::kBarPFull + wg]);
         }
         // epilogue: O (TMEM) -> bf16 -> staging (this tile's Q buffer) -> global
         if (!wg_wait(&bars[C::kBarOFull + wg], o_use & 1, ab, 8)) return;
@@ -390,11 +379,9 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_init(&bars[C::kBarVFull + s], 1);
             mbar_init(&bars[C::kBarKVEmpty + s], 1);
         }
-        mbar_init(&bars[C::kBarPFull], 128);
-        mbar_init(&bars[C::kBarPFree], 1);
         for (int w = 0; w < kNumWG; ++w) {
             mbar_init(&bars[C::kBarSFull + w], 1);
-            mbar_init(&bars[C::kBarSFree + w], 128);
+            mbar_init(&bars[C::kBarPFull + w], 128);
             mbar_init(&bars[C::kBarOFull + w], 1);
             mbar_init(&bars[C::kBarOFree + w], 128);
             mbar_init(&bars[C::kBarStage + w], 128);
