@@ -195,6 +195,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="training_cross_fwd_bwd")
+    ap.add_argument("--samples", type=int, default=0,
+                    help="use only the first N sequences of the workload (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
@@ -216,7 +218,12 @@ def main():
     gd.lib()
     pk, pk_kind = peaks()
 
-    x = make_inputs(w, device="cuda", seed=1000 + w.index + 7919 * rank)
+    lengths = None
+    if args.samples:
+        from workloads import draw_lengths
+        lq, lkv = draw_lengths(w)
+        lengths = (lq[:args.samples], lkv[:args.samples])
+    x = make_inputs(w, device="cuda", seed=1000 + w.index + 7919 * rank, lengths=lengths)
     stream = torch.cuda.current_stream()
     plan = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window)
     f32 = torch.float32
@@ -364,7 +371,8 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded lengths and RMSNorm'd N(0,1) inputs, random dO)",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "act": w.act,
+            "config": {"workload": w.name, "B": len(x["q_off"]) - 1, "H": w.H, "d": w.d,
+                       "act": w.act,
                        "Tq": Tq, "Tkv": Tkv, "useful_pairs": pairs,
                        "l2": "inputs larger than L2 (%.1f GB resident)" % (input_bytes / 1e9),
                        "parallelism": "samples sharded by rank, no exchange" if world > 1

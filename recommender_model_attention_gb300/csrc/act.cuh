@@ -8,10 +8,14 @@
 //
 // Two flavours:
 //  * Precise (CUDA-core float32 path): CUDA's erff / tanhf / expf.
-//  * Fast (bf16 tensor-core path, whose P is rounded to bf16 anyway):
-//    GELU-tanh through the tanh.approx.f32 instruction, SiLU through
-//    __expf and a fast reciprocal; GELU-erf still calls erff; the Taylor
-//    polynomial is the same FMA chain in both.
+//  * Fast (bf16 tensor-core path, whose P is rounded to bf16 anyway), all
+//    branch-free with at most one or two special-function ops per element:
+//    GELU-tanh through the tanh.approx.f32 instruction; SiLU as
+//    x/2 (1 + tanh(x/2)); GELU-erf with Phi from the rational approximation
+//    of Abramowitz & Stegun, Handbook of Mathematical Functions, eq. 7.1.28
+//    (erf z = 1 - (1 + a1 z + ... + a6 z^6)^-16, |error| <= 3e-7), one
+//    reciprocal per element; the normal density for act' through ex2.approx.
+//    The Taylor polynomial is the same FMA chain in both flavours.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -27,6 +31,45 @@ constexpr float kTanhCubic = 0.044715f;
 constexpr float kT6c2 = kRsqrt2Pi;
 constexpr float kT6c4 = -kRsqrt2Pi / 6.0f;
 constexpr float kT6c6 = kRsqrt2Pi / 40.0f;
+
+// Abramowitz & Stegun 7.1.28 coefficients
+constexpr float kAS1 = 0.0705230784f;
+constexpr float kAS2 = 0.0422820123f;
+constexpr float kAS3 = 0.0092705272f;
+constexpr float kAS4 = 0.0001520143f;
+constexpr float kAS5 = 0.0002765672f;
+constexpr float kAS6 = 0.0000430638f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Phi(x) = (1 + erf(x / sqrt 2)) / 2 with erf from A&S 7.1.28 (z >= 0; the
+// polynomial's 16th power overflows to +inf for large z, giving erf = 1).
+__device__ __forceinline__ float normal_cdf_fast(float x) {
+    const float z = fabsf(x) * kRsqrt2;
+    float p = fmaf(kAS6, z, kAS5);
+    p = fmaf(p, z, kAS4);
+    p = fmaf(p, z, kAS3);
+    p = fmaf(p, z, kAS2);
+    p = fmaf(p, z, kAS1);
+    p = fmaf(p, z, 1.0f);
+    p = p * p;
+    p = p * p;
+    p = p * p;
+    p = p * p;                          // (1 + ...)^16
+    const float half_tail = 0.5f * rcp_approx(p);   // (1 - erf z) / 2
+    return x >= 0.0f ? 1.0f - half_tail : half_tail;
+}
 
 __device__ __forceinline__ float tanh_approx(float x) {
     float y;
@@ -54,14 +97,19 @@ __device__ __forceinline__ float dtaylor6(float x) {
 template <int ACT, bool FAST>
 __device__ __forceinline__ float act_f(float x) {
     if constexpr (ACT == kGeluErf) {
-        return 0.5f * x * (1.0f + erff(x * kRsqrt2));
+        if constexpr (FAST) {
+            return x * normal_cdf_fast(x);
+        } else {
+            return 0.5f * x * (1.0f + erff(x * kRsqrt2));
+        }
     } else if constexpr (ACT == kGeluTanh) {
         const float u = kSqrt2OverPi * fmaf(kTanhCubic * x, x * x, x);
         const float t = FAST ? tanh_approx(u) : tanhf(u);
         return 0.5f * x * (1.0f + t);
     } else if constexpr (ACT == kSilu) {
         if constexpr (FAST) {
-            return __fdividef(x, 1.0f + __expf(-x));
+            const float hx = 0.5f * x;
+            return fmaf(hx, tanh_approx(hx), hx);
         } else {
             return x / (1.0f + expf(-x));
         }
@@ -75,8 +123,9 @@ __device__ __forceinline__ float act_f(float x) {
 template <int ACT, bool FAST>
 __device__ __forceinline__ float dact_f(float x) {
     if constexpr (ACT == kGeluErf) {
-        const float cdf = 0.5f * (1.0f + erff(x * kRsqrt2));
-        const float pdf = kRsqrt2Pi * (FAST ? __expf(-0.5f * x * x) : expf(-0.5f * x * x));
+        const float cdf = FAST ? normal_cdf_fast(x) : 0.5f * (1.0f + erff(x * kRsqrt2));
+        const float pdf = kRsqrt2Pi * (FAST ? ex2_approx(-0.5f * kLog2e * x * x)
+                                           : expf(-0.5f * x * x));
         return fmaf(x, pdf, cdf);
     } else if constexpr (ACT == kGeluTanh) {
         const float u = kSqrt2OverPi * fmaf(kTanhCubic * x, x * x, x);
@@ -84,7 +133,7 @@ __device__ __forceinline__ float dact_f(float x) {
         const float du = kSqrt2OverPi * fmaf(3.0f * kTanhCubic, x * x, 1.0f);
         return 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * du;
     } else if constexpr (ACT == kSilu) {
-        const float s = FAST ? __fdividef(1.0f, 1.0f + __expf(-x)) : 1.0f / (1.0f + expf(-x));
+        const float s = FAST ? fmaf(0.5f, tanh_approx(0.5f * x), 0.5f) : 1.0f / (1.0f + expf(-x));
         return s * fmaf(x, 1.0f - s, 1.0f);
     } else if constexpr (ACT == kTaylor6) {
         return dtaylor6(x);
@@ -97,8 +146,9 @@ __device__ __forceinline__ float dact_f(float x) {
 template <int ACT, bool FAST>
 __device__ __forceinline__ void act_dact_f(float x, float& a, float& da) {
     if constexpr (ACT == kGeluErf) {
-        const float cdf = 0.5f * (1.0f + erff(x * kRsqrt2));
-        const float pdf = kRsqrt2Pi * (FAST ? __expf(-0.5f * x * x) : expf(-0.5f * x * x));
+        const float cdf = FAST ? normal_cdf_fast(x) : 0.5f * (1.0f + erff(x * kRsqrt2));
+        const float pdf = kRsqrt2Pi * (FAST ? ex2_approx(-0.5f * kLog2e * x * x)
+                                           : expf(-0.5f * x * x));
         a = x * cdf;
         da = fmaf(x, pdf, cdf);
     } else if constexpr (ACT == kGeluTanh) {
@@ -108,7 +158,7 @@ __device__ __forceinline__ void act_dact_f(float x, float& a, float& da) {
         a = 0.5f * x * (1.0f + t);
         da = 0.5f * (1.0f + t) + 0.5f * x * (1.0f - t * t) * du;
     } else if constexpr (ACT == kSilu) {
-        const float s = FAST ? __fdividef(1.0f, 1.0f + __expf(-x)) : 1.0f / (1.0f + expf(-x));
+        const float s = FAST ? fmaf(0.5f, tanh_approx(0.5f * x), 0.5f) : 1.0f / (1.0f + expf(-x));
         a = x * s;
         da = s * fmaf(x, 1.0f - s, 1.0f);
     } else if constexpr (ACT == kTaylor6) {

@@ -14,9 +14,12 @@
 // a cleared dQ.
 //
 // Roles: warp 0 TMA producer (K, V once per unit; Q and dO per query tile
-// through 2-stage rings); warp 1 tcgen05.mma issuer; warps 2-5 one
-// warpgroup that turns S and dP (TMEM) into P and dS (bf16, shared memory)
-// and drains dQ, dK, dV from TMEM.  Per query tile:
+// through 2-stage rings); warp 1 tcgen05.mma issuer; warps 2-9 two
+// warpgroups that turn S and dP (TMEM) into P and dS (bf16, shared memory),
+// warpgroup j taking the 32-column key chunks c = j, j + 2, and drain dQ (j:
+// d columns [64j, 64j + 64)), dV (j = 0) and dK (j = 1) from TMEM through
+// its own half of the shared buffer.  The next query tile's S = Q K^T is
+// issued as soon as both warpgroups have read S.  Per query tile:
 //     S  = Q K^T   -> TMEM [0, 128)      dP = dO V^T -> TMEM [128, 256)
 //     P, dS        -> one 32 KB shared buffer, P first, then dS
 //     dV += P^T dO -> TMEM [256, 384)    dK += dS^T Q -> TMEM [384, 512)
@@ -35,7 +38,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreads = 64 + 128;
+constexpr int kThreads = 64 + 256;
 constexpr int kHalfBytes = 128 * 128;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 384;
@@ -53,7 +56,7 @@ struct BwdCfg {
     enum {
         kKVFull = 0, kKVEmpty, kQFull, kQFull1, kQEmpty, kQEmpty1, kDOFull, kDOFull1, kDOEmpty,
         kDOEmpty1, kSDFull, kSFree, kDQFree, kPFull, kPVDone, kDSFull, kDQFull, kAccFull,
-        kAccFree, kStage, kMmaDone, kNumBars
+        kAccFree, kStage, kStage1, kPSFree, kMmaDone, kNumBars
     };
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
 };
@@ -151,28 +154,28 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
         if (u.m1 <= u.m0) continue;
         const uint32_t nkv32 = (uint32_t)((u.nkv + 31) & ~31);
         const uint32_t idesc_s = idesc_bf16(128, nkv32, false, false);
-        if (!mbar_wait(&bars[C::kKVFull], nu & 1, ab, 31)) goto drain;
-        for (int m = u.m0; m < u.m1; ++m, ++i) {
-            const uint32_t s = i & 1, ph = (i >> 1) & 1;
-            const bool first = m == u.m0, last = m == u.m1 - 1;
-            const int nq = min(kBM, u.lq - m * kBM);
-            const uint32_t nq32 = (uint32_t)((nq + 31) & ~31);
-            const uint32_t qb = smem_u32(smem + C::kOffQ + s * C::kTileBytes);
-            const uint32_t dob = smem_u32(smem + C::kOffDO + s * C::kTileBytes);
-            // S = Q K^T
-            if (!mbar_wait(&bars[C::kQFull + s], ph, ab, 32)) goto drain;
-            if (!mbar_wait(&bars[C::kSFree], (i & 1) ^ 1, ab, 33)) goto drain;
+        // S = Q K^T of item j (after the warpgroups have read item j-1's S)
+        auto issue_s = [&](uint32_t j) -> bool {
+            const uint32_t st = j & 1, ph = (j >> 1) & 1;
+            if (!mbar_wait(&bars[C::kQFull + st], ph, ab, 32)) return false;
+            if (!mbar_wait(&bars[C::kSFree], (j & 1) ^ 1, ab, 33)) return false;
             tc_fence_after();
+            const uint32_t qb = smem_u32(smem + C::kOffQ + st * C::kTileBytes);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
                 const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
                 mma_ss(tmem + kColS, smem_desc_sw128(qb + off, 16, 1024),
                        smem_desc_sw128(kbase + off, 16, 1024), idesc_s, k > 0);
             }
-            // dP = dO V^T (into the columns dQ of the previous tile used)
-            if (!mbar_wait(&bars[C::kDOFull + s], ph, ab, 34)) goto drain;
-            if (!mbar_wait(&bars[C::kDQFree], (i & 1) ^ 1, ab, 35)) goto drain;
+            return true;
+        };
+        // dP = dO V^T of item j (into the columns item j-1's dQ used)
+        auto issue_dp = [&](uint32_t j) -> bool {
+            const uint32_t st = j & 1, ph = (j >> 1) & 1;
+            if (!mbar_wait(&bars[C::kDOFull + st], ph, ab, 34)) return false;
+            if (!mbar_wait(&bars[C::kDQFree], (j & 1) ^ 1, ab, 35)) return false;
             tc_fence_after();
+            const uint32_t dob = smem_u32(smem + C::kOffDO + st * C::kTileBytes);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
                 const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
@@ -180,6 +183,17 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
                        smem_desc_sw128(vbase + off, 16, 1024), idesc_s, k > 0);
             }
             mma_commit(&bars[C::kSDFull]);
+            return true;
+        };
+        if (!mbar_wait(&bars[C::kKVFull], nu & 1, ab, 31)) goto drain;
+        if (!issue_s(i) || !issue_dp(i)) goto drain;
+        for (int m = u.m0; m < u.m1; ++m, ++i) {
+            const uint32_t s = i & 1;
+            const bool first = m == u.m0, last = m == u.m1 - 1;
+            const int nq = min(kBM, u.lq - m * kBM);
+            const uint32_t nq32 = (uint32_t)((nq + 31) & ~31);
+            const uint32_t qb = smem_u32(smem + C::kOffQ + s * C::kTileBytes);
+            const uint32_t dob = smem_u32(smem + C::kOffDO + s * C::kTileBytes);
             // dV += P^T dO
             if (!mbar_wait(&bars[C::kPFull], i & 1, ab, 36)) goto drain;
             if (first && !mbar_wait(&bars[C::kAccFree], (nu & 1) ^ 1, ab, 37)) goto drain;
@@ -190,6 +204,8 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
                        (first && k == 0) ? 0u : 1u);
             mma_commit(&bars[C::kDOEmpty + s]);
             mma_commit(&bars[C::kPVDone]);
+            // the next tile's scores while this tile's dS is being written
+            if (!last && !issue_s(i + 1)) goto drain;
             // dK += dS^T Q, dQ = dS K
             if (!mbar_wait(&bars[C::kDSFull], i & 1, ab, 38)) goto drain;
             tc_fence_after();
@@ -206,6 +222,8 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             if (last) {
                 mma_commit(&bars[C::kAccFull]);
                 mma_commit(&bars[C::kKVEmpty]);
+            } else if (!issue_dp(i + 1)) {
+                goto drain;
             }
         }
         ++nu;
@@ -215,58 +233,47 @@ drain:
     mbar_wait_teardown(&bars[C::kMmaDone], 0);
 }
 
-// Store a [128 x 64] fp32 block staged in shared memory (row r at r * 256
-// bytes, 16-byte chunk c at (c ^ (r & 7))) to rows [0, nrows) of `dst`
-// (row stride `rs` floats); atomically added when `atomic`.
-__device__ __forceinline__ void store_staged(const uint8_t* stage, float* dst, int64_t rs,
-                                             int nrows, bool atomic, int tid) {
-    for (int idx = tid; idx < nrows * 16; idx += 128) {
-        const int row = idx >> 4, ch = idx & 15;
-        const float4 v =
-            *reinterpret_cast<const float4*>(stage + row * 256 + ((ch ^ (row & 7)) << 4));
-        float4* p = reinterpret_cast<float4*>(dst + (int64_t)row * rs + ch * 4);
-        if (atomic)
-            atomicAdd(p, v);
-        else
-            *p = v;
-    }
-}
-
-// Drain columns [col, col + D) of this warpgroup's TMEM rows to global rows
-// via the staging buffer, 64 columns at a time, scaled by `scale`.
-template <int D>
-__device__ __forceinline__ bool drain_rows(uint32_t tmem_row, uint32_t col, uint8_t* stage,
+// Drain TMEM columns [col, col + ncols) (multiple of 32) of this
+// warpgroup's lanes to rows [0, nrows) of `dst` (row stride `rs` floats, the
+// block's first column at dst), 32 columns per pass through `stage` (this
+// warpgroup's 16 KB: row r at r * 128 bytes, 16-byte chunk c at c ^ (r & 7)),
+// scaled by `scale`, atomically added when `atomic`.  `release` (if any) is
+// arrived once the last TMEM read is done.
+__device__ __forceinline__ bool drain_cols(uint32_t trow, uint32_t col, int ncols, uint8_t* stage,
                                            float* dst, int64_t rs, int nrows, bool atomic,
                                            float scale, bool warp_rows, int r, int tid,
                                            uint64_t* stage_bar, uint32_t& st_use, const Abort& ab,
-                                           uint64_t* release_bar) {
-#pragma unroll
-    for (int hf = 0; hf < D / 64; ++hf) {
+                                           uint64_t* release) {
+    for (int pass = 0; pass < ncols / 32; ++pass) {
         if (warp_rows) {
+            uint32_t v[32];
+            tmem_ld32(trow + col + pass * 32, v);
+            tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tmem_row + col + hf * 64 + c * 32, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int chunk = (c * 8 + u) ^ (r & 7);
-                    *reinterpret_cast<float4*>(stage + r * 256 + chunk * 16) =
-                        make_float4(scale * __uint_as_float(v[4 * u]),
-                                    scale * __uint_as_float(v[4 * u + 1]),
-                                    scale * __uint_as_float(v[4 * u + 2]),
-                                    scale * __uint_as_float(v[4 * u + 3]));
-                }
-            }
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<float4*>(stage + r * 128 + ((c ^ (r & 7)) << 4)) =
+                    make_float4(scale * __uint_as_float(v[4 * c]), scale * __uint_as_float(v[4 * c + 1]),
+                                scale * __uint_as_float(v[4 * c + 2]),
+                                scale * __uint_as_float(v[4 * c + 3]));
         }
-        if (hf == D / 64 - 1 && release_bar) {
+        if (pass == ncols / 32 - 1 && release) {
             tc_fence_before();
-            mbar_arrive(release_bar);
+            mbar_arrive(release);
         }
         mbar_arrive(stage_bar);
         if (!wg_wait(stage_bar, st_use & 1, ab, 41)) return false;
         ++st_use;
-        store_staged(stage, dst + hf * 64, rs, nrows, atomic, tid);
+        float* d = dst + pass * 32;
+        for (int idx = tid; idx < nrows * 8; idx += 128) {
+            const int row = idx >> 3, ch = idx & 7;
+            const float4 w =
+                *reinterpret_cast<const float4*>(stage + row * 128 + ((ch ^ (row & 7)) << 4));
+            float4* p = reinterpret_cast<float4*>(d + (int64_t)row * rs + ch * 4);
+            if (atomic)
+                atomicAdd(p, w);
+            else
+                *p = w;
+        }
         mbar_arrive(stage_bar);
         if (!wg_wait(stage_bar, st_use & 1, ab, 42)) return false;
         ++st_use;
@@ -283,127 +290,146 @@ __device__ __forceinline__ void zero_rows(float* dst, int64_t rs, int nrows, int
     }
 }
 
+// one 32-column chunk of P or dS into the [query x key] SW128 buffer
+__device__ __forceinline__ void store_chunk(uint8_t* ps, int c, int r, const uint32_t (&v)[16]) {
+    uint8_t* rowp = ps + (c >> 1) * kHalfBytes + r * 128;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const int chunk = ((c & 1) * 4 + w) ^ (r & 7);
+        *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+            make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+    }
+}
+
+// 16 columns (half hh of chunk c) of P into the [query x key] SW128 buffer
+__device__ __forceinline__ void store_half_chunk(uint8_t* ps, int c, int hh, int r,
+                                                 const uint32_t (&v)[8]) {
+    uint8_t* rowp = ps + (c >> 1) * kHalfBytes + r * 128;
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        const int chunk = ((c & 1) * 4 + hh * 2 + w) ^ (r & 7);
+        *reinterpret_cast<uint4*>(rowp + chunk * 16) =
+            make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
+    }
+}
+
 template <int D, int ACT>
 __device__ void bwd_compute(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
                             int seg0, int seg1, const Abort& ab) {
     using C = BwdCfg<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wg = (warp - 2) >> 2;      // key chunks c = wg, wg + 2
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;   // TMEM lane = row of this thread
-    const int tid = (int)threadIdx.x - 64;
+    const int tid = (int)threadIdx.x - 64 - 128 * wg;
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     uint8_t* ps = smem + C::kOffPS;
+    uint8_t* stage = ps + wg * kHalfBytes;
+    uint64_t* stage_bar = &bars[C::kStage + wg];
     const int64_t rs = (int64_t)prm.H * D;
-    uint32_t nu = 0, i = 0, st_use = 0;
+    uint32_t nu = 0, i = 0, st_use = 0, n_drain = 0;
     for (int t = seg0; t < seg1; ++t) {
         const BwdUnit u = load_unit(prm.units + t);
         const int h = u.hf & 0xffff;
         const bool atomic_dq = (u.hf >> 16) & kUnitAtomicDQ;
         if (u.m1 <= u.m0) {
-            zero_rows<D>(prm.dK + (int64_t)u.kvt0 * rs + h * D, rs, u.nkv, tid);
-            zero_rows<D>(prm.dV + (int64_t)u.kvt0 * rs + h * D, rs, u.nkv, tid);
+            float* base = (wg == 0 ? prm.dK : prm.dV) + (int64_t)u.kvt0 * rs + h * D;
+            zero_rows<D>(base, rs, u.nkv, tid);
             continue;
         }
-        const int nkv32 = (u.nkv + 31) & ~31;
-        const int nch = nkv32 >> 5;
+        const int nch = ((u.nkv + 31) & ~31) >> 5;
         for (int m = u.m0; m < u.m1; ++m, ++i) {
             const int nq = min(kBM, u.lq - m * kBM);
             const bool warp_rows = quarter * 32 < nq;
             const int ipos = m * kBM + r;        // query position in the sample
             const bool row_ok = r < nq;
             if (!wg_wait(&bars[C::kSDFull], i & 1, ab, 43)) return;
+            // the shared buffer must be clear of the previous tile's dQ (or
+            // unit's dK, dV) drain by both warpgroups before P goes in
+            if (n_drain > 0 && !wg_wait(&bars[C::kPSFree], (n_drain - 1) & 1, ab, 47)) return;
             tc_fence_after();
-            uint32_t pp[4][16], pd[4][16];
+            uint32_t pd[2][16];
             if (warp_rows) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = wg + 2 * cc;
                     if (c < nch) {
-                        uint32_t sv[32], dv[32];
-                        tmem_ld32(trow + kColS + c * 32, sv);
-                        tmem_ld32(trow + kColDP + c * 32, dv);
-                        tmem_ld_wait();
+                        // two 16-column halves of the chunk keep register use low
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            float p2[2], d2[2];
+                        for (int hh = 0; hh < 2; ++hh) {
+                            uint32_t sv[16], dv[16], pp[8];
+                            tmem_ld16(trow + kColS + c * 32 + hh * 16, sv);
+                            tmem_ld16(trow + kColDP + c * 32 + hh * 16, dv);
+                            tmem_ld_wait();
 #pragma unroll
-                            for (int w = 0; w < 2; ++w) {
-                                const int col = c * 32 + e + w;
-                                const int jpos = u.c0 + col;
-                                bool valid = row_ok && col < u.nkv;
-                                if (prm.mask == GDPA_MASK_CAUSAL_WINDOW)
-                                    valid = valid && jpos <= ipos && jpos > ipos - prm.window;
-                                float a, da;
-                                act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + w]), a, da);
-                                p2[w] = valid ? a : 0.0f;
-                                d2[w] = valid ? __uint_as_float(dv[e + w]) * da : 0.0f;
+                            for (int e = 0; e < 16; e += 2) {
+                                float p2[2], d2[2];
+#pragma unroll
+                                for (int w = 0; w < 2; ++w) {
+                                    const int col = c * 32 + hh * 16 + e + w;
+                                    const int jpos = u.c0 + col;
+                                    bool valid = row_ok && col < u.nkv;
+                                    if (prm.mask == GDPA_MASK_CAUSAL_WINDOW)
+                                        valid = valid && jpos <= ipos && jpos > ipos - prm.window;
+                                    float a, da;
+                                    act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + w]), a,
+                                                          da);
+                                    p2[w] = valid ? a : 0.0f;
+                                    d2[w] = valid ? __uint_as_float(dv[e + w]) * da : 0.0f;
+                                }
+                                pp[e >> 1] = pack_bf16x2(p2[0], p2[1]);
+                                pd[cc][hh * 8 + (e >> 1)] = pack_bf16x2(d2[0], d2[1]);
                             }
-                            pp[c][e >> 1] = pack_bf16x2(p2[0], p2[1]);
-                            pd[c][e >> 1] = pack_bf16x2(d2[0], d2[1]);
+                            store_half_chunk(ps, c, hh, r, pp);
                         }
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(&bars[C::kSFree]);
-            // P -> shared (the previous tile's dS and staging are done with:
-            // this warpgroup drained that tile's dQ after its MMAs finished)
-            if (warp_rows) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (c < nch) {
-                        uint8_t* rowp = ps + (c >> 1) * kHalfBytes + r * 128;
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const int chunk = ((c & 1) * 4 + w) ^ (r & 7);
-                            *reinterpret_cast<uint4*>(rowp + chunk * 16) =
-                                make_uint4(pp[c][4 * w], pp[c][4 * w + 1], pp[c][4 * w + 2],
-                                           pp[c][4 * w + 3]);
-                        }
-                    }
-                }
-            }
             fence_proxy_async_smem();
             mbar_arrive(&bars[C::kPFull]);
             // dS -> shared once P^T dO has read P
             if (!wg_wait(&bars[C::kPVDone], i & 1, ab, 44)) return;
             if (warp_rows) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    if (c < nch) {
-                        uint8_t* rowp = ps + (c >> 1) * kHalfBytes + r * 128;
-#pragma unroll
-                        for (int w = 0; w < 4; ++w) {
-                            const int chunk = ((c & 1) * 4 + w) ^ (r & 7);
-                            *reinterpret_cast<uint4*>(rowp + chunk * 16) =
-                                make_uint4(pd[c][4 * w], pd[c][4 * w + 1], pd[c][4 * w + 2],
-                                           pd[c][4 * w + 3]);
-                        }
-                    }
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = wg + 2 * cc;
+                    if (c < nch) store_chunk(ps, c, r, pd[cc]);
                 }
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars[C::kDSFull]);
-            // dQ tile: TMEM -> staging (the P/dS buffer, free once dQ is done) -> global
+            // dQ tile, d columns [64 wg, 64 wg + 64): TMEM -> own staging half
             if (!wg_wait(&bars[C::kDQFull], i & 1, ab, 45)) return;
             tc_fence_after();
             float* dq = prm.dQ + (int64_t)(u.qt0 + m * kBM) * rs + h * D;
-            if (!drain_rows<D>(trow, kColDP, ps, dq, rs, nq, atomic_dq, prm.alpha, warp_rows, r,
-                               tid, &bars[C::kStage], st_use, ab, &bars[C::kDQFree]))
-                return;
+            if (D == 128 || wg == 0) {
+                if (!drain_cols(trow, kColDP + 64 * wg, 64, stage, dq + 64 * wg, rs, nq, atomic_dq,
+                                prm.alpha, warp_rows, r, tid, stage_bar, st_use, ab,
+                                &bars[C::kDQFree]))
+                    return;
+            } else {
+                tc_fence_before();
+                mbar_arrive(&bars[C::kDQFree]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[C::kPSFree]);
+            ++n_drain;
         }
-        // the unit's dK, dV rows
+        // the unit's dV (warpgroup 0) and dK (warpgroup 1)
         if (!wg_wait(&bars[C::kAccFull], nu & 1, ab, 46)) return;
         tc_fence_after();
         {
             const bool kv_rows = quarter * 32 < u.nkv;
-            float* dv = prm.dV + (int64_t)u.kvt0 * rs + h * D;
-            float* dk = prm.dK + (int64_t)u.kvt0 * rs + h * D;
-            if (!drain_rows<D>(trow, kColDV, ps, dv, rs, u.nkv, false, 1.0f, kv_rows, r, tid,
-                               &bars[C::kStage], st_use, ab, nullptr))
+            float* dst = (wg == 0 ? prm.dV : prm.dK) + (int64_t)u.kvt0 * rs + h * D;
+            if (!drain_cols(trow, wg == 0 ? kColDV : kColDK, D, stage, dst, rs, u.nkv, false,
+                            wg == 0 ? 1.0f : prm.alpha, kv_rows, r, tid, stage_bar, st_use, ab,
+                            &bars[C::kAccFree]))
                 return;
-            if (!drain_rows<D>(trow, kColDK, ps, dk, rs, u.nkv, false, prm.alpha, kv_rows, r, tid,
-                               &bars[C::kStage], st_use, ab, &bars[C::kAccFree]))
-                return;
+            fence_proxy_async_smem();
+            mbar_arrive(&bars[C::kPSFree]);
+            ++n_drain;
         }
         ++nu;
     }
@@ -426,12 +452,13 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (threadIdx.x == 0) {
         t_start = globaltimer();
         const uint32_t counts[C::kNumBars] = {
-            1, 1,            // kv full / empty
-            1, 1, 1, 1,      // q full x2, q empty x2
-            1, 1, 1, 1,      // dO full x2, dO empty x2
-            1, 128, 128,     // sd full, s free, dq free
-            128, 1, 128, 1,  // p full, pv done, ds full, dq full
-            1, 128, 128, 1   // acc full, acc free, stage, mma done
+            1, 1,                 // kv full / empty
+            1, 1, 1, 1,           // q full x2, q empty x2
+            1, 1, 1, 1,           // dO full x2, dO empty x2
+            1, 256, 256,          // sd full, s free, dq free
+            256, 1, 256, 1,       // p full, pv done, ds full, dq full
+            1, 256, 128, 128,     // acc full, acc free, stage x2
+            256, 1                // ps free, mma done
         };
         for (int b = 0; b < C::kNumBars; ++b) mbar_init(&bars[b], counts[b]);
         *abort_flag = 0;
