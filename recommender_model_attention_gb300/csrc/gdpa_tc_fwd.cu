@@ -16,15 +16,18 @@
 //    when the two belong to different warpgroups, so the tensor core
 //    computes item i+1's scores while item i's activation runs (software
 //    pipelining across tile boundaries on one flattened loop).
-//  * warps 2-9: two activation/epilogue warpgroups taking alternate tiles,
-//    each with its own TMEM S (128 columns) and O (128 columns) accumulators.
-//    They read S with tcgen05.ld, apply alpha, the activation and the jagged /
-//    window mask (masked pairs become exactly 0 after the activation), and
-//    write P as packed bf16 back into the S columns they have read
-//    (tcgen05.st); P V then takes P straight from TMEM (A operand in TMEM).
-//    After the last key block they read O from TMEM, stage it in the tile's
-//    (now consumed) Q buffer and store the valid rows with coalesced 16-byte
-//    stores.  Zero tiles (no valid key) are written as zeros directly.
+//  * warps 2-17: four activation/epilogue warpgroups.  Tiles alternate
+//    between two slots, each with its own TMEM S (128 columns) and O (128
+//    columns) accumulators, and two warpgroups share a slot: part h takes
+//    the 32-column key chunks h and h + 2 of S and the O columns
+//    [h d/2, (h + 1) d/2).  They read S with tcgen05.ld, apply alpha, the
+//    activation and the jagged / window mask (masked pairs become exactly 0
+//    after the activation), and write P as packed bf16 back into the S
+//    columns already read (tcgen05.st); P V then takes P straight from TMEM
+//    (A operand in TMEM).  After the last key block they read O from TMEM,
+//    stage it in the tile's (now consumed) Q buffer and store the valid rows
+//    with coalesced 16-byte stores.  Zero tiles (no valid key) are written
+//    as zeros directly.
 //  * O accumulates P V over key blocks with no rescaling.
 //  * Every barrier wait is bounded; a timeout sets the plan's error word and
 //    the CTA unwinds (waits for its TMA loads and MMAs, frees TMEM, returns).
@@ -38,8 +41,9 @@ namespace {
 
 using namespace tc;
 
-constexpr int kNumWG = 2;                       // activation warpgroups
-constexpr int kThreads = 64 + 128 * kNumWG;     // producer, MMA, warpgroups
+constexpr int kNumWG = 2;                       // tile slots (TMEM S/P + O each)
+constexpr int kParts = 2;                       // warpgroups sharing one slot
+constexpr int kThreads = 64 + 128 * kNumWG * kParts;  // producer, MMA, warpgroups
 constexpr int kHalfBytes = 128 * 128;           // 128 rows x 128 bytes (64 bf16)
 constexpr uint32_t kTmemCols = 512;
 
@@ -64,8 +68,8 @@ struct FwdCfg {
     static constexpr int kBarPFull = kBarSFull + kNumWG;
     static constexpr int kBarOFull = kBarPFull + kNumWG;
     static constexpr int kBarOFree = kBarOFull + kNumWG;
-    static constexpr int kBarStage = kBarOFree + kNumWG;
-    static constexpr int kBarMmaDone = kBarStage + kNumWG;
+    static constexpr int kBarStage = kBarOFree + kNumWG;             // per warpgroup
+    static constexpr int kBarMmaDone = kBarStage + kNumWG * kParts;
     static constexpr int kNumBars = kBarMmaDone + 1;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
 };
@@ -247,29 +251,30 @@ __device__ void fwd_compute(const FwdParams& prm, uint8_t* smem, uint64_t* bars,
                             int seg0, int seg1, const Abort& ab) {
     using C = FwdCfg<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t wg = (uint32_t)(warp - 2) / 4;
-    const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
-    const int r = quarter * 32 + lane;          // tile row of this thread
-    const int tid = (int)threadIdx.x - 64 - 128 * (int)wg;
+    const int grp = (warp - 2) >> 2;                 // warpgroup 0..3
+    const uint32_t wg = (uint32_t)(grp % kNumWG);    // tile slot
+    const int part = grp / kNumWG;                   // column share within the slot
+    const int quarter = warp & 3;                    // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;               // tile row of this thread
+    const int tid = (int)threadIdx.x - 64 - 128 * grp;
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const uint32_t s_tmem = tmem + wg * 256 + lane_addr;
-    const uint32_t o_tmem = tmem + wg * 256 + 128 + lane_addr;
-    uint32_t a = 0, i = 0, s_use = 0, o_use = 0;
+    const uint32_t o_tmem = tmem + wg * 256 + 128 + lane_addr + part * (D / 2);
+    uint32_t a = 0, s_use = 0, o_use = 0;
     for (int t = seg0; t < seg1; ++t) {
         const FwdTile tile = load_tile(prm.tiles + t);
         if (tile.kb1 <= tile.kb0) {
-            if ((uint32_t)((t - seg0) % kNumWG) == wg) store_zero_rows<D>(tile, prm, tid);
+            if ((t - seg0) % (kNumWG * kParts) == grp) store_zero_rows<D>(tile, prm, tid);
             continue;
         }
         if (a % kNumWG != wg) {
-            i += tile.kb1 - tile.kb0;
             ++a;
             continue;
         }
         const uint32_t qs = a % C::kNQ;
         const bool warp_rows = quarter * 32 < tile.nq;
         const int ipos = tile.i0 + r;
-        for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++i) {
+        for (int kb = tile.kb0; kb < tile.kb1; ++kb) {
             const int nvalid = min(kBN, tile.lkv - kb * kBN);
             const int nch = (nvalid + 31) >> 5;
             if (!wg_wait(&bars[C::kBarSFull + wg], s_use & 1, ab, 6)) return;
@@ -281,7 +286,8 @@ __device__ void fwd_compute(const FwdParams& prm, uint8_t* smem, uint64_t* bars,
             if (warp_rows) {
                 const int jbase = kb * kBN;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = part + 2 * cc;
                     if (c < nch) {
                         uint32_t sv[32], pk[16];
                         tmem_ld32(s_tmem + c * 32, sv);
@@ -309,21 +315,24 @@ __device__ void fwd_compute(const FwdParams& prm, uint8_t* smem, uint64_t* bars,
             tc_fence_before();
             mbar_arrive(&bars[C::kBarPFull + wg]);
         }
-        // epilogue: O (TMEM) -> bf16 -> staging (this tile's Q buffer) -> global
+        // epilogue: this part's O columns (TMEM) -> bf16 -> this part's half of
+        // the tile's (consumed) Q buffer -> global
         if (!wg_wait(&bars[C::kBarOFull + wg], o_use & 1, ab, 8)) return;
         o_use++;
         tc_fence_after();
-        uint8_t* stage = smem + C::kOffQ + qs * C::kTileBytes;
-        constexpr int kRowBytes = D * 2;
+        constexpr int kRowBytes = D;                 // D/2 bf16 per row and part
+        constexpr int kChunks = kRowBytes / 16;      // 16-byte chunks per row
+        constexpr int kSwz = kChunks - 1 < 7 ? kChunks - 1 : 7;
+        uint8_t* stage = smem + C::kOffQ + qs * C::kTileBytes + part * (C::kTileBytes / 2);
         if (warp_rows) {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
+            for (int c = 0; c < D / 64; ++c) {
                 uint32_t ov[32];
                 tmem_ld32(o_tmem + c * 32, ov);
                 tmem_ld_wait();
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int chunk = (c * 4 + u) ^ (r & 7);
+                    const int chunk = (c * 4 + u) ^ (r & kSwz);
                     uint4 w;
                     w.x = pack_bf16x2(__uint_as_float(ov[8 * u + 0]), __uint_as_float(ov[8 * u + 1]));
                     w.y = pack_bf16x2(__uint_as_float(ov[8 * u + 2]), __uint_as_float(ov[8 * u + 3]));
@@ -336,16 +345,15 @@ __device__ void fwd_compute(const FwdParams& prm, uint8_t* smem, uint64_t* bars,
         tc_fence_before();
         mbar_arrive(&bars[C::kBarOFree + wg]);
         // the whole warpgroup's staging writes before anyone reads them back
-        mbar_arrive(&bars[C::kBarStage + wg]);
-        if (!wg_wait(&bars[C::kBarStage + wg], (o_use - 1) & 1, ab, 9)) return;
+        mbar_arrive(&bars[C::kBarStage + grp]);
+        if (!wg_wait(&bars[C::kBarStage + grp], (o_use - 1) & 1, ab, 9)) return;
         {
-            constexpr int kChunks = D / 8;
             const int64_t rs = (int64_t)prm.H * D;
-            __nv_bfloat16* obase = prm.O + (int64_t)tile.qt0 * rs + tile.h * D;
+            __nv_bfloat16* obase = prm.O + (int64_t)tile.qt0 * rs + tile.h * D + part * (D / 2);
             for (int idx = tid; idx < tile.nq * kChunks; idx += 128) {
                 const int row = idx / kChunks, ch = idx % kChunks;
                 const uint4 w = *reinterpret_cast<const uint4*>(stage + row * kRowBytes +
-                                                                ((ch ^ (row & 7)) * 16));
+                                                                ((ch ^ (row & kSwz)) * 16));
                 *reinterpret_cast<uint4*>(obase + (int64_t)row * rs + ch * 8) = w;
             }
         }
@@ -372,7 +380,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         t_start = globaltimer();
         for (int s = 0; s < C::kNQ; ++s) {
             mbar_init(&bars[C::kBarQFull + s], 1);
-            mbar_init(&bars[C::kBarQEmpty + s], 128);
+            mbar_init(&bars[C::kBarQEmpty + s], 128 * kParts);
         }
         for (int s = 0; s < C::kNKV; ++s) {
             mbar_init(&bars[C::kBarKFull + s], 1);
@@ -381,11 +389,11 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         for (int w = 0; w < kNumWG; ++w) {
             mbar_init(&bars[C::kBarSFull + w], 1);
-            mbar_init(&bars[C::kBarPFull + w], 128);
+            mbar_init(&bars[C::kBarPFull + w], 128 * kParts);
             mbar_init(&bars[C::kBarOFull + w], 1);
-            mbar_init(&bars[C::kBarOFree + w], 128);
-            mbar_init(&bars[C::kBarStage + w], 128);
+            mbar_init(&bars[C::kBarOFree + w], 128 * kParts);
         }
+        for (int g = 0; g < kNumWG * kParts; ++g) mbar_init(&bars[C::kBarStage + g], 128);
         mbar_init(&bars[C::kBarMmaDone], 1);
         *abort_flag = 0;
         fence_mbar_init();
