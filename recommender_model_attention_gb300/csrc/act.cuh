@@ -14,7 +14,10 @@
 //    x/2 (1 + tanh(x/2)); GELU-erf with Phi from the rational approximation
 //    of Abramowitz & Stegun, Handbook of Mathematical Functions, eq. 7.1.28
 //    (erf z = 1 - (1 + a1 z + ... + a6 z^6)^-16, |error| <= 3e-7), one
-//    reciprocal per element; the normal density for act' through ex2.approx.
+//    reciprocal per element.  act and act' together (backward) use A&S eq.
+//    7.1.26 instead (erfc z = t (a1 + ... + a5 t^4) exp(-z^2), t = 1/(1 + p z),
+//    |error| <= 1.5e-7), whose exp(-z^2) = exp(-x^2/2) is also the normal
+//    density's, so one reciprocal and one ex2 serve both.
 //    The Taylor polynomial is the same FMA chain in both flavours.
 #pragma once
 
@@ -69,6 +72,29 @@ __device__ __forceinline__ float normal_cdf_fast(float x) {
     p = p * p;                          // (1 + ...)^16
     const float half_tail = 0.5f * rcp_approx(p);   // (1 - erf z) / 2
     return x >= 0.0f ? 1.0f - half_tail : half_tail;
+}
+
+// A&S 7.1.26 coefficients
+constexpr float kASp = 0.3275911f;
+constexpr float kASb1 = 0.254829592f;
+constexpr float kASb2 = -0.284496736f;
+constexpr float kASb3 = 1.421413741f;
+constexpr float kASb4 = -1.453152027f;
+constexpr float kASb5 = 1.061405429f;
+
+// x Phi(x) and Phi(x) + x phi(x) with one reciprocal and one ex2
+__device__ __forceinline__ void gelu_erf_and_grad_fast(float x, float& a, float& da) {
+    const float z = fabsf(x) * kRsqrt2;
+    const float t = rcp_approx(fmaf(kASp, z, 1.0f));
+    float q = fmaf(kASb5, t, kASb4);
+    q = fmaf(q, t, kASb3);
+    q = fmaf(q, t, kASb2);
+    q = fmaf(q, t, kASb1);
+    const float e = ex2_approx(-0.5f * kLog2e * x * x);   // exp(-x^2 / 2)
+    const float half_tail = 0.5f * q * t * e;             // erfc(z) / 2
+    const float cdf = x >= 0.0f ? 1.0f - half_tail : half_tail;
+    a = x * cdf;
+    da = fmaf(x * kRsqrt2Pi, e, cdf);
 }
 
 __device__ __forceinline__ float tanh_approx(float x) {
@@ -146,11 +172,13 @@ __device__ __forceinline__ float dact_f(float x) {
 template <int ACT, bool FAST>
 __device__ __forceinline__ void act_dact_f(float x, float& a, float& da) {
     if constexpr (ACT == kGeluErf) {
-        const float cdf = FAST ? normal_cdf_fast(x) : 0.5f * (1.0f + erff(x * kRsqrt2));
-        const float pdf = kRsqrt2Pi * (FAST ? ex2_approx(-0.5f * kLog2e * x * x)
-                                           : expf(-0.5f * x * x));
-        a = x * cdf;
-        da = fmaf(x, pdf, cdf);
+        if constexpr (FAST) {
+            gelu_erf_and_grad_fast(x, a, da);
+        } else {
+            const float cdf = 0.5f * (1.0f + erff(x * kRsqrt2));
+            a = x * cdf;
+            da = fmaf(x, kRsqrt2Pi * expf(-0.5f * x * x), cdf);
+        }
     } else if constexpr (ACT == kGeluTanh) {
         const float u = kSqrt2OverPi * fmaf(kTanhCubic * x, x * x, x);
         const float t = FAST ? tanh_approx(u) : tanhf(u);

@@ -23,7 +23,8 @@
 //     S  = Q K^T   -> TMEM [0, 128)      dP = dO V^T -> TMEM [128, 256)
 //     P, dS        -> one 32 KB shared buffer, P first, then dS
 //     dV += P^T dO -> TMEM [256, 384)    dK += dS^T Q -> TMEM [384, 512)
-//     dQ  = dS K   -> TMEM [128, 256) (dP's columns, already read)
+//     dQ  = dS K   -> TMEM [128, 256) (dP's columns, already read), issued
+//                     before dK and drained through the tile's dO buffer
 // P^T and dS^T are the MN-major reading of the [query x key] buffer, and Q,
 // dO, K are the MN-major reading of their [row x d] tiles, so nothing is
 // transposed in memory.  Every wait is bounded (timeouts set the plan's
@@ -202,23 +203,22 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
                 mma_ss(tmem + kColDV, smem_desc_sw128(psbase + k * 2048, kHalfBytes, 1024),
                        smem_desc_sw128(dob + k * 2048, kHalfBytes, 1024), idesc_acc,
                        (first && k == 0) ? 0u : 1u);
-            mma_commit(&bars[C::kDOEmpty + s]);
             mma_commit(&bars[C::kPVDone]);
             // the next tile's scores while this tile's dS is being written
             if (!last && !issue_s(i + 1)) goto drain;
-            // dK += dS^T Q, dQ = dS K
+            // dQ = dS K first, so that its drain overlaps dK += dS^T Q
             if (!mbar_wait(&bars[C::kDSFull], i & 1, ab, 38)) goto drain;
             tc_fence_after();
-            for (uint32_t k = 0; k < nq32 / 16; ++k)
-                mma_ss(tmem + kColDK, smem_desc_sw128(psbase + k * 2048, kHalfBytes, 1024),
-                       smem_desc_sw128(qb + k * 2048, kHalfBytes, 1024), idesc_acc,
-                       (first && k == 0) ? 0u : 1u);
-            mma_commit(&bars[C::kQEmpty + s]);
             for (uint32_t k = 0; k < nkv32 / 16; ++k)
                 mma_ss(tmem + kColDP,
                        smem_desc_sw128(psbase + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024),
                        smem_desc_sw128(kbase + k * 2048, kHalfBytes, 1024), idesc_dq, k > 0);
             mma_commit(&bars[C::kDQFull]);
+            for (uint32_t k = 0; k < nq32 / 16; ++k)
+                mma_ss(tmem + kColDK, smem_desc_sw128(psbase + k * 2048, kHalfBytes, 1024),
+                       smem_desc_sw128(qb + k * 2048, kHalfBytes, 1024), idesc_acc,
+                       (first && k == 0) ? 0u : 1u);
+            mma_commit(&bars[C::kQEmpty + s]);
             if (last) {
                 mma_commit(&bars[C::kAccFull]);
                 mma_commit(&bars[C::kKVEmpty]);
@@ -327,7 +327,7 @@ __device__ void bwd_compute(const BwdParams& prm, uint8_t* smem, uint64_t* bars,
     uint8_t* stage = ps + wg * kHalfBytes;
     uint64_t* stage_bar = &bars[C::kStage + wg];
     const int64_t rs = (int64_t)prm.H * D;
-    uint32_t nu = 0, i = 0, st_use = 0, n_drain = 0;
+    uint32_t nu = 0, i = 0, st_use = 0;
     for (int t = seg0; t < seg1; ++t) {
         const BwdUnit u = load_unit(prm.units + t);
         const int h = u.hf & 0xffff;
@@ -343,10 +343,13 @@ __device__ void bwd_compute(const BwdParams& prm, uint8_t* smem, uint64_t* bars,
             const bool warp_rows = quarter * 32 < nq;
             const int ipos = m * kBM + r;        // query position in the sample
             const bool row_ok = r < nq;
+            const bool windowed = prm.mask == GDPA_MASK_CAUSAL_WINDOW;
             if (!wg_wait(&bars[C::kSDFull], i & 1, ab, 43)) return;
-            // the shared buffer must be clear of the previous tile's dQ (or
-            // unit's dK, dV) drain by both warpgroups before P goes in
-            if (n_drain > 0 && !wg_wait(&bars[C::kPSFree], (n_drain - 1) & 1, ab, 47)) return;
+            // the shared buffer must be clear of the previous unit's dK, dV
+            // drain by both warpgroups before P goes in (within a unit, S and
+            // dP being ready means the previous tile's dK MMA, the buffer's
+            // last reader, has finished: it precedes dP in the MMA pipe)
+            if (m == u.m0 && nu > 0 && !wg_wait(&bars[C::kPSFree], (nu - 1) & 1, ab, 47)) return;
             tc_fence_after();
             uint32_t pd[2][16];
             if (warp_rows) {
@@ -357,28 +360,53 @@ __device__ void bwd_compute(const BwdParams& prm, uint8_t* smem, uint64_t* bars,
                         // two 16-column halves of the chunk keep register use low
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
-                            uint32_t sv[16], dv[16], pp[8];
-                            tmem_ld16(trow + kColS + c * 32 + hh * 16, sv);
-                            tmem_ld16(trow + kColDP + c * 32 + hh * 16, dv);
-                            tmem_ld_wait();
+                            const int col0 = c * 32 + hh * 16;
+                            uint32_t pp[8];
+                            if (col0 >= u.nkv) {
+                                // past the keys: zeros feed the K-padded GEMMs
 #pragma unroll
-                            for (int e = 0; e < 16; e += 2) {
-                                float p2[2], d2[2];
+                                for (int e = 0; e < 8; ++e) pp[e] = pd[cc][hh * 8 + e] = 0u;
+                            } else {
+                                uint32_t sv[16], dv[16];
+                                tmem_ld16(trow + kColS + col0, sv);
+                                tmem_ld16(trow + kColDP + col0, dv);
+                                tmem_ld_wait();
+                                const bool full = !windowed && col0 + 16 <= u.nkv;
+                                if (!row_ok) {
 #pragma unroll
-                                for (int w = 0; w < 2; ++w) {
-                                    const int col = c * 32 + hh * 16 + e + w;
-                                    const int jpos = u.c0 + col;
-                                    bool valid = row_ok && col < u.nkv;
-                                    if (prm.mask == GDPA_MASK_CAUSAL_WINDOW)
-                                        valid = valid && jpos <= ipos && jpos > ipos - prm.window;
-                                    float a, da;
-                                    act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + w]), a,
-                                                          da);
-                                    p2[w] = valid ? a : 0.0f;
-                                    d2[w] = valid ? __uint_as_float(dv[e + w]) * da : 0.0f;
+                                    for (int e = 0; e < 8; ++e) pp[e] = pd[cc][hh * 8 + e] = 0u;
+                                } else if (full) {
+#pragma unroll
+                                    for (int e = 0; e < 16; e += 2) {
+                                        float a0, d0, a1, d1;
+                                        act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e]), a0, d0);
+                                        act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + 1]), a1, d1);
+                                        pp[e >> 1] = pack_bf16x2(a0, a1);
+                                        pd[cc][hh * 8 + (e >> 1)] =
+                                            pack_bf16x2(__uint_as_float(dv[e]) * d0,
+                                                        __uint_as_float(dv[e + 1]) * d1);
+                                    }
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 16; e += 2) {
+                                        float p2[2], d2[2];
+#pragma unroll
+                                        for (int w = 0; w < 2; ++w) {
+                                            const int col = col0 + e + w;
+                                            const int jpos = u.c0 + col;
+                                            bool valid = col < u.nkv;
+                                            if (windowed)
+                                                valid = valid && jpos <= ipos && jpos > ipos - prm.window;
+                                            float a, da;
+                                            act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + w]),
+                                                                  a, da);
+                                            p2[w] = valid ? a : 0.0f;
+                                            d2[w] = valid ? __uint_as_float(dv[e + w]) * da : 0.0f;
+                                        }
+                                        pp[e >> 1] = pack_bf16x2(p2[0], p2[1]);
+                                        pd[cc][hh * 8 + (e >> 1)] = pack_bf16x2(d2[0], d2[1]);
+                                    }
                                 }
-                                pp[e >> 1] = pack_bf16x2(p2[0], p2[1]);
-                                pd[cc][hh * 8 + (e >> 1)] = pack_bf16x2(d2[0], d2[1]);
                             }
                             store_half_chunk(ps, c, hh, r, pp);
                         }
@@ -400,13 +428,16 @@ __device__ void bwd_compute(const BwdParams& prm, uint8_t* smem, uint64_t* bars,
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars[C::kDSFull]);
-            // dQ tile, d columns [64 wg, 64 wg + 64): TMEM -> own staging half
+            // dQ tile, d columns [64 wg, 64 wg + 64): TMEM -> this warpgroup's
+            // half of the tile's dO buffer (dO's MMAs are done) -> global; the
+            // dO stage goes back to the producer afterwards
             if (!wg_wait(&bars[C::kDQFull], i & 1, ab, 45)) return;
             tc_fence_after();
             float* dq = prm.dQ + (int64_t)(u.qt0 + m * kBM) * rs + h * D;
+            uint8_t* dq_stage = smem + C::kOffDO + (i & 1) * C::kTileBytes + wg * kHalfBytes;
             if (D == 128 || wg == 0) {
-                if (!drain_cols(trow, kColDP + 64 * wg, 64, stage, dq + 64 * wg, rs, nq, atomic_dq,
-                                prm.alpha, warp_rows, r, tid, stage_bar, st_use, ab,
+                if (!drain_cols(trow, kColDP + 64 * wg, 64, dq_stage, dq + 64 * wg, rs, nq,
+                                atomic_dq, prm.alpha, warp_rows, r, tid, stage_bar, st_use, ab,
                                 &bars[C::kDQFree]))
                     return;
             } else {
@@ -414,8 +445,7 @@ __device__ void bwd_compute(const BwdParams& prm, uint8_t* smem, uint64_t* bars,
                 mbar_arrive(&bars[C::kDQFree]);
             }
             fence_proxy_async_smem();
-            mbar_arrive(&bars[C::kPSFree]);
-            ++n_drain;
+            mbar_arrive(&bars[C::kDOEmpty + (i & 1)]);
         }
         // the unit's dV (warpgroup 0) and dK (warpgroup 1)
         if (!wg_wait(&bars[C::kAccFull], nu & 1, ab, 46)) return;
@@ -429,7 +459,6 @@ __device__ void bwd_compute(const BwdParams& prm, uint8_t* smem, uint64_t* bars,
                 return;
             fence_proxy_async_smem();
             mbar_arrive(&bars[C::kPSFree]);
-            ++n_drain;
         }
         ++nu;
     }
@@ -454,7 +483,7 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         const uint32_t counts[C::kNumBars] = {
             1, 1,                 // kv full / empty
             1, 1, 1, 1,           // q full x2, q empty x2
-            1, 1, 1, 1,           // dO full x2, dO empty x2
+            1, 1, 256, 256,       // dO full x2, dO empty x2 (warpgroups, after dQ)
             1, 256, 256,          // sd full, s free, dq free
             256, 1, 256, 1,       // p full, pv done, ds full, dq full
             1, 256, 128, 128,     // acc full, acc free, stage x2

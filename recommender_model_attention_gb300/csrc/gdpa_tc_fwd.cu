@@ -22,9 +22,9 @@
 //    the 32-column key chunks h and h + 2 of S and the O columns
 //    [h d/2, (h + 1) d/2).  They read S with tcgen05.ld, apply alpha, the
 //    activation and the jagged / window mask (masked pairs become exactly 0
-//    after the activation), and write P as packed bf16 back into the S
-//    columns already read (tcgen05.st); P V then takes P straight from TMEM
-//    (A operand in TMEM).  After the last key block they read O from TMEM,
+//    after the activation), and write P as packed bf16 into the first half of
+//    each 32-column S chunk they have read (tcgen05.st); P V then takes P
+//    straight from TMEM (A operand in TMEM, one address per K = 16 step).  After the last key block they read O from TMEM,
 //    stage it in the tile's (now consumed) Q buffer and store the valid rows
 //    with coalesced 16-byte stores.  Zero tiles (no valid key) are written
 //    as zeros directly.
@@ -174,8 +174,10 @@ __device__ __forceinline__ bool issue_pv(const PendingPV& pd, uint8_t* smem, uin
     const uint32_t d_o = tmem + pd.wg * 256 + 128;
     const uint32_t vbase = smem_u32(smem + C::kOffV + pd.ks * C::kTileBytes);
     for (uint32_t k = 0; k < pd.nsteps; ++k) {
+        // keys [16k, 16k + 16) sit in S chunk k/2's first 16 columns, half k%2
         const uint64_t b_desc = smem_desc_sw128(vbase + k * 2048, kHalfBytes, 1024);
-        mma_ts(d_o, p_tmem + k * 8, b_desc, idesc, (pd.first && k == 0) ? 0u : 1u);
+        mma_ts(d_o, p_tmem + (k >> 1) * 32 + (k & 1) * 8, b_desc, idesc,
+               (pd.first && k == 0) ? 0u : 1u);
     }
     mma_commit(&bars[C::kBarKVEmpty + pd.ks]);
     if (pd.last) {
@@ -280,34 +282,47 @@ __device__ void fwd_compute(const FwdParams& prm, uint8_t* smem, uint64_t* bars,
             if (!wg_wait(&bars[C::kBarSFull + wg], s_use & 1, ab, 6)) return;
             s_use++;
             tc_fence_after();
-            // S -> registers one 32-column chunk at a time; alpha, activation
-            // and mask; P (bf16 pairs) back into the chunk's first 16 columns
-            // (already read: P column 16c+k holds S columns 32c+2k, +1)
+            // S -> registers 16 columns at a time; alpha, activation and mask;
+            // P (bf16 pairs) back into the first 16 columns of the same
+            // 32-column chunk, which only this warpgroup reads and has read
+            // (P column 32c + 8h + k holds keys 32c + 16h + 2k, +1)
             if (warp_rows) {
                 const int jbase = kb * kBN;
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const int c = part + 2 * cc;
                     if (c < nch) {
-                        uint32_t sv[32], pk[16];
-                        tmem_ld32(s_tmem + c * 32, sv);
-                        tmem_ld_wait();
+#pragma unroll 1
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int col0 = c * 32 + hh * 16;
+                            uint32_t sv[16], pk[8];
+                            tmem_ld16(s_tmem + col0, sv);
+                            tmem_ld_wait();
+                            if (prm.mask != GDPA_MASK_CAUSAL_WINDOW && col0 + 16 <= nvalid) {
 #pragma unroll
-                        for (int e = 0; e < 32; e += 2) {
-                            float pv[2];
+                                for (int e = 0; e < 16; e += 2)
+                                    pk[e >> 1] = pack_bf16x2(
+                                        act_f<ACT, true>(prm.alpha * __uint_as_float(sv[e])),
+                                        act_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + 1])));
+                            } else {
 #pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int col = c * 32 + e + u;
-                                const int jpos = jbase + col;
-                                bool valid = col < nvalid;
-                                if (prm.mask == GDPA_MASK_CAUSAL_WINDOW)
-                                    valid = valid && jpos <= ipos && jpos > ipos - prm.window;
-                                const float x = prm.alpha * __uint_as_float(sv[e + u]);
-                                pv[u] = valid ? act_f<ACT, true>(x) : 0.0f;
+                                for (int e = 0; e < 16; e += 2) {
+                                    float pv[2];
+#pragma unroll
+                                    for (int u = 0; u < 2; ++u) {
+                                        const int col = col0 + e + u;
+                                        const int jpos = jbase + col;
+                                        bool valid = col < nvalid;
+                                        if (prm.mask == GDPA_MASK_CAUSAL_WINDOW)
+                                            valid = valid && jpos <= ipos && jpos > ipos - prm.window;
+                                        const float x = prm.alpha * __uint_as_float(sv[e + u]);
+                                        pv[u] = valid ? act_f<ACT, true>(x) : 0.0f;
+                                    }
+                                    pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+                                }
                             }
-                            pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+                            tmem_st8(s_tmem + c * 32 + hh * 8, pk);
                         }
-                        tmem_st16(s_tmem + c * 16, pk);
                     }
                 }
                 tmem_st_wait();
