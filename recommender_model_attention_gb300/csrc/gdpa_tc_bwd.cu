@@ -233,52 +233,75 @@ drain:
     mbar_wait_teardown(&bars[C::kMmaDone], 0);
 }
 
-// Drain TMEM columns [col, col + ncols) (multiple of 32) of this
-// warpgroup's lanes to rows [0, nrows) of `dst` (row stride `rs` floats, the
-// block's first column at dst), 32 columns per pass through `stage` (this
-// warpgroup's 16 KB: row r at r * 128 bytes, 16-byte chunk c at c ^ (r & 7)),
-// scaled by `scale`, atomically added when `atomic`.  `release` (if any) is
-// arrived once the last TMEM read is done.
-__device__ __forceinline__ bool drain_cols(uint32_t trow, uint32_t col, int ncols, uint8_t* stage,
-                                           float* dst, int64_t rs, int nrows, bool atomic,
-                                           float scale, bool warp_rows, int r, int tid,
-                                           uint64_t* stage_bar, uint32_t& st_use, const Abort& ab,
-                                           uint64_t* release) {
+// Drain TMEM columns [col, col + ncols) (a multiple of 32) of this warp's
+// 32 lanes (block rows 32 * quarter + lane) into rows [0, nrows) of a block
+// of a [rows][H * d] fp32 tensor whose first element has tensor-map
+// coordinates (x0, y0) and address `dst` (row stride `rs` floats), scaled by
+// `scale`.  A warp whose 32 rows are all inside the block stages 32 columns
+// at a time in its own 4 KB of `stage` (128-byte rows, 16-byte chunks
+// swizzled by row, the layout of a 128-byte-swizzled TMA box) and writes
+// them with one TMA bulk store, or a bulk reduce-add when `atomic`; the warp
+// holding the block's ragged end writes its valid rows from registers.
+// `release` (if any) is arrived by every thread after its last TMEM read.
+// On return the warp's staging area is free again.
+__device__ __noinline__ void drain_warp(uint32_t trow, uint32_t col, int ncols, uint8_t* stage,
+                                           const CUtensorMap* map, int x0, int y0, float* dst,
+                                           int64_t rs, int nrows, bool atomic, float scale,
+                                           int quarter, int lane, uint64_t* release) {
+    const int row0 = quarter * 32;
+    const bool any = row0 < nrows;
+    const bool full = row0 + 32 <= nrows;
+    uint8_t* wst = stage + quarter * 4096;
     for (int pass = 0; pass < ncols / 32; ++pass) {
-        if (warp_rows) {
-            uint32_t v[32];
+        uint32_t v[32];
+        if (any) {
             tmem_ld32(trow + col + pass * 32, v);
             tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<float4*>(stage + r * 128 + ((c ^ (r & 7)) << 4)) =
-                    make_float4(scale * __uint_as_float(v[4 * c]), scale * __uint_as_float(v[4 * c + 1]),
-                                scale * __uint_as_float(v[4 * c + 2]),
-                                scale * __uint_as_float(v[4 * c + 3]));
         }
         if (pass == ncols / 32 - 1 && release) {
             tc_fence_before();
             mbar_arrive(release);
         }
-        mbar_arrive(stage_bar);
-        if (!wg_wait(stage_bar, st_use & 1, ab, 41)) return false;
-        ++st_use;
-        float* d = dst + pass * 32;
-        for (int idx = tid; idx < nrows * 8; idx += 128) {
-            const int row = idx >> 3, ch = idx & 7;
-            const float4 w =
-                *reinterpret_cast<const float4*>(stage + row * 128 + ((ch ^ (row & 7)) << 4));
-            float4* p = reinterpret_cast<float4*>(d + (int64_t)row * rs + ch * 4);
-            if (atomic)
-                atomicAdd(p, w);
-            else
-                *p = w;
+        if (!any) continue;
+        if (full) {
+            if (pass > 0) {
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<float4*>(wst + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                    make_float4(scale * __uint_as_float(v[4 * c]), scale * __uint_as_float(v[4 * c + 1]),
+                                scale * __uint_as_float(v[4 * c + 2]),
+                                scale * __uint_as_float(v[4 * c + 3]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (atomic)
+                    tma_reduce_add_2d(map, wst, x0 + pass * 32, y0 + row0);
+                else
+                    tma_store_2d(map, wst, x0 + pass * 32, y0 + row0);
+                bulk_commit();
+            }
+        } else if (row0 + lane < nrows) {
+            float* d = dst + (int64_t)(row0 + lane) * rs + pass * 32;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 w = make_float4(scale * __uint_as_float(v[4 * c]),
+                                             scale * __uint_as_float(v[4 * c + 1]),
+                                             scale * __uint_as_float(v[4 * c + 2]),
+                                             scale * __uint_as_float(v[4 * c + 3]));
+                if (atomic)
+                    atomicAdd(reinterpret_cast<float4*>(d + 4 * c), w);
+                else
+                    *reinterpret_cast<float4*>(d + 4 * c) = w;
+            }
         }
-        mbar_arrive(stage_bar);
-        if (!wg_wait(stage_bar, st_use & 1, ab, 42)) return false;
-        ++st_use;
     }
-    return true;
+    if (full) {
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+    }
 }
 
 template <int D>
@@ -314,7 +337,8 @@ __device__ __forceinline__ void store_half_chunk(uint8_t* ps, int c, int hh, int
 }
 
 template <int D, int ACT>
-__device__ void bwd_compute(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
+__device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const CUtensorMap* tmDK,
+                            const CUtensorMap* tmDV, uint8_t* smem, uint64_t* bars, uint32_t tmem,
                             int seg0, int seg1, const Abort& ab) {
     using C = BwdCfg<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -325,9 +349,8 @@ __device__ void bwd_compute(const BwdParams& prm, uint8_t* smem, uint64_t* bars,
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     uint8_t* ps = smem + C::kOffPS;
     uint8_t* stage = ps + wg * kHalfBytes;
-    uint64_t* stage_bar = &bars[C::kStage + wg];
     const int64_t rs = (int64_t)prm.H * D;
-    uint32_t nu = 0, i = 0, st_use = 0;
+    uint32_t nu = 0, i = 0;
     for (int t = seg0; t < seg1; ++t) {
         const BwdUnit u = load_unit(prm.units + t);
         const int h = u.hf & 0xffff;
@@ -436,10 +459,9 @@ __device__ void bwd_compute(const BwdParams& prm, uint8_t* smem, uint64_t* bars,
             float* dq = prm.dQ + (int64_t)(u.qt0 + m * kBM) * rs + h * D;
             uint8_t* dq_stage = smem + C::kOffDO + (i & 1) * C::kTileBytes + wg * kHalfBytes;
             if (D == 128 || wg == 0) {
-                if (!drain_cols(trow, kColDP + 64 * wg, 64, dq_stage, dq + 64 * wg, rs, nq,
-                                atomic_dq, prm.alpha, warp_rows, r, tid, stage_bar, st_use, ab,
-                                &bars[C::kDQFree]))
-                    return;
+                drain_warp(trow, kColDP + 64 * wg, 64, dq_stage, tmDQ, h * D + 64 * wg,
+                           u.qt0 + m * kBM, dq + 64 * wg, rs, nq, atomic_dq, prm.alpha, quarter,
+                           lane, &bars[C::kDQFree]);
             } else {
                 tc_fence_before();
                 mbar_arrive(&bars[C::kDQFree]);
@@ -451,12 +473,10 @@ __device__ void bwd_compute(const BwdParams& prm, uint8_t* smem, uint64_t* bars,
         if (!wg_wait(&bars[C::kAccFull], nu & 1, ab, 46)) return;
         tc_fence_after();
         {
-            const bool kv_rows = quarter * 32 < u.nkv;
             float* dst = (wg == 0 ? prm.dV : prm.dK) + (int64_t)u.kvt0 * rs + h * D;
-            if (!drain_cols(trow, wg == 0 ? kColDV : kColDK, D, stage, dst, rs, u.nkv, false,
-                            wg == 0 ? 1.0f : prm.alpha, kv_rows, r, tid, stage_bar, st_use, ab,
-                            &bars[C::kAccFree]))
-                return;
+            drain_warp(trow, wg == 0 ? kColDV : kColDK, D, stage, wg == 0 ? tmDV : tmDK, h * D,
+                       u.kvt0, dst, rs, u.nkv, false, wg == 0 ? 1.0f : prm.alpha, quarter, lane,
+                       &bars[C::kAccFree]);
             fence_proxy_async_smem();
             mbar_arrive(&bars[C::kPSFree]);
         }
@@ -468,7 +488,8 @@ template <int D, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
-              const BwdParams prm) {
+              const __grid_constant__ CUtensorMap tmDQ, const __grid_constant__ CUtensorMap tmDK,
+              const __grid_constant__ CUtensorMap tmDV, const BwdParams prm) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -513,7 +534,10 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (lane == 0) bwd_mma<D>(prm, smem, bars, tmem, seg0, seg1, ab);
         __syncwarp();
     } else {
-        bwd_compute<D, ACT>(prm, smem, bars, tmem, seg0, seg1, ab);
+        bwd_compute<D, ACT>(prm, &tmDQ, &tmDK, &tmDV, smem, bars, tmem, seg0, seg1, ab);
+        // every bulk store of this warp has landed before the CTA retires
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -536,7 +560,8 @@ gdpa_status launch(Plan& p, const CUtensorMap* maps, const BwdParams& prm, cudaS
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return GDPA_ERR_CUDA;
-    kern<<<p.S, kThreads, C::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], prm);
+    kern<<<p.S, kThreads, C::kSmemBytes, st>>>(maps[0], maps[1], maps[2], maps[3], maps[4],
+                                                maps[5], maps[6], prm);
     p.launches += 1;
     return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
@@ -552,14 +577,17 @@ gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, 
             return GDPA_ERR_CUDA;
     }
     if (p.n_bwd == 0) return GDPA_OK;
-    CUtensorMap maps[4];
+    CUtensorMap maps[7];
     const uint64_t q_rows = p.Tq > 0 ? (uint64_t)p.Tq : 1;
     const void* qp = p.Tq > 0 ? q : k;
     const void* dop = p.Tq > 0 ? d_o : k;
     if (!tc::make_tmap_bf16(&maps[0], qp, q_rows, row, 128) ||
         !tc::make_tmap_bf16(&maps[1], k, (uint64_t)p.Tkv, row, 128) ||
         !tc::make_tmap_bf16(&maps[2], v, (uint64_t)p.Tkv, row, 128) ||
-        !tc::make_tmap_bf16(&maps[3], dop, q_rows, row, 128))
+        !tc::make_tmap_bf16(&maps[3], dop, q_rows, row, 128) ||
+        !tc::make_tmap_f32(&maps[4], p.Tq > 0 ? (const void*)dq : (const void*)dk, q_rows, row, 32) ||
+        !tc::make_tmap_f32(&maps[5], dk, (uint64_t)p.Tkv, row, 32) ||
+        !tc::make_tmap_f32(&maps[6], dv, (uint64_t)p.Tkv, row, 32))
         return GDPA_ERR_CUDA;
     BwdParams prm;
     prm.units = p.d_bwd;

@@ -147,6 +147,41 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
         : "memory");
 }
 
+// 2-D tile store shared -> global (bulk-group completion); x * 4 bytes (fp32)
+// must be a multiple of 16 and no coordinate may be negative.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x,
+                                             int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            map),
+        "r"(x), "r"(y), "r"(smem_u32(src))
+        : "memory");
+}
+
+// Same, adding into global memory element-wise (f32 add, atomic per element).
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src,
+                                                  int32_t x, int32_t y) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
+        " [%0, {%1, %2}], [%3];" ::"l"(map),
+        "r"(x), "r"(y), "r"(smem_u32(src))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// this thread's bulk stores have finished reading shared memory
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// this thread's bulk stores have completed
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -310,6 +345,10 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // a [box_rows][64] box and 128-byte swizzle.  Returns false on failure.
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
                     uint32_t box_rows);
+
+// Same for fp32 with a [box_rows][32] box (128-byte rows, 128-byte swizzle).
+bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
+                   uint32_t box_rows);
 
 }  // namespace tc
 }  // namespace gdpa
