@@ -153,8 +153,8 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
     for (int t = seg0; t < seg1; ++t) {
         const BwdUnit u = load_unit(prm.units + t);
         if (u.m1 <= u.m0) continue;
-        const uint32_t nkv32 = (uint32_t)((u.nkv + 31) & ~31);
-        const uint32_t idesc_s = idesc_bf16(128, nkv32, false, false);
+        const uint32_t nkv16 = (uint32_t)((u.nkv + 15) & ~15);
+        const uint32_t idesc_s = idesc_bf16(128, nkv16, false, false);
         // S = Q K^T of item j (after the warpgroups have read item j-1's S)
         auto issue_s = [&](uint32_t j) -> bool {
             const uint32_t st = j & 1, ph = (j >> 1) & 1;
@@ -209,7 +209,7 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             // dQ = dS K first, so that its drain overlaps dK += dS^T Q
             if (!mbar_wait(&bars[C::kDSFull], i & 1, ab, 38)) goto drain;
             tc_fence_after();
-            for (uint32_t k = 0; k < nkv32 / 16; ++k)
+            for (uint32_t k = 0; k < nkv16 / 16; ++k)
                 mma_ss(tmem + kColDP,
                        smem_desc_sw128(psbase + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024),
                        smem_desc_sw128(kbase + k * 2048, kHalfBytes, 1024), idesc_dq, k > 0);
@@ -243,7 +243,8 @@ drain:
 // them with one TMA bulk store, or a bulk reduce-add when `atomic`; the warp
 // holding the block's ragged end writes its valid rows from registers.
 // `release` (if any) is arrived by every thread after its last TMEM read.
-// On return the warp's staging area is free again.
+// On return the last bulk store may still be reading the staging area: call
+// staging_release_wait before it is reused.
 __device__ __noinline__ void drain_warp(uint32_t trow, uint32_t col, int ncols, uint8_t* stage,
                                            const CUtensorMap* map, int x0, int y0, float* dst,
                                            int64_t rs, int nrows, bool atomic, float scale,
@@ -298,10 +299,13 @@ __device__ __noinline__ void drain_warp(uint32_t trow, uint32_t col, int ncols, 
             }
         }
     }
-    if (full) {
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
-    }
+}
+
+// The calling warp's bulk stores have read their staging: the area may be
+// reused or handed back.
+__device__ __forceinline__ void staging_release_wait(int lane) {
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
 }
 
 template <int D>
@@ -313,18 +317,8 @@ __device__ __forceinline__ void zero_rows(float* dst, int64_t rs, int nrows, int
     }
 }
 
-// one 32-column chunk of P or dS into the [query x key] SW128 buffer
-__device__ __forceinline__ void store_chunk(uint8_t* ps, int c, int r, const uint32_t (&v)[16]) {
-    uint8_t* rowp = ps + (c >> 1) * kHalfBytes + r * 128;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-        const int chunk = ((c & 1) * 4 + w) ^ (r & 7);
-        *reinterpret_cast<uint4*>(rowp + chunk * 16) =
-            make_uint4(v[4 * w], v[4 * w + 1], v[4 * w + 2], v[4 * w + 3]);
-    }
-}
-
-// 16 columns (half hh of chunk c) of P into the [query x key] SW128 buffer
+// 16 columns (half hh of 32-column chunk c) of P or dS into the [query x key]
+// SW128 buffer
 __device__ __forceinline__ void store_half_chunk(uint8_t* ps, int c, int hh, int r,
                                                  const uint32_t (&v)[8]) {
     uint8_t* rowp = ps + (c >> 1) * kHalfBytes + r * 128;
@@ -351,6 +345,7 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
     uint8_t* stage = ps + wg * kHalfBytes;
     const int64_t rs = (int64_t)prm.H * D;
     uint32_t nu = 0, i = 0;
+    int pending_do = -1;   // dO stage still read by this warp's last dQ stores
     for (int t = seg0; t < seg1; ++t) {
         const BwdUnit u = load_unit(prm.units + t);
         const int h = u.hf & 0xffff;
@@ -360,7 +355,7 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             zero_rows<D>(base, rs, u.nkv, tid);
             continue;
         }
-        const int nch = ((u.nkv + 31) & ~31) >> 5;
+        const int nh = (u.nkv + 15) >> 4;   // 16-column key steps; this warpgroup: s = wg + 2k
         for (int m = u.m0; m < u.m1; ++m, ++i) {
             const int nq = min(kBM, u.lq - m * kBM);
             const bool warp_rows = quarter * 32 < nq;
@@ -374,65 +369,53 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             // last reader, has finished: it precedes dP in the MMA pipe)
             if (m == u.m0 && nu > 0 && !wg_wait(&bars[C::kPSFree], (nu - 1) & 1, ab, 47)) return;
             tc_fence_after();
-            uint32_t pd[2][16];
+            uint32_t pd[4][8];
             if (warp_rows) {
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c = wg + 2 * cc;
-                    if (c < nch) {
-                        // two 16-column halves of the chunk keep register use low
+                for (int k = 0; k < 4; ++k) {
+                    const int sidx = wg + 2 * k;
+                    if (sidx < nh) {
+                        const int col0 = sidx * 16;
+                        uint32_t sv[16], dv[16], pp[8];
+                        tmem_ld16(trow + kColS + col0, sv);
+                        tmem_ld16(trow + kColDP + col0, dv);
+                        tmem_ld_wait();
+                        const bool full = !windowed && col0 + 16 <= u.nkv;
+                        if (!row_ok) {
 #pragma unroll
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int col0 = c * 32 + hh * 16;
-                            uint32_t pp[8];
-                            if (col0 >= u.nkv) {
-                                // past the keys: zeros feed the K-padded GEMMs
+                            for (int e = 0; e < 8; ++e) pp[e] = pd[k][e] = 0u;
+                        } else if (full) {
 #pragma unroll
-                                for (int e = 0; e < 8; ++e) pp[e] = pd[cc][hh * 8 + e] = 0u;
-                            } else {
-                                uint32_t sv[16], dv[16];
-                                tmem_ld16(trow + kColS + col0, sv);
-                                tmem_ld16(trow + kColDP + col0, dv);
-                                tmem_ld_wait();
-                                const bool full = !windowed && col0 + 16 <= u.nkv;
-                                if (!row_ok) {
-#pragma unroll
-                                    for (int e = 0; e < 8; ++e) pp[e] = pd[cc][hh * 8 + e] = 0u;
-                                } else if (full) {
-#pragma unroll
-                                    for (int e = 0; e < 16; e += 2) {
-                                        float a0, d0, a1, d1;
-                                        act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e]), a0, d0);
-                                        act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + 1]), a1, d1);
-                                        pp[e >> 1] = pack_bf16x2(a0, a1);
-                                        pd[cc][hh * 8 + (e >> 1)] =
-                                            pack_bf16x2(__uint_as_float(dv[e]) * d0,
-                                                        __uint_as_float(dv[e + 1]) * d1);
-                                    }
-                                } else {
-#pragma unroll
-                                    for (int e = 0; e < 16; e += 2) {
-                                        float p2[2], d2[2];
-#pragma unroll
-                                        for (int w = 0; w < 2; ++w) {
-                                            const int col = col0 + e + w;
-                                            const int jpos = u.c0 + col;
-                                            bool valid = col < u.nkv;
-                                            if (windowed)
-                                                valid = valid && jpos <= ipos && jpos > ipos - prm.window;
-                                            float a, da;
-                                            act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + w]),
-                                                                  a, da);
-                                            p2[w] = valid ? a : 0.0f;
-                                            d2[w] = valid ? __uint_as_float(dv[e + w]) * da : 0.0f;
-                                        }
-                                        pp[e >> 1] = pack_bf16x2(p2[0], p2[1]);
-                                        pd[cc][hh * 8 + (e >> 1)] = pack_bf16x2(d2[0], d2[1]);
-                                    }
-                                }
+                            for (int e = 0; e < 16; e += 2) {
+                                float a0, d0, a1, d1;
+                                act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e]), a0, d0);
+                                act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + 1]), a1, d1);
+                                pp[e >> 1] = pack_bf16x2(a0, a1);
+                                pd[k][e >> 1] = pack_bf16x2(__uint_as_float(dv[e]) * d0,
+                                                            __uint_as_float(dv[e + 1]) * d1);
                             }
-                            store_half_chunk(ps, c, hh, r, pp);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; e += 2) {
+                                float p2[2], d2[2];
+#pragma unroll
+                                for (int w = 0; w < 2; ++w) {
+                                    const int col = col0 + e + w;
+                                    const int jpos = u.c0 + col;
+                                    bool valid = col < u.nkv;
+                                    if (windowed)
+                                        valid = valid && jpos <= ipos && jpos > ipos - prm.window;
+                                    float a, da;
+                                    act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + w]), a,
+                                                          da);
+                                    p2[w] = valid ? a : 0.0f;
+                                    d2[w] = valid ? __uint_as_float(dv[e + w]) * da : 0.0f;
+                                }
+                                pp[e >> 1] = pack_bf16x2(p2[0], p2[1]);
+                                pd[k][e >> 1] = pack_bf16x2(d2[0], d2[1]);
+                            }
                         }
+                        store_half_chunk(ps, sidx >> 1, sidx & 1, r, pp);
                     }
                 }
             }
@@ -440,20 +423,27 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             mbar_arrive(&bars[C::kSFree]);
             fence_proxy_async_smem();
             mbar_arrive(&bars[C::kPFull]);
+            // the previous tile's dQ bulk stores have long been issued: once
+            // they have read their staging, its dO stage goes back to the
+            // producer
+            if (pending_do >= 0) {
+                staging_release_wait(lane);
+                mbar_arrive(&bars[C::kDOEmpty + pending_do]);
+                pending_do = -1;
+            }
             // dS -> shared once P^T dO has read P
             if (!wg_wait(&bars[C::kPVDone], i & 1, ab, 44)) return;
             if (warp_rows) {
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c = wg + 2 * cc;
-                    if (c < nch) store_chunk(ps, c, r, pd[cc]);
+                for (int k = 0; k < 4; ++k) {
+                    const int sidx = wg + 2 * k;
+                    if (sidx < nh) store_half_chunk(ps, sidx >> 1, sidx & 1, r, pd[k]);
                 }
             }
             fence_proxy_async_smem();
             mbar_arrive(&bars[C::kDSFull]);
             // dQ tile, d columns [64 wg, 64 wg + 64): TMEM -> this warpgroup's
-            // half of the tile's dO buffer (dO's MMAs are done) -> global; the
-            // dO stage goes back to the producer afterwards
+            // half of the tile's dO buffer (dO's MMAs are done) -> global
             if (!wg_wait(&bars[C::kDQFull], i & 1, ab, 45)) return;
             tc_fence_after();
             float* dq = prm.dQ + (int64_t)(u.qt0 + m * kBM) * rs + h * D;
@@ -466,18 +456,22 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                 tc_fence_before();
                 mbar_arrive(&bars[C::kDQFree]);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&bars[C::kDOEmpty + (i & 1)]);
+            pending_do = (int)(i & 1);
         }
         // the unit's dV (warpgroup 0) and dK (warpgroup 1)
         if (!wg_wait(&bars[C::kAccFull], nu & 1, ab, 46)) return;
         tc_fence_after();
+        if (pending_do >= 0) {
+            staging_release_wait(lane);
+            mbar_arrive(&bars[C::kDOEmpty + pending_do]);
+            pending_do = -1;
+        }
         {
             float* dst = (wg == 0 ? prm.dV : prm.dK) + (int64_t)u.kvt0 * rs + h * D;
             drain_warp(trow, wg == 0 ? kColDV : kColDK, D, stage, wg == 0 ? tmDV : tmDK, h * D,
                        u.kvt0, dst, rs, u.nkv, false, wg == 0 ? 1.0f : prm.alpha, quarter, lane,
                        &bars[C::kAccFree]);
-            fence_proxy_async_smem();
+            staging_release_wait(lane);
             mbar_arrive(&bars[C::kPSFree]);
         }
         ++nu;
