@@ -149,6 +149,10 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
     const uint32_t psbase = smem_u32(smem + C::kOffPS);
     constexpr uint32_t idesc_acc = idesc_bf16(128, D, true, true);   // P^T dO, dS^T Q
     constexpr uint32_t idesc_dq = idesc_bf16(128, D, false, true);   // dS K
+    // K-major descriptors of the resident K and V tiles
+    const uint64_t kd_k = smem_desc_sw128(kbase, 16, 1024);
+    const uint64_t vd_k = smem_desc_sw128(vbase, 16, 1024);
+
     uint32_t nu = 0, i = 0;
     for (int t = seg0; t < seg1; ++t) {
         const BwdUnit u = load_unit(prm.units + t);
@@ -162,12 +166,10 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             if (!mbar_wait(&bars[C::kSFree], (j & 1) ^ 1, ab, 33)) return false;
             tc_fence_after();
             const uint32_t qb = smem_u32(smem + C::kOffQ + st * C::kTileBytes);
+            const uint64_t qd = smem_desc_sw128(qb, 16, 1024);
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-                mma_ss(tmem + kColS, smem_desc_sw128(qb + off, 16, 1024),
-                       smem_desc_sw128(kbase + off, 16, 1024), idesc_s, k > 0);
-            }
+            for (int k = 0; k < D / 16; ++k)
+                mma_ss(tmem + kColS, qd + kmajor_step(k), kd_k + kmajor_step(k), idesc_s, k > 0);
             return true;
         };
         // dP = dO V^T of item j (into the columns item j-1's dQ used)
@@ -177,12 +179,10 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             if (!mbar_wait(&bars[C::kDQFree], (j & 1) ^ 1, ab, 35)) return false;
             tc_fence_after();
             const uint32_t dob = smem_u32(smem + C::kOffDO + st * C::kTileBytes);
+            const uint64_t dd = smem_desc_sw128(dob, 16, 1024);
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-                mma_ss(tmem + kColDP, smem_desc_sw128(dob + off, 16, 1024),
-                       smem_desc_sw128(vbase + off, 16, 1024), idesc_s, k > 0);
-            }
+            for (int k = 0; k < D / 16; ++k)
+                mma_ss(tmem + kColDP, dd + kmajor_step(k), vd_k + kmajor_step(k), idesc_s, k > 0);
             mma_commit(&bars[C::kSDFull]);
             return true;
         };

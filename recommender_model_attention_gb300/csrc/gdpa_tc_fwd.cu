@@ -173,11 +173,13 @@ __device__ __forceinline__ bool issue_pv(const PendingPV& pd, uint8_t* smem, uin
     const uint32_t p_tmem = tmem + pd.wg * 256;
     const uint32_t d_o = tmem + pd.wg * 256 + 128;
     const uint32_t vbase = smem_u32(smem + C::kOffV + pd.ks * C::kTileBytes);
-    for (uint32_t k = 0; k < pd.nsteps; ++k) {
+    const uint64_t vdesc = smem_desc_sw128(vbase, kHalfBytes, 1024);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
         // keys [16k, 16k + 16) sit in S chunk k/2's first 16 columns, half k%2
-        const uint64_t b_desc = smem_desc_sw128(vbase + k * 2048, kHalfBytes, 1024);
-        mma_ts(d_o, p_tmem + (k >> 1) * 32 + (k & 1) * 8, b_desc, idesc,
-               (pd.first && k == 0) ? 0u : 1u);
+        if (k < (int)pd.nsteps)
+            mma_ts(d_o, p_tmem + (k >> 1) * 32 + (k & 1) * 8, vdesc + mnmajor_step(k), idesc,
+                   (pd.first && k == 0) ? 0u : 1u);
     }
     mma_commit(&bars[C::kBarKVEmpty + pd.ks]);
     if (pd.last) {
@@ -217,12 +219,12 @@ __device__ void fwd_mma(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             const uint32_t idesc = idesc_bf16(128, n32, false, false);
             const uint32_t qbase = smem_u32(smem + C::kOffQ + qs * C::kTileBytes);
             const uint32_t kbase = smem_u32(smem + C::kOffK + ks * C::kTileBytes);
+            const uint64_t qdesc = smem_desc_sw128(qbase, 16, 1024);
+            const uint64_t kdesc = smem_desc_sw128(kbase, 16, 1024);
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-                mma_ss(tmem + wg * 256, smem_desc_sw128(qbase + off, 16, 1024),
-                       smem_desc_sw128(kbase + off, 16, 1024), idesc, k > 0 ? 1u : 0u);
-            }
+            for (int k = 0; k < D / 16; ++k)
+                mma_ss(tmem + wg * 256, qdesc + kmajor_step(k), kdesc + kmajor_step(k), idesc,
+                       k > 0 ? 1u : 0u);
             mma_commit(&bars[C::kBarSFull + wg]);
             if (have_pend && !issue_pv<D>(pend, smem, bars, tmem, p_use, o_use, ab)) goto drain;
             pend = PendingPV{wg, ks, kph, n32 / 16, kb == tile.kb0, kb == tile.kb1 - 1};

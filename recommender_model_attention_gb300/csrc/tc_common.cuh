@@ -318,6 +318,16 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
     return d;
 }
 
+// Advance of a descriptor's start-address field (16-byte units) for K step
+// k (16 elements) of a 128-byte-swizzled tile stored as 64-element halves of
+// 128 rows: K-major (k-th 32 bytes of the row, next half after 4 steps) and
+// MN-major (16 rows of 128 bytes per step).  Adding it to a descriptor built
+// for the tile's base keeps the other fields (addresses stay below 256 KB).
+__host__ __device__ constexpr uint64_t kmajor_step(int k) {
+    return (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
+}
+__host__ __device__ constexpr uint64_t mnmajor_step(int k) { return (uint64_t)((k * 2048) >> 4); }
+
 // Instruction descriptor of kind::f16 with bf16 A and B, fp32 D.
 //   bits 4-5 D format (1 = f32), 7-9 A format (1 = bf16), 10-12 B format,
 //   15 A MN-major, 16 B MN-major, 17-22 N >> 3, 24-28 M >> 4.
