@@ -24,10 +24,11 @@
 //    activation and the jagged / window mask (masked pairs become exactly 0
 //    after the activation), and write P as packed bf16 into the first half of
 //    each 32-column S chunk they have read (tcgen05.st); P V then takes P
-//    straight from TMEM (A operand in TMEM, one address per K = 16 step).  After the last key block they read O from TMEM,
-//    stage it in the tile's (now consumed) Q buffer and store the valid rows
-//    with coalesced 16-byte stores.  Zero tiles (no valid key) are written
-//    as zeros directly.
+//    straight from TMEM (A operand in TMEM, one address per K = 16 step).
+//    After the last key block they read O from TMEM and stage it (bf16) in
+//    the tile's consumed Q buffer; each warp writes its 32 rows with one TMA
+//    bulk store (the warp at a tile's ragged end with plain stores of its
+//    valid rows).  Zero tiles (no valid key) are written as zeros directly.
 //  * O accumulates P V over key blocks with no rescaling.
 //  * Every barrier wait is bounded; a timeout sets the plan's error word and
 //    the CTA unwinds (waits for its TMA loads and MMAs, frees TMEM, returns).
@@ -206,7 +207,7 @@ __device__ void fwd_mma(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uin
         for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++i) {
             const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
             const int nvalid = min(kBN, tile.lkv - kb * kBN);
-            const uint32_t n32 = (uint32_t)((nvalid + 31) & ~31);
+            const uint32_t n16 = (uint32_t)((nvalid + 15) & ~15);
             // S[wg] holds the previous item's P when that item is this
             // warpgroup's too: its P V goes first (the tensor pipe runs its
             // MMAs in issue order, so the S overwrite follows the P read)
@@ -216,7 +217,7 @@ __device__ void fwd_mma(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             }
             if (!mbar_wait(&bars[C::kBarKFull + ks], kph, ab, 4)) goto drain;
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16(128, n32, false, false);
+            const uint32_t idesc = idesc_bf16(128, n16, false, false);
             const uint32_t qbase = smem_u32(smem + C::kOffQ + qs * C::kTileBytes);
             const uint32_t kbase = smem_u32(smem + C::kOffK + ks * C::kTileBytes);
             const uint64_t qdesc = smem_desc_sw128(qbase, 16, 1024);
@@ -227,7 +228,7 @@ __device__ void fwd_mma(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uin
                        k > 0 ? 1u : 0u);
             mma_commit(&bars[C::kBarSFull + wg]);
             if (have_pend && !issue_pv<D>(pend, smem, bars, tmem, p_use, o_use, ab)) goto drain;
-            pend = PendingPV{wg, ks, kph, n32 / 16, kb == tile.kb0, kb == tile.kb1 - 1};
+            pend = PendingPV{wg, ks, kph, n16 / 16, kb == tile.kb0, kb == tile.kb1 - 1};
             have_pend = true;
         }
         ++a;
@@ -251,8 +252,8 @@ __device__ __forceinline__ void store_zero_rows(const FwdTile& tile, const FwdPa
 }
 
 template <int D, int ACT>
-__device__ void fwd_compute(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
-                            int seg0, int seg1, const Abort& ab) {
+__device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, uint8_t* smem,
+                            uint64_t* bars, uint32_t tmem, int seg0, int seg1, const Abort& ab) {
     using C = FwdCfg<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int grp = (warp - 2) >> 2;                 // warpgroup 0..3
@@ -297,6 +298,7 @@ __device__ void fwd_compute(const FwdParams& prm, uint8_t* smem, uint64_t* bars,
 #pragma unroll 1
                         for (int hh = 0; hh < 2; ++hh) {
                             const int col0 = c * 32 + hh * 16;
+                            if (col0 >= nvalid) break;   // GEMMs stop at 16-column granularity
                             uint32_t sv[16], pk[8];
                             tmem_ld16(s_tmem + col0, sv);
                             tmem_ld_wait();
@@ -361,10 +363,35 @@ __device__ void fwd_compute(const FwdParams& prm, uint8_t* smem, uint64_t* bars,
         }
         tc_fence_before();
         mbar_arrive(&bars[C::kBarOFree + wg]);
-        // the whole warpgroup's staging writes before anyone reads them back
-        mbar_arrive(&bars[C::kBarStage + grp]);
-        if (!wg_wait(&bars[C::kBarStage + grp], (o_use - 1) & 1, ab, 9)) return;
-        {
+        if constexpr (D == 128) {
+            // each warp writes its own 32 rows: one TMA bulk store of the
+            // [32 x 64] box it staged (128-byte rows, 128-byte swizzle), or
+            // plain stores of the valid rows for the tile's ragged warp
+            const int row0 = quarter * 32;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (row0 + 32 <= tile.nq) {
+                if (lane == 0) {
+                    tma_store_2d(tmO, stage + quarter * 4096, tile.h * D + part * (D / 2),
+                                 tile.qt0 + row0);
+                    bulk_commit();
+                    bulk_wait_read_all();
+                }
+                __syncwarp();
+            } else if (row0 < tile.nq) {
+                const int64_t rs = (int64_t)prm.H * D;
+                __nv_bfloat16* obase = prm.O + (int64_t)tile.qt0 * rs + tile.h * D + part * (D / 2);
+                for (int idx = lane; idx < (tile.nq - row0) * kChunks; idx += 32) {
+                    const int row = row0 + idx / kChunks, ch = idx % kChunks;
+                    const uint4 w = *reinterpret_cast<const uint4*>(stage + row * kRowBytes +
+                                                                    ((ch ^ (row & kSwz)) * 16));
+                    *reinterpret_cast<uint4*>(obase + (int64_t)row * rs + ch * 8) = w;
+                }
+            }
+        } else {
+            // the whole warpgroup's staging writes before anyone reads them back
+            mbar_arrive(&bars[C::kBarStage + grp]);
+            if (!wg_wait(&bars[C::kBarStage + grp], (o_use - 1) & 1, ab, 9)) return;
             const int64_t rs = (int64_t)prm.H * D;
             __nv_bfloat16* obase = prm.O + (int64_t)tile.qt0 * rs + tile.h * D + part * (D / 2);
             for (int idx = tid; idx < tile.nq * kChunks; idx += 128) {
@@ -383,7 +410,8 @@ __device__ void fwd_compute(const FwdParams& prm, uint8_t* smem, uint64_t* bars,
 template <int D, int ACT>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-              const __grid_constant__ CUtensorMap tmV, const FwdParams prm) {
+              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+              const FwdParams prm) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -419,6 +447,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tma_prefetch_desc(&tmQ);
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
+        tma_prefetch_desc(&tmO);
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
@@ -434,7 +463,9 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (lane == 0) fwd_mma<D>(prm, smem, bars, tmem, seg0, seg1, ab);
         __syncwarp();
     } else {
-        fwd_compute<D, ACT>(prm, smem, bars, tmem, seg0, seg1, ab);
+        fwd_compute<D, ACT>(prm, &tmO, smem, bars, tmem, seg0, seg1, ab);
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -452,13 +483,13 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
 
 template <int D, int ACT>
 gdpa_status launch(int S, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                   const FwdParams& prm, cudaStream_t st) {
+                   const CUtensorMap& mo, const FwdParams& prm, cudaStream_t st) {
     using C = FwdCfg<D>;
     auto kern = tc_fwd_kernel<D, ACT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return GDPA_ERR_CUDA;
-    kern<<<S, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, prm);
+    kern<<<S, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mo, prm);
     return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
@@ -470,14 +501,15 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
                               const void* v, void* o, float alpha, int act, cudaStream_t st) {
     if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
     if (Tq == 0) return GDPA_OK;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     const uint64_t row = (uint64_t)H * d;
     const uint64_t kv_rows = Tkv > 0 ? (uint64_t)Tkv : 1;
     const void* kp = Tkv > 0 ? k : q;
     const void* vp = Tkv > 0 ? v : q;
     if (!tc::make_tmap_bf16(&mq, q, (uint64_t)Tq, row, 128) ||
         !tc::make_tmap_bf16(&mk, kp, kv_rows, row, 128) ||
-        !tc::make_tmap_bf16(&mv, vp, kv_rows, row, 128))
+        !tc::make_tmap_bf16(&mv, vp, kv_rows, row, 128) ||
+        !tc::make_tmap_bf16(&mo, o, (uint64_t)Tq, row, 32))
         return GDPA_ERR_CUDA;
     FwdParams prm;
     prm.tiles = tiles;
@@ -493,9 +525,9 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
     prm.timing = times != nullptr && smid != nullptr;
     gdpa_status s = GDPA_OK;
     if (d == 128) {
-        GDPA_DISPATCH_ACT(act, A, s = launch<128, A>(S, mq, mk, mv, prm, st))
+        GDPA_DISPATCH_ACT(act, A, s = launch<128, A>(S, mq, mk, mv, mo, prm, st))
     } else {
-        GDPA_DISPATCH_ACT(act, A, s = launch<64, A>(S, mq, mk, mv, prm, st))
+        GDPA_DISPATCH_ACT(act, A, s = launch<64, A>(S, mq, mk, mv, mo, prm, st))
     }
     return s;
 }
