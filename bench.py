@@ -71,6 +71,25 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(w, rank):
+    """Tensor seed of a rank: every rank draws its own batch of the same shape."""
+    return 1000 + w.index + 7919 * rank
+
+
+def reduce_across_ranks(ms, flops, device):
+    """(max of `ms`, sum of `flops`) over the process group; identity when the
+    job is not distributed.  Whole-job throughput = summed work / slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms), float(flops)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    f = torch.tensor([float(flops)], dtype=torch.float64, device=device)
+    dist.all_reduce(f, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(f.item())
+
+
 def useful_pairs(q_off, kv_off, mask, window):
     """Valid (query, key) pairs summed over samples (per head), closed form."""
     lq = np.diff(np.asarray(q_off, dtype=np.int64))
@@ -247,7 +266,7 @@ def main():
         from workloads import draw_lengths
         lq, lkv = draw_lengths(w)
         lengths = (lq[:args.samples], lkv[:args.samples])
-    x = make_inputs(w, device="cuda", seed=1000 + w.index + 7919 * rank, lengths=lengths)
+    x = make_inputs(w, device="cuda", seed=rank_seed(w, rank), lengths=lengths)
     stream = torch.cuda.current_stream()
     plan = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window)
     f32 = torch.float32
@@ -306,15 +325,12 @@ def main():
     clk = clocks.stop()
     launches = plan.launches - launches0
     plan.check()
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms, job_flops = reduce_across_ranks(start.elapsed_time(end),
+                                                (fwd_flops + bwd_flops) * args.steps, "cuda")
     ms_step = elapsed_ms / args.steps
     fwd_ms = float(np.mean([a.elapsed_time(b) for a, b, _ in ev]))
     bwd_ms = float(np.mean([b.elapsed_time(c) for _, b, c in ev])) if backward else 0.0
-    value = (fwd_flops + bwd_flops) * world / (ms_step * 1e-3) / 1e12
+    value = job_flops / (elapsed_ms * 1e-3) / 1e12
 
     # roofline of the dominant phase (kernel time measured live above)
     if bwd_ms > fwd_ms:
@@ -363,11 +379,13 @@ def main():
             e2e_step()
         b.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = a.elapsed_time(b) / n_e2e
+        e2e_total, e2e_flops = reduce_across_ranks(a.elapsed_time(b),
+                                                   (fwd_flops + bwd_flops) * n_e2e, "cuda")
+        e2e_ms = e2e_total / n_e2e
         h2d = input_bytes
         d2h = o.numel() * o.element_size() + (sum(t.numel() * 4 for t in (dq, dk, dv))
                                               if backward else 0)
-        e2e = {"value": (fwd_flops + bwd_flops) / (e2e_ms * 1e-3) / 1e12 * world, "unit": UNIT,
+        e2e = {"value": e2e_flops / (e2e_total * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": e2e_ms}
 
