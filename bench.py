@@ -38,8 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # launch by algorithmic bytes).  Valid only for the kernel sources they were
 # measured on (hash of the kernel's source files); otherwise reported null.
 TRAFFIC_RATIO = {
-    "gdpa_fwd": ("84d7d49d07a50c73", 0.9728),
-    "gdpa_bwd": ("b3d191d22fbfd4fb", 1.0212),
+    "gdpa_fwd": ("9e37cbba0968c169", 0.9614),
+    "gdpa_bwd": ("fd5b1884e60a8c1d", 1.0212),
 }
 KERNEL_SOURCES = {
     "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "act.cuh"),

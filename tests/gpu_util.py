@@ -32,23 +32,28 @@ def to_dev(case, device="cuda"):
 
 
 def run_gpu(gd, x, H, d, alpha, act, mask="none", window=0, kernel="auto", backward=True,
-            sched="zigzag"):
+            sched="zigzag", num_sms=0, stream=None):
     import torch
-    plan = gd.Plan(x["q_off"], x["kv_off"], H, d, mask=mask, window=window, sched=sched)
+    plan = gd.Plan(x["q_off"], x["kv_off"], H, d, mask=mask, window=window, sched=sched,
+                   num_sms=num_sms, stream=stream)
     plan.set_kernel(kernel)
-    o = gd.gdpa_fwd(plan, x["q"], x["k"], x["v"], alpha=alpha, act=act)
+    if stream is not None:
+        stream.wait_stream(torch.cuda.current_stream())
+    o = gd.gdpa_fwd(plan, x["q"], x["k"], x["v"], alpha=alpha, act=act, stream=stream)
     grads = None
     if backward:
-        grads = gd.gdpa_bwd(plan, x["q"], x["k"], x["v"], x["do"], alpha=alpha, act=act)
-    plan.check()
+        grads = gd.gdpa_bwd(plan, x["q"], x["k"], x["v"], x["do"], alpha=alpha, act=act,
+                            stream=stream)
+    plan.check(stream)
     torch.cuda.synchronize()
     return plan, o, grads
 
 
 def compare_full(gd, x, H, d, alpha, act, dtype, mask="none", window=0, kernel="auto",
-                 backward=True):
-    """Whole-batch comparison; returns the max relative errors."""
-    plan, o, grads = run_gpu(gd, x, H, d, alpha, act, mask, window, kernel, backward)
+                 backward=True, **launch):
+    """Whole-batch comparison; returns the max relative errors.  `launch` goes
+    to run_gpu (sched, num_sms, stream)."""
+    plan, o, grads = run_gpu(gd, x, H, d, alpha, act, mask, window, kernel, backward, **launch)
     args = (x["q_off"], x["kv_off"], x["q"], x["k"], x["v"])
     errs = {"o": max_rel(ref.to_f64(o), ref.fwd(*args, alpha, act, mask, window))}
     if backward:

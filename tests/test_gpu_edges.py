@@ -1,0 +1,123 @@
+"""GPU parity on edge cases of the jagged layout and of the launch.
+
+Same tolerances as the main parity file (bf16 inputs: 1e-2 of max|ref| for
+O, dQ, dK, dV separately).  Cases: a batch of zero samples, a batch whose
+lengths are all zero, lengths on and next to the 128-row tile boundaries,
+many heads, d = 64 with the causal window in the backward pass, the
+round-robin dealing policy, fewer persistent CTAs than SMs, and a launch on
+a side stream.
+"""
+
+import numpy as np
+import pytest
+
+from gpu_util import TOL, compare_full, to_dev
+from workloads import offsets_from_lengths
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gd():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import recommender_model_attention_gb300 as g
+    g.build()
+    return g
+
+
+def _case(lq, lkv, H, d, seed):
+    import torch
+    qo, ko = offsets_from_lengths(np.asarray(lq)), offsets_from_lengths(np.asarray(lkv))
+    g = torch.Generator().manual_seed(seed)
+    x = {"q_off": qo, "kv_off": ko}
+    for n, rows in (("q", qo[-1]), ("k", ko[-1]), ("v", ko[-1]), ("do", qo[-1])):
+        x[n] = (torch.randn((int(rows), H, d), generator=g) / 4).to(torch.bfloat16)
+    return to_dev(x)
+
+
+def _assert(errs, tol=TOL["bf16"]):
+    for name, e in errs.items():
+        assert e <= tol, "%s: max rel err %.3e > %.1e (%s)" % (name, e, tol, errs)
+
+
+def test_zero_samples(gd):
+    import torch
+    x = _case([], [], 2, 128, 0)
+    plan = gd.Plan(x["q_off"], x["kv_off"], 2, 128)
+    assert plan.sizes()[:2] == (0, 0)
+    o = gd.gdpa_fwd(plan, x["q"], x["k"], x["v"])
+    dq, dk, dv = gd.gdpa_bwd(plan, x["q"], x["k"], x["v"], x["do"])
+    plan.check()
+    assert o.shape == (0, 2, 128) and dq.numel() == dk.numel() == dv.numel() == 0
+    assert plan.launches == 0
+    plan.destroy()
+    torch.cuda.synchronize()
+
+
+def test_all_lengths_zero_keys(gd):
+    # queries but no keys anywhere: O = 0 and dQ = 0 (zero tiles, cleared dQ)
+    import torch
+    x = _case([5, 130, 0, 256], [0, 0, 0, 0], 2, 128, 1)
+    plan = gd.Plan(x["q_off"], x["kv_off"], 2, 128)
+    o = torch.full_like(x["q"], 3.0)
+    gd.gdpa_fwd(plan, x["q"], x["k"], x["v"], o=o)
+    dq = torch.full(x["q"].shape, 3.0, device="cuda")
+    dk = torch.empty((0, 2, 128), device="cuda")
+    gd.gdpa_bwd(plan, x["q"], x["k"], x["v"], x["do"], dq, dk, dk.clone())
+    plan.check()
+    assert torch.all(o == 0) and torch.all(dq == 0)
+    plan.destroy()
+
+
+@pytest.mark.parametrize("act", ["gelu_erf", "silu"])
+def test_tile_boundary_lengths(gd, act):
+    lens = [127, 128, 129, 255, 256, 257, 383, 384, 385, 1]
+    x = _case(lens, lens[::-1], 2, 128, 2)
+    _assert(compare_full(gd, x, 2, 128, 128 ** -0.5, act, "bf16"))
+
+
+def test_tile_boundary_lengths_window(gd):
+    lens = [127, 128, 129, 255, 256, 257, 511, 512, 513]
+    x = _case(lens, lens, 2, 128, 3)
+    _assert(compare_full(gd, x, 2, 128, 128 ** -0.5, "gelu_tanh", "bf16", "causal_window", 128))
+
+
+def test_many_heads(gd):
+    x = _case([200, 37, 300], [150, 260, 9], 16, 64, 4)
+    _assert(compare_full(gd, x, 16, 64, 0.125, "gelu_erf", "bf16"))
+
+
+@pytest.mark.parametrize("window", [1, 64, 129])
+def test_d64_window_backward(gd, window):
+    lens = [300, 129, 64, 500]
+    x = _case(lens, lens, 2, 64, 5 + window)
+    _assert(compare_full(gd, x, 2, 64, 0.125, "gelu_taylor6", "bf16", "causal_window", window))
+
+
+@pytest.mark.parametrize("sched", ["round_robin", "zigzag"])
+@pytest.mark.parametrize("num_sms", [1, 7])
+def test_dealing_and_cta_count(gd, sched, num_sms):
+    x = _case([400, 3, 129, 0, 260, 77], [90, 300, 128, 5, 0, 200], 2, 128, 6)
+    _assert(compare_full(gd, x, 2, 128, 128 ** -0.5, "gelu_erf", "bf16", sched=sched,
+                         num_sms=num_sms))
+
+
+def test_side_stream(gd):
+    import torch
+    x = _case([300, 64, 129], [200, 128, 1], 2, 128, 7)
+    s = torch.cuda.Stream()
+    _assert(compare_full(gd, x, 2, 128, 128 ** -0.5, "silu", "bf16", stream=s))
+
+
+def test_repeat_calls_identical_forward(gd):
+    # the forward has no atomics: repeated launches give identical bytes
+    import torch
+    x = _case([300, 64, 129, 700], [200, 128, 1, 90], 2, 128, 8)
+    plan = gd.Plan(x["q_off"], x["kv_off"], 2, 128)
+    o1 = gd.gdpa_fwd(plan, x["q"], x["k"], x["v"])
+    o2 = gd.gdpa_fwd(plan, x["q"], x["k"], x["v"])
+    plan.check()
+    assert torch.equal(o1, o2)
+    plan.destroy()
