@@ -15,18 +15,21 @@
 //
 // Roles: warp 0 TMA producer (K, V once per unit; Q and dO per query tile
 // through 2-stage rings); warp 1 tcgen05.mma issuer; warps 2-9 two
-// warpgroups that turn S and dP (TMEM) into P and dS (bf16, shared memory),
-// warpgroup j taking the 32-column key chunks c = j, j + 2, and drain dQ (j:
-// d columns [64j, 64j + 64)), dV (j = 0) and dK (j = 1) from TMEM through
-// its own half of the shared buffer.  The next query tile's S = Q K^T is
-// issued as soon as both warpgroups have read S.  Per query tile:
+// warpgroups that turn S and dP (TMEM) into dS and P (bf16, shared memory),
+// warpgroup j taking the 16-column key steps j, j + 2, ..., and drain dQ (j:
+// d columns [64j, 64j + 64)), dV (j = 0) and dK (j = 1) from TMEM.  Per
+// query tile:
 //     S  = Q K^T   -> TMEM [0, 128)      dP = dO V^T -> TMEM [128, 256)
-//     P, dS        -> one 32 KB shared buffer, P first, then dS
-//     dV += P^T dO -> TMEM [256, 384)    dK += dS^T Q -> TMEM [384, 512)
-//     dQ  = dS K   -> TMEM [128, 256) (dP's columns, already read), issued
-//                     before dK and drained through the tile's dO buffer
-// P^T and dS^T are the MN-major reading of the [query x key] buffer, and Q,
-// dO, K are the MN-major reading of their [row x d] tiles, so nothing is
+//     dS           -> the 32 KB shared [query x key] buffer
+//     dQ  = dS K   -> TMEM [128, 256) (dP's columns, already read)
+//     dK += dS^T Q -> TMEM [384, 512)
+//     P            -> the same buffer, once dQ and dK have read dS
+//     dV += P^T dO -> TMEM [256, 384), while the warpgroups drain dQ through
+//                     the tile's Q buffer (its MMAs are done)
+// The next tile's S is issued as soon as both warpgroups have read S, its dP
+// once dQ is drained; dV stays off the warpgroups' critical path.  P^T and
+// dS^T are the MN-major reading of the [query x key] buffer, and Q, dO, K
+// are the MN-major reading of their [row x d] tiles, so nothing is
 // transposed in memory.  Every wait is bounded (timeouts set the plan's
 // error word; the CTA unwinds, frees TMEM and returns).
 #include <cuda_bf16.h>
@@ -56,7 +59,7 @@ struct BwdCfg {
     static constexpr int kOffBar = kOffPS + 128 * 128 * 2;
     enum {
         kKVFull = 0, kKVEmpty, kQFull, kQFull1, kQEmpty, kQEmpty1, kDOFull, kDOFull1, kDOEmpty,
-        kDOEmpty1, kSDFull, kSFree, kDQFree, kPFull, kPVDone, kDSFull, kDQFull, kAccFull,
+        kDOEmpty1, kSDFull, kSFree, kDQFree, kPFull, kPVDone, kDSFull, kDKDone, kAccFull,
         kAccFree, kStage, kStage1, kPSFree, kMmaDone, kNumBars
     };
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
@@ -195,34 +198,34 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             const uint32_t nq32 = (uint32_t)((nq + 31) & ~31);
             const uint32_t qb = smem_u32(smem + C::kOffQ + s * C::kTileBytes);
             const uint32_t dob = smem_u32(smem + C::kOffDO + s * C::kTileBytes);
-            // dV += P^T dO
-            if (!mbar_wait(&bars[C::kPFull], i & 1, ab, 36)) goto drain;
+            // dQ = dS K (into dP's columns, already read) and dK += dS^T Q
+            if (!mbar_wait(&bars[C::kDSFull], i & 1, ab, 38)) goto drain;
             if (first && !mbar_wait(&bars[C::kAccFree], (nu & 1) ^ 1, ab, 37)) goto drain;
+            tc_fence_after();
+            for (uint32_t k = 0; k < nkv16 / 16; ++k)
+                mma_ss(tmem + kColDP,
+                       smem_desc_sw128(psbase + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024),
+                       smem_desc_sw128(kbase + k * 2048, kHalfBytes, 1024), idesc_dq, k > 0);
+            for (uint32_t k = 0; k < nq32 / 16; ++k)
+                mma_ss(tmem + kColDK, smem_desc_sw128(psbase + k * 2048, kHalfBytes, 1024),
+                       smem_desc_sw128(qb + k * 2048, kHalfBytes, 1024), idesc_acc,
+                       (first && k == 0) ? 0u : 1u);
+            mma_commit(&bars[C::kDKDone]);
+            // the next tile's scores (the warpgroups have read this tile's S)
+            if (!last && !issue_s(i + 1)) goto drain;
+            // dV += P^T dO once P has replaced dS in shared memory
+            if (!mbar_wait(&bars[C::kPFull], i & 1, ab, 36)) goto drain;
             tc_fence_after();
             for (uint32_t k = 0; k < nq32 / 16; ++k)
                 mma_ss(tmem + kColDV, smem_desc_sw128(psbase + k * 2048, kHalfBytes, 1024),
                        smem_desc_sw128(dob + k * 2048, kHalfBytes, 1024), idesc_acc,
                        (first && k == 0) ? 0u : 1u);
             mma_commit(&bars[C::kPVDone]);
-            // the next tile's scores while this tile's dS is being written
-            if (!last && !issue_s(i + 1)) goto drain;
-            // dQ = dS K first, so that its drain overlaps dK += dS^T Q
-            if (!mbar_wait(&bars[C::kDSFull], i & 1, ab, 38)) goto drain;
-            tc_fence_after();
-            for (uint32_t k = 0; k < nkv16 / 16; ++k)
-                mma_ss(tmem + kColDP,
-                       smem_desc_sw128(psbase + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024),
-                       smem_desc_sw128(kbase + k * 2048, kHalfBytes, 1024), idesc_dq, k > 0);
-            mma_commit(&bars[C::kDQFull]);
-            for (uint32_t k = 0; k < nq32 / 16; ++k)
-                mma_ss(tmem + kColDK, smem_desc_sw128(psbase + k * 2048, kHalfBytes, 1024),
-                       smem_desc_sw128(qb + k * 2048, kHalfBytes, 1024), idesc_acc,
-                       (first && k == 0) ? 0u : 1u);
-            mma_commit(&bars[C::kQEmpty + s]);
+            mma_commit(&bars[C::kDOEmpty + s]);
             if (last) {
                 mma_commit(&bars[C::kAccFull]);
                 mma_commit(&bars[C::kKVEmpty]);
-            } else if (!issue_dp(i + 1)) {
+            } else if (!issue_dp(i + 1)) {   // once this tile's dQ is drained
                 goto drain;
             }
         }
@@ -345,7 +348,7 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
     uint8_t* stage = ps + wg * kHalfBytes;
     const int64_t rs = (int64_t)prm.H * D;
     uint32_t nu = 0, i = 0;
-    int pending_do = -1;   // dO stage still read by this warp's last dQ stores
+    int pending_q = -1;   // Q stage still read by this warp's last dQ stores
     for (int t = seg0; t < seg1; ++t) {
         const BwdUnit u = load_unit(prm.units + t);
         const int h = u.hf & 0xffff;
@@ -363,36 +366,44 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             const bool row_ok = r < nq;
             const bool windowed = prm.mask == GDPA_MASK_CAUSAL_WINDOW;
             if (!wg_wait(&bars[C::kSDFull], i & 1, ab, 43)) return;
+            // the previous tile's dQ bulk stores have long been issued: once
+            // they have read their staging, its Q stage goes back to the
+            // producer
+            if (pending_q >= 0) {
+                staging_release_wait(lane);
+                mbar_arrive(&bars[C::kQEmpty + pending_q]);
+                pending_q = -1;
+            }
             // the shared buffer must be clear of the previous unit's dK, dV
-            // drain by both warpgroups before P goes in (within a unit, S and
-            // dP being ready means the previous tile's dK MMA, the buffer's
-            // last reader, has finished: it precedes dP in the MMA pipe)
+            // drain by both warpgroups and of the previous tile's P (read by
+            // its dV MMA) before dS goes in
             if (m == u.m0 && nu > 0 && !wg_wait(&bars[C::kPSFree], (nu - 1) & 1, ab, 47)) return;
+            if (!wg_wait(&bars[C::kPVDone], (i & 1) ^ 1, ab, 44)) return;
             tc_fence_after();
-            uint32_t pd[4][8];
+            uint32_t pp[4][8];
             if (warp_rows) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int sidx = wg + 2 * k;
                     if (sidx < nh) {
                         const int col0 = sidx * 16;
-                        uint32_t sv[16], dv[16], pp[8];
+                        uint32_t sv[16], dv[16], pd[8];
                         tmem_ld16(trow + kColS + col0, sv);
                         tmem_ld16(trow + kColDP + col0, dv);
                         tmem_ld_wait();
                         const bool full = !windowed && col0 + 16 <= u.nkv;
                         if (!row_ok) {
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) pp[e] = pd[k][e] = 0u;
+                            for (int e = 0; e < 8; ++e) pp[k][e] = pd[e] = 0u;
                         } else if (full) {
 #pragma unroll
                             for (int e = 0; e < 16; e += 2) {
                                 float a0, d0, a1, d1;
                                 act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e]), a0, d0);
                                 act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + 1]), a1, d1);
-                                pp[e >> 1] = pack_bf16x2(a0, a1);
-                                pd[k][e >> 1] = pack_bf16x2(__uint_as_float(dv[e]) * d0,
-                                                            __uint_as_float(dv[e + 1]) * d1);
+                                pp[k][e >> 1] = pack_bf16x2(a0, a1);
+                                pd[e >> 1] = pack_bf16x2(__uint_as_float(dv[e]) * d0,
+                                                         __uint_as_float(dv[e + 1]) * d1);
                             }
                         } else {
 #pragma unroll
@@ -411,43 +422,34 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                                     p2[w] = valid ? a : 0.0f;
                                     d2[w] = valid ? __uint_as_float(dv[e + w]) * da : 0.0f;
                                 }
-                                pp[e >> 1] = pack_bf16x2(p2[0], p2[1]);
-                                pd[k][e >> 1] = pack_bf16x2(d2[0], d2[1]);
+                                pp[k][e >> 1] = pack_bf16x2(p2[0], p2[1]);
+                                pd[e >> 1] = pack_bf16x2(d2[0], d2[1]);
                             }
                         }
-                        store_half_chunk(ps, sidx >> 1, sidx & 1, r, pp);
+                        store_half_chunk(ps, sidx >> 1, sidx & 1, r, pd);
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(&bars[C::kSFree]);
             fence_proxy_async_smem();
-            mbar_arrive(&bars[C::kPFull]);
-            // the previous tile's dQ bulk stores have long been issued: once
-            // they have read their staging, its dO stage goes back to the
-            // producer
-            if (pending_do >= 0) {
-                staging_release_wait(lane);
-                mbar_arrive(&bars[C::kDOEmpty + pending_do]);
-                pending_do = -1;
-            }
-            // dS -> shared once P^T dO has read P
-            if (!wg_wait(&bars[C::kPVDone], i & 1, ab, 44)) return;
+            mbar_arrive(&bars[C::kDSFull]);
+            // P -> shared once dQ = dS K and dK += dS^T Q have read dS
+            if (!wg_wait(&bars[C::kDKDone], i & 1, ab, 45)) return;
             if (warp_rows) {
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int sidx = wg + 2 * k;
-                    if (sidx < nh) store_half_chunk(ps, sidx >> 1, sidx & 1, r, pd[k]);
+                    if (sidx < nh) store_half_chunk(ps, sidx >> 1, sidx & 1, r, pp[k]);
                 }
             }
             fence_proxy_async_smem();
-            mbar_arrive(&bars[C::kDSFull]);
+            mbar_arrive(&bars[C::kPFull]);
             // dQ tile, d columns [64 wg, 64 wg + 64): TMEM -> this warpgroup's
-            // half of the tile's dO buffer (dO's MMAs are done) -> global
-            if (!wg_wait(&bars[C::kDQFull], i & 1, ab, 45)) return;
+            // half of the tile's Q buffer (its MMAs are done) -> global
             tc_fence_after();
             float* dq = prm.dQ + (int64_t)(u.qt0 + m * kBM) * rs + h * D;
-            uint8_t* dq_stage = smem + C::kOffDO + (i & 1) * C::kTileBytes + wg * kHalfBytes;
+            uint8_t* dq_stage = smem + C::kOffQ + (i & 1) * C::kTileBytes + wg * kHalfBytes;
             if (D == 128 || wg == 0) {
                 drain_warp(trow, kColDP + 64 * wg, 64, dq_stage, tmDQ, h * D + 64 * wg,
                            u.qt0 + m * kBM, dq + 64 * wg, rs, nq, atomic_dq, prm.alpha, quarter,
@@ -456,15 +458,15 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                 tc_fence_before();
                 mbar_arrive(&bars[C::kDQFree]);
             }
-            pending_do = (int)(i & 1);
+            pending_q = (int)(i & 1);
         }
         // the unit's dV (warpgroup 0) and dK (warpgroup 1)
         if (!wg_wait(&bars[C::kAccFull], nu & 1, ab, 46)) return;
         tc_fence_after();
-        if (pending_do >= 0) {
+        if (pending_q >= 0) {
             staging_release_wait(lane);
-            mbar_arrive(&bars[C::kDOEmpty + pending_do]);
-            pending_do = -1;
+            mbar_arrive(&bars[C::kQEmpty + pending_q]);
+            pending_q = -1;
         }
         {
             float* dst = (wg == 0 ? prm.dV : prm.dK) + (int64_t)u.kvt0 * rs + h * D;
@@ -497,10 +499,10 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         t_start = globaltimer();
         const uint32_t counts[C::kNumBars] = {
             1, 1,                 // kv full / empty
-            1, 1, 1, 1,           // q full x2, q empty x2
-            1, 1, 256, 256,       // dO full x2, dO empty x2 (warpgroups, after dQ)
+            1, 1, 256, 256,       // q full x2, q empty x2 (warpgroups, after dQ staging)
+            1, 1, 1, 1,           // dO full x2, dO empty x2
             1, 256, 256,          // sd full, s free, dq free
-            256, 1, 256, 1,       // p full, pv done, ds full, dq full
+            256, 1, 256, 1,       // p full, pv done, ds full, dk done
             1, 256, 128, 128,     // acc full, acc free, stage x2
             256, 1                // ps free, mma done
         };
