@@ -14,7 +14,8 @@
 // a cleared dQ.
 //
 // Roles: warp 0 TMA producer (K, V once per unit; Q and dO per query tile
-// through 2-stage rings); warp 1 tcgen05.mma issuer; warps 2-9 two
+// through 2-stage rings); warp 1 tcgen05.mma issuer (the whole warp runs
+// the issue code, one elected lane issues); warps 2-9 two
 // warpgroups that turn S and dP (TMEM) into dS and P (bf16, shared memory),
 // warpgroup j taking the 16-column key steps j, j + 2, ..., and drain dQ (j:
 // d columns [64j, 64j + 64)), dV (j = 0) and dK (j = 1) from TMEM.  Per
@@ -165,8 +166,8 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
         // S = Q K^T of item j (after the warpgroups have read item j-1's S)
         auto issue_s = [&](uint32_t j) -> bool {
             const uint32_t st = j & 1, ph = (j >> 1) & 1;
-            if (!mbar_wait(&bars[C::kQFull + st], ph, ab, 32)) return false;
-            if (!mbar_wait(&bars[C::kSFree], (j & 1) ^ 1, ab, 33)) return false;
+            if (!wg_wait(&bars[C::kQFull + st], ph, ab, 32)) return false;
+            if (!wg_wait(&bars[C::kSFree], (j & 1) ^ 1, ab, 33)) return false;
             tc_fence_after();
             const uint32_t qb = smem_u32(smem + C::kOffQ + st * C::kTileBytes);
             const uint64_t qd = smem_desc_sw128(qb, 16, 1024);
@@ -178,8 +179,8 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
         // dP = dO V^T of item j (into the columns item j-1's dQ used)
         auto issue_dp = [&](uint32_t j) -> bool {
             const uint32_t st = j & 1, ph = (j >> 1) & 1;
-            if (!mbar_wait(&bars[C::kDOFull + st], ph, ab, 34)) return false;
-            if (!mbar_wait(&bars[C::kDQFree], (j & 1) ^ 1, ab, 35)) return false;
+            if (!wg_wait(&bars[C::kDOFull + st], ph, ab, 34)) return false;
+            if (!wg_wait(&bars[C::kDQFree], (j & 1) ^ 1, ab, 35)) return false;
             tc_fence_after();
             const uint32_t dob = smem_u32(smem + C::kOffDO + st * C::kTileBytes);
             const uint64_t dd = smem_desc_sw128(dob, 16, 1024);
@@ -189,7 +190,7 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             mma_commit(&bars[C::kSDFull]);
             return true;
         };
-        if (!mbar_wait(&bars[C::kKVFull], nu & 1, ab, 31)) goto drain;
+        if (!wg_wait(&bars[C::kKVFull], nu & 1, ab, 31)) goto drain;
         if (!issue_s(i) || !issue_dp(i)) goto drain;
         for (int m = u.m0; m < u.m1; ++m, ++i) {
             const uint32_t s = i & 1;
@@ -199,8 +200,8 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             const uint32_t qb = smem_u32(smem + C::kOffQ + s * C::kTileBytes);
             const uint32_t dob = smem_u32(smem + C::kOffDO + s * C::kTileBytes);
             // dQ = dS K (into dP's columns, already read) and dK += dS^T Q
-            if (!mbar_wait(&bars[C::kDSFull], i & 1, ab, 38)) goto drain;
-            if (first && !mbar_wait(&bars[C::kAccFree], (nu & 1) ^ 1, ab, 37)) goto drain;
+            if (!wg_wait(&bars[C::kDSFull], i & 1, ab, 38)) goto drain;
+            if (first && !wg_wait(&bars[C::kAccFree], (nu & 1) ^ 1, ab, 37)) goto drain;
             tc_fence_after();
             for (uint32_t k = 0; k < nkv16 / 16; ++k)
                 mma_ss(tmem + kColDP,
@@ -214,7 +215,7 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             // the next tile's scores (the warpgroups have read this tile's S)
             if (!last && !issue_s(i + 1)) goto drain;
             // dV += P^T dO once P has replaced dS in shared memory
-            if (!mbar_wait(&bars[C::kPFull], i & 1, ab, 36)) goto drain;
+            if (!wg_wait(&bars[C::kPFull], i & 1, ab, 36)) goto drain;
             tc_fence_after();
             for (uint32_t k = 0; k < nq32 / 16; ++k)
                 mma_ss(tmem + kColDV, smem_desc_sw128(psbase + k * 2048, kHalfBytes, 1024),
@@ -527,7 +528,7 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (lane == 0) bwd_producer<D>(&tmQ, &tmK, &tmV, &tmDO, prm, smem, bars, seg0, seg1, ab);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) bwd_mma<D>(prm, smem, bars, tmem, seg0, seg1, ab);
+        bwd_mma<D>(prm, smem, bars, tmem, seg0, seg1, ab);   // the whole warp
         __syncwarp();
     } else {
         bwd_compute<D, ACT>(prm, &tmDQ, &tmDK, &tmDV, smem, bars, tmem, seg0, seg1, ab);

@@ -11,7 +11,8 @@
 //  * warp 0 (one lane): TMA producer.  Q tile [128 x d] per tile through a
 //    3-stage ring, K and V blocks [128 x d] per (tile, key block) item
 //    through 2-stage rings.
-//  * warp 1 (one lane): tcgen05.mma issuer.  Per item: S = Q K^T into TMEM;
+//  * warp 1: tcgen05.mma issuer (the whole warp runs the issue code, one
+//    elected lane issues).  Per item: S = Q K^T into TMEM;
 //    the P V product of the previous item is issued after the next item's S
 //    when the two belong to different warpgroups, so the tensor core
 //    computes item i+1's scores while item i's activation runs (software
@@ -164,10 +165,10 @@ __device__ __forceinline__ bool issue_pv(const PendingPV& pd, uint8_t* smem, uin
                                          uint32_t tmem, uint32_t* p_use, uint32_t* o_use,
                                          const Abort& ab) {
     using C = FwdCfg<D>;
-    if (!mbar_wait(&bars[C::kBarVFull + pd.ks], pd.kph, ab, 10)) return false;
-    if (!mbar_wait(&bars[C::kBarPFull + pd.wg], p_use[pd.wg] & 1, ab, 11)) return false;
+    if (!wg_wait(&bars[C::kBarVFull + pd.ks], pd.kph, ab, 10)) return false;
+    if (!wg_wait(&bars[C::kBarPFull + pd.wg], p_use[pd.wg] & 1, ab, 11)) return false;
     p_use[pd.wg]++;
-    if (pd.first && !mbar_wait(&bars[C::kBarOFree + pd.wg], (o_use[pd.wg] & 1) ^ 1, ab, 12))
+    if (pd.first && !wg_wait(&bars[C::kBarOFree + pd.wg], (o_use[pd.wg] & 1) ^ 1, ab, 12))
         return false;
     tc_fence_after();
     constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
@@ -203,7 +204,7 @@ __device__ void fwd_mma(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uin
         if (tile.kb1 <= tile.kb0) continue;
         const uint32_t wg = a % kNumWG;
         const uint32_t qs = a % C::kNQ, qph = (a / C::kNQ) & 1;
-        if (!mbar_wait(&bars[C::kBarQFull + qs], qph, ab, 3)) goto drain;
+        if (!wg_wait(&bars[C::kBarQFull + qs], qph, ab, 3)) goto drain;
         for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++i) {
             const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
             const int nvalid = min(kBN, tile.lkv - kb * kBN);
@@ -215,7 +216,7 @@ __device__ void fwd_mma(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uin
                 if (!issue_pv<D>(pend, smem, bars, tmem, p_use, o_use, ab)) goto drain;
                 have_pend = false;
             }
-            if (!mbar_wait(&bars[C::kBarKFull + ks], kph, ab, 4)) goto drain;
+            if (!wg_wait(&bars[C::kBarKFull + ks], kph, ab, 4)) goto drain;
             tc_fence_after();
             const uint32_t idesc = idesc_bf16(128, n16, false, false);
             const uint32_t qbase = smem_u32(smem + C::kOffQ + qs * C::kTileBytes);
@@ -460,7 +461,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (lane == 0) fwd_producer<D>(&tmQ, &tmK, &tmV, prm, smem, bars, seg0, seg1, ab);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) fwd_mma<D>(prm, smem, bars, tmem, seg0, seg1, ab);
+        fwd_mma<D>(prm, smem, bars, tmem, seg0, seg1, ab);
         __syncwarp();
     } else {
         fwd_compute<D, ACT>(prm, &tmO, smem, bars, tmem, seg0, seg1, ab);
