@@ -237,6 +237,27 @@ gdpa_status gdpa_fwd_noalloc(const int32_t* q_off_host, const int32_t* kv_off_ho
                              int d, gdpa_mask mask, int window, const void* q, const void* k,
                              const void* v, void* o, float alpha, gdpa_act act, void* stream);
 
+/* Activation test hook.
+ *
+ * Evaluates act(x) and act'(x) element-wise with the same device functions
+ * the kernels use: fast != 0 selects the tensor-core kernels' flavour (the
+ * one P and dS are computed with on the bf16 path), fast == 0 the CUDA-core
+ * float32 path's.  The activations are those of the GDPA page ("범용 내적
+ * 어텐션(GDPA)", aitrends.kr: GELU, SiLU and the Taylor-6 GELU replacing
+ * softmax), plus identity.  It exists so that tests can check those
+ * functions against reference values directly.
+ *
+ *   x, y, dy   device float32 arrays of n elements (caller-owned); y = act(x),
+ *              dy = act'(x).
+ *   n          >= 0; n == 0 does nothing.
+ *   stream     cudaStream_t; asynchronous.
+ *
+ * Errors: INVALID_ARG for an unknown act, n < 0 or NULL arrays; CUDA if the
+ * launch fails.
+ */
+gdpa_status gdpa_act_eval(gdpa_act act, int fast, const float* x, float* y, float* dy, int64_t n,
+                          void* stream);
+
 const char* gdpa_status_str(gdpa_status status);
 
 #ifdef __cplusplus

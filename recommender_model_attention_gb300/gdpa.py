@@ -65,6 +65,7 @@ def lib():
             "gdpa_sm_times": [vp, st, ctypes.POINTER(ctypes.c_uint64), i32p],
             "gdpa_fwd_noalloc": [i32p, i32p, st, st, st, st, st, vp, vp, vp, vp, ctypes.c_float,
                                  st, vp],
+            "gdpa_act_eval": [st, st, vp, vp, vp, ctypes.c_int64, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -275,3 +276,17 @@ def gdpa_fwd_noalloc(q_off, kv_off, q, k, v, o, alpha=None, act: str = "gelu_erf
                                _ptr(o), ctypes.c_float(alpha), ACT[act], _stream_ptr(stream)),
         "gdpa_fwd_noalloc")
     return o
+
+
+def act_eval(x, act: str = "gelu_erf", fast: bool = True, stream=None):
+    """(act(x), act'(x)) element-wise with the kernels' device functions
+    (``fast``: the tensor-core flavour; else the float32 CUDA-core one).
+    ``x``: a contiguous float32 CUDA tensor."""
+    import torch
+    if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous float32 CUDA tensor")
+    y = torch.empty_like(x)
+    dy = torch.empty_like(x)
+    _ok(lib().gdpa_act_eval(ACT[act], 1 if fast else 0, _ptr(x), _ptr(y), _ptr(dy),
+                            ctypes.c_int64(x.numel()), _stream_ptr(stream)), "gdpa_act_eval")
+    return y, dy
