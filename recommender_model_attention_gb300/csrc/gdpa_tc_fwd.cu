@@ -11,12 +11,14 @@
 //  * warp 0 (one lane): TMA producer.  Q tile [128 x d] per tile through a
 //    3-stage ring, K and V blocks [128 x d] per (tile, key block) item
 //    through 2-stage rings.
-//  * warp 1: tcgen05.mma issuer (the whole warp runs the issue code, one
-//    elected lane issues).  Per item: S = Q K^T into TMEM;
-//    the P V product of the previous item is issued after the next item's S
-//    when the two belong to different warpgroups, so the tensor core
-//    computes item i+1's scores while item i's activation runs (software
-//    pipelining across tile boundaries on one flattened loop).
+//  * warps 1 and 18: tcgen05.mma issuers (the whole warp runs the issue
+//    code, one elected lane issues).  Warp 1 issues S = Q K^T of each tile's
+//    first item as soon as its Q and K are loaded and its slot's previous
+//    P V is done; warp 18 issues P V of every item as soon as its P is in
+//    TMEM, then S of the tile's next item.  So the tensor core computes the
+//    next tile's scores while this tile's activation runs, and a tile's P V
+//    never waits for the next tile's loads (software pipelining across tile
+//    boundaries on one flattened loop).
 //  * warps 2-17: four activation/epilogue warpgroups.  Tiles alternate
 //    between two slots, each with its own TMEM S (128 columns) and O (128
 //    columns) accumulators, and two warpgroups share a slot: part h takes
@@ -45,7 +47,9 @@ using namespace tc;
 
 constexpr int kNumWG = 2;                       // tile slots (TMEM S/P + O each)
 constexpr int kParts = 2;                       // warpgroups sharing one slot
-constexpr int kThreads = 64 + 128 * kNumWG * kParts;  // producer, MMA, warpgroups
+// producer, S issuer, warpgroups, P V issuer
+constexpr int kThreads = 64 + 128 * kNumWG * kParts + 32;
+constexpr int kPvWarp = 2 + 4 * kNumWG * kParts;
 constexpr int kHalfBytes = 128 * 128;           // 128 rows x 128 bytes (64 bf16)
 constexpr uint32_t kTmemCols = 512;
 
@@ -71,8 +75,8 @@ struct FwdCfg {
     static constexpr int kBarOFull = kBarPFull + kNumWG;
     static constexpr int kBarOFree = kBarOFull + kNumWG;
     static constexpr int kBarStage = kBarOFree + kNumWG;             // per warpgroup
-    static constexpr int kBarMmaDone = kBarStage + kNumWG * kParts;
-    static constexpr int kNumBars = kBarMmaDone + 1;
+    static constexpr int kBarMmaDone = kBarStage + kNumWG * kParts;   // S issuer, P V issuer
+    static constexpr int kNumBars = kBarMmaDone + 2;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
 };
 
@@ -153,92 +157,119 @@ unwind:
         }
 }
 
-struct PendingPV {
-    uint32_t wg, ks, kph, nsteps;
-    bool first, last;
-};
-
-// O[wg] (+)= P V: P from the warpgroup's S columns in TMEM, V (MN-major) from
-// shared memory.
+// S = Q K^T of one item into slot w's S columns (K-major Q and K tiles),
+// N = the item's valid keys rounded up to 16; commits the slot's S-full.
 template <int D>
-__device__ __forceinline__ bool issue_pv(const PendingPV& pd, uint8_t* smem, uint64_t* bars,
-                                         uint32_t tmem, uint32_t* p_use, uint32_t* o_use,
-                                         const Abort& ab) {
+__device__ __forceinline__ void issue_s(uint8_t* smem, uint64_t* bars, uint32_t tmem, uint32_t w,
+                                        uint32_t qs, uint32_t ks, int nvalid) {
     using C = FwdCfg<D>;
-    if (!wg_wait(&bars[C::kBarVFull + pd.ks], pd.kph, ab, 10)) return false;
-    if (!wg_wait(&bars[C::kBarPFull + pd.wg], p_use[pd.wg] & 1, ab, 11)) return false;
-    p_use[pd.wg]++;
-    if (pd.first && !wg_wait(&bars[C::kBarOFree + pd.wg], (o_use[pd.wg] & 1) ^ 1, ab, 12))
-        return false;
-    tc_fence_after();
-    constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
-    const uint32_t p_tmem = tmem + pd.wg * 256;
-    const uint32_t d_o = tmem + pd.wg * 256 + 128;
-    const uint32_t vbase = smem_u32(smem + C::kOffV + pd.ks * C::kTileBytes);
-    const uint64_t vdesc = smem_desc_sw128(vbase, kHalfBytes, 1024);
+    const uint32_t n16 = (uint32_t)((nvalid + 15) & ~15);
+    const uint32_t idesc = idesc_bf16(128, n16, false, false);
+    const uint64_t qdesc = smem_desc_sw128(smem_u32(smem + C::kOffQ + qs * C::kTileBytes), 16, 1024);
+    const uint64_t kdesc = smem_desc_sw128(smem_u32(smem + C::kOffK + ks * C::kTileBytes), 16, 1024);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        // keys [16k, 16k + 16) sit in S chunk k/2's first 16 columns, half k%2
-        if (k < (int)pd.nsteps)
-            mma_ts(d_o, p_tmem + (k >> 1) * 32 + (k & 1) * 8, vdesc + mnmajor_step(k), idesc,
-                   (pd.first && k == 0) ? 0u : 1u);
-    }
-    mma_commit(&bars[C::kBarKVEmpty + pd.ks]);
-    if (pd.last) {
-        mma_commit(&bars[C::kBarOFull + pd.wg]);
-        o_use[pd.wg]++;
-    }
-    return true;
+    for (int k = 0; k < D / 16; ++k)
+        mma_ss(tmem + w * 256, qdesc + kmajor_step(k), kdesc + kmajor_step(k), idesc,
+               k > 0 ? 1u : 0u);
+    mma_commit(&bars[C::kBarSFull + w]);
 }
 
+// S issuer (warp 1, the whole warp; one elected lane issues): S of each
+// tile's first item, as soon as its Q and K are loaded and the slot's
+// previous item has had its P V complete (its S columns hold that item's P;
+// P V runs on another warp, whose commit of the item's K/V-empty arrival
+// this waits for).  S of a tile's later items follows the P V of the item
+// before it on the P V warp, in issue order.
 template <int D>
-__device__ void fwd_mma(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
-                        int seg0, int seg1, const Abort& ab) {
+__device__ void fwd_mma_s(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
+                          int seg0, int seg1, const Abort& ab) {
     using C = FwdCfg<D>;
-    uint32_t p_use[kNumWG] = {}, o_use[kNumWG] = {};
+    static_assert(kNumWG == 2, "slot bookkeeping below is written for two slots");
+    int64_t last0 = -1, last1 = -1;   // each slot's last item so far
     uint32_t a = 0, i = 0;
-    PendingPV pend{};
-    bool have_pend = false;
     for (int t = seg0; t < seg1; ++t) {
         const FwdTile tile = load_tile(prm.tiles + t);
         if (tile.kb1 <= tile.kb0) continue;
         const uint32_t wg = a % kNumWG;
         const uint32_t qs = a % C::kNQ, qph = (a / C::kNQ) & 1;
-        if (!wg_wait(&bars[C::kBarQFull + qs], qph, ab, 3)) goto drain;
+        const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
+        int64_t& last = wg ? last1 : last0;
+        // (an item kNKV or more before this one has had its K/V stage
+        // refilled since, which took its P V's completion: no wait, and its
+        // K/V-empty phase would be stale)
+        if (last >= 0 && last + C::kNKV >= (int64_t)i) {
+            const uint32_t ls = (uint32_t)(last % C::kNKV), lph = (uint32_t)((last / C::kNKV) & 1);
+            if (!wg_wait(&bars[C::kBarKVEmpty + ls], lph, ab, 13)) goto drain;
+        }
+        if (!wg_wait(&bars[C::kBarQFull + qs], qph, ab, 3) ||
+            !wg_wait(&bars[C::kBarKFull + ks], kph, ab, 4))
+            goto drain;
+        tc_fence_after();
+        issue_s<D>(smem, bars, tmem, wg, qs, ks, min(kBN, tile.lkv - tile.kb0 * kBN));
+        i += (uint32_t)(tile.kb1 - tile.kb0);
+        last = (int64_t)i - 1;
+        ++a;
+    }
+drain:
+    // all MMAs issued by this warp complete before TMEM is released
+    mma_commit(&bars[C::kBarMmaDone]);
+    mbar_wait_teardown(&bars[C::kBarMmaDone], 0);
+}
+
+// P V issuer (its own warp; one elected lane issues): O[slot] (+)= P V of
+// every item in queue order as soon as the warpgroups have put P in TMEM, so
+// it never waits for the next tile's loads; then S of the tile's next item,
+// which overwrites the P just read (in issue order on this thread).  P comes
+// from the slot's S columns (keys [16k, 16k + 16) in 32-column chunk k/2's
+// first 16 columns, half k%2), V MN-major from shared memory.
+template <int D>
+__device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
+                           int seg0, int seg1, const Abort& ab) {
+    using C = FwdCfg<D>;
+    uint32_t p_use0 = 0, p_use1 = 0, o_use0 = 0, o_use1 = 0;
+    uint32_t a = 0, i = 0;
+    for (int t = seg0; t < seg1; ++t) {
+        const FwdTile tile = load_tile(prm.tiles + t);
+        if (tile.kb1 <= tile.kb0) continue;
+        const uint32_t wg = a % kNumWG;
+        const uint32_t qs = a % C::kNQ;
+        uint32_t& p_use = wg ? p_use1 : p_use0;
+        uint32_t& o_use = wg ? o_use1 : o_use0;
         for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++i) {
             const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
-            const int nvalid = min(kBN, tile.lkv - kb * kBN);
-            const uint32_t n16 = (uint32_t)((nvalid + 15) & ~15);
-            // S[wg] holds the previous item's P when that item is this
-            // warpgroup's too: its P V goes first (the tensor pipe runs its
-            // MMAs in issue order, so the S overwrite follows the P read)
-            if (have_pend && pend.wg == wg) {
-                if (!issue_pv<D>(pend, smem, bars, tmem, p_use, o_use, ab)) goto drain;
-                have_pend = false;
-            }
-            if (!wg_wait(&bars[C::kBarKFull + ks], kph, ab, 4)) goto drain;
+            const bool first = kb == tile.kb0, last = kb == tile.kb1 - 1;
+            if (!wg_wait(&bars[C::kBarPFull + wg], p_use & 1, ab, 11)) goto drain;
+            p_use++;
+            if (!wg_wait(&bars[C::kBarVFull + ks], kph, ab, 10)) goto drain;
+            if (first && !wg_wait(&bars[C::kBarOFree + wg], (o_use & 1) ^ 1, ab, 12)) goto drain;
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16(128, n16, false, false);
-            const uint32_t qbase = smem_u32(smem + C::kOffQ + qs * C::kTileBytes);
-            const uint32_t kbase = smem_u32(smem + C::kOffK + ks * C::kTileBytes);
-            const uint64_t qdesc = smem_desc_sw128(qbase, 16, 1024);
-            const uint64_t kdesc = smem_desc_sw128(kbase, 16, 1024);
+            const int nsteps = (min(kBN, tile.lkv - kb * kBN) + 15) >> 4;
+            constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
+            const uint32_t p_tmem = tmem + wg * 256;
+            const uint32_t d_o = tmem + wg * 256 + 128;
+            const uint64_t vdesc =
+                smem_desc_sw128(smem_u32(smem + C::kOffV + ks * C::kTileBytes), kHalfBytes, 1024);
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k)
-                mma_ss(tmem + wg * 256, qdesc + kmajor_step(k), kdesc + kmajor_step(k), idesc,
-                       k > 0 ? 1u : 0u);
-            mma_commit(&bars[C::kBarSFull + wg]);
-            if (have_pend && !issue_pv<D>(pend, smem, bars, tmem, p_use, o_use, ab)) goto drain;
-            pend = PendingPV{wg, ks, kph, n16 / 16, kb == tile.kb0, kb == tile.kb1 - 1};
-            have_pend = true;
+            for (int k = 0; k < 8; ++k)
+                if (k < nsteps)
+                    mma_ts(d_o, p_tmem + (k >> 1) * 32 + (k & 1) * 8, vdesc + mnmajor_step(k), idesc,
+                           (first && k == 0) ? 0u : 1u);
+            mma_commit(&bars[C::kBarKVEmpty + ks]);
+            if (last) {
+                mma_commit(&bars[C::kBarOFull + wg]);
+                o_use++;
+            } else {
+                const uint32_t ks1 = (i + 1) % C::kNKV, kph1 = ((i + 1) / C::kNKV) & 1;
+                if (!wg_wait(&bars[C::kBarKFull + ks1], kph1, ab, 4)) goto drain;
+                tc_fence_after();
+                issue_s<D>(smem, bars, tmem, wg, qs, ks1, min(kBN, tile.lkv - (kb + 1) * kBN));
+            }
         }
         ++a;
     }
-    if (have_pend) issue_pv<D>(pend, smem, bars, tmem, p_use, o_use, ab);
 drain:
-    // all MMAs issued by this thread complete before TMEM is released
-    mma_commit(&bars[C::kBarMmaDone]);
-    mbar_wait_teardown(&bars[C::kBarMmaDone], 0);
+    mma_commit(&bars[C::kBarMmaDone + 1]);
+    mbar_wait_teardown(&bars[C::kBarMmaDone + 1], 0);
 }
 
 template <int D>
@@ -441,6 +472,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         }
         for (int g = 0; g < kNumWG * kParts; ++g) mbar_init(&bars[C::kBarStage + g], 128);
         mbar_init(&bars[C::kBarMmaDone], 1);
+        mbar_init(&bars[C::kBarMmaDone + 1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -461,7 +493,10 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (lane == 0) fwd_producer<D>(&tmQ, &tmK, &tmV, prm, smem, bars, seg0, seg1, ab);
         __syncwarp();
     } else if (warp == 1) {
-        fwd_mma<D>(prm, smem, bars, tmem, seg0, seg1, ab);
+        fwd_mma_s<D>(prm, smem, bars, tmem, seg0, seg1, ab);
+        __syncwarp();
+    } else if (warp == kPvWarp) {
+        fwd_mma_pv<D>(prm, smem, bars, tmem, seg0, seg1, ab);
         __syncwarp();
     } else {
         fwd_compute<D, ACT>(prm, &tmO, smem, bars, tmem, seg0, seg1, ab);
