@@ -153,6 +153,71 @@ __device__ __forceinline__ void act_dact_f(float x, float& a, float& da) {
     }
 }
 
+// The tensor-core kernels' form: the scale folded into the constants.
+// GELU-erf, GELU-tanh and SiLU are all x/2 (1 + tanh(u)) with u = x (g0 +
+// g1 x^2) (SiLU: g0 = 1/2, g1 = 0); with x = alpha s the kernels evaluate
+// them from the raw score s: x/2 = h s, u = s (c0 + c1 s^2), and
+// u'(x) = d0 + d1 s^2, so the scaling costs nothing per element.
+struct ActScale {
+    float alpha, h, c0, c1, d0, d1;
+};
+
+template <int ACT>
+__host__ __device__ constexpr bool tanh_form() {
+    return ACT == kGeluErf || ACT == kGeluTanh || ACT == kSilu;
+}
+
+template <int ACT>
+__device__ __forceinline__ ActScale act_scale(float alpha) {
+    float g0 = 0.0f, g1 = 0.0f;
+    if constexpr (ACT == kGeluErf) {
+        g0 = kG0;
+        g1 = kG1;
+    } else if constexpr (ACT == kGeluTanh) {
+        g0 = kSqrt2OverPi;
+        g1 = kSqrt2OverPi * kTanhCubic;
+    } else if constexpr (ACT == kSilu) {
+        g0 = 0.5f;
+    }
+    const float a2 = alpha * alpha;
+    return ActScale{alpha, 0.5f * alpha, g0 * alpha, g1 * a2 * alpha, g0, 3.0f * g1 * a2};
+}
+
+// act(alpha s), fast flavour
+template <int ACT>
+__device__ __forceinline__ float act_s(float s, const ActScale& k) {
+    if constexpr (ACT == kSilu) {   // g1 = 0
+        const float hx = k.h * s;
+        return fmaf(hx, tanh_approx(hx), hx);
+    } else if constexpr (tanh_form<ACT>()) {
+        const float t = tanh_approx(s * fmaf(k.c1, s * s, k.c0));
+        const float hx = k.h * s;
+        return fmaf(hx, t, hx);
+    } else {
+        return act_f<ACT, true>(k.alpha * s);
+    }
+}
+
+// act(alpha s) and act'(alpha s), fast flavour
+template <int ACT>
+__device__ __forceinline__ void act_dact_s(float s, const ActScale& k, float& a, float& da) {
+    if constexpr (ACT == kSilu) {   // u = x/2, u' = 1/2
+        const float hx = k.h * s;
+        const float t = tanh_approx(hx);
+        a = fmaf(hx, t, hx);
+        da = fmaf(hx * fmaf(-t, t, 1.0f), 0.5f, fmaf(0.5f, t, 0.5f));
+    } else if constexpr (tanh_form<ACT>()) {
+        // d/dx [x/2 (1 + tanh(u))] = (1 + t)/2 + x/2 (1 - t^2) u'
+        const float s2 = s * s;
+        const float t = tanh_approx(s * fmaf(k.c1, s2, k.c0));
+        const float hx = k.h * s;
+        a = fmaf(hx, t, hx);
+        da = fmaf(hx * fmaf(-t, t, 1.0f), fmaf(k.d1, s2, k.d0), fmaf(0.5f, t, 0.5f));
+    } else {
+        act_dact_f<ACT, true>(k.alpha * s, a, da);
+    }
+}
+
 // Runtime activation id -> template instantiation.
 #define GDPA_DISPATCH_ACT(act, ACTC, ...)                      \
     switch (act) {                                             \

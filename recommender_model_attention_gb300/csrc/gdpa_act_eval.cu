@@ -13,8 +13,15 @@ __global__ void act_eval_kernel(const float* x, float* y, float* dy, int64_t n) 
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t k = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; k < n; k += stride) {
         float a, da;
-        act_dact_f<ACT, FAST>(x[k], a, da);
-        y[k] = act_f<ACT, FAST>(x[k]);
+        if constexpr (FAST) {
+            // the tensor-core kernels' form (scale folded into the constants)
+            const ActScale sc = act_scale<ACT>(1.0f);
+            act_dact_s<ACT>(x[k], sc, a, da);
+            y[k] = act_s<ACT>(x[k], sc);
+        } else {
+            act_dact_f<ACT, false>(x[k], a, da);
+            y[k] = act_f<ACT, false>(x[k]);
+        }
         dy[k] = da;
     }
 }

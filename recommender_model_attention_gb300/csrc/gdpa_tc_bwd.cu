@@ -348,6 +348,7 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
     uint8_t* ps = smem + C::kOffPS;
     uint8_t* stage = ps + wg * kHalfBytes;
     const int64_t rs = (int64_t)prm.H * D;
+    const ActScale ksc = act_scale<ACT>(prm.alpha);
     uint32_t nu = 0, i = 0;
     int pending_q = -1;   // Q stage still read by this warp's last dQ stores
     for (int t = seg0; t < seg1; ++t) {
@@ -400,8 +401,8 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
 #pragma unroll
                             for (int e = 0; e < 16; e += 2) {
                                 float a0, d0, a1, d1;
-                                act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e]), a0, d0);
-                                act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + 1]), a1, d1);
+                                act_dact_s<ACT>(__uint_as_float(sv[e]), ksc, a0, d0);
+                                act_dact_s<ACT>(__uint_as_float(sv[e + 1]), ksc, a1, d1);
                                 pp[k][e >> 1] = pack_bf16x2(a0, a1);
                                 pd[e >> 1] = pack_bf16x2(__uint_as_float(dv[e]) * d0,
                                                          __uint_as_float(dv[e + 1]) * d1);
@@ -418,8 +419,7 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                                     if (windowed)
                                         valid = valid && jpos <= ipos && jpos > ipos - prm.window;
                                     float a, da;
-                                    act_dact_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + w]), a,
-                                                          da);
+                                    act_dact_s<ACT>(__uint_as_float(sv[e + w]), ksc, a, da);
                                     p2[w] = valid ? a : 0.0f;
                                     d2[w] = valid ? __uint_as_float(dv[e + w]) * da : 0.0f;
                                 }

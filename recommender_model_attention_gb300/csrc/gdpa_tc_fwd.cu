@@ -297,6 +297,7 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, uint8_
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const uint32_t s_tmem = tmem + wg * 256 + lane_addr;
     const uint32_t o_tmem = tmem + wg * 256 + 128 + lane_addr + part * (D / 2);
+    const ActScale ksc = act_scale<ACT>(prm.alpha);
     uint32_t a = 0, s_use = 0, o_use = 0;
     for (int t = seg0; t < seg1; ++t) {
         const FwdTile tile = load_tile(prm.tiles + t);
@@ -337,9 +338,8 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, uint8_
                             if (prm.mask != GDPA_MASK_CAUSAL_WINDOW && col0 + 16 <= nvalid) {
 #pragma unroll
                                 for (int e = 0; e < 16; e += 2)
-                                    pk[e >> 1] = pack_bf16x2(
-                                        act_f<ACT, true>(prm.alpha * __uint_as_float(sv[e])),
-                                        act_f<ACT, true>(prm.alpha * __uint_as_float(sv[e + 1])));
+                                    pk[e >> 1] = pack_bf16x2(act_s<ACT>(__uint_as_float(sv[e]), ksc),
+                                                             act_s<ACT>(__uint_as_float(sv[e + 1]), ksc));
                             } else {
 #pragma unroll
                                 for (int e = 0; e < 16; e += 2) {
@@ -351,8 +351,8 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, uint8_
                                         bool valid = col < nvalid;
                                         if (prm.mask == GDPA_MASK_CAUSAL_WINDOW)
                                             valid = valid && jpos <= ipos && jpos > ipos - prm.window;
-                                        const float x = prm.alpha * __uint_as_float(sv[e + u]);
-                                        pv[u] = valid ? act_f<ACT, true>(x) : 0.0f;
+                                        const float a = act_s<ACT>(__uint_as_float(sv[e + u]), ksc);
+                                        pv[u] = valid ? a : 0.0f;
                                     }
                                     pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
                                 }
