@@ -269,6 +269,13 @@ def main():
     x = make_inputs(w, device="cuda", seed=rank_seed(w, rank), lengths=lengths)
     stream = torch.cuda.current_stream()
     plan = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window)
+    # host planning + upload of one batch's plan (it synchronises on its upload)
+    plan_times = []
+    for _ in range(3):
+        t0 = time.perf_counter()
+        gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window).destroy()
+        plan_times.append((time.perf_counter() - t0) * 1e3)
+    n_fwd_tiles, n_bwd_units, _ = plan.sizes()
     f32 = torch.float32
     o = torch.empty_like(x["q"])
     dq = torch.empty(x["q"].shape, dtype=f32, device="cuda")
@@ -344,7 +351,10 @@ def main():
                 "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
                 "algorithmic_bytes": dom_bytes, "peak_kind": pk_kind}
 
-    # end to end through the public API: pinned host inputs in, results out
+    # end to end through the public API: pinned host inputs in, results out.
+    # Steps are pipelined the way a training loader runs them: step k's
+    # inputs go up on one stream while step k-1 computes, and its results come
+    # down on another; two device buffer sets alternate.
     e2e = None
     if not args.no_e2e:
         hq = x["q"].cpu().pin_memory()
@@ -353,30 +363,56 @@ def main():
         hdo = x["do"].cpu().pin_memory() if backward else None
         ho = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
         hgrads = [torch.empty(t.shape, dtype=f32, pin_memory=True) for t in (dq, dk, dv)]
-        q_d, k_d, v_d = (torch.empty_like(t) for t in (x["q"], x["k"], x["v"]))
-        do_d = torch.empty_like(x["q"]) if backward else None
+        sets = []
+        for _ in range(2):
+            ins = [torch.empty_like(t) for t in (x["q"], x["k"], x["v"])]
+            ins.append(torch.empty_like(x["q"]) if backward else None)
+            outs = [torch.empty_like(o)] + ([torch.empty_like(t) for t in (dq, dk, dv)]
+                                            if backward else [])
+            sets.append((ins, outs))
+        up, down, plan_stream = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in", "done", "out")}
 
-        def e2e_step():
-            q_d.copy_(hq, non_blocking=True)
-            k_d.copy_(hk, non_blocking=True)
-            v_d.copy_(hv, non_blocking=True)
-            if backward:
-                do_d.copy_(hdo, non_blocking=True)
-            gd.gdpa_fwd(plan, q_d, k_d, v_d, o=o, alpha=w.alpha, act=w.act)
-            ho.copy_(o, non_blocking=True)
-            if backward:
-                gd.gdpa_bwd(plan, q_d, k_d, v_d, do_d, dq, dk, dv, alpha=w.alpha, act=w.act)
-                for h, d_ in zip(hgrads, (dq, dk, dv)):
-                    h.copy_(d_, non_blocking=True)
+        def e2e_run(n, replan=False):
+            plans = []
+            for k in range(n):
+                sl = k % 2
+                (q_d, k_d, v_d, do_d), outs = sets[sl]
+                if k >= 2:
+                    up.wait_event(ev["done"][sl])      # step k-2 has read this set
+                with torch.cuda.stream(up):
+                    for dst, src in zip((q_d, k_d, v_d, do_d), (hq, hk, hv, hdo)):
+                        if dst is not None:
+                            dst.copy_(src, non_blocking=True)
+                    ev["in"][sl].record(up)
+                p = plan
+                if replan:   # each step's batch planned afresh, as in training
+                    p = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window,
+                                stream=plan_stream)
+                    plans.append(p)
+                stream.wait_event(ev["in"][sl])
+                if k >= 2:
+                    stream.wait_event(ev["out"][sl])   # step k-2's results are down
+                gd.gdpa_fwd(p, q_d, k_d, v_d, o=outs[0], alpha=w.alpha, act=w.act)
+                if backward:
+                    gd.gdpa_bwd(p, q_d, k_d, v_d, do_d, *outs[1:], alpha=w.alpha, act=w.act)
+                ev["done"][sl].record(stream)
+                down.wait_event(ev["done"][sl])
+                with torch.cuda.stream(down):
+                    for h, d_ in zip([ho] + hgrads, outs):
+                        h.copy_(d_, non_blocking=True)
+                    ev["out"][sl].record(down)
+            for sl in range(2):
+                stream.wait_event(ev["out"][sl])
+            return plans
 
-        e2e_step()
+        e2e_run(2)
         torch.cuda.synchronize()
-        n_e2e = max(2, min(args.steps, 5))
+        n_e2e = max(3, min(args.steps, 6))
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
+        e2e_run(n_e2e)
         b.record(stream)
         torch.cuda.synchronize()
         e2e_total, e2e_flops = reduce_across_ranks(a.elapsed_time(b),
@@ -385,9 +421,20 @@ def main():
         h2d = input_bytes
         d2h = o.numel() * o.element_size() + (sum(t.numel() * 4 for t in (dq, dk, dv))
                                               if backward else 0)
+        # the same with each step's batch planned afresh (host planning and plan
+        # upload inside the timed region)
+        a.record(stream)
+        plans = e2e_run(n_e2e, replan=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        for p in plans:
+            p.destroy()
+        replan_total, _ = reduce_across_ranks(a.elapsed_time(b), 0.0, "cuda")
         e2e = {"value": e2e_flops / (e2e_total * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e2e_ms}
+               "ms_per_step": e2e_ms, "ms_per_step_with_planning": replan_total / n_e2e,
+               "pipelining": "inputs up, compute, results down on three streams, "
+                             "two buffer sets"}
 
     # SM busy-time spread of each policy (separate, untimed launches)
     spread = {}
@@ -431,6 +478,8 @@ def main():
             "clocks": clk,
             "e2e": e2e,
             "sm_spread_fwd": spread,
+            "plan": {"host_ms_median": float(np.median(plan_times)), "fwd_tiles": int(n_fwd_tiles),
+                     "bwd_units": int(n_bwd_units)},
             "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

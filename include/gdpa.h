@@ -199,6 +199,8 @@ gdpa_status gdpa_sm_times(gdpa_plan plan, int which, uint64_t* start_end, int32_
 /* Number of kernel launches this plan has issued since creation. */
 int64_t gdpa_plan_launches(gdpa_plan plan);
 
+/* Frees the plan (NULL is a no-op).  Synchronous: first waits for the work
+ * queued on the plan's device, which may still read the plan's buffers. */
 void gdpa_plan_destroy(gdpa_plan plan);
 
 /*

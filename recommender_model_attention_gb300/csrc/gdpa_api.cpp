@@ -25,6 +25,10 @@ gdpa_status upload(T** dst, const void* src, size_t bytes, cudaStream_t st) {
 void free_plan(Plan* p) {
     if (!p) return;
     if (!p->host_only) {
+        // work still queued on the device may read the plan's buffers
+        int cur = -1;
+        if (cudaGetDevice(&cur) == cudaSuccess && cur != p->device) cudaSetDevice(p->device);
+        cudaDeviceSynchronize();
         cudaFree(p->d_fwd);
         cudaFree(p->d_fwd_seg);
         cudaFree(p->d_bwd);
@@ -32,6 +36,7 @@ void free_plan(Plan* p) {
         cudaFree(p->d_err);
         cudaFree(p->d_times);
         cudaFree(p->d_smid);
+        if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
     }
     delete p;
 }
