@@ -11,7 +11,8 @@ loops is checked against whole-matrix algebra on small inputs:
     dV = P^T dO,  dQ = alpha G K,  dK = alpha G^T Q
 
 The activations are evaluated through SciPy's special functions (normal CDF,
-logistic) rather than the formulas used by the C loops.
+logistic, softmax for the softmax variant) rather than the formulas used by
+the C loops.
 """
 
 from __future__ import annotations
@@ -104,12 +105,22 @@ def _setup(q_off, kv_off, q, k, v, mask, window):
 def fwd(q_off, kv_off, q, k, v, alpha, kind, mask="none", window=0):
     q_off, kv_off, Lq, Lkv, Qp, Kp, Vp, M = _setup(q_off, kv_off, q, k, v, mask, window)
     X = alpha * np.einsum("bihc,bjhc->bhij", Qp, Kp)
-    P = np.where(M, act(kind, X), 0.0)
+    if kind == "softmax":
+        # SciPy's softmax over the key axis with masked scores at -inf; rows
+        # with no valid key are all -inf (NaN from SciPy) and are set to 0
+        Xm = np.where(M, X, -np.inf)
+        with np.errstate(invalid="ignore"):
+            P = special.softmax(Xm, axis=-1)
+        P = np.where(M, P, 0.0)
+    else:
+        P = np.where(M, act(kind, X), 0.0)
     Op = np.einsum("bhij,bjhc->bihc", P, Vp)
     return _unpad(Op, q_off, int(q_off[-1]))
 
 
 def bwd(q_off, kv_off, q, k, v, do, alpha, kind, mask="none", window=0):
+    if kind == "softmax":
+        raise ValueError("the softmax variant is forward only")
     q_off, kv_off, Lq, Lkv, Qp, Kp, Vp, M = _setup(q_off, kv_off, q, k, v, mask, window)
     dOp = _pad(np.asarray(do, np.float64), q_off, Lq)
     X = alpha * np.einsum("bihc,bjhc->bhij", Qp, Kp)

@@ -24,6 +24,14 @@
  *     (positions counted from the start of each sample).
  *   - Rows with no valid key give zero output and zero dQ.
  *
+ * The softmax variant (kind 5) is the other attention kernel the GEM page
+ * ("Meta GEM ... 맞춤형 커널과 정밀도", the kernel list) names next to GDPA:
+ * Jagged Flash Attention, softmax attention over the same jagged batches.
+ * Per query row, over its valid keys only: O_i = sum_j w_j V_j with
+ * w_j = exp(s_j - m) / sum_l exp(s_l - m), s_j = alpha q_i.k_j, m = max_j s_j
+ * (the standard softmax, evaluated with the max subtracted); a row with no
+ * valid key gives zero.  Forward only.
+ *
  * Layout: token-major with heads interleaved, X[t][h][c], t a global token
  * index, q_off / kv_off exclusive prefix sums of the per-sample lengths.
  * Everything is double; inputs are the (possibly bf16-rounded) values upcast.
@@ -35,7 +43,8 @@
 #include <omp.h>
 #endif
 
-enum { REF_GELU_ERF = 0, REF_GELU_TANH = 1, REF_SILU = 2, REF_TAYLOR6 = 3, REF_IDENTITY = 4 };
+enum { REF_GELU_ERF = 0, REF_GELU_TANH = 1, REF_SILU = 2, REF_TAYLOR6 = 3, REF_IDENTITY = 4,
+       REF_SOFTMAX = 5 };
 enum { REF_MASK_NONE = 0, REF_MASK_CAUSAL_WINDOW = 1 };
 
 static const double REF_PI = 3.14159265358979323846;
@@ -120,7 +129,35 @@ int64_t gdpa_ref_pairs(int B, const int32_t* q_off, const int32_t* kv_off, int m
     return n;
 }
 
-/* O[t][h][:] = sum over valid j of act(alpha * Q_t . K_j) V_j */
+/* Softmax row (kind 5): O_i over the valid keys of row i of sample b, head h */
+static void ref_softmax_row(const double* q, const double* K, const double* V, double* o, int i,
+                            int lkv, int64_t row, int d, double alpha, int mask, int window) {
+    double m = -INFINITY;
+    for (int j = 0; j < lkv; ++j) {
+        if (!ref_valid(i, j, mask, window)) continue;
+        const double* k = K + (int64_t)j * row;
+        double s = 0.0;
+        for (int c = 0; c < d; ++c) s += q[c] * k[c];
+        if (alpha * s > m) m = alpha * s;
+    }
+    for (int c = 0; c < d; ++c) o[c] = 0.0;
+    if (m == -INFINITY) return;   /* no valid key */
+    double z = 0.0;
+    for (int j = 0; j < lkv; ++j) {
+        if (!ref_valid(i, j, mask, window)) continue;
+        const double* k = K + (int64_t)j * row;
+        const double* v = V + (int64_t)j * row;
+        double s = 0.0;
+        for (int c = 0; c < d; ++c) s += q[c] * k[c];
+        const double w = exp(alpha * s - m);
+        z += w;
+        for (int c = 0; c < d; ++c) o[c] += w * v[c];
+    }
+    for (int c = 0; c < d; ++c) o[c] /= z;
+}
+
+/* O[t][h][:] = sum over valid j of act(alpha * Q_t . K_j) V_j (kind 5: the
+ * softmax-weighted sum instead) */
 void gdpa_ref_fwd(int B, int H, int d, const int32_t* q_off, const int32_t* kv_off,
                   const double* Q, const double* K, const double* V, double* O,
                   double alpha, int act, int mask, int window) {
@@ -132,6 +169,12 @@ void gdpa_ref_fwd(int B, int H, int d, const int32_t* q_off, const int32_t* kv_o
             for (int i = 0; i < lq; ++i) {
                 const double* q = Q + (int64_t)(q_off[b] + i) * row + (int64_t)h * d;
                 double* o = O + (int64_t)(q_off[b] + i) * row + (int64_t)h * d;
+                if (act == REF_SOFTMAX) {
+                    ref_softmax_row(q, K + (int64_t)kv_off[b] * row + (int64_t)h * d,
+                                    V + (int64_t)kv_off[b] * row + (int64_t)h * d, o, i, lkv, row,
+                                    d, alpha, mask, window);
+                    continue;
+                }
                 for (int c = 0; c < d; ++c) o[c] = 0.0;
                 for (int j = 0; j < lkv; ++j) {
                     if (!ref_valid(i, j, mask, window)) continue;

@@ -113,6 +113,8 @@ def fwd(q_off, kv_off, q, k, v, alpha: float, act: str, mask: str = "none",
 def bwd(q_off, kv_off, q, k, v, do, alpha: float, act: str, mask: str = "none",
         window: int = 0):
     """(dQ, dK, dV) for a jagged batch given the upstream gradient dO."""
+    if act == "softmax":
+        raise ValueError("the softmax variant is forward only")
     qo, qp = _i32(q_off)
     ko, kp = _i32(kv_off)
     Q, Qp = _f64(to_f64(q))
