@@ -60,7 +60,13 @@ typedef enum {
     GDPA_ACT_GELU_TANH = 1,     /* x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) */
     GDPA_ACT_SILU = 2,          /* x / (1 + exp(-x)) */
     GDPA_ACT_GELU_TAYLOR6 = 3,  /* x/2 + (x^2 - x^4/6 + x^6/40) / sqrt(2 pi) */
-    GDPA_ACT_IDENTITY = 4       /* x (for tests of the linear algebra) */
+    GDPA_ACT_IDENTITY = 4,      /* x (for tests of the linear algebra) */
+    /* Softmax variant: O_i = sum_j softmax_j(alpha q_i.k_j) V_j over the row's
+     * valid keys (0 for a row without one), i.e. Jagged Flash Attention, the
+     * softmax kernel the GEM page (aitrends.kr, kernel list) names beside
+     * GDPA.  gdpa_fwd and gdpa_fwd_noalloc only; gdpa_bwd returns
+     * UNSUPPORTED, gdpa_act_eval INVALID_ARG. */
+    GDPA_ACT_SOFTMAX = 5
 } gdpa_act;
 
 typedef enum {

@@ -24,7 +24,9 @@
 
 namespace gdpa {
 
-enum : int { kGeluErf = 0, kGeluTanh = 1, kSilu = 2, kTaylor6 = 3, kIdentity = 4 };
+// kSoftmax is not element-wise: it selects the softmax variant (Jagged Flash
+// Attention) of the forward kernels, whose rows are normalised.
+enum : int { kGeluErf = 0, kGeluTanh = 1, kSilu = 2, kTaylor6 = 3, kIdentity = 4, kSoftmax = 5 };
 
 constexpr float kRsqrt2 = 0.70710678118654752440f;     // 1/sqrt(2)
 constexpr float kRsqrt2Pi = 0.39894228040143267794f;   // 1/sqrt(2 pi)

@@ -39,6 +39,7 @@ void launch_eval(int act, const float* x, float* y, float* dy, int64_t n, cudaSt
 extern "C" gdpa_status gdpa_act_eval(gdpa_act act, int fast, const float* x, float* y, float* dy,
                                      int64_t n, void* stream) {
     if (act < GDPA_ACT_GELU_ERF || act > GDPA_ACT_IDENTITY || n < 0) return GDPA_ERR_INVALID_ARG;
+    // (the softmax variant is a row operation, not an element-wise one)
     if (n == 0) return GDPA_OK;
     if (!x || !y || !dy) return GDPA_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;

@@ -41,7 +41,7 @@ void free_plan(Plan* p) {
     delete p;
 }
 
-bool valid_act(int a) { return a >= GDPA_ACT_GELU_ERF && a <= GDPA_ACT_IDENTITY; }
+bool valid_act(int a) { return a >= GDPA_ACT_GELU_ERF && a <= GDPA_ACT_SOFTMAX; }
 
 // true when this plan/dtype combination runs on the tcgen05 kernels
 bool use_tc(const Plan& p, gdpa_dtype dt) {
@@ -233,6 +233,7 @@ gdpa_status gdpa_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void
     Plan& p = *(Plan*)plan;
     if (dtype != GDPA_BF16 && dtype != GDPA_F32) return GDPA_ERR_INVALID_ARG;
     if (!valid_act(act)) return GDPA_ERR_INVALID_ARG;
+    if (act == GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;   // forward only
     if (p.Tq > 0 && (!q || !d_o || !dq)) return GDPA_ERR_INVALID_ARG;
     if (p.Tkv > 0 && (!k || !v || !dk || !dv)) return GDPA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) || !aligned16(dq) ||

@@ -164,7 +164,7 @@ extern "C" gdpa_status gdpa_fwd_noalloc(const int32_t* q_off_host, const int32_t
     if (!q_off_host || !kv_off_host || B < 0 || H < 1) return GDPA_ERR_INVALID_ARG;
     if (mask != GDPA_MASK_NONE && mask != GDPA_MASK_CAUSAL_WINDOW) return GDPA_ERR_INVALID_ARG;
     if (mask == GDPA_MASK_CAUSAL_WINDOW && window < 1) return GDPA_ERR_INVALID_ARG;
-    if (act < GDPA_ACT_GELU_ERF || act > GDPA_ACT_IDENTITY) return GDPA_ERR_INVALID_ARG;
+    if (act < GDPA_ACT_GELU_ERF || act > GDPA_ACT_SOFTMAX) return GDPA_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
     const int64_t Tq = q_off_host[B], Tkv = kv_off_host[B];
     if (Tq > 0 && (!q || !o)) return GDPA_ERR_INVALID_ARG;

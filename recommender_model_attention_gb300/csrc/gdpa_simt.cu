@@ -87,6 +87,48 @@ simt_fwd_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__ Q, cons
     }
 }
 
+// Softmax variant (Jagged Flash Attention): O_i = sum_j w_j V_j over the
+// valid keys of row i, w = softmax_j(alpha q_i.k_j), one pass with a running
+// maximum m and sum l (O rescaled by exp(m_old - m_new) when m grows); a row
+// without a valid key gets zero.
+template <typename T>
+__global__ void __launch_bounds__(kWarps * 32)
+simt_softmax_fwd_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__ Q,
+                        const T* __restrict__ K, const T* __restrict__ V, T* __restrict__ O, int H,
+                        int d, float alpha, int mask, int window) {
+    const FwdTile t = tiles[blockIdx.x];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)H * d;
+    for (int r = warp; r < t.nq; r += kWarps) {
+        const int64_t qrow = (int64_t)(t.qt0 + r) * row + (int64_t)t.h * d;
+        float q[kPer], o[kPer] = {0.f, 0.f, 0.f, 0.f};
+        load_row(q, Q + qrow, d, lane);
+        int lo, hi;
+        key_range(t.i0 + r, t.kb0, t.kb1, t.lkv, mask, window, lo, hi);
+        float m = -INFINITY, l = 0.0f;
+        for (int j = lo; j < hi; ++j) {
+            const int64_t krow = (int64_t)(t.kvt0 + j) * row + (int64_t)t.h * d;
+            float kx[kPer], vx[kPer];
+            load_row(kx, K + krow, d, lane);
+            load_row(vx, V + krow, d, lane);
+            const float x = alpha * dot_row(q, kx);
+            const float mn = fmaxf(m, x);
+            const float scale = expf(m - mn);   // 0 on the first key (m = -inf)
+            const float w = expf(x - mn);
+            l = fmaf(l, scale, w);
+#pragma unroll
+            for (int c = 0; c < kPer; ++c) o[c] = fmaf(w, vx[c], o[c] * scale);
+            m = mn;
+        }
+        const float inv = l > 0.0f ? 1.0f / l : 0.0f;
+#pragma unroll
+        for (int c = 0; c < kPer; ++c) {
+            const int e = lane + 32 * c;
+            if (e < d) stf(O + qrow + e, o[c] * inv);
+        }
+    }
+}
+
 // dQ_i = alpha sum_j (dO_i . V_j) act'(x_ij) K_j over the tile's rows
 template <int ACT, typename T>
 __global__ void __launch_bounds__(kWarps * 32)
@@ -173,6 +215,13 @@ template <typename T>
 gdpa_status fwd_impl(Plan& p, const void* q, const void* k, const void* v, void* o, float alpha,
                      int act, cudaStream_t st) {
     const unsigned grid = (unsigned)p.n_fwd;
+    if (act == kSoftmax) {
+        simt_softmax_fwd_kernel<T><<<grid, kWarps * 32, 0, st>>>(
+            p.d_fwd, (const T*)q, (const T*)k, (const T*)v, (T*)o, p.H, p.d, alpha, p.mask,
+            p.window);
+        p.launches += 1;
+        return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+    }
     GDPA_DISPATCH_ACT(act, A,
         simt_fwd_kernel<A, T><<<grid, kWarps * 32, 0, st>>>(
             p.d_fwd, (const T*)q, (const T*)k, (const T*)v, (T*)o, p.H, p.d, alpha, p.mask,

@@ -76,7 +76,8 @@ struct FwdCfg {
     static constexpr int kBarOFree = kBarOFull + kNumWG;
     static constexpr int kBarStage = kBarOFree + kNumWG;             // per warpgroup
     static constexpr int kBarMmaDone = kBarStage + kNumWG * kParts;   // S issuer, P V issuer
-    static constexpr int kNumBars = kBarMmaDone + 2;
+    static constexpr int kBarXchg = kBarMmaDone + 2;   // per slot: softmax part exchange
+    static constexpr int kNumBars = kBarXchg + kNumWG;
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
 };
 
@@ -103,7 +104,29 @@ __device__ __forceinline__ FwdTile load_tile(const FwdTile* p) {
     return t;
 }
 
-template <int D>
+// Items of a tile: one per key block.  The softmax variant makes two passes
+// over a tile with more than one key block: the row maxima first (S only),
+// then the weights and P V; with one key block both come from one S.
+template <bool SM>
+__device__ __forceinline__ int tile_items(const FwdTile& t) {
+    const int nb = t.kb1 - t.kb0;
+    return (SM && nb > 1) ? 2 * nb : nb;
+}
+
+template <bool SM>
+__device__ __forceinline__ int item_block(const FwdTile& t, int it) {
+    const int nb = t.kb1 - t.kb0;
+    return t.kb0 + ((SM && nb > 1) ? it % nb : it);
+}
+
+// does the item carry a P V product (and, for the softmax variant, weights)?
+template <bool SM>
+__device__ __forceinline__ bool item_pv(const FwdTile& t, int it) {
+    const int nb = t.kb1 - t.kb0;
+    return !SM || nb == 1 || it >= nb;
+}
+
+template <int D, bool SM>
 __device__ void fwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, const CUtensorMap* tmV,
                              const FwdParams& prm, uint8_t* smem, uint64_t* bars, int seg0,
                              int seg1, const Abort& ab) {
@@ -126,10 +149,11 @@ __device__ void fwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
             tma_load_2d(tmQ, &bars[C::kBarQFull + qs],
                         smem + C::kOffQ + qs * C::kTileBytes + hf * kHalfBytes,
                         tile.h * D + hf * 64, tile.qt0, pol_q);
-        for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++i) {
+        const int nit = tile_items<SM>(tile);
+        for (int it = 0; it < nit; ++it, ++i) {
             const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
             if (!mbar_wait(&bars[C::kBarKVEmpty + ks], kph ^ 1, ab, 2)) goto unwind;
-            const int y = tile.kvt0 + kb * kBN;
+            const int y = tile.kvt0 + item_block<SM>(tile, it) * kBN;
             mbar_arrive_expect_tx(&bars[C::kBarKFull + ks], C::kTileBytes);
 #pragma unroll
             for (int hf = 0; hf < C::kHalves; ++hf)
@@ -180,7 +204,7 @@ __device__ __forceinline__ void issue_s(uint8_t* smem, uint64_t* bars, uint32_t 
 // P V runs on another warp, whose commit of the item's K/V-empty arrival
 // this waits for).  S of a tile's later items follows the P V of the item
 // before it on the P V warp, in issue order.
-template <int D>
+template <int D, bool SM>
 __device__ void fwd_mma_s(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
                           int seg0, int seg1, const Abort& ab) {
     using C = FwdCfg<D>;
@@ -206,7 +230,7 @@ __device__ void fwd_mma_s(const FwdParams& prm, uint8_t* smem, uint64_t* bars, u
             goto drain;
         tc_fence_after();
         issue_s<D>(smem, bars, tmem, wg, qs, ks, min(kBN, tile.lkv - tile.kb0 * kBN));
-        i += (uint32_t)(tile.kb1 - tile.kb0);
+        i += (uint32_t)tile_items<SM>(tile);
         last = (int64_t)i - 1;
         ++a;
     }
@@ -222,7 +246,7 @@ drain:
 // which overwrites the P just read (in issue order on this thread).  P comes
 // from the slot's S columns (keys [16k, 16k + 16) in 32-column chunk k/2's
 // first 16 columns, half k%2), V MN-major from shared memory.
-template <int D>
+template <int D, bool SM>
 __device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
                            int seg0, int seg1, const Abort& ab) {
     using C = FwdCfg<D>;
@@ -235,25 +259,33 @@ __device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, 
         const uint32_t qs = a % C::kNQ;
         uint32_t& p_use = wg ? p_use1 : p_use0;
         uint32_t& o_use = wg ? o_use1 : o_use0;
-        for (int kb = tile.kb0; kb < tile.kb1; ++kb, ++i) {
+        const int nit = tile_items<SM>(tile);
+        for (int it = 0; it < nit; ++it, ++i) {
             const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
-            const bool first = kb == tile.kb0, last = kb == tile.kb1 - 1;
+            const int kb = item_block<SM>(tile, it);
+            const bool pv = item_pv<SM>(tile, it);
+            const bool first = pv && (it == 0 || !item_pv<SM>(tile, it - 1));
+            const bool last = it == nit - 1;
             if (!wg_wait(&bars[C::kBarPFull + wg], p_use & 1, ab, 11)) goto drain;
             p_use++;
+            // (also for an item without P V: its V load must have landed
+            // before the stage goes back to the producer)
             if (!wg_wait(&bars[C::kBarVFull + ks], kph, ab, 10)) goto drain;
             if (first && !wg_wait(&bars[C::kBarOFree + wg], (o_use & 1) ^ 1, ab, 12)) goto drain;
             tc_fence_after();
-            const int nsteps = (min(kBN, tile.lkv - kb * kBN) + 15) >> 4;
-            constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
-            const uint32_t p_tmem = tmem + wg * 256;
-            const uint32_t d_o = tmem + wg * 256 + 128;
-            const uint64_t vdesc =
-                smem_desc_sw128(smem_u32(smem + C::kOffV + ks * C::kTileBytes), kHalfBytes, 1024);
+            if (pv) {
+                const int nsteps = (min(kBN, tile.lkv - kb * kBN) + 15) >> 4;
+                constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
+                const uint32_t p_tmem = tmem + wg * 256;
+                const uint32_t d_o = tmem + wg * 256 + 128;
+                const uint64_t vdesc =
+                    smem_desc_sw128(smem_u32(smem + C::kOffV + ks * C::kTileBytes), kHalfBytes, 1024);
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-                if (k < nsteps)
-                    mma_ts(d_o, p_tmem + (k >> 1) * 32 + (k & 1) * 8, vdesc + mnmajor_step(k), idesc,
-                           (first && k == 0) ? 0u : 1u);
+                for (int k = 0; k < 8; ++k)
+                    if (k < nsteps)
+                        mma_ts(d_o, p_tmem + (k >> 1) * 32 + (k & 1) * 8, vdesc + mnmajor_step(k),
+                               idesc, (first && k == 0) ? 0u : 1u);
+            }
             mma_commit(&bars[C::kBarKVEmpty + ks]);
             if (last) {
                 mma_commit(&bars[C::kBarOFull + wg]);
@@ -262,7 +294,8 @@ __device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, 
                 const uint32_t ks1 = (i + 1) % C::kNKV, kph1 = ((i + 1) / C::kNKV) & 1;
                 if (!wg_wait(&bars[C::kBarKFull + ks1], kph1, ab, 4)) goto drain;
                 tc_fence_after();
-                issue_s<D>(smem, bars, tmem, wg, qs, ks1, min(kBN, tile.lkv - (kb + 1) * kBN));
+                issue_s<D>(smem, bars, tmem, wg, qs, ks1,
+                           min(kBN, tile.lkv - item_block<SM>(tile, it + 1) * kBN));
             }
         }
         ++a;
@@ -283,6 +316,139 @@ __device__ __forceinline__ void store_zero_rows(const FwdTile& tile, const FwdPa
     }
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Softmax variant (Jagged Flash Attention), one tile, one thread = one row
+// of this part's key columns.  With t = alpha log2(e) s, the row maximum m
+// of t over every valid key (a first pass over the key blocks when there are
+// several), then P = 2^(t - m) (exactly zero for invalid pairs) into TMEM as
+// for GDPA, and the row sum l.  The slot's two parts combine m, then l,
+// through a TMEM column that no one else reads at that point: the first
+// column of this part's O share before the tile's first P V (for m), the
+// 17th column of this part's first S chunk, already read, before the last
+// P is released (for l), meeting at the slot's exchange barrier (all 256
+// threads, a bounded wait like every other).
+// Returns 1 / l for the epilogue (0 for a row without a valid key), or a
+// negative value if a wait gave up.
+template <int D>
+__device__ float softmax_tile(const FwdTile& tile, const FwdParams& prm, uint64_t* bars,
+                              uint32_t& s_use, uint32_t& x_use, uint32_t s_tmem,
+                              uint32_t o_tmem_part0, int wg, int part, int r, bool warp_rows,
+                              const Abort& ab) {
+    using C = FwdCfg<D>;
+    const float c2 = prm.alpha * 1.44269504088896340736f;   // alpha log2(e)
+    const int ipos = tile.i0 + r;
+    const int nit = tile_items<true>(tile);
+    float m = -INFINITY, l = 0.0f;
+    // write v to my column, meet the other part, read its value
+    auto exchange = [&](uint32_t mine, uint32_t theirs, float v, float& out) -> bool {
+        tmem_st1(mine, __float_as_uint(v));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars[C::kBarXchg + wg]);
+        if (!wg_wait(&bars[C::kBarXchg + wg], x_use & 1, ab, 14)) return false;
+        x_use++;
+        tc_fence_after();
+        out = __uint_as_float(tmem_ld1(theirs));
+        tmem_ld_wait();
+        return true;
+    };
+    for (int it = 0; it < nit; ++it) {
+        const int kb = item_block<true>(tile, it);
+        const bool pv = item_pv<true>(tile, it);
+        const bool single = tile.kb1 - tile.kb0 == 1;
+        const int nvalid = min(kBN, tile.lkv - kb * kBN);
+        const int nch = (nvalid + 31) >> 5;
+        const int jbase = kb * kBN;
+        if (!wg_wait(&bars[C::kBarSFull + wg], s_use & 1, ab, 6)) return -1.0f;
+        s_use++;
+        tc_fence_after();
+        auto valid_at = [&](int col) {
+            const int jpos = jbase + col;
+            bool v = col < nvalid;
+            if (prm.mask == GDPA_MASK_CAUSAL_WINDOW)
+                v = v && jpos <= ipos && jpos > ipos - prm.window;
+            return v;
+        };
+        if (!pv || single) {   // row maxima
+            if (warp_rows) {
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = part + 2 * cc;
+                    if (c < nch) {
+#pragma unroll 1
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int col0 = c * 32 + hh * 16;
+                            if (col0 >= nvalid) break;
+                            uint32_t sv[16];
+                            tmem_ld16(s_tmem + col0, sv);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const float t = c2 * __uint_as_float(sv[e]);
+                                m = valid_at(col0 + e) ? fmaxf(m, t) : m;
+                            }
+                        }
+                    }
+                }
+            }
+            if (single || it == nit / 2 - 1) {   // the maxima are complete: combine the parts
+                float mo;
+                if (!exchange(o_tmem_part0 + (uint32_t)(part * (D / 2)),
+                              o_tmem_part0 + (uint32_t)((1 - part) * (D / 2)), m, mo))
+                    return -1.0f;
+                m = fmaxf(m, mo);
+                if (m == -INFINITY) m = 0.0f;   // no valid key: every P is zero
+            }
+        }
+        if (pv) {   // P = 2^(t - m), row sums
+            if (warp_rows) {
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c = part + 2 * cc;
+                    if (c < nch) {
+#pragma unroll 1
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int col0 = c * 32 + hh * 16;
+                            if (col0 >= nvalid) break;
+                            uint32_t sv[16], pk[8];
+                            tmem_ld16(s_tmem + col0, sv);
+                            tmem_ld_wait();
+#pragma unroll
+                            for (int e = 0; e < 16; e += 2) {
+                                float pv2[2];
+#pragma unroll
+                                for (int u = 0; u < 2; ++u) {
+                                    const float w = ex2_approx(fmaf(c2, __uint_as_float(sv[e + u]), -m));
+                                    pv2[u] = valid_at(col0 + e + u) ? w : 0.0f;
+                                    l += pv2[u];
+                                }
+                                pk[e >> 1] = pack_bf16x2(pv2[0], pv2[1]);
+                            }
+                            tmem_st8(s_tmem + c * 32 + hh * 8, pk);
+                        }
+                    }
+                }
+                tmem_st_wait();
+            }
+            if (it == nit - 1) {   // the sums are complete: combine the parts
+                float lo;
+                if (!exchange(s_tmem + (uint32_t)(32 * part + 16),
+                              s_tmem + (uint32_t)(32 * (1 - part) + 16), l, lo))
+                    return -1.0f;
+                l += lo;
+            }
+        }
+        tc_fence_before();
+        mbar_arrive(&bars[C::kBarPFull + wg]);
+    }
+    return l > 0.0f ? 1.0f / l : 0.0f;
+}
+
 template <int D, int ACT>
 __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, uint8_t* smem,
                             uint64_t* bars, uint32_t tmem, int seg0, int seg1, const Abort& ab) {
@@ -298,7 +464,7 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, uint8_
     const uint32_t s_tmem = tmem + wg * 256 + lane_addr;
     const uint32_t o_tmem = tmem + wg * 256 + 128 + lane_addr + part * (D / 2);
     const ActScale ksc = act_scale<ACT>(prm.alpha);
-    uint32_t a = 0, s_use = 0, o_use = 0;
+    uint32_t a = 0, s_use = 0, o_use = 0, x_use = 0;
     for (int t = seg0; t < seg1; ++t) {
         const FwdTile tile = load_tile(prm.tiles + t);
         if (tile.kb1 <= tile.kb0) {
@@ -312,6 +478,13 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, uint8_
         const uint32_t qs = a % C::kNQ;
         const bool warp_rows = quarter * 32 < tile.nq;
         const int ipos = tile.i0 + r;
+        float oscale = 1.0f;   // the softmax variant's 1 / (row sum)
+        if constexpr (ACT == kSoftmax) {
+            oscale = softmax_tile<D>(tile, prm, bars, s_use, x_use, s_tmem,
+                                     tmem + wg * 256 + 128 + lane_addr, (int)wg, part, r, warp_rows,
+                                     ab);
+            if (__any_sync(0xffffffffu, oscale < 0.0f)) return;
+        } else
         for (int kb = tile.kb0; kb < tile.kb1; ++kb) {
             const int nvalid = min(kBN, tile.lkv - kb * kBN);
             const int nch = (nvalid + 31) >> 5;
@@ -385,10 +558,10 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, uint8_
                 for (int u = 0; u < 4; ++u) {
                     const int chunk = (c * 4 + u) ^ (r & kSwz);
                     uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(ov[8 * u + 0]), __uint_as_float(ov[8 * u + 1]));
-                    w.y = pack_bf16x2(__uint_as_float(ov[8 * u + 2]), __uint_as_float(ov[8 * u + 3]));
-                    w.z = pack_bf16x2(__uint_as_float(ov[8 * u + 4]), __uint_as_float(ov[8 * u + 5]));
-                    w.w = pack_bf16x2(__uint_as_float(ov[8 * u + 6]), __uint_as_float(ov[8 * u + 7]));
+                    w.x = pack_bf16x2(oscale * __uint_as_float(ov[8 * u + 0]), oscale * __uint_as_float(ov[8 * u + 1]));
+                    w.y = pack_bf16x2(oscale * __uint_as_float(ov[8 * u + 2]), oscale * __uint_as_float(ov[8 * u + 3]));
+                    w.z = pack_bf16x2(oscale * __uint_as_float(ov[8 * u + 4]), oscale * __uint_as_float(ov[8 * u + 5]));
+                    w.w = pack_bf16x2(oscale * __uint_as_float(ov[8 * u + 6]), oscale * __uint_as_float(ov[8 * u + 7]));
                     *reinterpret_cast<uint4*>(stage + r * kRowBytes + chunk * 16) = w;
                 }
             }
@@ -473,6 +646,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int g = 0; g < kNumWG * kParts; ++g) mbar_init(&bars[C::kBarStage + g], 128);
         mbar_init(&bars[C::kBarMmaDone], 1);
         mbar_init(&bars[C::kBarMmaDone + 1], 1);
+        for (int w = 0; w < kNumWG; ++w) mbar_init(&bars[C::kBarXchg + w], 128 * kParts);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -490,13 +664,13 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     const Abort ab{abort_flag, prm.err};
 
     if (warp == 0) {
-        if (lane == 0) fwd_producer<D>(&tmQ, &tmK, &tmV, prm, smem, bars, seg0, seg1, ab);
+        if (lane == 0) fwd_producer<D, ACT == kSoftmax>(&tmQ, &tmK, &tmV, prm, smem, bars, seg0, seg1, ab);
         __syncwarp();
     } else if (warp == 1) {
-        fwd_mma_s<D>(prm, smem, bars, tmem, seg0, seg1, ab);
+        fwd_mma_s<D, ACT == kSoftmax>(prm, smem, bars, tmem, seg0, seg1, ab);
         __syncwarp();
     } else if (warp == kPvWarp) {
-        fwd_mma_pv<D>(prm, smem, bars, tmem, seg0, seg1, ab);
+        fwd_mma_pv<D, ACT == kSoftmax>(prm, smem, bars, tmem, seg0, seg1, ab);
         __syncwarp();
     } else {
         fwd_compute<D, ACT>(prm, &tmO, smem, bars, tmem, seg0, seg1, ab);
@@ -561,9 +735,15 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
     prm.timing = times != nullptr && smid != nullptr;
     gdpa_status s = GDPA_OK;
     if (d == 128) {
-        GDPA_DISPATCH_ACT(act, A, s = launch<128, A>(S, mq, mk, mv, mo, prm, st))
+        if (act == kSoftmax)
+            s = launch<128, kSoftmax>(S, mq, mk, mv, mo, prm, st);
+        else
+            GDPA_DISPATCH_ACT(act, A, s = launch<128, A>(S, mq, mk, mv, mo, prm, st))
     } else {
-        GDPA_DISPATCH_ACT(act, A, s = launch<64, A>(S, mq, mk, mv, mo, prm, st))
+        if (act == kSoftmax)
+            s = launch<64, kSoftmax>(S, mq, mk, mv, mo, prm, st);
+        else
+            GDPA_DISPATCH_ACT(act, A, s = launch<64, A>(S, mq, mk, mv, mo, prm, st))
     }
     return s;
 }

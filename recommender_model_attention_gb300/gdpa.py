@@ -15,7 +15,8 @@ import numpy as np
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libgdpa_gb300.so")
 
-ACT = {"gelu_erf": 0, "gelu_tanh": 1, "silu": 2, "gelu_taylor6": 3, "identity": 4}
+ACT = {"gelu_erf": 0, "gelu_tanh": 1, "silu": 2, "gelu_taylor6": 3, "identity": 4,
+       "softmax": 5}
 MASK = {"none": 0, "causal_window": 1}
 SCHED = {"zigzag": 0, "round_robin": 1}
 KERNEL = {"auto": 0, "tcgen05": 1, "simt": 2}

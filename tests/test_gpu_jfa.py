@@ -1,0 +1,110 @@
+"""GPU parity of the softmax variant (Jagged Flash Attention forward) against
+the float64 oracle, through the C ABI.
+
+Tolerances as for GDPA: float32 inputs 1e-5 of max|ref|, bf16 inputs 1e-2 of
+max|ref| (P rounded to bf16 before its GEMM).  Cases cover tiles with one key
+block (one pass) and with several (a maxima pass, then weights and P V), the
+causal window, empty samples and rows without a valid key, both head dims of
+the tensor-core kernel and the CUDA-core path.
+"""
+
+import numpy as np
+import pytest
+
+from gpu_util import TOL, compare_full, compare_sampled, pick_samples, small_case, to_dev
+from workloads import get_config, make_inputs, offsets_from_lengths
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gd():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import recommender_model_attention_gb300 as g
+    g.build()
+    return g
+
+
+def _assert(errs, tol):
+    for name, e in errs.items():
+        assert e <= tol, "%s: max rel err %.3e > %.1e (%s)" % (name, e, tol, errs)
+
+
+def _case(lq, lkv, H, d, seed, dtype="bf16", scale=1.0):
+    import torch
+    qo, ko = offsets_from_lengths(np.asarray(lq)), offsets_from_lengths(np.asarray(lkv))
+    g = torch.Generator().manual_seed(seed)
+    x = {"q_off": qo, "kv_off": ko}
+    for n, rows in (("q", qo[-1]), ("k", ko[-1]), ("v", ko[-1])):
+        t = torch.randn((int(rows), H, d), generator=g) * scale
+        x[n] = t.to(torch.bfloat16) if dtype == "bf16" else t
+    x["do"] = None
+    return to_dev(x)
+
+
+@pytest.mark.parametrize("mask,window", [("none", 0), ("causal_window", 40)])
+def test_softmax_f32_simt(gd, mask, window):
+    c = small_case(41, B=6, H=2, d=64, q_range=(0, 300),
+                   kv_range=None if mask != "none" else (0, 200), zero_lengths=True)
+    _assert(compare_full(gd, to_dev(c), 2, 64, 0.125, "softmax", "f32", mask, window,
+                         backward=False), TOL["f32"])
+
+
+@pytest.mark.parametrize("kernel", ["simt", "auto"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_softmax_bf16_one_and_many_key_blocks(gd, kernel, d):
+    # key lengths 1..700: tiles with one key block and with up to six
+    x = _case([300, 5, 129, 64, 1], [700, 128, 1, 257, 40], 3, d, 42 + d)
+    _assert(compare_full(gd, x, 3, d, d ** -0.5, "softmax", "bf16", kernel=kernel,
+                         backward=False), TOL["bf16"])
+
+
+@pytest.mark.parametrize("kernel", ["simt", "auto"])
+@pytest.mark.parametrize("window", [1, 77, 256])
+def test_softmax_bf16_causal_window(gd, kernel, window):
+    lens = [700, 130, 1, 300]
+    x = _case(lens, lens, 2, 128, 50 + window)
+    _assert(compare_full(gd, x, 2, 128, 128 ** -0.5, "softmax", "bf16", "causal_window", window,
+                         kernel=kernel, backward=False), TOL["bf16"])
+
+
+def test_softmax_bf16_empty_samples_and_rows(gd):
+    # zero-length samples on either side; rows past a short key set under a
+    # window of 1 have no valid key and must be zero
+    x = _case([0, 7, 130, 3, 0], [5, 0, 2, 200, 0], 2, 128, 60)
+    _assert(compare_full(gd, x, 2, 128, 128 ** -0.5, "softmax", "bf16", "causal_window", 1,
+                         backward=False), TOL["bf16"])
+
+
+def test_softmax_large_scores_stay_finite(gd):
+    # scores of a few hundred: the maxima keep every exponent <= 0
+    import torch
+    x = _case([200, 64], [500, 90], 2, 128, 61, scale=3.0)
+    plan = gd.Plan(x["q_off"], x["kv_off"], 2, 128)
+    o = gd.gdpa_fwd(plan, x["q"], x["k"], x["v"], alpha=1.0, act="softmax")
+    plan.check()
+    assert torch.isfinite(o.float()).all()
+    _assert(compare_full(gd, x, 2, 128, 1.0, "softmax", "bf16", backward=False), TOL["bf16"])
+
+
+@pytest.mark.parametrize("idx", [2, 3])
+def test_softmax_workload_sampled(gd, idx):
+    # user-ad cross-attention (one key block per tile) and PMA pooling (up to
+    # 64 key blocks per tile) shapes
+    w = get_config(idx)
+    x = make_inputs(w, device="cuda")
+    samples = pick_samples(x["q_off"], x["kv_off"], seed=idx)
+    _assert(compare_sampled(gd, x, samples, w.H, w.d, w.alpha, "softmax", w.mask, w.window),
+            TOL["bf16"])
+
+
+def test_softmax_backward_unsupported(gd):
+    x = _case([10], [10], 1, 64, 62)
+    import torch
+    plan = gd.Plan(x["q_off"], x["kv_off"], 1, 64)
+    do = torch.zeros_like(x["q"])
+    with pytest.raises(gd.GdpaError):
+        gd.gdpa_bwd(plan, x["q"], x["k"], x["v"], do, act="softmax")
+    plan.destroy()
