@@ -210,6 +210,8 @@ def run_reference(args, w):
     per = lq * lkv * w.H * w.d * 12
     n = int(min(w.B, np.searchsorted(np.cumsum(per), 4e10) + 1))
     xh = make_inputs(w, device="cpu", lengths=(lq[:n], lkv[:n]))
+    if w.act == "softmax":
+        xh["do"] = None   # the softmax variant is forward only
     budget = 20.0 / max(1, args.steps + args.warmup)
     vals = []
     base = None
@@ -242,10 +244,16 @@ def main():
                     help="use only the first N sequences of the workload (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--act", default=None,
+                    help="override the workload's activation; 'softmax' times the softmax "
+                         "variant (Jagged Flash Attention, forward only) on the same batch")
     args = ap.parse_args()
 
+    import dataclasses
     from workloads import get_config, make_inputs
     w = get_config(args.workload)
+    if args.act:
+        w = dataclasses.replace(w, act=args.act)
     if args.impl == "reference":
         run_reference(args, w)
         return
@@ -267,6 +275,8 @@ def main():
         lq, lkv = draw_lengths(w)
         lengths = (lq[:args.samples], lkv[:args.samples])
     x = make_inputs(w, device="cuda", seed=rank_seed(w, rank), lengths=lengths)
+    if w.act == "softmax":
+        x["do"] = None   # the softmax variant is forward only
     stream = torch.cuda.current_stream()
     plan = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window)
     # host planning + upload of one batch's plan (it synchronises on its upload)
