@@ -38,8 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # launch by algorithmic bytes).  Valid only for the kernel sources they were
 # measured on (hash of the kernel's source files); otherwise reported null.
 TRAFFIC_RATIO = {
-    "gdpa_fwd": ("d1e2ba50ec136737", 0.9572),
-    "gdpa_bwd": ("60f75169cc1e2d74", 1.0210),
+    "gdpa_fwd": ("b2f68e6006dc4ef3", 0.9641),
+    "gdpa_bwd": ("f9858867097ad2ac", 1.0208),
 }
 KERNEL_SOURCES = {
     "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "act.cuh"),
