@@ -120,7 +120,7 @@ def fwd(q_off, kv_off, q, k, v, alpha, kind, mask="none", window=0):
 
 def bwd(q_off, kv_off, q, k, v, do, alpha, kind, mask="none", window=0):
     if kind == "softmax":
-        raise ValueError("the softmax variant is forward only")
+        raise ValueError("the dense form has no softmax backward (finite differences pin it)")
     q_off, kv_off, Lq, Lkv, Qp, Kp, Vp, M = _setup(q_off, kv_off, q, k, v, mask, window)
     dOp = _pad(np.asarray(do, np.float64), q_off, Lq)
     X = alpha * np.einsum("bihc,bjhc->bhij", Qp, Kp)

@@ -30,7 +30,11 @@
  * Per query row, over its valid keys only: O_i = sum_j w_j V_j with
  * w_j = exp(s_j - m) / sum_l exp(s_l - m), s_j = alpha q_i.k_j, m = max_j s_j
  * (the standard softmax, evaluated with the max subtracted); a row with no
- * valid key gives zero.  Forward only.
+ * valid key gives zero.  Its row statistic lse_i = log sum_j exp(s_j) (-inf
+ * without a valid key) and its gradients, with P_ij the softmax weights,
+ * dP_ij = dO_i.V_j and D_i = sum_j P_ij dP_ij = dO_i.O_i:
+ *     dV_j += P_ij dO_i,  dS_ij = P_ij (dP_ij - D_i),
+ *     dQ_i += alpha dS_ij K_j,  dK_j += alpha dS_ij Q_i.
  *
  * Layout: token-major with heads interleaved, X[t][h][c], t a global token
  * index, q_off / kv_off exclusive prefix sums of the per-sample lengths.
@@ -154,6 +158,106 @@ static void ref_softmax_row(const double* q, const double* K, const double* V, d
         for (int c = 0; c < d; ++c) o[c] += w * v[c];
     }
     for (int c = 0; c < d; ++c) o[c] /= z;
+}
+
+/* lse[t][h] of the softmax variant */
+void gdpa_ref_lse(int B, int H, int d, const int32_t* q_off, const int32_t* kv_off,
+                  const double* Q, const double* K, double* lse, double alpha, int mask,
+                  int window) {
+    const int64_t row = (int64_t)H * d;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            int lq = q_off[b + 1] - q_off[b], lkv = kv_off[b + 1] - kv_off[b];
+            for (int i = 0; i < lq; ++i) {
+                const double* q = Q + (int64_t)(q_off[b] + i) * row + (int64_t)h * d;
+                double m = -INFINITY, z = 0.0;
+                for (int pass = 0; pass < 2; ++pass) {
+                    for (int j = 0; j < lkv; ++j) {
+                        if (!ref_valid(i, j, mask, window)) continue;
+                        const double* k = K + (int64_t)(kv_off[b] + j) * row + (int64_t)h * d;
+                        double s = 0.0;
+                        for (int c = 0; c < d; ++c) s += q[c] * k[c];
+                        if (pass == 0) {
+                            if (alpha * s > m) m = alpha * s;
+                        } else {
+                            z += exp(alpha * s - m);
+                        }
+                    }
+                    if (m == -INFINITY) break;
+                }
+                lse[(int64_t)(q_off[b] + i) * H + h] = m == -INFINITY ? -INFINITY : m + log(z);
+            }
+        }
+    }
+}
+
+/* Gradients of the softmax variant (see the header comment) */
+void gdpa_ref_softmax_bwd(int B, int H, int d, const int32_t* q_off, const int32_t* kv_off,
+                          const double* Q, const double* K, const double* V, const double* dO,
+                          double* dQ, double* dK, double* dV, double alpha, int mask, int window) {
+    const int64_t row = (int64_t)H * d;
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b) {
+        for (int h = 0; h < H; ++h) {
+            int lq = q_off[b + 1] - q_off[b], lkv = kv_off[b + 1] - kv_off[b];
+            for (int i = 0; i < lq; ++i) {
+                double* dq = dQ + (int64_t)(q_off[b] + i) * row + (int64_t)h * d;
+                for (int c = 0; c < d; ++c) dq[c] = 0.0;
+            }
+            for (int j = 0; j < lkv; ++j) {
+                double* dk = dK + (int64_t)(kv_off[b] + j) * row + (int64_t)h * d;
+                double* dv = dV + (int64_t)(kv_off[b] + j) * row + (int64_t)h * d;
+                for (int c = 0; c < d; ++c) { dk[c] = 0.0; dv[c] = 0.0; }
+            }
+            for (int i = 0; i < lq; ++i) {
+                const double* q = Q + (int64_t)(q_off[b] + i) * row + (int64_t)h * d;
+                const double* go = dO + (int64_t)(q_off[b] + i) * row + (int64_t)h * d;
+                double* dq = dQ + (int64_t)(q_off[b] + i) * row + (int64_t)h * d;
+                /* the row's weights P_ij and dP_ij, then D_i */
+                double m = -INFINITY, z = 0.0, dsum = 0.0;
+                for (int j = 0; j < lkv; ++j) {
+                    if (!ref_valid(i, j, mask, window)) continue;
+                    const double* k = K + (int64_t)(kv_off[b] + j) * row + (int64_t)h * d;
+                    double s = 0.0;
+                    for (int c = 0; c < d; ++c) s += q[c] * k[c];
+                    if (alpha * s > m) m = alpha * s;
+                }
+                if (m == -INFINITY) continue;   /* no valid key: no gradient */
+                for (int j = 0; j < lkv; ++j) {
+                    if (!ref_valid(i, j, mask, window)) continue;
+                    const double* k = K + (int64_t)(kv_off[b] + j) * row + (int64_t)h * d;
+                    double s = 0.0;
+                    for (int c = 0; c < d; ++c) s += q[c] * k[c];
+                    z += exp(alpha * s - m);
+                }
+                for (int j = 0; j < lkv; ++j) {
+                    if (!ref_valid(i, j, mask, window)) continue;
+                    const double* k = K + (int64_t)(kv_off[b] + j) * row + (int64_t)h * d;
+                    const double* v = V + (int64_t)(kv_off[b] + j) * row + (int64_t)h * d;
+                    double s = 0.0, dp = 0.0;
+                    for (int c = 0; c < d; ++c) { s += q[c] * k[c]; dp += go[c] * v[c]; }
+                    dsum += exp(alpha * s - m) / z * dp;
+                }
+                for (int j = 0; j < lkv; ++j) {
+                    if (!ref_valid(i, j, mask, window)) continue;
+                    const double* k = K + (int64_t)(kv_off[b] + j) * row + (int64_t)h * d;
+                    const double* v = V + (int64_t)(kv_off[b] + j) * row + (int64_t)h * d;
+                    double* dk = dK + (int64_t)(kv_off[b] + j) * row + (int64_t)h * d;
+                    double* dv = dV + (int64_t)(kv_off[b] + j) * row + (int64_t)h * d;
+                    double s = 0.0, dp = 0.0;
+                    for (int c = 0; c < d; ++c) { s += q[c] * k[c]; dp += go[c] * v[c]; }
+                    const double p = exp(alpha * s - m) / z;
+                    const double g = p * (dp - dsum);
+                    for (int c = 0; c < d; ++c) {
+                        dv[c] += p * go[c];
+                        dq[c] += alpha * g * k[c];
+                        dk[c] += alpha * g * q[c];
+                    }
+                }
+            }
+        }
+    }
 }
 
 /* O[t][h][:] = sum over valid j of act(alpha * Q_t . K_j) V_j (kind 5: the

@@ -54,6 +54,12 @@ def _load():
         lib.gdpa_ref_bwd.restype = None
         lib.gdpa_ref_bwd.argtypes = [ctypes.c_int] * 3 + [i32p, i32p] + [dp] * 7 + [
             ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_int]
+        lib.gdpa_ref_lse.restype = None
+        lib.gdpa_ref_lse.argtypes = [ctypes.c_int] * 3 + [i32p, i32p] + [dp] * 3 + [
+            ctypes.c_double, ctypes.c_int, ctypes.c_int]
+        lib.gdpa_ref_softmax_bwd.restype = None
+        lib.gdpa_ref_softmax_bwd.argtypes = [ctypes.c_int] * 3 + [i32p, i32p] + [dp] * 7 + [
+            ctypes.c_double, ctypes.c_int, ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -113,8 +119,6 @@ def fwd(q_off, kv_off, q, k, v, alpha: float, act: str, mask: str = "none",
 def bwd(q_off, kv_off, q, k, v, do, alpha: float, act: str, mask: str = "none",
         window: int = 0):
     """(dQ, dK, dV) for a jagged batch given the upstream gradient dO."""
-    if act == "softmax":
-        raise ValueError("the softmax variant is forward only")
     qo, qp = _i32(q_off)
     ko, kp = _i32(kv_off)
     Q, Qp = _f64(to_f64(q))
@@ -126,10 +130,31 @@ def bwd(q_off, kv_off, q, k, v, do, alpha: float, act: str, mask: str = "none",
     dK = np.zeros_like(K)
     dV = np.zeros_like(V)
     dp = ctypes.POINTER(ctypes.c_double)
+    if act == "softmax":
+        _load().gdpa_ref_softmax_bwd(len(qo) - 1, H, d, qp, kp, Qp, Kp, Vp, dOp,
+                                     dQ.ctypes.data_as(dp), dK.ctypes.data_as(dp),
+                                     dV.ctypes.data_as(dp), float(alpha), MASK_IDS[mask],
+                                     int(window))
+        return dQ, dK, dV
     _load().gdpa_ref_bwd(len(qo) - 1, H, d, qp, kp, Qp, Kp, Vp, dOp,
                          dQ.ctypes.data_as(dp), dK.ctypes.data_as(dp), dV.ctypes.data_as(dp),
                          float(alpha), ACT_IDS[act], MASK_IDS[mask], int(window))
     return dQ, dK, dV
+
+
+def lse(q_off, kv_off, q, k, alpha: float, mask: str = "none", window: int = 0):
+    """Row log-sum-exp [T, H] of the softmax variant (-inf for a row without
+    a valid key)."""
+    qo, qp = _i32(q_off)
+    ko, kp = _i32(kv_off)
+    Q, Qp = _f64(to_f64(q))
+    K, Kp = _f64(to_f64(k))
+    T, H, d = Q.shape
+    out = np.zeros((T, H), dtype=np.float64)
+    _load().gdpa_ref_lse(len(qo) - 1, H, d, qp, kp, Qp, Kp,
+                         out.ctypes.data_as(ctypes.POINTER(ctypes.c_double)), float(alpha),
+                         MASK_IDS[mask], int(window))
+    return out
 
 
 def sub_batch(q_off, kv_off, samples):

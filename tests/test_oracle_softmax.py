@@ -1,5 +1,5 @@
-"""Pins of the oracle's softmax variant (Jagged Flash Attention, forward) to
-facts outside its loops (CPU only):
+"""Pins of the oracle's softmax variant (Jagged Flash Attention) to facts
+outside its loops (CPU only):
 
 * the dense padded formulation through SciPy's softmax (brute force);
 * partition of unity: with V = 1 every row with a valid key gives exactly 1;
@@ -7,7 +7,10 @@ facts outside its loops (CPU only):
 * a row-wise constant added to every score of a row (an extra feature
   dimension) changes nothing (shift invariance);
 * a single valid key returns its V row; a huge scale selects the argmax key;
-* rows without a valid key are zero.
+* rows without a valid key are zero;
+* the gradients against central differences of the forward, the row
+  log-sum-exp against SciPy's logsumexp, and dV's column sums (each query
+  row's weights sum to one).
 """
 
 import numpy as np
@@ -92,3 +95,59 @@ def test_softmax_bf16_like_case_against_brute():
     want = brute.fwd(c["q_off"], c["kv_off"], ref.to_f64(c["q"]), ref.to_f64(c["k"]),
                      ref.to_f64(c["v"]), 0.25, "softmax")
     assert np.max(np.abs(got - want)) <= 1e-12 * np.max(np.abs(want))
+
+
+@pytest.mark.parametrize("mask,window", [("none", 0), ("causal_window", 2)])
+def test_softmax_gradients_by_finite_differences(mask, window):
+    rng = np.random.Generator(np.random.PCG64(9))
+    lq = np.array([3, 5]) if mask == "causal_window" else np.array([3, 4])
+    lkv = lq.copy() if mask == "causal_window" else np.array([5, 2])
+    qo, ko = offsets_from_lengths(lq), offsets_from_lengths(lkv)
+    H, d, alpha = 1, 4, 0.8
+    q = rng.standard_normal((qo[-1], H, d))
+    k = rng.standard_normal((ko[-1], H, d))
+    v = rng.standard_normal((ko[-1], H, d))
+    do = rng.standard_normal((qo[-1], H, d))
+    dq, dk, dv = ref.bwd(qo, ko, q, k, v, do, alpha, "softmax", mask, window)
+
+    def loss(qq, kk, vv):
+        return float(np.sum(ref.fwd(qo, ko, qq, kk, vv, alpha, "softmax", mask, window) * do))
+
+    h = 1e-6
+    for which, grad in ((0, dq), (1, dk), (2, dv)):
+        base = [q, k, v]
+        fd = np.zeros_like(base[which])
+        for idx in np.ndindex(*fd.shape):
+            plus = [x.copy() for x in base]
+            minus = [x.copy() for x in base]
+            plus[which][idx] += h
+            minus[which][idx] -= h
+            fd[idx] = (loss(*plus) - loss(*minus)) / (2 * h)
+        assert np.max(np.abs(grad - fd)) <= 1e-6 * max(1.0, np.max(np.abs(fd)))
+
+
+def test_softmax_lse_against_scipy_logsumexp():
+    from scipy import special
+    qo, ko, q, k, v = _case(10, [6, 3, 0, 5], [4, 0, 3, 5])
+    got = ref.lse(qo, ko, q, k, 0.6, "causal_window", 3)
+    for b in range(4):
+        for i in range(qo[b + 1] - qo[b]):
+            js = [j for j in range(ko[b + 1] - ko[b]) if i - 3 < j <= i]
+            for h in range(q.shape[1]):
+                if not js:
+                    assert got[qo[b] + i, h] == -np.inf
+                    continue
+                s = 0.6 * (k[ko[b] + np.array(js), h] @ q[qo[b] + i, h])
+                assert abs(got[qo[b] + i, h] - special.logsumexp(s)) <= 1e-12
+
+
+def test_softmax_gradient_of_values_is_weighted_do():
+    # dV_j = sum_i P_ij dO_i: with dO = 1 per row, each column of dV is the
+    # total softmax weight key j receives
+    qo, ko, q, k, v = _case(11, [4, 2], [3, 3])
+    do = np.ones_like(q)
+    _, _, dv = ref.bwd(qo, ko, q, k, v, do, 1.0, "softmax")
+    # every query row's weights sum to 1, so a sample's dV rows sum to its Lq
+    for b in range(2):
+        tot = dv[ko[b]:ko[b + 1]].sum(axis=0)
+        assert np.allclose(tot, qo[b + 1] - qo[b], atol=1e-12)
