@@ -64,8 +64,9 @@ typedef enum {
     /* Softmax variant: O_i = sum_j softmax_j(alpha q_i.k_j) V_j over the row's
      * valid keys (0 for a row without one), i.e. Jagged Flash Attention, the
      * softmax kernel the GEM page (aitrends.kr, kernel list) names beside
-     * GDPA.  gdpa_fwd and gdpa_fwd_noalloc only; gdpa_bwd returns
-     * UNSUPPORTED, gdpa_act_eval INVALID_ARG. */
+     * GDPA.  gdpa_fwd, gdpa_fwd_noalloc and gdpa_softmax_fwd; its gradients
+     * come from gdpa_softmax_bwd (gdpa_bwd returns UNSUPPORTED);
+     * gdpa_act_eval returns INVALID_ARG. */
     GDPA_ACT_SOFTMAX = 5
 } gdpa_act;
 
@@ -244,6 +245,33 @@ void gdpa_plan_destroy(gdpa_plan plan);
 gdpa_status gdpa_fwd_noalloc(const int32_t* q_off_host, const int32_t* kv_off_host, int B, int H,
                              int d, gdpa_mask mask, int window, const void* q, const void* k,
                              const void* v, void* o, float alpha, gdpa_act act, void* stream);
+
+/* Softmax variant (Jagged Flash Attention) with its row statistics.
+ *
+ * As gdpa_fwd with act = GDPA_ACT_SOFTMAX, and also writes
+ *   lse[t][h] = log sum_j exp(alpha q_t.k_j)   (natural log; over the row's
+ *               valid keys; -inf for a row without one),
+ * device float32 [Tq][H] (caller-owned; required when Tq > 0), which the
+ * backward needs.  Same dtypes, shapes, errors and kernels as gdpa_fwd.
+ */
+gdpa_status gdpa_softmax_fwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k,
+                             const void* v, void* o, float* lse, float alpha, void* stream);
+
+/* Gradients of the softmax variant.
+ *
+ * With P_tj = exp(alpha q_t.k_j - lse_t) over the valid pairs, dP_tj =
+ * dO_t.V_j and D_t = dO_t.O_t:
+ *   dV_j = sum_t P_tj dO_t,   dS_tj = P_tj (dP_tj - D_t),
+ *   dQ_t = alpha sum_j dS_tj K_j,   dK_j = alpha sum_t dS_tj Q_t.
+ * o and lse are gdpa_softmax_fwd's outputs for the same q, k, v, plan and
+ * alpha; d_o has o's dtype and shape; dq, dk, dv as gdpa_bwd (float32, fully
+ * written).  D goes to a [Tq][H] float32 workspace the plan allocates on the
+ * first call (ALLOC on failure) and keeps until gdpa_plan_destroy.  Errors
+ * as gdpa_bwd, plus INVALID_ARG for a NULL or misaligned o or a NULL lse.
+ */
+gdpa_status gdpa_softmax_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k,
+                             const void* v, const void* o, const void* d_o, const float* lse,
+                             float* dq, float* dk, float* dv, float alpha, void* stream);
 
 /* Activation test hook.
  *

@@ -22,6 +22,8 @@ from .gdpa import (  # noqa: F401
     gdpa_bwd,
     gdpa_fwd,
     gdpa_fwd_noalloc,
+    gdpa_softmax_bwd,
+    gdpa_softmax_fwd,
     lib,
 )
 

@@ -39,6 +39,14 @@ constexpr float kT6c6 = kRsqrt2Pi / 40.0f;
 // tanh-form Gaussian CDF for GELU-erf (see the header)
 constexpr float kG0 = 0.7999136459f;
 constexpr float kG1 = 0.0349731511f;
+constexpr float kLog2e = 1.44269504088896340736f;
+
+// 2^x (the softmax variant's weights)
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 __device__ __forceinline__ float tanh_approx(float x) {
     float y;
@@ -180,6 +188,8 @@ __device__ __forceinline__ ActScale act_scale(float alpha) {
         g1 = kSqrt2OverPi * kTanhCubic;
     } else if constexpr (ACT == kSilu) {
         g0 = 0.5f;
+    } else if constexpr (ACT == kSoftmax) {
+        g0 = kLog2e;   // c0 = alpha log2(e): exponents in base 2
     }
     const float a2 = alpha * alpha;
     return ActScale{alpha, 0.5f * alpha, g0 * alpha, g1 * a2 * alpha, g0, 3.0f * g1 * a2};

@@ -36,6 +36,7 @@ void free_plan(Plan* p) {
         cudaFree(p->d_err);
         cudaFree(p->d_times);
         cudaFree(p->d_smid);
+        cudaFree(p->d_delta);
         if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
     }
     delete p;
@@ -209,8 +210,11 @@ gdpa_status gdpa_plan_set_timing(gdpa_plan plan, int enable) {
 
 int64_t gdpa_plan_launches(gdpa_plan plan) { return plan ? ((Plan*)plan)->launches : -1; }
 
-gdpa_status gdpa_fwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k, const void* v,
-                     void* o, float alpha, gdpa_act act, void* stream) {
+namespace {
+
+gdpa_status fwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k,
+                       const void* v, void* o, float* lse, float alpha, gdpa_act act,
+                       void* stream) {
     if (!plan || ((Plan*)plan)->host_only) return GDPA_ERR_INVALID_ARG;
     Plan& p = *(Plan*)plan;
     if (dtype != GDPA_BF16 && dtype != GDPA_F32) return GDPA_ERR_INVALID_ARG;
@@ -222,18 +226,20 @@ gdpa_status gdpa_fwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void
     if (p.n_fwd == 0) return GDPA_OK;
     cudaStream_t st = (cudaStream_t)stream;
     if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
-    if (use_tc(p, dtype)) return gdpa::launch_tc_fwd(p, q, k, v, o, alpha, act, st);
-    return gdpa::launch_simt_fwd(p, dtype, q, k, v, o, alpha, act, st);
+    if (use_tc(p, dtype)) return gdpa::launch_tc_fwd(p, q, k, v, o, lse, alpha, act, st);
+    return gdpa::launch_simt_fwd(p, dtype, q, k, v, o, lse, alpha, act, st);
 }
 
-gdpa_status gdpa_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k, const void* v,
-                     const void* d_o, float* dq, float* dk, float* dv, float alpha, gdpa_act act,
-                     void* stream) {
+gdpa_status bwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k,
+                       const void* v, const void* o, const void* d_o, const float* lse, float* dq,
+                       float* dk, float* dv, float alpha, gdpa_act act, void* stream) {
     if (!plan || ((Plan*)plan)->host_only) return GDPA_ERR_INVALID_ARG;
     Plan& p = *(Plan*)plan;
     if (dtype != GDPA_BF16 && dtype != GDPA_F32) return GDPA_ERR_INVALID_ARG;
     if (!valid_act(act)) return GDPA_ERR_INVALID_ARG;
-    if (act == GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;   // forward only
+    const bool sm = act == GDPA_ACT_SOFTMAX;
+    if (sm && p.Tq > 0 && (!o || !lse)) return GDPA_ERR_INVALID_ARG;
+    if (sm && !aligned16(o)) return GDPA_ERR_INVALID_ARG;
     if (p.Tq > 0 && (!q || !d_o || !dq)) return GDPA_ERR_INVALID_ARG;
     if (p.Tkv > 0 && (!k || !v || !dk || !dv)) return GDPA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) || !aligned16(dq) ||
@@ -242,8 +248,49 @@ gdpa_status gdpa_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void
     if (p.fwd_split) return GDPA_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
-    if (use_tc(p, dtype)) return gdpa::launch_tc_bwd(p, q, k, v, d_o, dq, dk, dv, alpha, act, st);
-    return gdpa::launch_simt_bwd(p, dtype, q, k, v, d_o, dq, dk, dv, alpha, act, st);
+    const float* delta = nullptr;
+    if (sm && p.Tq > 0) {
+        // D = dO . O per row, in the plan's workspace (allocated once)
+        if (!p.d_delta &&
+            cudaMalloc((void**)&p.d_delta, (size_t)p.Tq * p.H * sizeof(float)) != cudaSuccess) {
+            p.d_delta = nullptr;
+            return GDPA_ERR_ALLOC;
+        }
+        const gdpa_status s = gdpa::launch_row_dot(p, dtype, d_o, o, p.d_delta, st);
+        if (s != GDPA_OK) return s;
+        delta = p.d_delta;
+    }
+    if (use_tc(p, dtype))
+        return gdpa::launch_tc_bwd(p, q, k, v, d_o, dq, dk, dv, alpha, act, lse, delta, st);
+    return gdpa::launch_simt_bwd(p, dtype, q, k, v, d_o, dq, dk, dv, alpha, act, lse, delta, st);
+}
+
+}  // namespace
+
+gdpa_status gdpa_fwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k, const void* v,
+                     void* o, float alpha, gdpa_act act, void* stream) {
+    return fwd_common(plan, dtype, q, k, v, o, nullptr, alpha, act, stream);
+}
+
+gdpa_status gdpa_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k, const void* v,
+                     const void* d_o, float* dq, float* dk, float* dv, float alpha, gdpa_act act,
+                     void* stream) {
+    // the softmax variant's gradients need O and the row statistics
+    if (act == GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
+    return bwd_common(plan, dtype, q, k, v, nullptr, d_o, nullptr, dq, dk, dv, alpha, act, stream);
+}
+
+gdpa_status gdpa_softmax_fwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k,
+                             const void* v, void* o, float* lse, float alpha, void* stream) {
+    if (plan && ((Plan*)plan)->Tq > 0 && !lse) return GDPA_ERR_INVALID_ARG;
+    return fwd_common(plan, dtype, q, k, v, o, lse, alpha, GDPA_ACT_SOFTMAX, stream);
+}
+
+gdpa_status gdpa_softmax_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k,
+                             const void* v, const void* o, const void* d_o, const float* lse,
+                             float* dq, float* dk, float* dv, float alpha, void* stream) {
+    return bwd_common(plan, dtype, q, k, v, o, d_o, lse, dq, dk, dv, alpha, GDPA_ACT_SOFTMAX,
+                      stream);
 }
 
 gdpa_status gdpa_check(gdpa_plan plan, void* stream) {

@@ -63,6 +63,9 @@ struct Plan {
     int32_t* d_smid = nullptr;               // [2][S]
     int timed[2] = {0, 0};
     int64_t launches = 0;
+    // softmax-variant backward: dO_t . O_t per row and head, [Tq][H] float,
+    // allocated on first use
+    float* d_delta = nullptr;
 };
 
 // Host planner (gdpa_plan.cpp): fills the host-side vectors of `p` from the
@@ -70,20 +73,27 @@ struct Plan {
 gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off);
 
 // Kernel launchers.  Arguments are already validated by the ABI layer.
+// lse (softmax variant, may be NULL): row log-sum-exp out; lse / delta in
+// the backward: that output and dO.O per row (softmax variant only).
 gdpa_status launch_simt_fwd(Plan& p, gdpa_dtype dt, const void* q, const void* k, const void* v,
-                            void* o, float alpha, int act, cudaStream_t st);
+                            void* o, float* lse, float alpha, int act, cudaStream_t st);
 gdpa_status launch_simt_bwd(Plan& p, gdpa_dtype dt, const void* q, const void* k, const void* v,
                             const void* d_o, float* dq, float* dk, float* dv, float alpha, int act,
-                            cudaStream_t st);
+                            const float* lse, const float* delta, cudaStream_t st);
 gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, void* o,
-                          float alpha, int act, cudaStream_t st);
+                          float* lse, float alpha, int act, cudaStream_t st);
 // Forward tensor-core launch on explicit device buffers (tile queue, queue
 // starts, error word; times/smid may be NULL to skip per-CTA timing).
 gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, int32_t* err,
                               unsigned long long* times, int32_t* smid, int H, int d, int64_t Tq,
                               int64_t Tkv, int mask, int window, const void* q, const void* k,
-                              const void* v, void* o, float alpha, int act, cudaStream_t st);
+                              const void* v, void* o, float* lse, float alpha, int act,
+                              cudaStream_t st);
 gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, const void* d_o,
-                          float* dq, float* dk, float* dv, float alpha, int act, cudaStream_t st);
+                          float* dq, float* dk, float* dv, float alpha, int act, const float* lse,
+                          const float* delta, cudaStream_t st);
+// delta[t][h] = dO[t][h][:] . O[t][h][:] over rows t < Tq (softmax variant)
+gdpa_status launch_row_dot(Plan& p, gdpa_dtype dt, const void* d_o, const void* o, float* delta,
+                           cudaStream_t st);
 
 }  // namespace gdpa

@@ -94,8 +94,8 @@ simt_fwd_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__ Q, cons
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 simt_softmax_fwd_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__ Q,
-                        const T* __restrict__ K, const T* __restrict__ V, T* __restrict__ O, int H,
-                        int d, float alpha, int mask, int window) {
+                        const T* __restrict__ K, const T* __restrict__ V, T* __restrict__ O,
+                        float* __restrict__ lse, int H, int d, float alpha, int mask, int window) {
     const FwdTile t = tiles[blockIdx.x];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)H * d;
@@ -126,6 +126,7 @@ simt_softmax_fwd_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__
             const int e = lane + 32 * c;
             if (e < d) stf(O + qrow + e, o[c] * inv);
         }
+        if (lse && lane == 0) lse[(int64_t)(t.qt0 + r) * H + t.h] = l > 0.0f ? m + logf(l) : -INFINITY;
     }
 }
 
@@ -134,7 +135,8 @@ template <int ACT, typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 simt_bwd_dq_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__ Q,
                    const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
-                   float* __restrict__ dQ, int H, int d, float alpha, int mask, int window) {
+                   float* __restrict__ dQ, int H, int d, float alpha, int mask, int window,
+                   const float* __restrict__ lse, const float* __restrict__ delta) {
     const FwdTile t = tiles[blockIdx.x];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)H * d;
@@ -145,13 +147,22 @@ simt_bwd_dq_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__ Q,
         load_row(go, dO + qrow, d, lane);
         int lo, hi;
         key_range(t.i0 + r, t.kb0, t.kb1, t.lkv, mask, window, lo, hi);
+        float lse_i = 0.0f, d_i = 0.0f;   // softmax variant: the row's lse and dO.O
+        if constexpr (ACT == kSoftmax) {
+            lse_i = lse[(int64_t)(t.qt0 + r) * H + t.h];
+            d_i = delta[(int64_t)(t.qt0 + r) * H + t.h];
+        }
         for (int j = lo; j < hi; ++j) {
             const int64_t krow = (int64_t)(t.kvt0 + j) * row + (int64_t)t.h * d;
             float kx[kPer], vx[kPer];
             load_row(kx, K + krow, d, lane);
             load_row(vx, V + krow, d, lane);
             const float x = alpha * dot_row(q, kx);
-            const float g = dot_row(go, vx) * dact_f<ACT, false>(x);
+            float g;
+            if constexpr (ACT == kSoftmax)
+                g = expf(x - lse_i) * (dot_row(go, vx) - d_i);
+            else
+                g = dot_row(go, vx) * dact_f<ACT, false>(x);
 #pragma unroll
             for (int c = 0; c < kPer; ++c) acc[c] = fmaf(g, kx[c], acc[c]);
         }
@@ -169,7 +180,8 @@ __global__ void __launch_bounds__(kWarps * 32)
 simt_bwd_dkdv_kernel(const BwdUnit* __restrict__ units, const T* __restrict__ Q,
                      const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
                      float* __restrict__ dK, float* __restrict__ dV, int H, int d, float alpha,
-                     int mask, int window) {
+                     int mask, int window, const float* __restrict__ lse,
+                     const float* __restrict__ delta) {
     const BwdUnit u = units[blockIdx.x];
     const int h = u.hf & 0xffff;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -191,9 +203,16 @@ simt_bwd_dkdv_kernel(const BwdUnit* __restrict__ units, const T* __restrict__ Q,
             load_row(q, Q + qrow, d, lane);
             load_row(go, dO + qrow, d, lane);
             const float x = alpha * dot_row(q, kx);
-            float a, da;
-            act_dact_f<ACT, false>(x, a, da);
-            const float g = dot_row(go, vx) * da;
+            float a, g;
+            if constexpr (ACT == kSoftmax) {
+                const int64_t ri = (int64_t)(u.qt0 + i) * H + h;
+                a = expf(x - lse[ri]);
+                g = a * (dot_row(go, vx) - delta[ri]);
+            } else {
+                float da;
+                act_dact_f<ACT, false>(x, a, da);
+                g = dot_row(go, vx) * da;
+            }
 #pragma unroll
             for (int c = 0; c < kPer; ++c) {
                 ak[c] = fmaf(g, q[c], ak[c]);
@@ -212,12 +231,12 @@ simt_bwd_dkdv_kernel(const BwdUnit* __restrict__ units, const T* __restrict__ Q,
 }
 
 template <typename T>
-gdpa_status fwd_impl(Plan& p, const void* q, const void* k, const void* v, void* o, float alpha,
-                     int act, cudaStream_t st) {
+gdpa_status fwd_impl(Plan& p, const void* q, const void* k, const void* v, void* o, float* lse,
+                     float alpha, int act, cudaStream_t st) {
     const unsigned grid = (unsigned)p.n_fwd;
     if (act == kSoftmax) {
         simt_softmax_fwd_kernel<T><<<grid, kWarps * 32, 0, st>>>(
-            p.d_fwd, (const T*)q, (const T*)k, (const T*)v, (T*)o, p.H, p.d, alpha, p.mask,
+            p.d_fwd, (const T*)q, (const T*)k, (const T*)v, (T*)o, lse, p.H, p.d, alpha, p.mask,
             p.window);
         p.launches += 1;
         return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
@@ -232,7 +251,23 @@ gdpa_status fwd_impl(Plan& p, const void* q, const void* k, const void* v, void*
 
 template <typename T>
 gdpa_status bwd_impl(Plan& p, const void* q, const void* k, const void* v, const void* d_o,
-                     float* dq, float* dk, float* dv, float alpha, int act, cudaStream_t st) {
+                     float* dq, float* dk, float* dv, float alpha, int act, const float* lse,
+                     const float* delta, cudaStream_t st) {
+    if (act == kSoftmax) {
+        if (p.n_fwd > 0) {
+            simt_bwd_dq_kernel<kSoftmax, T><<<(unsigned)p.n_fwd, kWarps * 32, 0, st>>>(
+                p.d_fwd, (const T*)q, (const T*)k, (const T*)v, (const T*)d_o, dq, p.H, p.d,
+                alpha, p.mask, p.window, lse, delta);
+            p.launches += 1;
+        }
+        if (p.n_bwd > 0) {
+            simt_bwd_dkdv_kernel<kSoftmax, T><<<(unsigned)p.n_bwd, kWarps * 32, 0, st>>>(
+                p.d_bwd, (const T*)q, (const T*)k, (const T*)v, (const T*)d_o, dk, dv, p.H, p.d,
+                alpha, p.mask, p.window, lse, delta);
+            p.launches += 1;
+        }
+        return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+    }
     // The forward tiles (zero tiles included) cover every query row once and
     // the backward units every key row once, so both kernels store their
     // rows directly and nothing needs clearing first.
@@ -240,14 +275,14 @@ gdpa_status bwd_impl(Plan& p, const void* q, const void* k, const void* v, const
         GDPA_DISPATCH_ACT(act, A,
             simt_bwd_dq_kernel<A, T><<<(unsigned)p.n_fwd, kWarps * 32, 0, st>>>(
                 p.d_fwd, (const T*)q, (const T*)k, (const T*)v, (const T*)d_o, dq, p.H, p.d,
-                alpha, p.mask, p.window))
+                alpha, p.mask, p.window, nullptr, nullptr))
         p.launches += 1;
     }
     if (p.n_bwd > 0) {
         GDPA_DISPATCH_ACT(act, A,
             simt_bwd_dkdv_kernel<A, T><<<(unsigned)p.n_bwd, kWarps * 32, 0, st>>>(
                 p.d_bwd, (const T*)q, (const T*)k, (const T*)v, (const T*)d_o, dk, dv, p.H, p.d,
-                alpha, p.mask, p.window))
+                alpha, p.mask, p.window, nullptr, nullptr))
         p.launches += 1;
     }
     return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
@@ -256,16 +291,51 @@ gdpa_status bwd_impl(Plan& p, const void* q, const void* k, const void* v, const
 }  // namespace
 
 gdpa_status launch_simt_fwd(Plan& p, gdpa_dtype dt, const void* q, const void* k, const void* v,
-                            void* o, float alpha, int act, cudaStream_t st) {
-    if (dt == GDPA_F32) return fwd_impl<float>(p, q, k, v, o, alpha, act, st);
-    return fwd_impl<__nv_bfloat16>(p, q, k, v, o, alpha, act, st);
+                            void* o, float* lse, float alpha, int act, cudaStream_t st) {
+    if (dt == GDPA_F32) return fwd_impl<float>(p, q, k, v, o, lse, alpha, act, st);
+    return fwd_impl<__nv_bfloat16>(p, q, k, v, o, lse, alpha, act, st);
 }
 
 gdpa_status launch_simt_bwd(Plan& p, gdpa_dtype dt, const void* q, const void* k, const void* v,
                             const void* d_o, float* dq, float* dk, float* dv, float alpha, int act,
-                            cudaStream_t st) {
-    if (dt == GDPA_F32) return bwd_impl<float>(p, q, k, v, d_o, dq, dk, dv, alpha, act, st);
-    return bwd_impl<__nv_bfloat16>(p, q, k, v, d_o, dq, dk, dv, alpha, act, st);
+                            const float* lse, const float* delta, cudaStream_t st) {
+    if (dt == GDPA_F32)
+        return bwd_impl<float>(p, q, k, v, d_o, dq, dk, dv, alpha, act, lse, delta, st);
+    return bwd_impl<__nv_bfloat16>(p, q, k, v, d_o, dq, dk, dv, alpha, act, lse, delta, st);
+}
+
+namespace {
+
+// one warp per (token, head) row
+template <typename T>
+__global__ void __launch_bounds__(256)
+row_dot_kernel(const T* __restrict__ a, const T* __restrict__ b, float* __restrict__ out,
+               int64_t rows, int d) {
+    const int64_t rw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (rw >= rows) return;
+    float x[kPer], y[kPer];
+    load_row(x, a + rw * d, d, lane);
+    load_row(y, b + rw * d, d, lane);
+    const float s = dot_row(x, y);
+    if (lane == 0) out[rw] = s;
+}
+
+}  // namespace
+
+gdpa_status launch_row_dot(Plan& p, gdpa_dtype dt, const void* d_o, const void* o, float* delta,
+                           cudaStream_t st) {
+    const int64_t rows = p.Tq * p.H;
+    if (rows == 0) return GDPA_OK;
+    const unsigned grid = (unsigned)((rows + 7) / 8);
+    if (dt == GDPA_F32)
+        row_dot_kernel<float><<<grid, 256, 0, st>>>((const float*)d_o, (const float*)o, delta, rows,
+                                                    p.d);
+    else
+        row_dot_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+            (const __nv_bfloat16*)d_o, (const __nv_bfloat16*)o, delta, rows, p.d);
+    p.launches += 1;
+    return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
 }  // namespace gdpa

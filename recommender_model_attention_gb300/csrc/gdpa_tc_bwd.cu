@@ -72,6 +72,8 @@ struct BwdParams {
     float* dQ;
     float* dK;
     float* dV;
+    const float* lse;     // softmax variant: row log-sum-exp [Tq][H]
+    const float* delta;   // softmax variant: dO . O per row [Tq][H]
     int H;
     float alpha;
     int mask;
@@ -334,6 +336,22 @@ __device__ __forceinline__ void store_half_chunk(uint8_t* ps, int c, int hh, int
     }
 }
 
+// P and dS of one pair from its score s and dP: GDPA, P = act(alpha s) and
+// dS = dP act'(alpha s); the softmax variant, P = exp(alpha s - lse) (in base
+// 2 with lse2 = lse log2 e) and dS = P (dP - D), lse2 and D being the row's.
+template <int ACT>
+__device__ __forceinline__ void bwd_p_ds(float s, float dp, const ActScale& k, float lse2,
+                                         float drow, float& p, float& ds) {
+    if constexpr (ACT == kSoftmax) {
+        p = ex2_approx(fmaf(s, k.c0, -lse2));
+        ds = p * (dp - drow);
+    } else {
+        float da;
+        act_dact_s<ACT>(s, k, p, da);
+        ds = dp * da;
+    }
+}
+
 template <int D, int ACT>
 __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const CUtensorMap* tmDK,
                             const CUtensorMap* tmDV, uint8_t* smem, uint64_t* bars, uint32_t tmem,
@@ -367,6 +385,15 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             const int ipos = m * kBM + r;        // query position in the sample
             const bool row_ok = r < nq;
             const bool windowed = prm.mask == GDPA_MASK_CAUSAL_WINDOW;
+            float lse2 = 0.0f, drow = 0.0f;   // softmax variant: this row's statistics
+            if constexpr (ACT == kSoftmax) {
+                if (row_ok) {
+                    const int64_t ri = (int64_t)(u.qt0 + m * kBM + r) * prm.H + h;
+                    const float l = prm.lse[ri];
+                    lse2 = l == -INFINITY ? INFINITY : l * kLog2e;   // no valid key: P = 0
+                    drow = prm.delta[ri];
+                }
+            }
             if (!wg_wait(&bars[C::kSDFull], i & 1, ab, 43)) return;
             // the previous tile's dQ bulk stores have long been issued: once
             // they have read their staging, its Q stage goes back to the
@@ -401,11 +428,12 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
 #pragma unroll
                             for (int e = 0; e < 16; e += 2) {
                                 float a0, d0, a1, d1;
-                                act_dact_s<ACT>(__uint_as_float(sv[e]), ksc, a0, d0);
-                                act_dact_s<ACT>(__uint_as_float(sv[e + 1]), ksc, a1, d1);
+                                bwd_p_ds<ACT>(__uint_as_float(sv[e]), __uint_as_float(dv[e]), ksc,
+                                              lse2, drow, a0, d0);
+                                bwd_p_ds<ACT>(__uint_as_float(sv[e + 1]), __uint_as_float(dv[e + 1]),
+                                              ksc, lse2, drow, a1, d1);
                                 pp[k][e >> 1] = pack_bf16x2(a0, a1);
-                                pd[e >> 1] = pack_bf16x2(__uint_as_float(dv[e]) * d0,
-                                                         __uint_as_float(dv[e + 1]) * d1);
+                                pd[e >> 1] = pack_bf16x2(d0, d1);
                             }
                         } else {
 #pragma unroll
@@ -418,10 +446,11 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                                     bool valid = col < u.nkv;
                                     if (windowed)
                                         valid = valid && jpos <= ipos && jpos > ipos - prm.window;
-                                    float a, da;
-                                    act_dact_s<ACT>(__uint_as_float(sv[e + w]), ksc, a, da);
+                                    float a, ds;
+                                    bwd_p_ds<ACT>(__uint_as_float(sv[e + w]), __uint_as_float(dv[e + w]),
+                                                  ksc, lse2, drow, a, ds);
                                     p2[w] = valid ? a : 0.0f;
-                                    d2[w] = valid ? __uint_as_float(dv[e + w]) * da : 0.0f;
+                                    d2[w] = valid ? ds : 0.0f;
                                 }
                                 pp[k][e >> 1] = pack_bf16x2(p2[0], p2[1]);
                                 pd[e >> 1] = pack_bf16x2(d2[0], d2[1]);
@@ -566,7 +595,8 @@ gdpa_status launch(Plan& p, const CUtensorMap* maps, const BwdParams& prm, cudaS
 }  // namespace
 
 gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, const void* d_o,
-                          float* dq, float* dk, float* dv, float alpha, int act, cudaStream_t st) {
+                          float* dq, float* dk, float* dv, float alpha, int act, const float* lse,
+                          const float* delta, cudaStream_t st) {
     if (p.d != 64 && p.d != 128) return GDPA_ERR_UNSUPPORTED;
     const uint64_t row = (uint64_t)p.H * p.d;
     if (p.zero_dq && p.Tq > 0) {
@@ -592,6 +622,8 @@ gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, 
     prm.dQ = dq;
     prm.dK = dk;
     prm.dV = dv;
+    prm.lse = lse;
+    prm.delta = delta;
     prm.H = p.H;
     prm.alpha = alpha;
     prm.mask = p.mask;
@@ -603,9 +635,15 @@ gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, 
     if (p.timing) p.timed[1] = 1;
     gdpa_status s = GDPA_OK;
     if (p.d == 128) {
-        GDPA_DISPATCH_ACT(act, A, s = launch<128, A>(p, maps, prm, st))
+        if (act == kSoftmax)
+            s = launch<128, kSoftmax>(p, maps, prm, st);
+        else
+            GDPA_DISPATCH_ACT(act, A, s = launch<128, A>(p, maps, prm, st))
     } else {
-        GDPA_DISPATCH_ACT(act, A, s = launch<64, A>(p, maps, prm, st))
+        if (act == kSoftmax)
+            s = launch<64, kSoftmax>(p, maps, prm, st);
+        else
+            GDPA_DISPATCH_ACT(act, A, s = launch<64, A>(p, maps, prm, st))
     }
     return s;
 }

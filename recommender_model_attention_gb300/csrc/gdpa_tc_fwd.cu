@@ -85,6 +85,7 @@ struct FwdParams {
     const FwdTile* tiles;
     const int32_t* seg;
     __nv_bfloat16* O;
+    float* lse;   // softmax variant: row log-sum-exp [Tq][H] out, or NULL
     int H;
     float alpha;
     int mask;
@@ -316,12 +317,6 @@ __device__ __forceinline__ void store_zero_rows(const FwdTile& tile, const FwdPa
     }
 }
 
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // Softmax variant (Jagged Flash Attention), one tile, one thread = one row
 // of this part's key columns.  With t = alpha log2(e) s, the row maximum m
 // of t over every valid key (a first pass over the key blocks when there are
@@ -446,6 +441,9 @@ __device__ float softmax_tile(const FwdTile& tile, const FwdParams& prm, uint64_
         tc_fence_before();
         mbar_arrive(&bars[C::kBarPFull + wg]);
     }
+    if (prm.lse && part == 0 && r < tile.nq)   // natural log of the row's sum of exp(alpha s)
+        prm.lse[(int64_t)(tile.qt0 + r) * prm.H + tile.h] =
+            l > 0.0f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
     return l > 0.0f ? 1.0f / l : 0.0f;
 }
 
@@ -708,7 +706,8 @@ gdpa_status launch(int S, const CUtensorMap& mq, const CUtensorMap& mk, const CU
 gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, int32_t* err,
                               unsigned long long* times, int32_t* smid, int H, int d, int64_t Tq,
                               int64_t Tkv, int mask, int window, const void* q, const void* k,
-                              const void* v, void* o, float alpha, int act, cudaStream_t st) {
+                              const void* v, void* o, float* lse, float alpha, int act,
+                              cudaStream_t st) {
     if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
     if (Tq == 0) return GDPA_OK;
     CUtensorMap mq, mk, mv, mo;
@@ -725,6 +724,7 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
     prm.tiles = tiles;
     prm.seg = seg;
     prm.O = (__nv_bfloat16*)o;
+    prm.lse = lse;
     prm.H = H;
     prm.alpha = alpha;
     prm.mask = mask;
@@ -749,13 +749,13 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
 }
 
 gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, void* o,
-                          float alpha, int act, cudaStream_t st) {
+                          float* lse, float alpha, int act, cudaStream_t st) {
     if (p.n_fwd == 0) return GDPA_OK;
     if (p.timing) p.timed[0] = 1;
     const gdpa_status s = launch_tc_fwd_raw(
         p.d_fwd, p.d_fwd_seg, p.S, p.d_err, p.timing ? p.d_times : nullptr,
-        p.timing ? p.d_smid : nullptr, p.H, p.d, p.Tq, p.Tkv, p.mask, p.window, q, k, v, o, alpha,
-        act, st);
+        p.timing ? p.d_smid : nullptr, p.H, p.d, p.Tq, p.Tkv, p.mask, p.window, q, k, v, o, lse,
+        alpha, act, st);
     if (s == GDPA_OK) p.launches += 1;
     return s;
 }

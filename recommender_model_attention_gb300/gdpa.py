@@ -67,6 +67,8 @@ def lib():
             "gdpa_fwd_noalloc": [i32p, i32p, st, st, st, st, st, vp, vp, vp, vp, ctypes.c_float,
                                  st, vp],
             "gdpa_act_eval": [st, st, vp, vp, vp, ctypes.c_int64, vp],
+            "gdpa_softmax_fwd": [vp, st, vp, vp, vp, vp, vp, ctypes.c_float, vp],
+            "gdpa_softmax_bwd": [vp, st, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -291,3 +293,48 @@ def act_eval(x, act: str = "gelu_erf", fast: bool = True, stream=None):
     _ok(lib().gdpa_act_eval(ACT[act], 1 if fast else 0, _ptr(x), _ptr(y), _ptr(dy),
                             ctypes.c_int64(x.numel()), _stream_ptr(stream)), "gdpa_act_eval")
     return y, dy
+
+
+def gdpa_softmax_fwd(plan: Plan, q, k, v, o=None, lse=None, alpha=None, stream=None):
+    """Softmax variant (Jagged Flash Attention): (O, lse), lse the row
+    log-sum-exp [Tq, H] float32 the backward needs."""
+    import torch
+    _check(q, plan.Tq, plan, "q")
+    _check(k, plan.Tkv, plan, "k", q.dtype)
+    _check(v, plan.Tkv, plan, "v", q.dtype)
+    if o is None:
+        o = torch.empty_like(q)
+    _check(o, plan.Tq, plan, "o", q.dtype)
+    if lse is None:
+        lse = torch.empty((plan.Tq, plan.H), dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (plan.Tq, plan.H) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [Tq, H] tensor")
+    alpha = plan.d ** -0.5 if alpha is None else float(alpha)
+    _ok(lib().gdpa_softmax_fwd(plan.handle, _dtype_id(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                               _ptr(lse), ctypes.c_float(alpha), _stream_ptr(stream)),
+        "gdpa_softmax_fwd")
+    return o, lse
+
+
+def gdpa_softmax_bwd(plan: Plan, q, k, v, o, do, lse, dq=None, dk=None, dv=None, alpha=None,
+                     stream=None):
+    """(dQ, dK, dV) of the softmax variant from its forward's O and lse."""
+    import torch
+    f32 = torch.float32
+    _check(q, plan.Tq, plan, "q")
+    _check(k, plan.Tkv, plan, "k", q.dtype)
+    _check(v, plan.Tkv, plan, "v", q.dtype)
+    _check(o, plan.Tq, plan, "o", q.dtype)
+    _check(do, plan.Tq, plan, "do", q.dtype)
+    if lse.dtype != f32 or tuple(lse.shape) != (plan.Tq, plan.H) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [Tq, H] tensor")
+    dq = torch.empty(q.shape, dtype=f32, device=q.device) if dq is None else dq
+    dk = torch.empty(k.shape, dtype=f32, device=k.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=f32, device=v.device) if dv is None else dv
+    for t, n, rows in ((dq, "dq", plan.Tq), (dk, "dk", plan.Tkv), (dv, "dv", plan.Tkv)):
+        _check(t, rows, plan, n, f32)
+    alpha = plan.d ** -0.5 if alpha is None else float(alpha)
+    _ok(lib().gdpa_softmax_bwd(plan.handle, _dtype_id(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
+                               _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv),
+                               ctypes.c_float(alpha), _stream_ptr(stream)), "gdpa_softmax_bwd")
+    return dq, dk, dv

@@ -1,5 +1,5 @@
-"""GPU parity of the softmax variant (Jagged Flash Attention forward) against
-the float64 oracle, through the C ABI.
+"""GPU parity of the softmax variant (Jagged Flash Attention: forward, row
+log-sum-exp and backward) against the float64 oracle, through the C ABI.
 
 Tolerances as for GDPA: float32 inputs 1e-5 of max|ref|, bf16 inputs 1e-2 of
 max|ref| (P rounded to bf16 before its GEMM).  Cases cover tiles with one key
@@ -100,7 +100,8 @@ def test_softmax_workload_sampled(gd, idx):
             TOL["bf16"])
 
 
-def test_softmax_backward_unsupported(gd):
+def test_plain_backward_refuses_softmax(gd):
+    # the softmax gradients need O and lse: gdpa_softmax_bwd, not gdpa_bwd
     x = _case([10], [10], 1, 64, 62)
     import torch
     plan = gd.Plan(x["q_off"], x["kv_off"], 1, 64)
@@ -108,3 +109,60 @@ def test_softmax_backward_unsupported(gd):
     with pytest.raises(gd.GdpaError):
         gd.gdpa_bwd(plan, x["q"], x["k"], x["v"], do, act="softmax")
     plan.destroy()
+
+
+def _softmax_fwd_bwd(gd, x, H, d, alpha, mask="none", window=0, kernel="auto", seed=0):
+    """gdpa_softmax_fwd + gdpa_softmax_bwd on the GPU against the oracle;
+    returns the max relative errors of O, dQ, dK, dV and the max absolute
+    error of lse over rows with a valid key (and whether rows without one
+    are -inf)."""
+    import torch
+    from gpu_util import max_rel
+    from oracle import ref
+    g = torch.Generator().manual_seed(seed)
+    do = torch.randn(x["q"].shape, generator=g).to(x["q"].dtype).to(x["q"].device)
+    plan = gd.Plan(x["q_off"], x["kv_off"], H, d, mask=mask, window=window)
+    plan.set_kernel(kernel)
+    o, lse = gd.gdpa_softmax_fwd(plan, x["q"], x["k"], x["v"], alpha=alpha)
+    dq, dk, dv = gd.gdpa_softmax_bwd(plan, x["q"], x["k"], x["v"], o, do, lse, alpha=alpha)
+    plan.check()
+    torch.cuda.synchronize()
+    args = (x["q_off"], x["kv_off"], x["q"], x["k"], x["v"])
+    errs = {"o": max_rel(ref.to_f64(o), ref.fwd(*args, alpha, "softmax", mask, window))}
+    for name, got, want in zip(("dq", "dk", "dv"), (dq, dk, dv),
+                               ref.bwd(*args, do, alpha, "softmax", mask, window)):
+        errs[name] = max_rel(ref.to_f64(got), want)
+    want_lse = ref.lse(x["q_off"], x["kv_off"], x["q"], x["k"], alpha, mask, window)
+    got_lse = ref.to_f64(lse)
+    fin = np.isfinite(want_lse)
+    assert np.array_equal(np.isfinite(got_lse), fin)
+    lse_err = float(np.max(np.abs(got_lse[fin] - want_lse[fin]), initial=0.0))
+    plan.destroy()
+    return errs, lse_err
+
+
+@pytest.mark.parametrize("kernel", ["simt", "auto"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_softmax_backward_bf16(gd, kernel, d):
+    x = _case([300, 5, 129, 64, 1], [700, 128, 1, 257, 40], 2, d, 70 + d)
+    errs, lse_err = _softmax_fwd_bwd(gd, x, 2, d, d ** -0.5, kernel=kernel, seed=d)
+    _assert(errs, TOL["bf16"])
+    assert lse_err <= 1e-3
+
+
+@pytest.mark.parametrize("kernel", ["simt", "auto"])
+@pytest.mark.parametrize("window", [1, 77])
+def test_softmax_backward_window_bf16(gd, kernel, window):
+    lens = [300, 129, 7, 0]
+    x = _case(lens, lens, 2, 128, 80 + window)
+    errs, lse_err = _softmax_fwd_bwd(gd, x, 2, 128, 128 ** -0.5, "causal_window", window,
+                                     kernel=kernel, seed=window)
+    _assert(errs, TOL["bf16"])
+    assert lse_err <= 1e-3
+
+
+def test_softmax_backward_f32(gd):
+    c = small_case(43, B=5, H=2, d=64, q_range=(0, 200), kv_range=(0, 150), zero_lengths=True)
+    errs, lse_err = _softmax_fwd_bwd(gd, to_dev(c), 2, 64, 0.125, seed=3)
+    _assert(errs, TOL["f32"])
+    assert lse_err <= 1e-5
