@@ -210,8 +210,6 @@ def run_reference(args, w):
     per = lq * lkv * w.H * w.d * 12
     n = int(min(w.B, np.searchsorted(np.cumsum(per), 4e10) + 1))
     xh = make_inputs(w, device="cpu", lengths=(lq[:n], lkv[:n]))
-    if w.act == "softmax":
-        xh["do"] = None   # the softmax variant is forward only
     budget = 20.0 / max(1, args.steps + args.warmup)
     vals = []
     base = None
@@ -246,7 +244,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--act", default=None,
                     help="override the workload's activation; 'softmax' times the softmax "
-                         "variant (Jagged Flash Attention, forward only) on the same batch")
+                         "variant (Jagged Flash Attention) on the same batch")
     args = ap.parse_args()
 
     import dataclasses
@@ -275,8 +273,6 @@ def main():
         lq, lkv = draw_lengths(w)
         lengths = (lq[:args.samples], lkv[:args.samples])
     x = make_inputs(w, device="cuda", seed=rank_seed(w, rank), lengths=lengths)
-    if w.act == "softmax":
-        x["do"] = None   # the softmax variant is forward only
     stream = torch.cuda.current_stream()
     plan = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window)
     # host planning + upload of one batch's plan (it synchronises on its upload)
@@ -292,12 +288,30 @@ def main():
     dk = torch.empty(x["k"].shape, dtype=f32, device="cuda")
     dv = torch.empty(x["v"].shape, dtype=f32, device="cuda")
     backward = x["do"] is not None
+    # the softmax variant goes through its own calls (its backward needs O
+    # and the row log-sum-exp, kept per output buffer)
+    softmax = w.act == "softmax"
+    lse_of = {}
+
+    def fwd_call(p, q, k, v, o_):
+        if softmax:
+            lse = lse_of.setdefault(o_.data_ptr(), torch.empty((q.shape[0], w.H), dtype=f32,
+                                                               device=q.device))
+            gd.gdpa_softmax_fwd(p, q, k, v, o=o_, lse=lse, alpha=w.alpha)
+        else:
+            gd.gdpa_fwd(p, q, k, v, o=o_, alpha=w.alpha, act=w.act)
+
+    def bwd_call(p, q, k, v, o_, do_, dq_, dk_, dv_):
+        if softmax:
+            gd.gdpa_softmax_bwd(p, q, k, v, o_, do_, lse_of[o_.data_ptr()], dq_, dk_, dv_,
+                                alpha=w.alpha)
+        else:
+            gd.gdpa_bwd(p, q, k, v, do_, dq_, dk_, dv_, alpha=w.alpha, act=w.act)
 
     def step():
-        gd.gdpa_fwd(plan, x["q"], x["k"], x["v"], o=o, alpha=w.alpha, act=w.act)
+        fwd_call(plan, x["q"], x["k"], x["v"], o)
         if backward:
-            gd.gdpa_bwd(plan, x["q"], x["k"], x["v"], x["do"], dq, dk, dv, alpha=w.alpha,
-                        act=w.act)
+            bwd_call(plan, x["q"], x["k"], x["v"], o, x["do"], dq, dk, dv)
 
     Tq, Tkv = int(x["q_off"][-1]), int(x["kv_off"][-1])
     pairs = useful_pairs(x["q_off"], x["kv_off"], w.mask, w.window)
@@ -306,6 +320,8 @@ def main():
     row = w.H * w.d
     fwd_bytes = (2 * Tq + 2 * Tkv) * row * 2
     bwd_bytes = (2 * Tq + 2 * Tkv) * row * 2 + (Tq + 2 * Tkv) * row * 4 if backward else 0
+    if backward and softmax:
+        bwd_bytes += Tq * row * 2   # O, read for the dO.O rows
     input_bytes = sum(t.numel() * t.element_size() for t in (x["q"], x["k"], x["v"], x["do"])
                       if t is not None)
 
@@ -329,11 +345,10 @@ def main():
     start.record(stream)
     for s in range(args.steps):
         ev[s][0].record(stream)
-        gd.gdpa_fwd(plan, x["q"], x["k"], x["v"], o=o, alpha=w.alpha, act=w.act)
+        fwd_call(plan, x["q"], x["k"], x["v"], o)
         ev[s][1].record(stream)
         if backward:
-            gd.gdpa_bwd(plan, x["q"], x["k"], x["v"], x["do"], dq, dk, dv, alpha=w.alpha,
-                        act=w.act)
+            bwd_call(plan, x["q"], x["k"], x["v"], o, x["do"], dq, dk, dv)
         ev[s][2].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
@@ -403,9 +418,9 @@ def main():
                 stream.wait_event(ev["in"][sl])
                 if k >= 2:
                     stream.wait_event(ev["out"][sl])   # step k-2's results are down
-                gd.gdpa_fwd(p, q_d, k_d, v_d, o=outs[0], alpha=w.alpha, act=w.act)
+                fwd_call(p, q_d, k_d, v_d, outs[0])
                 if backward:
-                    gd.gdpa_bwd(p, q_d, k_d, v_d, do_d, *outs[1:], alpha=w.alpha, act=w.act)
+                    bwd_call(p, q_d, k_d, v_d, outs[0], do_d, *outs[1:])
                 ev["done"][sl].record(stream)
                 down.wait_event(ev["done"][sl])
                 with torch.cuda.stream(down):
@@ -452,7 +467,7 @@ def main():
         for pol in ("zigzag", "round_robin"):
             pp = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window, sched=pol)
             pp.set_timing(True)
-            gd.gdpa_fwd(pp, x["q"], x["k"], x["v"], o=o, alpha=w.alpha, act=w.act)
+            fwd_call(pp, x["q"], x["k"], x["v"], o)
             pp.check()
             se, _ = pp.sm_times("fwd")
             busy = (se[:, 1] - se[:, 0]).astype(np.float64)

@@ -379,6 +379,19 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             continue;
         }
         const int nh = (u.nkv + 15) >> 4;   // 16-column key steps; this warpgroup: s = wg + 2k
+        // softmax variant: the row statistics of query tile m, loaded one tile
+        // ahead so that their latency hides behind the previous tile
+        auto row_stats = [&](int m, float& l_out, float& d_out) {
+            l_out = -INFINITY;
+            d_out = 0.0f;
+            if (m * kBM + r < u.lq) {
+                const int64_t ri = (int64_t)(u.qt0 + m * kBM + r) * prm.H + h;
+                l_out = prm.lse[ri];
+                d_out = prm.delta[ri];
+            }
+        };
+        float lse_next = 0.0f, d_next = 0.0f;
+        if constexpr (ACT == kSoftmax) row_stats(u.m0, lse_next, d_next);
         for (int m = u.m0; m < u.m1; ++m, ++i) {
             const int nq = min(kBM, u.lq - m * kBM);
             const bool warp_rows = quarter * 32 < nq;
@@ -387,12 +400,9 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             const bool windowed = prm.mask == GDPA_MASK_CAUSAL_WINDOW;
             float lse2 = 0.0f, drow = 0.0f;   // softmax variant: this row's statistics
             if constexpr (ACT == kSoftmax) {
-                if (row_ok) {
-                    const int64_t ri = (int64_t)(u.qt0 + m * kBM + r) * prm.H + h;
-                    const float l = prm.lse[ri];
-                    lse2 = l == -INFINITY ? INFINITY : l * kLog2e;   // no valid key: P = 0
-                    drow = prm.delta[ri];
-                }
+                lse2 = lse_next == -INFINITY ? INFINITY : lse_next * kLog2e;   // no key: P = 0
+                drow = d_next;
+                if (m + 1 < u.m1) row_stats(m + 1, lse_next, d_next);
             }
             if (!wg_wait(&bars[C::kSDFull], i & 1, ab, 43)) return;
             // the previous tile's dQ bulk stores have long been issued: once
