@@ -376,10 +376,12 @@ def main():
                 "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
                 "algorithmic_bytes": dom_bytes, "peak_kind": pk_kind}
 
-    # end to end through the public API: pinned host inputs in, results out.
-    # Steps are pipelined the way a training loader runs them: step k's
-    # inputs go up on one stream while step k-1 computes, and its results come
-    # down on another; two device buffer sets alternate.
+    # end to end through the public API: pinned host inputs in, the step's
+    # metric out (the L2 norms of O, dQ, dK, dV, as a training loop logs
+    # them; reduced by torch on the device), and separately with every output
+    # copied back.  Steps are pipelined the way a training loader runs them:
+    # step k's inputs go up on one stream while step k-1 computes, and its
+    # results come down on another; two device buffer sets alternate.
     e2e = None
     if not args.no_e2e:
         hq = x["q"].cpu().pin_memory()
@@ -397,8 +399,11 @@ def main():
             sets.append((ins, outs))
         up, down, plan_stream = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
         ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("in", "done", "out")}
+        n_out = len(sets[0][1])
+        metric_d = [torch.empty(n_out, dtype=f32, device="cuda") for _ in range(2)]
+        metric_h = torch.empty(n_out, dtype=f32, pin_memory=True)
 
-        def e2e_run(n, replan=False):
+        def e2e_run(n, replan=False, full=False):
             plans = []
             for k in range(n):
                 sl = k % 2
@@ -421,11 +426,17 @@ def main():
                 fwd_call(p, q_d, k_d, v_d, outs[0])
                 if backward:
                     bwd_call(p, q_d, k_d, v_d, outs[0], do_d, *outs[1:])
+                if not full:
+                    for j, t in enumerate(outs):
+                        metric_d[sl][j] = torch.linalg.vector_norm(t, dtype=f32)
                 ev["done"][sl].record(stream)
                 down.wait_event(ev["done"][sl])
                 with torch.cuda.stream(down):
-                    for h, d_ in zip([ho] + hgrads, outs):
-                        h.copy_(d_, non_blocking=True)
+                    if full:
+                        for h, d_ in zip([ho] + hgrads, outs):
+                            h.copy_(d_, non_blocking=True)
+                    else:
+                        metric_h.copy_(metric_d[sl], non_blocking=True)
                     ev["out"][sl].record(down)
             for sl in range(2):
                 stream.wait_event(ev["out"][sl])
@@ -444,8 +455,14 @@ def main():
                                                    (fwd_flops + bwd_flops) * n_e2e, "cuda")
         e2e_ms = e2e_total / n_e2e
         h2d = input_bytes
-        d2h = o.numel() * o.element_size() + (sum(t.numel() * 4 for t in (dq, dk, dv))
-                                              if backward else 0)
+        d2h = n_out * 4
+        d2h_full = o.numel() * o.element_size() + (sum(t.numel() * 4 for t in (dq, dk, dv))
+                                                   if backward else 0)
+        a.record(stream)
+        e2e_run(n_e2e, full=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        full_total, _ = reduce_across_ranks(a.elapsed_time(b), 0.0, "cuda")
         # the same with each step's batch planned afresh (host planning and plan
         # upload inside the timed region)
         a.record(stream)
@@ -457,7 +474,11 @@ def main():
         replan_total, _ = reduce_across_ranks(a.elapsed_time(b), 0.0, "cuda")
         e2e = {"value": e2e_flops / (e2e_total * 1e-3) / 1e12, "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": e2e_ms, "ms_per_step_with_planning": replan_total / n_e2e,
+               "ms_per_step": e2e_ms, "readback": "L2 norms of O, dQ, dK, dV (float32)",
+               "ms_per_step_with_planning": replan_total / n_e2e,
+               "full_readback": {"value": e2e_flops / (full_total * 1e-3) / 1e12,
+                                 "d2h_bytes_per_step": int(d2h_full),
+                                 "ms_per_step": full_total / n_e2e},
                "pipelining": "inputs up, compute, results down on three streams, "
                              "two buffer sets"}
 
