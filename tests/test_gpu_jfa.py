@@ -166,3 +166,59 @@ def test_softmax_backward_f32(gd):
     errs, lse_err = _softmax_fwd_bwd(gd, to_dev(c), 2, 64, 0.125, seed=3)
     _assert(errs, TOL["f32"])
     assert lse_err <= 1e-5
+
+
+def test_softmax_noalloc_matches_plan_path(gd):
+    import torch
+    x = _case([300, 7, 129], [200, 600, 1], 2, 128, 90)
+    plan = gd.Plan(x["q_off"], x["kv_off"], 2, 128)
+    want = gd.gdpa_fwd(plan, x["q"], x["k"], x["v"], act="softmax")
+    plan.check()
+    got = torch.empty_like(x["q"])
+    gd.gdpa_fwd_noalloc(x["q_off"], x["kv_off"], x["q"], x["k"], x["v"], got, act="softmax")
+    torch.cuda.synchronize()
+    assert torch.equal(got, want)
+    plan.destroy()
+
+
+def test_softmax_backward_twice_reuses_workspace(gd):
+    # the plan's dO.O workspace is allocated once and rewritten per call
+    import torch
+    x = _case([130, 40], [90, 100], 2, 64, 91)   # one key block per sample
+    plan = gd.Plan(x["q_off"], x["kv_off"], 2, 64)
+    o, lse = gd.gdpa_softmax_fwd(plan, x["q"], x["k"], x["v"])
+    g = torch.Generator().manual_seed(5)
+    do1 = torch.randn(x["q"].shape, generator=g).to(torch.bfloat16).cuda()
+    do2 = torch.randn(x["q"].shape, generator=g).to(torch.bfloat16).cuda()
+    a = gd.gdpa_softmax_bwd(plan, x["q"], x["k"], x["v"], o, do1, lse)
+    b = gd.gdpa_softmax_bwd(plan, x["q"], x["k"], x["v"], o, do2, lse)
+    c = gd.gdpa_softmax_bwd(plan, x["q"], x["k"], x["v"], o, do1, lse)
+    plan.check()
+    for t1, t2, t3 in zip(a, b, c):
+        assert not torch.equal(t1, t2)
+        # no atomics on these shapes (one key block per query tile), so
+        # repeating a call reproduces it bit for bit
+        assert torch.equal(t1, t3)
+    plan.destroy()
+
+
+def test_softmax_entry_points_reject_missing_statistics(gd):
+    import torch
+    x = _case([10], [12], 1, 64, 92)
+    plan = gd.Plan(x["q_off"], x["kv_off"], 1, 64)
+    o, lse = gd.gdpa_softmax_fwd(plan, x["q"], x["k"], x["v"])
+    lib = gd.lib()
+    from recommender_model_attention_gb300.gdpa import _ptr, _stream_ptr
+    import ctypes
+    z = ctypes.c_void_p(0)
+    st = lib.gdpa_softmax_fwd(plan.handle, 0, _ptr(x["q"]), _ptr(x["k"]), _ptr(x["v"]), _ptr(o),
+                              z, ctypes.c_float(0.1), _stream_ptr(None))
+    assert st == 1   # GDPA_ERR_INVALID_ARG
+    dq = torch.empty(x["q"].shape, device="cuda")
+    dk = torch.empty(x["k"].shape, device="cuda")
+    st = lib.gdpa_softmax_bwd(plan.handle, 0, _ptr(x["q"]), _ptr(x["k"]), _ptr(x["v"]), z,
+                              _ptr(x["q"]), _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dk.clone()),
+                              ctypes.c_float(0.1), _stream_ptr(None))
+    assert st == 1   # GDPA_ERR_INVALID_ARG
+    plan.check()
+    plan.destroy()
