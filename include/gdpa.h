@@ -107,8 +107,19 @@ typedef struct gdpa_plan_s* gdpa_plan;   /* opaque, owned by the library */
  *   num_sms                  S, the number of persistent CTAs (0 = the
  *                            current device's SM count).
  *   max_kv_blocks_per_tile   0 = one forward tile per query tile; > 0 cuts
- *                            longer key ranges into chunks (planning only:
- *                            gdpa_fwd rejects such plans with UNSUPPORTED).
+ *                            longer key ranges into chunks of at most this
+ *                            many 128-row key blocks, each its own tile
+ *                            (spreads few-query, many-key samples over more
+ *                            SMs).  The forward of such a plan adds float32
+ *                            partial sums of O into a plan-owned workspace
+ *                            ([Tq][H][d] float, allocated on first use and
+ *                            cleared on every call) and rounds it into O with
+ *                            a second kernel; it needs the tensor-core path
+ *                            with d = 128 and a GDPA activation: other
+ *                            combinations (d = 64, float32 inputs, the
+ *                            softmax variant) return UNSUPPORTED.  The
+ *                            backward does not use the forward tiles and
+ *                            takes split plans on the tensor-core path.
  *   out                      receives the plan; *out is NULL on failure.
  *
  * Forward tiles: one per (sample, head, 128-row query tile), with the range

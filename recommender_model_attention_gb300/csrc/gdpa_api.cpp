@@ -37,6 +37,7 @@ void free_plan(Plan* p) {
         cudaFree(p->d_times);
         cudaFree(p->d_smid);
         cudaFree(p->d_delta);
+        cudaFree(p->d_wsplit);
         if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
     }
     delete p;
@@ -222,10 +223,11 @@ gdpa_status fwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const vo
     if (p.Tq > 0 && (!q || !o)) return GDPA_ERR_INVALID_ARG;
     if (p.Tkv > 0 && (!k || !v)) return GDPA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return GDPA_ERR_INVALID_ARG;
-    if (p.fwd_split) return GDPA_ERR_UNSUPPORTED;
     if (p.n_fwd == 0) return GDPA_OK;
     cudaStream_t st = (cudaStream_t)stream;
     if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
+    // key-split tiles: tensor-core path with d = 128 only (partial sums of O)
+    if (p.fwd_split && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
     if (use_tc(p, dtype)) return gdpa::launch_tc_fwd(p, q, k, v, o, lse, alpha, act, st);
     return gdpa::launch_simt_fwd(p, dtype, q, k, v, o, lse, alpha, act, st);
 }
@@ -245,9 +247,11 @@ gdpa_status bwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const vo
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) || !aligned16(dq) ||
         !aligned16(dk) || !aligned16(dv))
         return GDPA_ERR_INVALID_ARG;
-    if (p.fwd_split) return GDPA_ERR_UNSUPPORTED;
     cudaStream_t st = (cudaStream_t)stream;
     if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
+    // the CUDA-core dQ kernel walks the forward tiles and owns each row: no
+    // key-split plans there (the tensor-core backward has its own units)
+    if (p.fwd_split && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
     const float* delta = nullptr;
     if (sm && p.Tq > 0) {
         // D = dO . O per row, in the plan's workspace (allocated once)

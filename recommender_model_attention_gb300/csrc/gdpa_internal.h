@@ -66,6 +66,9 @@ struct Plan {
     // softmax-variant backward: dO_t . O_t per row and head, [Tq][H] float,
     // allocated on first use
     float* d_delta = nullptr;
+    // key-split forward (d = 128): float32 partial sums of O, [Tq][H][d],
+    // allocated on first use
+    float* d_wsplit = nullptr;
 };
 
 // Host planner (gdpa_plan.cpp): fills the host-side vectors of `p` from the
@@ -87,7 +90,7 @@ gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, 
 gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, int32_t* err,
                               unsigned long long* times, int32_t* smid, int H, int d, int64_t Tq,
                               int64_t Tkv, int mask, int window, const void* q, const void* k,
-                              const void* v, void* o, float* lse, float alpha, int act,
+                              const void* v, void* o, float* lse, float* w, float alpha, int act,
                               cudaStream_t st);
 gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, const void* d_o,
                           float* dq, float* dk, float* dv, float alpha, int act, const float* lse,

@@ -37,6 +37,7 @@
 
 #include "act.cuh"
 #include "tc_common.cuh"
+#include "tc_drain.cuh"
 
 namespace gdpa {
 namespace {
@@ -237,81 +238,6 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
 drain:
     mma_commit(&bars[C::kMmaDone]);
     mbar_wait_teardown(&bars[C::kMmaDone], 0);
-}
-
-// Drain TMEM columns [col, col + ncols) (a multiple of 32) of this warp's
-// 32 lanes (block rows 32 * quarter + lane) into rows [0, nrows) of a block
-// of a [rows][H * d] fp32 tensor whose first element has tensor-map
-// coordinates (x0, y0) and address `dst` (row stride `rs` floats), scaled by
-// `scale`.  A warp whose 32 rows are all inside the block stages 32 columns
-// at a time in its own 4 KB of `stage` (128-byte rows, 16-byte chunks
-// swizzled by row, the layout of a 128-byte-swizzled TMA box) and writes
-// them with one TMA bulk store, or a bulk reduce-add when `atomic`; the warp
-// holding the block's ragged end writes its valid rows from registers.
-// `release` (if any) is arrived by every thread after its last TMEM read.
-// On return the last bulk store may still be reading the staging area: call
-// staging_release_wait before it is reused.
-__device__ __noinline__ void drain_warp(uint32_t trow, uint32_t col, int ncols, uint8_t* stage,
-                                           const CUtensorMap* map, int x0, int y0, float* dst,
-                                           int64_t rs, int nrows, bool atomic, float scale,
-                                           int quarter, int lane, uint64_t* release) {
-    const int row0 = quarter * 32;
-    const bool any = row0 < nrows;
-    const bool full = row0 + 32 <= nrows;
-    uint8_t* wst = stage + quarter * 4096;
-    for (int pass = 0; pass < ncols / 32; ++pass) {
-        uint32_t v[32];
-        if (any) {
-            tmem_ld32(trow + col + pass * 32, v);
-            tmem_ld_wait();
-        }
-        if (pass == ncols / 32 - 1 && release) {
-            tc_fence_before();
-            mbar_arrive(release);
-        }
-        if (!any) continue;
-        if (full) {
-            if (pass > 0) {
-                if (lane == 0) bulk_wait_read_all();
-                __syncwarp();
-            }
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<float4*>(wst + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                    make_float4(scale * __uint_as_float(v[4 * c]), scale * __uint_as_float(v[4 * c + 1]),
-                                scale * __uint_as_float(v[4 * c + 2]),
-                                scale * __uint_as_float(v[4 * c + 3]));
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                if (atomic)
-                    tma_reduce_add_2d(map, wst, x0 + pass * 32, y0 + row0);
-                else
-                    tma_store_2d(map, wst, x0 + pass * 32, y0 + row0);
-                bulk_commit();
-            }
-        } else if (row0 + lane < nrows) {
-            float* d = dst + (int64_t)(row0 + lane) * rs + pass * 32;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 w = make_float4(scale * __uint_as_float(v[4 * c]),
-                                             scale * __uint_as_float(v[4 * c + 1]),
-                                             scale * __uint_as_float(v[4 * c + 2]),
-                                             scale * __uint_as_float(v[4 * c + 3]));
-                if (atomic)
-                    atomicAdd(reinterpret_cast<float4*>(d + 4 * c), w);
-                else
-                    *reinterpret_cast<float4*>(d + 4 * c) = w;
-            }
-        }
-    }
-}
-
-// The calling warp's bulk stores have read their staging: the area may be
-// reused or handed back.
-__device__ __forceinline__ void staging_release_wait(int lane) {
-    if (lane == 0) bulk_wait_read_all();
-    __syncwarp();
 }
 
 template <int D>

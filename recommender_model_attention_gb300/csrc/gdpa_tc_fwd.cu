@@ -35,10 +35,12 @@
 //  * O accumulates P V over key blocks with no rescaling.
 //  * Every barrier wait is bounded; a timeout sets the plan's error word and
 //    the CTA unwinds (waits for its TMA loads and MMAs, frees TMEM, returns).
+#include <algorithm>
 #include <cuda_bf16.h>
 
 #include "act.cuh"
 #include "tc_common.cuh"
+#include "tc_drain.cuh"
 
 namespace gdpa {
 namespace {
@@ -86,6 +88,7 @@ struct FwdParams {
     const int32_t* seg;
     __nv_bfloat16* O;
     float* lse;   // softmax variant: row log-sum-exp [Tq][H] out, or NULL
+    float* W;     // key-split plans: float32 [Tq][H][D] partial-sum target, or NULL
     int H;
     float alpha;
     int mask;
@@ -447,8 +450,9 @@ __device__ float softmax_tile(const FwdTile& tile, const FwdParams& prm, uint64_
     return l > 0.0f ? 1.0f / l : 0.0f;
 }
 
-template <int D, int ACT>
-__device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, uint8_t* smem,
+template <int D, int ACT, bool SPLIT>
+__device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const CUtensorMap* tmW,
+                            uint8_t* smem,
                             uint64_t* bars, uint32_t tmem, int seg0, int seg1, const Abort& ab) {
     using C = FwdCfg<D>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -466,7 +470,7 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, uint8_
     for (int t = seg0; t < seg1; ++t) {
         const FwdTile tile = load_tile(prm.tiles + t);
         if (tile.kb1 <= tile.kb0) {
-            if ((t - seg0) % (kNumWG * kParts) == grp) store_zero_rows<D>(tile, prm, tid);
+            if (!SPLIT && (t - seg0) % (kNumWG * kParts) == grp) store_zero_rows<D>(tile, prm, tid);
             continue;
         }
         if (a % kNumWG != wg) {
@@ -542,6 +546,25 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, uint8_
         if (!wg_wait(&bars[C::kBarOFull + wg], o_use & 1, ab, 8)) return;
         o_use++;
         tc_fence_after();
+        if constexpr (SPLIT) {
+            {
+                // key-split plan: this tile holds a partial sum of its rows' O;
+                // add it (float32, TMA bulk reduce-add) into the workspace that
+                // a second kernel converts once every tile has landed
+                static_assert(D == 128 && ACT != kSoftmax, "key split: d = 128 GDPA only");
+                const int64_t rs = (int64_t)prm.H * D;
+                drain_warp_inl(tmem + wg * 256 + lane_addr, 128 + part * (D / 2), D / 2,
+                           smem + C::kOffQ + qs * C::kTileBytes + part * (C::kTileBytes / 2), tmW,
+                           tile.h * D + part * (D / 2), tile.qt0,
+                           prm.W + (int64_t)tile.qt0 * rs + tile.h * D + part * (D / 2), rs,
+                           tile.nq, true, 1.0f, quarter, lane, &bars[C::kBarOFree + wg]);
+                staging_release_wait(lane);
+                fence_proxy_async_smem();
+                mbar_arrive(&bars[C::kBarQEmpty + qs]);
+                ++a;
+                continue;
+            }
+        }
         constexpr int kRowBytes = D;                 // D/2 bf16 per row and part
         constexpr int kChunks = kRowBytes / 16;      // 16-byte chunks per row
         constexpr int kSwz = kChunks - 1 < 7 ? kChunks - 1 : 7;
@@ -610,11 +633,11 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, uint8_
     }
 }
 
-template <int D, int ACT>
+template <int D, int ACT, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
-              const FwdParams prm) {
+              const __grid_constant__ CUtensorMap tmW, const FwdParams prm) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -653,6 +676,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         tma_prefetch_desc(&tmK);
         tma_prefetch_desc(&tmV);
         tma_prefetch_desc(&tmO);
+        if (SPLIT) tma_prefetch_desc(&tmW);
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
@@ -671,7 +695,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         fwd_mma_pv<D, ACT == kSoftmax>(prm, smem, bars, tmem, seg0, seg1, ab);
         __syncwarp();
     } else {
-        fwd_compute<D, ACT>(prm, &tmO, smem, bars, tmem, seg0, seg1, ab);
+        fwd_compute<D, ACT, SPLIT>(prm, &tmO, &tmW, smem, bars, tmem, seg0, seg1, ab);
         if (lane == 0) bulk_wait_all();
         __syncwarp();
     }
@@ -689,16 +713,26 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
 }
 
-template <int D, int ACT>
+template <int D, int ACT, bool SPLIT = false>
 gdpa_status launch(int S, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                   const CUtensorMap& mo, const FwdParams& prm, cudaStream_t st) {
+                   const CUtensorMap& mo, const CUtensorMap& mw, const FwdParams& prm,
+                   cudaStream_t st) {
     using C = FwdCfg<D>;
-    auto kern = tc_fwd_kernel<D, ACT>;
+    auto kern = tc_fwd_kernel<D, ACT, SPLIT>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return GDPA_ERR_CUDA;
-    kern<<<S, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mo, prm);
+    kern<<<S, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mo, mw, prm);
     return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+// Key-split plans: O = bf16(W), four elements per thread and step.
+__global__ void __launch_bounds__(256) split_finalize_kernel(const float4* __restrict__ w,
+                                                             uint2* __restrict__ o, int64_t n4) {
+    for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < n4; i += (int64_t)gridDim.x * 256) {
+        const float4 x = w[i];
+        o[i] = make_uint2(pack_bf16x2(x.x, x.y), pack_bf16x2(x.z, x.w));
+    }
 }
 
 }  // namespace
@@ -706,11 +740,12 @@ gdpa_status launch(int S, const CUtensorMap& mq, const CUtensorMap& mk, const CU
 gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, int32_t* err,
                               unsigned long long* times, int32_t* smid, int H, int d, int64_t Tq,
                               int64_t Tkv, int mask, int window, const void* q, const void* k,
-                              const void* v, void* o, float* lse, float alpha, int act,
+                              const void* v, void* o, float* lse, float* w, float alpha, int act,
                               cudaStream_t st) {
     if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
+    if (w && (d != 128 || act == kSoftmax)) return GDPA_ERR_UNSUPPORTED;
     if (Tq == 0) return GDPA_OK;
-    CUtensorMap mq, mk, mv, mo;
+    CUtensorMap mq, mk, mv, mo, mw;
     const uint64_t row = (uint64_t)H * d;
     const uint64_t kv_rows = Tkv > 0 ? (uint64_t)Tkv : 1;
     const void* kp = Tkv > 0 ? k : q;
@@ -720,11 +755,17 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
         !tc::make_tmap_bf16(&mv, vp, kv_rows, row, 128) ||
         !tc::make_tmap_bf16(&mo, o, (uint64_t)Tq, row, 32))
         return GDPA_ERR_CUDA;
+    if (w) {
+        if (!tc::make_tmap_f32(&mw, w, (uint64_t)Tq, row, 32)) return GDPA_ERR_CUDA;
+    } else {
+        mw = mo;   // not read
+    }
     FwdParams prm;
     prm.tiles = tiles;
     prm.seg = seg;
     prm.O = (__nv_bfloat16*)o;
     prm.lse = lse;
+    prm.W = w;
     prm.H = H;
     prm.alpha = alpha;
     prm.mask = mask;
@@ -734,16 +775,18 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
     prm.smid = smid;
     prm.timing = times != nullptr && smid != nullptr;
     gdpa_status s = GDPA_OK;
-    if (d == 128) {
+    if (w) {
+        GDPA_DISPATCH_ACT(act, A, s = launch<128, A, true>(S, mq, mk, mv, mo, mw, prm, st))
+    } else if (d == 128) {
         if (act == kSoftmax)
-            s = launch<128, kSoftmax>(S, mq, mk, mv, mo, prm, st);
+            s = launch<128, kSoftmax>(S, mq, mk, mv, mo, mw, prm, st);
         else
-            GDPA_DISPATCH_ACT(act, A, s = launch<128, A>(S, mq, mk, mv, mo, prm, st))
+            GDPA_DISPATCH_ACT(act, A, s = launch<128, A>(S, mq, mk, mv, mo, mw, prm, st))
     } else {
         if (act == kSoftmax)
-            s = launch<64, kSoftmax>(S, mq, mk, mv, mo, prm, st);
+            s = launch<64, kSoftmax>(S, mq, mk, mv, mo, mw, prm, st);
         else
-            GDPA_DISPATCH_ACT(act, A, s = launch<64, A>(S, mq, mk, mv, mo, prm, st))
+            GDPA_DISPATCH_ACT(act, A, s = launch<64, A>(S, mq, mk, mv, mo, mw, prm, st))
     }
     return s;
 }
@@ -751,12 +794,33 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
 gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, void* o,
                           float* lse, float alpha, int act, cudaStream_t st) {
     if (p.n_fwd == 0) return GDPA_OK;
+    float* w = nullptr;
+    if (p.fwd_split) {
+        // key-split plan: the tiles of one query tile add float32 partial sums
+        // into a zeroed workspace; a second kernel rounds it into O
+        if (p.d != 128 || act == kSoftmax) return GDPA_ERR_UNSUPPORTED;
+        const size_t bytes = (size_t)p.Tq * p.H * p.d * sizeof(float);
+        if (!p.d_wsplit && cudaMalloc((void**)&p.d_wsplit, bytes) != cudaSuccess) {
+            p.d_wsplit = nullptr;
+            return GDPA_ERR_ALLOC;
+        }
+        if (cudaMemsetAsync(p.d_wsplit, 0, bytes, st) != cudaSuccess) return GDPA_ERR_CUDA;
+        w = p.d_wsplit;
+    }
     if (p.timing) p.timed[0] = 1;
-    const gdpa_status s = launch_tc_fwd_raw(
+    gdpa_status s = launch_tc_fwd_raw(
         p.d_fwd, p.d_fwd_seg, p.S, p.d_err, p.timing ? p.d_times : nullptr,
         p.timing ? p.d_smid : nullptr, p.H, p.d, p.Tq, p.Tkv, p.mask, p.window, q, k, v, o, lse,
-        alpha, act, st);
+        w, alpha, act, st);
     if (s == GDPA_OK) p.launches += 1;
+    if (s == GDPA_OK && w) {
+        const int64_t n4 = p.Tq * p.H * p.d / 4;
+        const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, 152 * 8);
+        split_finalize_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(w),
+                                                      reinterpret_cast<uint2*>(o), n4);
+        s = cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+        if (s == GDPA_OK) p.launches += 1;
+    }
     return s;
 }
 

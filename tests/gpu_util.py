@@ -32,10 +32,10 @@ def to_dev(case, device="cuda"):
 
 
 def run_gpu(gd, x, H, d, alpha, act, mask="none", window=0, kernel="auto", backward=True,
-            sched="zigzag", num_sms=0, stream=None):
+            sched="zigzag", num_sms=0, stream=None, max_kv_blocks=0):
     import torch
     plan = gd.Plan(x["q_off"], x["kv_off"], H, d, mask=mask, window=window, sched=sched,
-                   num_sms=num_sms, stream=stream)
+                   num_sms=num_sms, stream=stream, max_kv_blocks=max_kv_blocks)
     plan.set_kernel(kernel)
     if stream is not None:
         stream.wait_stream(torch.cuda.current_stream())
@@ -52,7 +52,7 @@ def run_gpu(gd, x, H, d, alpha, act, mask="none", window=0, kernel="auto", backw
 def compare_full(gd, x, H, d, alpha, act, dtype, mask="none", window=0, kernel="auto",
                  backward=True, **launch):
     """Whole-batch comparison; returns the max relative errors.  `launch` goes
-    to run_gpu (sched, num_sms, stream)."""
+    to run_gpu (sched, num_sms, stream, max_kv_blocks)."""
     plan, o, grads = run_gpu(gd, x, H, d, alpha, act, mask, window, kernel, backward, **launch)
     args = (x["q_off"], x["kv_off"], x["q"], x["k"], x["v"])
     errs = {"o": max_rel(ref.to_f64(o), ref.fwd(*args, alpha, act, mask, window))}

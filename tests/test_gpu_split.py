@@ -1,0 +1,122 @@
+"""GPU parity of key-split forward plans (max_kv_blocks > 0).
+
+A key-split plan cuts a query tile's key range into chunks of at most
+`max_kv_blocks` 128-row key blocks, each its own forward tile, so that a
+sample with a long key sequence and few query rows (the pooling-attention
+shape) spreads over many SMs.  Each chunk adds its float32 partial sum of O
+into a zeroed workspace and a second kernel rounds it to bf16.  Since
+O = act(alpha Q K^T) V is a plain sum over keys for GDPA, the result must
+match the oracle to the same bf16 tolerance as an unsplit plan; the backward
+pass (which has its own per-key-block units) must be unaffected.  The
+tensor-core path with d = 128 supports it; d = 64, float32 inputs and the
+softmax variant (whose normalisation couples the chunks) refuse it.
+"""
+
+import numpy as np
+import pytest
+
+from gpu_util import TOL, compare_full, max_rel, to_dev
+from oracle import ref
+from workloads import offsets_from_lengths
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def gd():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import recommender_model_attention_gb300 as g
+    g.build()
+    return g
+
+
+def _case(lq, lkv, H, d, seed, dtype="bf16"):
+    import torch
+    qo, ko = offsets_from_lengths(np.asarray(lq)), offsets_from_lengths(np.asarray(lkv))
+    g = torch.Generator().manual_seed(seed)
+    x = {"q_off": qo, "kv_off": ko}
+    for n, rows in (("q", qo[-1]), ("k", ko[-1]), ("v", ko[-1]), ("do", qo[-1])):
+        t = torch.randn((int(rows), H, d), generator=g) / 4
+        x[n] = t.to(torch.bfloat16) if dtype == "bf16" else t
+    return to_dev(x)
+
+
+def _assert(errs, tol=TOL["bf16"]):
+    for name, e in errs.items():
+        assert e <= tol, "%s: max rel err %.3e > %.1e (%s)" % (name, e, tol, errs)
+
+
+# few query rows against long key sequences (the pooling-attention shape),
+# a sample with several query tiles, ragged key tails, an empty sample
+LQ = [32, 1, 300, 0, 129, 64]
+LKV = [1000, 700, 900, 50, 0, 1]
+
+
+@pytest.mark.parametrize("max_kvb", [1, 2, 3])
+@pytest.mark.parametrize("act", ["gelu_erf", "gelu_tanh", "silu", "gelu_taylor6", "identity"])
+def test_split_matches_oracle(gd, max_kvb, act):
+    x = _case(LQ, LKV, 2, 128, 11 + max_kvb)
+    errs = compare_full(gd, x, 2, 128, 128 ** -0.5, act, "bf16", max_kv_blocks=max_kvb)
+    _assert(errs)
+
+
+@pytest.mark.parametrize("window", [1, 100, 300])
+def test_split_causal_window(gd, window):
+    lq = [700, 260, 5]
+    x = _case(lq, lq, 2, 128, 40 + window)
+    errs = compare_full(gd, x, 2, 128, 128 ** -0.5, "gelu_erf", "bf16",
+                        mask="causal_window", window=window, max_kv_blocks=1)
+    _assert(errs)
+
+
+def test_split_plan_is_split_and_counts_two_launches(gd):
+    import torch
+    x = _case(LQ, LKV, 2, 128, 5)
+    plan = gd.Plan(x["q_off"], x["kv_off"], 2, 128, max_kv_blocks=2)
+    whole = gd.Plan(x["q_off"], x["kv_off"], 2, 128)
+    assert plan.sizes()[0] > whole.sizes()[0]
+    n0 = plan.launches
+    gd.gdpa_fwd(plan, x["q"], x["k"], x["v"])
+    plan.check()
+    assert plan.launches == n0 + 2   # the tile kernel and the bf16 rounding kernel
+    plan.destroy()
+    whole.destroy()
+    torch.cuda.synchronize()
+
+
+def test_split_repeat_is_stable_and_close_to_whole(gd):
+    # the workspace is cleared on every call: a second forward gives the same
+    # O up to summation order, and so does the unsplit plan
+    import torch
+    x = _case([16, 16], [1024, 640], 1, 128, 9)
+    split = gd.Plan(x["q_off"], x["kv_off"], 1, 128, max_kv_blocks=1)
+    whole = gd.Plan(x["q_off"], x["kv_off"], 1, 128)
+    o1 = gd.gdpa_fwd(split, x["q"], x["k"], x["v"]).clone()
+    o2 = gd.gdpa_fwd(split, x["q"], x["k"], x["v"])
+    ow = gd.gdpa_fwd(whole, x["q"], x["k"], x["v"])
+    split.check()
+    whole.check()
+    torch.cuda.synchronize()
+    # (the chunks' float32 adds may land in a different order on each call,
+    # so the bound is one bf16 rounding step, not bit equality)
+    assert max_rel(ref.to_f64(o1), ref.to_f64(o2)) <= 2 ** -8
+    assert max_rel(ref.to_f64(o1), ref.to_f64(ow)) <= 2 ** -7
+    split.destroy()
+    whole.destroy()
+
+
+@pytest.mark.parametrize("what", ["d64", "f32", "softmax"])
+def test_split_refused_where_unsupported(gd, what):
+    import torch
+    d = 64 if what == "d64" else 128
+    x = _case([8], [600], 1, d, 3, dtype="f32" if what == "f32" else "bf16")
+    plan = gd.Plan(x["q_off"], x["kv_off"], 1, d, max_kv_blocks=1)
+    with pytest.raises(gd.GdpaError):
+        if what == "softmax":
+            gd.gdpa_softmax_fwd(plan, x["q"], x["k"], x["v"])
+        else:
+            gd.gdpa_fwd(plan, x["q"], x["k"], x["v"])
+    plan.destroy()
+    torch.cuda.synchronize()
