@@ -38,12 +38,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # launch by algorithmic bytes).  Valid only for the kernel sources they were
 # measured on (hash of the kernel's source files); otherwise reported null.
 TRAFFIC_RATIO = {
-    "gdpa_fwd": ("b2f68e6006dc4ef3", 0.9641),
-    "gdpa_bwd": ("f9858867097ad2ac", 1.0208),
+    "gdpa_fwd": ("5d8a14aaafbbec8a", 0.9644),
+    "gdpa_bwd": ("6786290a062b0e8a", 1.0207),
 }
 KERNEL_SOURCES = {
-    "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "act.cuh"),
-    "gdpa_bwd": ("gdpa_tc_bwd.cu", "tc_common.cuh", "act.cuh"),
+    "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh"),
+    "gdpa_bwd": ("gdpa_tc_bwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh"),
 }
 
 
@@ -242,6 +242,9 @@ def main():
                     help="use only the first N sequences of the workload (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--max-kv-blocks", type=int, default=0,
+                    help="key-split plans: at most this many 128-row key blocks per forward "
+                         "tile (0 = whole key range per tile)")
     ap.add_argument("--act", default=None,
                     help="override the workload's activation; 'softmax' times the softmax "
                          "variant (Jagged Flash Attention) on the same batch")
@@ -274,12 +277,16 @@ def main():
         lengths = (lq[:args.samples], lkv[:args.samples])
     x = make_inputs(w, device="cuda", seed=rank_seed(w, rank), lengths=lengths)
     stream = torch.cuda.current_stream()
-    plan = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window)
+    def make_plan(**kw):
+        return gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window,
+                       max_kv_blocks=args.max_kv_blocks, **kw)
+
+    plan = make_plan()
     # host planning + upload of one batch's plan (it synchronises on its upload)
     plan_times = []
     for _ in range(3):
         t0 = time.perf_counter()
-        gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window).destroy()
+        make_plan().destroy()
         plan_times.append((time.perf_counter() - t0) * 1e3)
     n_fwd_tiles, n_bwd_units, _ = plan.sizes()
     f32 = torch.float32
@@ -417,8 +424,7 @@ def main():
                     ev["in"][sl].record(up)
                 p = plan
                 if replan:   # each step's batch planned afresh, as in training
-                    p = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window,
-                                stream=plan_stream)
+                    p = make_plan(stream=plan_stream)
                     plans.append(p)
                 stream.wait_event(ev["in"][sl])
                 if k >= 2:
@@ -486,7 +492,7 @@ def main():
     spread = {}
     try:
         for pol in ("zigzag", "round_robin"):
-            pp = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window, sched=pol)
+            pp = make_plan(sched=pol)
             pp.set_timing(True)
             fwd_call(pp, x["q"], x["k"], x["v"], o)
             pp.check()
@@ -509,7 +515,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded lengths and RMSNorm'd N(0,1) inputs, random dO)",
             "config": {"workload": w.name, "B": len(x["q_off"]) - 1, "H": w.H, "d": w.d,
-                       "act": w.act,
+                       "act": w.act, "max_kv_blocks": args.max_kv_blocks,
                        "Tq": Tq, "Tkv": Tkv, "useful_pairs": pairs,
                        "l2": "inputs larger than L2 (%.1f GB resident)" % (input_bytes / 1e9),
                        "parallelism": "samples sharded by rank, no exchange" if world > 1
