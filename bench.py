@@ -242,9 +242,10 @@ def main():
                     help="use only the first N sequences of the workload (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--max-kv-blocks", type=int, default=0,
+    ap.add_argument("--max-kv-blocks", default="auto",
                     help="key-split plans: at most this many 128-row key blocks per forward "
-                         "tile (0 = whole key range per tile)")
+                         "tile (0 = whole key range per tile; 'auto' = the planner's choice, "
+                         "no split for the softmax variant, which refuses split plans)")
     ap.add_argument("--act", default=None,
                     help="override the workload's activation; 'softmax' times the softmax "
                          "variant (Jagged Flash Attention) on the same batch")
@@ -277,9 +278,13 @@ def main():
         lengths = (lq[:args.samples], lkv[:args.samples])
     x = make_inputs(w, device="cuda", seed=rank_seed(w, rank), lengths=lengths)
     stream = torch.cuda.current_stream()
+    mkb = args.max_kv_blocks if args.max_kv_blocks == "auto" else int(args.max_kv_blocks)
+    if w.act == "softmax" and mkb == "auto":
+        mkb = 0
+
     def make_plan(**kw):
         return gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window,
-                       max_kv_blocks=args.max_kv_blocks, **kw)
+                       max_kv_blocks=mkb, **kw)
 
     plan = make_plan()
     # host planning + upload of one batch's plan (it synchronises on its upload)
@@ -288,7 +293,11 @@ def main():
         t0 = time.perf_counter()
         make_plan().destroy()
         plan_times.append((time.perf_counter() - t0) * 1e3)
-    n_fwd_tiles, n_bwd_units, _ = plan.sizes()
+    n_fwd_tiles, n_bwd_units, plan_sms = plan.sizes()
+    whole = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window,
+                    num_sms=plan_sms, host_only=True)
+    key_split = whole.sizes()[0] != n_fwd_tiles   # the plan cut some key ranges
+    whole.destroy()
     f32 = torch.float32
     o = torch.empty_like(x["q"])
     dq = torch.empty(x["q"].shape, dtype=f32, device="cuda")
@@ -515,7 +524,8 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded lengths and RMSNorm'd N(0,1) inputs, random dO)",
             "config": {"workload": w.name, "B": len(x["q_off"]) - 1, "H": w.H, "d": w.d,
-                       "act": w.act, "max_kv_blocks": args.max_kv_blocks,
+                       "act": w.act, "max_kv_blocks": mkb,
+                       "key_split": key_split,
                        "Tq": Tq, "Tkv": Tkv, "useful_pairs": pairs,
                        "l2": "inputs larger than L2 (%.1f GB resident)" % (input_bytes / 1e9),
                        "parallelism": "samples sharded by rank, no exchange" if world > 1

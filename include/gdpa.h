@@ -93,6 +93,8 @@ typedef struct gdpa_plan_s* gdpa_plan;   /* opaque, owned by the library */
 /* Tile sizes of every plan: 128 query rows x 128 key rows. */
 #define GDPA_BLOCK_M 128
 #define GDPA_BLOCK_N 128
+/* max_kv_blocks_per_tile value that lets the planner choose the key split */
+#define GDPA_KV_SPLIT_AUTO (-1)
 
 /*
  * Build the tile plan of a jagged batch on the host and upload it on
@@ -120,6 +122,13 @@ typedef struct gdpa_plan_s* gdpa_plan;   /* opaque, owned by the library */
  *                            softmax variant) return UNSUPPORTED.  The
  *                            backward does not use the forward tiles and
  *                            takes split plans on the tensor-core path.
+ *                            GDPA_KV_SPLIT_AUTO (-1): the planner picks
+ *                            chunks of 2 key blocks when some query tile
+ *                            reaches 8 or more key blocks (the fastest
+ *                            setting measured for 32-query samples against
+ *                            up to 8192 keys), else no split; such a plan
+ *                            may therefore be split, with the limits above.
+ *                            Values below -1 are INVALID_ARG.
  *   out                      receives the plan; *out is NULL on failure.
  *
  * Forward tiles: one per (sample, head, 128-row query tile), with the range

@@ -14,6 +14,12 @@
 //  * backward unit = (b, h, key block j); its query tiles are the hull of the
 //    queries that see a key of the block.  A sample whose query tiles are
 //    reached by more than one key block gets its dQ by atomic adds.
+//  * key split (max_kv_blocks_per_tile = k > 0): a forward tile's key blocks
+//    are cut into chunks of at most k, each its own tile; automatic choice
+//    (k = GDPA_KV_SPLIT_AUTO): chunks of 2 when some query tile reaches 8 or
+//    more key blocks, else no split (measured on the pooling workload,
+//    32 queries against up to 8192 keys per sample: 2-block chunks were the
+//    fastest at 16, 64 and 1024 samples).
 //  * cost = blocks on the inner loop; zigzag = stable sort by cost,
 //    descending, then snake dealing over the S SMs; round robin = tile r to
 //    SM r % S in enumeration order.
@@ -86,6 +92,31 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
     p.Tkv = kv_off[B];
     const bool win = p.mask == GDPA_MASK_CAUSAL_WINDOW;
     const int64_t W = p.window;
+    // key-block hull of query tile m of sample b (empty: k0 = k1 = 0)
+    auto kv_hull = [&](int b, int64_t m, int64_t& k0, int64_t& k1) {
+        const int64_t lq = q_off[b + 1] - q_off[b], lkv = kv_off[b + 1] - kv_off[b];
+        const int64_t r0 = m * kBM, r1 = std::min<int64_t>(r0 + kBM, lq);
+        int64_t lo = 0, hi = lkv;
+        if (win) {
+            lo = std::max<int64_t>(0, r0 - W + 1);
+            hi = std::min<int64_t>(lkv, r1);
+        }
+        k0 = k1 = 0;
+        if (lo < hi) {
+            k0 = lo / kBN;
+            k1 = cdiv(hi, kBN);
+        }
+    };
+    if (p.max_kvb == GDPA_KV_SPLIT_AUTO) {
+        int64_t widest = 0;
+        for (int b = 0; b < B; ++b)
+            for (int64_t m = 0; m < cdiv(q_off[b + 1] - q_off[b], kBM); ++m) {
+                int64_t k0, k1;
+                kv_hull(b, m, k0, k1);
+                widest = std::max(widest, k1 - k0);
+            }
+        p.max_kvb = widest >= 8 ? 2 : 0;
+    }
 
     // forward tiles, enumerated b -> h -> m (-> chunk)
     std::vector<Item> ft;
@@ -97,16 +128,8 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
         for (int h = 0; h < H; ++h) {
             for (int64_t m = 0; m < cdiv(lq, kBM); ++m) {
                 const int64_t r0 = m * kBM, r1 = std::min<int64_t>(r0 + kBM, lq);
-                int64_t lo = 0, hi = lkv;
-                if (win) {
-                    lo = std::max<int64_t>(0, r0 - W + 1);
-                    hi = std::min<int64_t>(lkv, r1);
-                }
-                int64_t k0 = 0, k1 = 0;
-                if (lo < hi) {
-                    k0 = lo / kBN;
-                    k1 = cdiv(hi, kBN);
-                }
+                int64_t k0, k1;
+                kv_hull(b, m, k0, k1);
                 const int64_t step = (p.max_kvb > 0 && k1 > k0) ? p.max_kvb : std::max<int64_t>(1, k1 - k0);
                 int64_t s = k0;
                 do {

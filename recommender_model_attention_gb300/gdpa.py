@@ -20,6 +20,7 @@ ACT = {"gelu_erf": 0, "gelu_tanh": 1, "silu": 2, "gelu_taylor6": 3, "identity": 
 MASK = {"none": 0, "causal_window": 1}
 SCHED = {"zigzag": 0, "round_robin": 1}
 KERNEL = {"auto": 0, "tcgen05": 1, "simt": 2}
+KV_SPLIT_AUTO = -1   # max_kv_blocks_per_tile: the planner chooses
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",
           4: "allocation failed", 5: "kernel barrier wait timed out",
           6: "kernel reported an internal error",
@@ -102,7 +103,12 @@ def _stream_ptr(stream):
 
 
 class Plan:
-    """A GDPA tile plan (forward tiles and backward units dealt to SMs)."""
+    """A GDPA tile plan (forward tiles and backward units dealt to SMs).
+
+    max_kv_blocks: 0 = one forward tile per query tile; k > 0 = key ranges
+    cut into chunks of at most k 128-row key blocks; "auto" = the planner's
+    choice (2-block chunks when some query tile reaches 8 key blocks).
+    """
 
     def __init__(self, q_off, kv_off, H: int, d: int, mask: str = "none", window: int = 0,
                  sched: str = "zigzag", num_sms: int = 0, max_kv_blocks: int = 0,
@@ -116,14 +122,15 @@ class Plan:
         self.mask, self.window = mask, int(window)
         self.Tq, self.Tkv = int(qo[-1]), int(ko[-1])
         self.q_off, self.kv_off = qo.copy(), ko.copy()
+        mkb = KV_SPLIT_AUTO if max_kv_blocks == "auto" else int(max_kv_blocks)
         h = ctypes.c_void_p()
         if host_only:
             _ok(L.gdpa_plan_create_host(qp, kp, self.B, self.H, self.d, MASK[mask], int(window),
-                                        SCHED[sched], int(num_sms), int(max_kv_blocks),
+                                        SCHED[sched], int(num_sms), mkb,
                                         ctypes.byref(h)), "gdpa_plan_create_host")
         else:
             _ok(L.gdpa_plan_create(qp, kp, self.B, self.H, self.d, MASK[mask], int(window),
-                                   SCHED[sched], int(num_sms), int(max_kv_blocks),
+                                   SCHED[sched], int(num_sms), mkb,
                                    _stream_ptr(stream), ctypes.byref(h)), "gdpa_plan_create")
         self._h = h
 

@@ -77,6 +77,32 @@ def test_planner_matches_oracle_random(gd, seed, S):
                  max_kvb=(seed % 3))
 
 
+@pytest.mark.parametrize("mask,window", [("none", 0), ("causal_window", 300),
+                                         ("causal_window", 1200)])
+def test_planner_automatic_key_split(gd, mask, window):
+    # "auto" resolves to 2-block chunks when some query tile's key hull has
+    # 8 or more blocks, else to no split: compare with the explicit plans
+    for lkv_max, seed in ((1000, 1), (1100, 2), (3000, 3)):
+        rng = np.random.default_rng(seed)
+        lq = rng.integers(1, 400, size=7)
+        lkv = rng.integers(0, lkv_max, size=7) if mask == "none" else lq
+        if mask == "causal_window":
+            lq = lkv = rng.integers(1, lkv_max, size=7)
+        qo, ko = offsets_from_lengths(lq), offsets_from_lengths(lkv)
+        widest = 0
+        for t in ref_planner.fwd_tiles(qo, ko, 1, 128, 128, mask, window):
+            widest = max(widest, t[4] - t[3])
+        want = 2 if widest >= 8 else 0
+        auto = gd.Plan(qo, ko, 2, 128, mask=mask, window=window, num_sms=19,
+                       max_kv_blocks="auto", host_only=True)
+        expl = gd.Plan(qo, ko, 2, 128, mask=mask, window=window, num_sms=19,
+                       max_kv_blocks=want, host_only=True)
+        for a, b in zip(auto.export(), expl.export()):
+            assert np.array_equal(a, b)
+        auto.destroy()
+        expl.destroy()
+
+
 def test_planner_rejects_bad_arguments(gd):
     from recommender_model_attention_gb300 import GdpaError
     good = offsets_from_lengths([3, 4])
@@ -95,6 +121,9 @@ def test_planner_rejects_bad_arguments(gd):
     assert e.value.status == 1
     with pytest.raises(GdpaError) as e:
         gd.Plan(good, good, 1, 64, num_sms=0, host_only=True)
+    assert e.value.status == 1
+    with pytest.raises(GdpaError) as e:
+        gd.Plan(good, good, 1, 64, num_sms=4, max_kv_blocks=-2, host_only=True)
     assert e.value.status == 1
 
 

@@ -120,3 +120,15 @@ def test_split_refused_where_unsupported(gd, what):
             gd.gdpa_fwd(plan, x["q"], x["k"], x["v"])
     plan.destroy()
     torch.cuda.synchronize()
+
+
+def test_automatic_split_matches_oracle(gd):
+    # keys up to 1500 rows (12 blocks): the planner picks 2-block chunks
+    x = _case([32, 32, 5, 200], [1500, 900, 1200, 30], 2, 128, 21)
+    plan = gd.Plan(x["q_off"], x["kv_off"], 2, 128, max_kv_blocks="auto")
+    whole = gd.Plan(x["q_off"], x["kv_off"], 2, 128)
+    assert plan.sizes()[0] > whole.sizes()[0]
+    plan.destroy()
+    whole.destroy()
+    errs = compare_full(gd, x, 2, 128, 128 ** -0.5, "gelu_erf", "bf16", max_kv_blocks="auto")
+    _assert(errs)

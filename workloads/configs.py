@@ -160,8 +160,9 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None,
 
     if w.shared_q:
         seeds = rows(w.shared_q, w.qk_gain)
-        assert tq == w.shared_q * w.B
-        q = seeds.repeat(w.B, 1, 1).contiguous()
+        nb = len(lq)   # w.B, or fewer when a prefix of the batch is drawn
+        assert tq == w.shared_q * nb
+        q = seeds.repeat(nb, 1, 1).contiguous()
     else:
         q = rows(tq, w.qk_gain)
     k = rows(tkv, w.qk_gain)
