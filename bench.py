@@ -36,7 +36,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # ncu captures summarised in profiles/ (first 256 sequences of the training
 # workload; traffic grows with the rows processed, so it is scaled to a full
 # launch by algorithmic bytes).  Valid only for the kernel sources they were
-# measured on (hash of the kernel's source files); otherwise reported null.
+# measured on (hash of the kernel's source files), the training workload and
+# the unsplit softmax-free kernels; otherwise reported null.
+TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
     "gdpa_fwd": ("5d8a14aaafbbec8a", 0.9644),
     "gdpa_bwd": ("6786290a062b0e8a", 1.0207),
@@ -387,7 +389,8 @@ def main():
         dom, dom_ms, dom_bytes = "gdpa_fwd", fwd_ms, fwd_bytes
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     src_hash, ratio = TRAFFIC_RATIO[dom]
-    traffic = ratio * dom_bytes if kernel_source_hash(dom) == src_hash else None
+    traffic = (ratio * dom_bytes if kernel_source_hash(dom) == src_hash and
+               w.name == TRAFFIC_WORKLOAD and not key_split and not softmax else None)
     roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
                 "algorithmic_bytes": dom_bytes, "peak_kind": pk_kind}
