@@ -63,7 +63,9 @@ typedef enum {
     GDPA_ACT_IDENTITY = 4,      /* x (for tests of the linear algebra) */
     /* Softmax variant: O_i = sum_j softmax_j(alpha q_i.k_j) V_j over the row's
      * valid keys (0 for a row without one), i.e. Jagged Flash Attention, the
-     * softmax kernel the GEM page (aitrends.kr, kernel list) names beside
+     * softmax kernel the GEM page ("GEM 트레이닝: Meta가 LLM 규모의 광고
+     * 파운데이션 모델 효율성을 두 배로 높인 방법", techlist.io, section "GPU
+     * 연산 효율을 높인 맞춤형 커널과 정밀도", its kernel list) names beside
      * GDPA.  gdpa_fwd, gdpa_fwd_noalloc and gdpa_softmax_fwd; its gradients
      * come from gdpa_softmax_bwd (gdpa_bwd returns UNSUPPORTED);
      * gdpa_act_eval returns INVALID_ARG. */
@@ -181,6 +183,26 @@ gdpa_status gdpa_plan_export_bwd(gdpa_plan plan, int32_t* units_out, int64_t cap
 
 /* Choose the kernel family (default AUTO); INVALID_ARG for unknown values. */
 gdpa_status gdpa_plan_set_kernel(gdpa_plan plan, gdpa_kernel kernel);
+
+/*
+ * Shared-query mode, for pooling attention (PMA: a fixed set of learned seed
+ * queries attends to each sample's history, compressing it into short
+ * queries against long keys; GEM page "GEM 트레이닝: Meta가 LLM 규모의 광고
+ * 파운데이션 모델 효율성을 두 배로 높인 방법", techlist.io, section on the
+ * asymmetric attention shapes; the GDPA page's diagram of self-attention,
+ * PMA and pFFN sharing one kernel).  n_seeds > 0: the q of gdpa_fwd,
+ * gdpa_bwd, gdpa_softmax_fwd and gdpa_softmax_bwd on this plan is a
+ * [n_seeds][H][d] tensor of seed rows shared by every sample, sample b's
+ * queries being seeds 0 .. Lq_b - 1, so Q is never replicated per sample;
+ * O, dO and lse keep their per-token layout.  The backward's dq is then
+ * [n_seeds][H][d] float32, each seed's gradient summed over the samples
+ * (cleared by the call, then accumulated with atomic adds).  INVALID_ARG if
+ * some sample has more than n_seeds queries; forward and backward calls
+ * return UNSUPPORTED off the tensor-core path (float32 inputs, head dims
+ * other than 64 and 128).  n_seeds = 0 restores per-token queries.
+ * gdpa_fwd_noalloc has no such mode.
+ */
+gdpa_status gdpa_plan_set_shared_q(gdpa_plan plan, int n_seeds);
 
 /* Record per-CTA start/end times (%globaltimer, ns) and SM ids on the next
  * launches (enable != 0), readable with gdpa_sm_times. */

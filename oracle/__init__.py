@@ -15,7 +15,10 @@ The method follows the GDPA page ("범용 내적 어텐션(GDPA): 실제 추천 
 학습 부하를 위한 커널 최적화", aitrends.kr): its summary and first detailed
 section for the formula, the scheduling paragraph and diagram for the planner,
 and the Taylor GELU code figure for the polynomial activation.  The softmax
-variant is the Jagged Flash Attention kernel the GEM page lists beside GDPA.
+variant is the Jagged Flash Attention kernel the GEM page ("GEM 트레이닝:
+Meta가 LLM 규모의 광고 파운데이션 모델 효율성을 두 배로 높인 방법",
+techlist.io, section "GPU 연산 효율을 높인 맞춤형 커널과 정밀도") lists beside
+GDPA.
 """
 
 ACT_IDS = {"gelu_erf": 0, "gelu_tanh": 1, "silu": 2, "gelu_taylor6": 3, "identity": 4,

@@ -25,7 +25,9 @@
  *   - Rows with no valid key give zero output and zero dQ.
  *
  * The softmax variant (kind 5) is the other attention kernel the GEM page
- * ("Meta GEM ... 맞춤형 커널과 정밀도", the kernel list) names next to GDPA:
+ * ("GEM 트레이닝: Meta가 LLM 규모의 광고 파운데이션 모델 효율성을 두 배로
+ * 높인 방법", techlist.io; section "GPU 연산 효율을 높인 맞춤형 커널과
+ * 정밀도", the kernel list) names next to GDPA:
  * Jagged Flash Attention, softmax attention over the same jagged batches.
  * Per query row, over its valid keys only: O_i = sum_j w_j V_j with
  * w_j = exp(s_j - m) / sum_l exp(s_l - m), s_j = alpha q_i.k_j, m = max_j s_j

@@ -172,3 +172,30 @@ def sub_batch(q_off, kv_off, samples):
     q_idx = np.concatenate([np.arange(q_off[b], q_off[b + 1]) for b in samples] or [np.zeros(0)]).astype(np.int64)
     kv_idx = np.concatenate([np.arange(kv_off[b], kv_off[b + 1]) for b in samples] or [np.zeros(0)]).astype(np.int64)
     return sq, skv, q_idx, kv_idx
+
+
+def shared_q_tokens(seeds, q_off) -> np.ndarray:
+    """Shared-query mode (pooling attention: learned seed queries attend to
+    each sample's sequence; GEM page, section on the asymmetric attention
+    shapes).  Sample b's queries are seed rows 0 .. Lq_b - 1, so the
+    per-token Q [Tq, H, d] is the seeds repeated per sample; the forward and
+    backward of shared-query mode are the ordinary ones on this Q."""
+    seeds = to_f64(seeds)
+    q_off = np.asarray(q_off, dtype=np.int64)
+    rows = [seeds[: q_off[b + 1] - q_off[b]] for b in range(len(q_off) - 1)]
+    if not rows:
+        return np.zeros((0,) + seeds.shape[1:])
+    return np.concatenate(rows, axis=0)
+
+
+def shared_q_grad(dq_tokens, q_off, n_seeds: int) -> np.ndarray:
+    """Gradient of the seeds: a parameter used by every sample receives the
+    sum of its per-use gradients, i.e. seed i gets the dQ rows of position i
+    of all samples."""
+    dq_tokens = to_f64(dq_tokens)
+    q_off = np.asarray(q_off, dtype=np.int64)
+    out = np.zeros((n_seeds,) + dq_tokens.shape[1:])
+    for b in range(len(q_off) - 1):
+        n = q_off[b + 1] - q_off[b]
+        out[:n] += dq_tokens[q_off[b]:q_off[b + 1]]
+    return out

@@ -203,6 +203,14 @@ gdpa_status gdpa_plan_set_kernel(gdpa_plan plan, gdpa_kernel kernel) {
     return GDPA_OK;
 }
 
+gdpa_status gdpa_plan_set_shared_q(gdpa_plan plan, int n_seeds) {
+    if (!plan || n_seeds < 0) return GDPA_ERR_INVALID_ARG;
+    Plan& p = *(Plan*)plan;
+    if (n_seeds > 0 && p.max_lq > n_seeds) return GDPA_ERR_INVALID_ARG;
+    p.shared_q = n_seeds;
+    return GDPA_OK;
+}
+
 gdpa_status gdpa_plan_set_timing(gdpa_plan plan, int enable) {
     if (!plan) return GDPA_ERR_INVALID_ARG;
     ((Plan*)plan)->timing = enable ? 1 : 0;
@@ -226,8 +234,9 @@ gdpa_status fwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const vo
     if (p.n_fwd == 0) return GDPA_OK;
     cudaStream_t st = (cudaStream_t)stream;
     if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
-    // key-split tiles: tensor-core path with d = 128 only (partial sums of O)
-    if (p.fwd_split && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
+    // key-split tiles: tensor-core path with d = 128 only (partial sums of O);
+    // shared seed queries: tensor-core path
+    if ((p.fwd_split || p.shared_q) && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
     if (use_tc(p, dtype)) return gdpa::launch_tc_fwd(p, q, k, v, o, lse, alpha, act, st);
     return gdpa::launch_simt_fwd(p, dtype, q, k, v, o, lse, alpha, act, st);
 }
@@ -251,7 +260,7 @@ gdpa_status bwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const vo
     if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
     // the CUDA-core dQ kernel walks the forward tiles and owns each row: no
     // key-split plans there (the tensor-core backward has its own units)
-    if (p.fwd_split && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
+    if ((p.fwd_split || p.shared_q) && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
     const float* delta = nullptr;
     if (sm && p.Tq > 0) {
         // D = dO . O per row, in the plan's workspace (allocated once)

@@ -69,6 +69,10 @@ struct Plan {
     // key-split forward (d = 128): float32 partial sums of O, [Tq][H][d],
     // allocated on first use
     float* d_wsplit = nullptr;
+    // shared-query mode: > 0 = number of seed rows in Q (every sample's
+    // queries are seeds 0 .. Lq_b - 1); dQ is then [shared_q][H][d]
+    int shared_q = 0;
+    int64_t max_lq = 0;   // longest sample (query rows)
 };
 
 // Host planner (gdpa_plan.cpp): fills the host-side vectors of `p` from the
@@ -89,9 +93,9 @@ gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, 
 // starts, error word; times/smid may be NULL to skip per-CTA timing).
 gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, int32_t* err,
                               unsigned long long* times, int32_t* smid, int H, int d, int64_t Tq,
-                              int64_t Tkv, int mask, int window, const void* q, const void* k,
-                              const void* v, void* o, float* lse, float* w, float alpha, int act,
-                              cudaStream_t st);
+                              int64_t Tkv, int mask, int window, const void* q, int64_t q_rows,
+                              int shared_q, const void* k, const void* v, void* o, float* lse,
+                              float* w, float alpha, int act, cudaStream_t st);
 gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, const void* d_o,
                           float* dq, float* dk, float* dv, float alpha, int act, const float* lse,
                           const float* delta, cudaStream_t st);

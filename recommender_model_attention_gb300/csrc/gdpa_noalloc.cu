@@ -204,5 +204,5 @@ extern "C" gdpa_status gdpa_fwd_noalloc(const int32_t* q_off_host, const int32_t
         return GDPA_ERR_CUDA;
     slot->pending = true;
     return launch_tc_fwd_raw(d_tiles, d_seg, S, d_err, nullptr, nullptr, H, d, Tq, Tkv, mask,
-                             window, q, k, v, o, nullptr, nullptr, alpha, act, st);
+                             window, q, Tq, 0, k, v, o, nullptr, nullptr, alpha, act, st);
 }

@@ -90,6 +90,8 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
         if (q_off[b + 1] < q_off[b] || kv_off[b + 1] < kv_off[b]) return GDPA_ERR_INVALID_ARG;
     p.Tq = q_off[B];
     p.Tkv = kv_off[B];
+    p.max_lq = 0;
+    for (int b = 0; b < B; ++b) p.max_lq = std::max<int64_t>(p.max_lq, q_off[b + 1] - q_off[b]);
     const bool win = p.mask == GDPA_MASK_CAUSAL_WINDOW;
     const int64_t W = p.window;
     // key-block hull of query tile m of sample b (empty: k0 = k1 = 0)

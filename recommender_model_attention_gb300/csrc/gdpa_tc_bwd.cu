@@ -75,6 +75,7 @@ struct BwdParams {
     float* dV;
     const float* lse;     // softmax variant: row log-sum-exp [Tq][H]
     const float* delta;   // softmax variant: dO . O per row [Tq][H]
+    int shared_q;         // Q and dQ hold seed rows shared by all samples
     int H;
     float alpha;
     int mask;
@@ -119,7 +120,8 @@ __device__ void bwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
         }
         for (int m = u.m0; m < u.m1; ++m, ++i) {
             const uint32_t s = i & 1, ph = (i >> 1) & 1;
-            const int y = u.qt0 + m * kBM;
+            const int y = u.qt0 + m * kBM;   // dO rows
+            const int yq = prm.shared_q ? m * kBM : y;
             if (!mbar_wait(&bars[C::kQEmpty + s], ph ^ 1, ab, 22)) goto unwind;
             mbar_arrive_expect_tx(&bars[C::kQFull + s], C::kTileBytes);
             q_armed[s] = (int32_t)ph;
@@ -127,7 +129,7 @@ __device__ void bwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
             for (int hf = 0; hf < C::kHalves; ++hf)
                 tma_load_2d(tmQ, &bars[C::kQFull + s],
                             smem + C::kOffQ + s * C::kTileBytes + hf * kHalfBytes, h * D + hf * 64,
-                            y, pol_stream);
+                            yq, pol_stream);
             if (!mbar_wait(&bars[C::kDOEmpty + s], ph ^ 1, ab, 23)) goto unwind;
             mbar_arrive_expect_tx(&bars[C::kDOFull + s], C::kTileBytes);
             do_armed[s] = (int32_t)ph;
@@ -298,7 +300,9 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
     for (int t = seg0; t < seg1; ++t) {
         const BwdUnit u = load_unit(prm.units + t);
         const int h = u.hf & 0xffff;
-        const bool atomic_dq = (u.hf >> 16) & kUnitAtomicDQ;
+        // shared seeds: every sample adds its dQ into the same seed rows
+        const bool atomic_dq = prm.shared_q || ((u.hf >> 16) & kUnitAtomicDQ);
+        const int dq_row0 = prm.shared_q ? 0 : u.qt0;   // dQ row of the sample's query 0
         if (u.m1 <= u.m0) {
             float* base = (wg == 0 ? prm.dK : prm.dV) + (int64_t)u.kvt0 * rs + h * D;
             zero_rows<D>(base, rs, u.nkv, tid);
@@ -414,11 +418,11 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             // dQ tile, d columns [64 wg, 64 wg + 64): TMEM -> this warpgroup's
             // half of the tile's Q buffer (its MMAs are done) -> global
             tc_fence_after();
-            float* dq = prm.dQ + (int64_t)(u.qt0 + m * kBM) * rs + h * D;
+            float* dq = prm.dQ + (int64_t)(dq_row0 + m * kBM) * rs + h * D;
             uint8_t* dq_stage = smem + C::kOffQ + (i & 1) * C::kTileBytes + wg * kHalfBytes;
             if (D == 128 || wg == 0) {
                 drain_warp(trow, kColDP + 64 * wg, 64, dq_stage, tmDQ, h * D + 64 * wg,
-                           u.qt0 + m * kBM, dq + 64 * wg, rs, nq, atomic_dq, prm.alpha, quarter,
+                           dq_row0 + m * kBM, dq + 64 * wg, rs, nq, atomic_dq, prm.alpha, quarter,
                            lane, &bars[C::kDQFree]);
             } else {
                 tc_fence_before();
@@ -535,20 +539,24 @@ gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, 
                           const float* delta, cudaStream_t st) {
     if (p.d != 64 && p.d != 128) return GDPA_ERR_UNSUPPORTED;
     const uint64_t row = (uint64_t)p.H * p.d;
-    if (p.zero_dq && p.Tq > 0) {
-        if (cudaMemsetAsync(dq, 0, (size_t)p.Tq * row * sizeof(float), st) != cudaSuccess)
+    const bool shared = p.shared_q > 0;
+    // dQ rows: the tokens', or the shared seeds' (a sum over samples)
+    const int64_t dq_rows = shared ? p.shared_q : p.Tq;
+    if ((p.zero_dq || shared) && dq_rows > 0) {
+        if (cudaMemsetAsync(dq, 0, (size_t)dq_rows * row * sizeof(float), st) != cudaSuccess)
             return GDPA_ERR_CUDA;
     }
     if (p.n_bwd == 0) return GDPA_OK;
     CUtensorMap maps[7];
     const uint64_t q_rows = p.Tq > 0 ? (uint64_t)p.Tq : 1;
+    const uint64_t qt_rows = dq_rows > 0 ? (uint64_t)dq_rows : 1;   // Q and dQ tensors
     const void* qp = p.Tq > 0 ? q : k;
     const void* dop = p.Tq > 0 ? d_o : k;
-    if (!tc::make_tmap_bf16(&maps[0], qp, q_rows, row, 128) ||
+    if (!tc::make_tmap_bf16(&maps[0], qp, qt_rows, row, 128) ||
         !tc::make_tmap_bf16(&maps[1], k, (uint64_t)p.Tkv, row, 128) ||
         !tc::make_tmap_bf16(&maps[2], v, (uint64_t)p.Tkv, row, 128) ||
         !tc::make_tmap_bf16(&maps[3], dop, q_rows, row, 128) ||
-        !tc::make_tmap_f32(&maps[4], p.Tq > 0 ? (const void*)dq : (const void*)dk, q_rows, row, 32) ||
+        !tc::make_tmap_f32(&maps[4], p.Tq > 0 ? (const void*)dq : (const void*)dk, qt_rows, row, 32) ||
         !tc::make_tmap_f32(&maps[5], dk, (uint64_t)p.Tkv, row, 32) ||
         !tc::make_tmap_f32(&maps[6], dv, (uint64_t)p.Tkv, row, 32))
         return GDPA_ERR_CUDA;
@@ -560,6 +568,7 @@ gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, 
     prm.dV = dv;
     prm.lse = lse;
     prm.delta = delta;
+    prm.shared_q = shared ? 1 : 0;
     prm.H = p.H;
     prm.alpha = alpha;
     prm.mask = p.mask;

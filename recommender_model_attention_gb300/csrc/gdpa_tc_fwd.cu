@@ -89,6 +89,8 @@ struct FwdParams {
     __nv_bfloat16* O;
     float* lse;   // softmax variant: row log-sum-exp [Tq][H] out, or NULL
     float* W;     // key-split plans: float32 [Tq][H][D] partial-sum target, or NULL
+    int shared_q; // Q holds seed rows shared by all samples: a tile's Q rows
+                  // start at its position in the sample, not at its token row
     int H;
     float alpha;
     int mask;
@@ -152,7 +154,7 @@ __device__ void fwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
         for (int hf = 0; hf < C::kHalves; ++hf)
             tma_load_2d(tmQ, &bars[C::kBarQFull + qs],
                         smem + C::kOffQ + qs * C::kTileBytes + hf * kHalfBytes,
-                        tile.h * D + hf * 64, tile.qt0, pol_q);
+                        tile.h * D + hf * 64, prm.shared_q ? tile.i0 : tile.qt0, pol_q);
         const int nit = tile_items<SM>(tile);
         for (int it = 0; it < nit; ++it, ++i) {
             const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
@@ -739,9 +741,9 @@ __global__ void __launch_bounds__(256) split_finalize_kernel(const float4* __res
 
 gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, int32_t* err,
                               unsigned long long* times, int32_t* smid, int H, int d, int64_t Tq,
-                              int64_t Tkv, int mask, int window, const void* q, const void* k,
-                              const void* v, void* o, float* lse, float* w, float alpha, int act,
-                              cudaStream_t st) {
+                              int64_t Tkv, int mask, int window, const void* q, int64_t q_rows,
+                              int shared_q, const void* k, const void* v, void* o, float* lse,
+                              float* w, float alpha, int act, cudaStream_t st) {
     if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
     if (w && (d != 128 || act == kSoftmax)) return GDPA_ERR_UNSUPPORTED;
     if (Tq == 0) return GDPA_OK;
@@ -750,7 +752,8 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
     const uint64_t kv_rows = Tkv > 0 ? (uint64_t)Tkv : 1;
     const void* kp = Tkv > 0 ? k : q;
     const void* vp = Tkv > 0 ? v : q;
-    if (!tc::make_tmap_bf16(&mq, q, (uint64_t)Tq, row, 128) ||
+    if (q_rows < 1) return GDPA_ERR_INVALID_ARG;
+    if (!tc::make_tmap_bf16(&mq, q, (uint64_t)q_rows, row, 128) ||
         !tc::make_tmap_bf16(&mk, kp, kv_rows, row, 128) ||
         !tc::make_tmap_bf16(&mv, vp, kv_rows, row, 128) ||
         !tc::make_tmap_bf16(&mo, o, (uint64_t)Tq, row, 32))
@@ -766,6 +769,7 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
     prm.O = (__nv_bfloat16*)o;
     prm.lse = lse;
     prm.W = w;
+    prm.shared_q = shared_q;
     prm.H = H;
     prm.alpha = alpha;
     prm.mask = mask;
@@ -810,8 +814,9 @@ gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, 
     if (p.timing) p.timed[0] = 1;
     gdpa_status s = launch_tc_fwd_raw(
         p.d_fwd, p.d_fwd_seg, p.S, p.d_err, p.timing ? p.d_times : nullptr,
-        p.timing ? p.d_smid : nullptr, p.H, p.d, p.Tq, p.Tkv, p.mask, p.window, q, k, v, o, lse,
-        w, alpha, act, st);
+        p.timing ? p.d_smid : nullptr, p.H, p.d, p.Tq, p.Tkv, p.mask, p.window, q,
+        p.shared_q > 0 ? (int64_t)p.shared_q : p.Tq, p.shared_q > 0, k, v, o, lse, w, alpha, act,
+        st);
     if (s == GDPA_OK) p.launches += 1;
     if (s == GDPA_OK && w) {
         const int64_t n4 = p.Tq * p.H * p.d / 4;

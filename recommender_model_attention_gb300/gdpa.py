@@ -61,6 +61,7 @@ def lib():
             "gdpa_plan_export_bwd": [vp, i32p, ctypes.c_int64, i64p, i32p, ctypes.POINTER(ctypes.c_int)],
             "gdpa_plan_set_kernel": [vp, st],
             "gdpa_plan_set_timing": [vp, st],
+            "gdpa_plan_set_shared_q": [vp, st],
             "gdpa_fwd": [vp, st, vp, vp, vp, vp, ctypes.c_float, st, vp],
             "gdpa_bwd": [vp, st, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, st, vp],
             "gdpa_check": [vp, vp],
@@ -122,6 +123,8 @@ class Plan:
         self.mask, self.window = mask, int(window)
         self.Tq, self.Tkv = int(qo[-1]), int(ko[-1])
         self.q_off, self.kv_off = qo.copy(), ko.copy()
+        self.shared_q = 0
+        self.q_rows = self.Tq   # rows of q and dq (the seeds in shared-query mode)
         mkb = KV_SPLIT_AUTO if max_kv_blocks == "auto" else int(max_kv_blocks)
         h = ctypes.c_void_p()
         if host_only:
@@ -175,6 +178,14 @@ class Plan:
 
     def set_kernel(self, kernel: str):
         _ok(lib().gdpa_plan_set_kernel(self.handle, KERNEL[kernel]), "gdpa_plan_set_kernel")
+
+    def set_shared_q(self, n_seeds: int):
+        """Shared-query mode: q (and the backward's dq) hold n_seeds seed rows
+        shared by every sample, sample b's queries being seeds 0 .. Lq_b - 1;
+        0 restores per-token queries."""
+        _ok(lib().gdpa_plan_set_shared_q(self.handle, int(n_seeds)), "gdpa_plan_set_shared_q")
+        self.shared_q = int(n_seeds)
+        self.q_rows = self.shared_q if self.shared_q > 0 else self.Tq
 
     def set_timing(self, enable: bool):
         _ok(lib().gdpa_plan_set_timing(self.handle, 1 if enable else 0), "gdpa_plan_set_timing")
@@ -235,11 +246,11 @@ def _ptr(t):
 def gdpa_fwd(plan: Plan, q, k, v, o=None, alpha=None, act: str = "gelu_erf", stream=None):
     """O = act(alpha Q K^T) V per sample and head; returns O ([Tq, H, d], dtype of q)."""
     import torch
-    _check(q, plan.Tq, plan, "q")
+    _check(q, plan.q_rows, plan, "q")
     _check(k, plan.Tkv, plan, "k", q.dtype)
     _check(v, plan.Tkv, plan, "v", q.dtype)
     if o is None:
-        o = torch.empty_like(q)
+        o = torch.empty((plan.Tq, plan.H, plan.d), dtype=q.dtype, device=q.device)
     _check(o, plan.Tq, plan, "o", q.dtype)
     alpha = plan.d ** -0.5 if alpha is None else float(alpha)
     _ok(lib().gdpa_fwd(plan.handle, _dtype_id(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o),
@@ -249,9 +260,10 @@ def gdpa_fwd(plan: Plan, q, k, v, o=None, alpha=None, act: str = "gelu_erf", str
 
 def gdpa_bwd(plan: Plan, q, k, v, do, dq=None, dk=None, dv=None, alpha=None,
              act: str = "gelu_erf", stream=None):
-    """(dQ, dK, dV) as float32 tensors given the upstream gradient dO."""
+    """(dQ, dK, dV) as float32 tensors given the upstream gradient dO (dQ per
+    seed row, summed over the samples, in shared-query mode)."""
     import torch
-    _check(q, plan.Tq, plan, "q")
+    _check(q, plan.q_rows, plan, "q")
     _check(k, plan.Tkv, plan, "k", q.dtype)
     _check(v, plan.Tkv, plan, "v", q.dtype)
     _check(do, plan.Tq, plan, "do", q.dtype)
@@ -259,7 +271,7 @@ def gdpa_bwd(plan: Plan, q, k, v, do, dq=None, dk=None, dv=None, alpha=None,
     dq = torch.empty(q.shape, dtype=f32, device=q.device) if dq is None else dq
     dk = torch.empty(k.shape, dtype=f32, device=k.device) if dk is None else dk
     dv = torch.empty(v.shape, dtype=f32, device=v.device) if dv is None else dv
-    _check(dq, plan.Tq, plan, "dq", f32)
+    _check(dq, plan.q_rows, plan, "dq", f32)
     _check(dk, plan.Tkv, plan, "dk", f32)
     _check(dv, plan.Tkv, plan, "dv", f32)
     alpha = plan.d ** -0.5 if alpha is None else float(alpha)
@@ -306,11 +318,11 @@ def gdpa_softmax_fwd(plan: Plan, q, k, v, o=None, lse=None, alpha=None, stream=N
     """Softmax variant (Jagged Flash Attention): (O, lse), lse the row
     log-sum-exp [Tq, H] float32 the backward needs."""
     import torch
-    _check(q, plan.Tq, plan, "q")
+    _check(q, plan.q_rows, plan, "q")
     _check(k, plan.Tkv, plan, "k", q.dtype)
     _check(v, plan.Tkv, plan, "v", q.dtype)
     if o is None:
-        o = torch.empty_like(q)
+        o = torch.empty((plan.Tq, plan.H, plan.d), dtype=q.dtype, device=q.device)
     _check(o, plan.Tq, plan, "o", q.dtype)
     if lse is None:
         lse = torch.empty((plan.Tq, plan.H), dtype=torch.float32, device=q.device)
@@ -328,7 +340,7 @@ def gdpa_softmax_bwd(plan: Plan, q, k, v, o, do, lse, dq=None, dk=None, dv=None,
     """(dQ, dK, dV) of the softmax variant from its forward's O and lse."""
     import torch
     f32 = torch.float32
-    _check(q, plan.Tq, plan, "q")
+    _check(q, plan.q_rows, plan, "q")
     _check(k, plan.Tkv, plan, "k", q.dtype)
     _check(v, plan.Tkv, plan, "v", q.dtype)
     _check(o, plan.Tq, plan, "o", q.dtype)
@@ -338,7 +350,7 @@ def gdpa_softmax_bwd(plan: Plan, q, k, v, o, do, lse, dq=None, dk=None, dv=None,
     dq = torch.empty(q.shape, dtype=f32, device=q.device) if dq is None else dq
     dk = torch.empty(k.shape, dtype=f32, device=k.device) if dk is None else dk
     dv = torch.empty(v.shape, dtype=f32, device=v.device) if dv is None else dv
-    for t, n, rows in ((dq, "dq", plan.Tq), (dk, "dk", plan.Tkv), (dv, "dv", plan.Tkv)):
+    for t, n, rows in ((dq, "dq", plan.q_rows), (dk, "dk", plan.Tkv), (dv, "dv", plan.Tkv)):
         _check(t, rows, plan, n, f32)
     alpha = plan.d ** -0.5 if alpha is None else float(alpha)
     _ok(lib().gdpa_softmax_bwd(plan.handle, _dtype_id(q), _ptr(q), _ptr(k), _ptr(v), _ptr(o),

@@ -127,6 +127,23 @@ def test_planner_rejects_bad_arguments(gd):
     assert e.value.status == 1
 
 
+def test_shared_q_needs_enough_seeds(gd):
+    from recommender_model_attention_gb300 import GdpaError
+    qo = offsets_from_lengths([32, 5, 0])
+    p = gd.Plan(qo, qo, 1, 128, num_sms=4, host_only=True)
+    with pytest.raises(GdpaError) as e:
+        p.set_shared_q(31)          # a sample has 32 queries
+    assert e.value.status == 1
+    with pytest.raises(GdpaError) as e:
+        p.set_shared_q(-1)
+    assert e.value.status == 1
+    p.set_shared_q(32)
+    assert p.q_rows == 32
+    p.set_shared_q(0)
+    assert p.q_rows == 37
+    p.destroy()
+
+
 def test_host_only_plan_cannot_launch(gd):
     off = offsets_from_lengths([3, 4])
     p = gd.Plan(off, off, 1, 64, num_sms=4, host_only=True)
