@@ -248,6 +248,9 @@ def main():
                     help="key-split plans: at most this many 128-row key blocks per forward "
                          "tile (0 = whole key range per tile; 'auto' = the planner's choice, "
                          "no split for the softmax variant, which refuses split plans)")
+    ap.add_argument("--materialise-q", action="store_true",
+                    help="shared-query workloads: pass Q replicated per sample instead of "
+                         "the seed rows (shared-query mode)")
     ap.add_argument("--act", default=None,
                     help="override the workload's activation; 'softmax' times the softmax "
                          "variant (Jagged Flash Attention) on the same batch")
@@ -284,9 +287,17 @@ def main():
     if w.act == "softmax" and mkb == "auto":
         mkb = 0
 
+    # shared-query workloads (pooling): Q is the seed rows, unless asked to
+    # materialise it per sample
+    n_seeds = w.shared_q if (w.shared_q and not args.materialise_q) else 0
+    q_in = x["q_seeds"] if n_seeds else x["q"]
+
     def make_plan(**kw):
-        return gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window,
-                       max_kv_blocks=mkb, **kw)
+        p = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window,
+                    max_kv_blocks=mkb, **kw)
+        if n_seeds:
+            p.set_shared_q(n_seeds)
+        return p
 
     plan = make_plan()
     # host planning + upload of one batch's plan (it synchronises on its upload)
@@ -302,7 +313,7 @@ def main():
     whole.destroy()
     f32 = torch.float32
     o = torch.empty_like(x["q"])
-    dq = torch.empty(x["q"].shape, dtype=f32, device="cuda")
+    dq = torch.empty(q_in.shape, dtype=f32, device="cuda")
     dk = torch.empty(x["k"].shape, dtype=f32, device="cuda")
     dv = torch.empty(x["v"].shape, dtype=f32, device="cuda")
     backward = x["do"] is not None
@@ -313,7 +324,7 @@ def main():
 
     def fwd_call(p, q, k, v, o_):
         if softmax:
-            lse = lse_of.setdefault(o_.data_ptr(), torch.empty((q.shape[0], w.H), dtype=f32,
+            lse = lse_of.setdefault(o_.data_ptr(), torch.empty((o_.shape[0], w.H), dtype=f32,
                                                                device=q.device))
             gd.gdpa_softmax_fwd(p, q, k, v, o=o_, lse=lse, alpha=w.alpha)
         else:
@@ -327,20 +338,21 @@ def main():
             gd.gdpa_bwd(p, q, k, v, do_, dq_, dk_, dv_, alpha=w.alpha, act=w.act)
 
     def step():
-        fwd_call(plan, x["q"], x["k"], x["v"], o)
+        fwd_call(plan, q_in, x["k"], x["v"], o)
         if backward:
-            bwd_call(plan, x["q"], x["k"], x["v"], o, x["do"], dq, dk, dv)
+            bwd_call(plan, q_in, x["k"], x["v"], o, x["do"], dq, dk, dv)
 
     Tq, Tkv = int(x["q_off"][-1]), int(x["kv_off"][-1])
     pairs = useful_pairs(x["q_off"], x["kv_off"], w.mask, w.window)
     fwd_flops = 4.0 * w.d * w.H * pairs
     bwd_flops = 8.0 * w.d * w.H * pairs if backward else 0.0
     row = w.H * w.d
-    fwd_bytes = (2 * Tq + 2 * Tkv) * row * 2
-    bwd_bytes = (2 * Tq + 2 * Tkv) * row * 2 + (Tq + 2 * Tkv) * row * 4 if backward else 0
+    Rq = int(q_in.shape[0])   # Q and dQ rows (the seeds in shared-query mode)
+    fwd_bytes = (Rq + Tq + 2 * Tkv) * row * 2
+    bwd_bytes = (Rq + Tq + 2 * Tkv) * row * 2 + (Rq + 2 * Tkv) * row * 4 if backward else 0
     if backward and softmax:
         bwd_bytes += Tq * row * 2   # O, read for the dO.O rows
-    input_bytes = sum(t.numel() * t.element_size() for t in (x["q"], x["k"], x["v"], x["do"])
+    input_bytes = sum(t.numel() * t.element_size() for t in (q_in, x["k"], x["v"], x["do"])
                       if t is not None)
 
     for _ in range(args.warmup):
@@ -363,10 +375,10 @@ def main():
     start.record(stream)
     for s in range(args.steps):
         ev[s][0].record(stream)
-        fwd_call(plan, x["q"], x["k"], x["v"], o)
+        fwd_call(plan, q_in, x["k"], x["v"], o)
         ev[s][1].record(stream)
         if backward:
-            bwd_call(plan, x["q"], x["k"], x["v"], o, x["do"], dq, dk, dv)
+            bwd_call(plan, q_in, x["k"], x["v"], o, x["do"], dq, dk, dv)
         ev[s][2].record(stream)
     end.record(stream)
     torch.cuda.synchronize()
@@ -403,7 +415,7 @@ def main():
     # results come down on another; two device buffer sets alternate.
     e2e = None
     if not args.no_e2e:
-        hq = x["q"].cpu().pin_memory()
+        hq = q_in.cpu().pin_memory()
         hk = x["k"].cpu().pin_memory()
         hv = x["v"].cpu().pin_memory()
         hdo = x["do"].cpu().pin_memory() if backward else None
@@ -411,8 +423,8 @@ def main():
         hgrads = [torch.empty(t.shape, dtype=f32, pin_memory=True) for t in (dq, dk, dv)]
         sets = []
         for _ in range(2):
-            ins = [torch.empty_like(t) for t in (x["q"], x["k"], x["v"])]
-            ins.append(torch.empty_like(x["q"]) if backward else None)
+            ins = [torch.empty_like(t) for t in (q_in, x["k"], x["v"])]
+            ins.append(torch.empty_like(x["do"]) if backward else None)
             outs = [torch.empty_like(o)] + ([torch.empty_like(t) for t in (dq, dk, dv)]
                                             if backward else [])
             sets.append((ins, outs))
@@ -506,7 +518,7 @@ def main():
         for pol in ("zigzag", "round_robin"):
             pp = make_plan(sched=pol)
             pp.set_timing(True)
-            fwd_call(pp, x["q"], x["k"], x["v"], o)
+            fwd_call(pp, q_in, x["k"], x["v"], o)
             pp.check()
             se, _ = pp.sm_times("fwd")
             busy = (se[:, 1] - se[:, 0]).astype(np.float64)
@@ -528,7 +540,7 @@ def main():
             "data": "synthetic (seeded lengths and RMSNorm'd N(0,1) inputs, random dO)",
             "config": {"workload": w.name, "B": len(x["q_off"]) - 1, "H": w.H, "d": w.d,
                        "act": w.act, "max_kv_blocks": mkb,
-                       "key_split": key_split,
+                       "key_split": key_split, "shared_q": n_seeds,
                        "Tq": Tq, "Tkv": Tkv, "useful_pairs": pairs,
                        "l2": "inputs larger than L2 (%.1f GB resident)" % (input_bytes / 1e9),
                        "parallelism": "samples sharded by rank, no exchange" if world > 1

@@ -133,7 +133,9 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None,
 
     Returns a dict with int32 numpy offsets ``q_off``/``kv_off`` and torch
     tensors ``q``, ``k``, ``v`` ([T, H, d], contiguous) and ``do`` (or None),
-    all in the workload's dtype on ``device``.
+    all in the workload's dtype on ``device``; for shared-query workloads also
+    ``q_seeds`` ([shared_q, H, d]; ``q`` is then the seeds repeated per
+    sample), else ``q_seeds`` is None.
     """
     import torch
 
@@ -158,6 +160,7 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None,
             out[s:e] = x.to(dt)
         return out
 
+    seeds = None
     if w.shared_q:
         seeds = rows(w.shared_q, w.qk_gain)
         nb = len(lq)   # w.B, or fewer when a prefix of the batch is drawn
@@ -174,7 +177,7 @@ def make_inputs(w: Workload, device="cpu", seed: Optional[int] = None,
             e = min(tq, s + chunk_rows)
             do[s:e] = torch.randn((e - s, w.H, w.d), generator=g, device=device,
                                   dtype=torch.float32).to(dt)
-    return dict(q_off=q_off, kv_off=kv_off, q=q, k=k, v=v, do=do)
+    return dict(q_off=q_off, kv_off=kv_off, q=q, k=k, v=v, do=do, q_seeds=seeds)
 
 
 def small_case(seed: int, B: int, H: int, d: int, q_range=(1, 64), kv_range=None,
