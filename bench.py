@@ -40,8 +40,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the unsplit softmax-free kernels; otherwise reported null.
 TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
-    "gdpa_fwd": ("5d8a14aaafbbec8a", 0.9644),
-    "gdpa_bwd": ("6786290a062b0e8a", 1.0207),
+    "gdpa_fwd": ("6058eb4427101988", 0.9644),
+    "gdpa_bwd": ("a24f15ff534237b6", 1.0206),
 }
 KERNEL_SOURCES = {
     "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh"),
