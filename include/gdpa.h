@@ -118,12 +118,17 @@ typedef struct gdpa_plan_s* gdpa_plan;   /* opaque, owned by the library */
  *                            partial sums of O into a plan-owned workspace
  *                            ([Tq][H][d] float, allocated on first use and
  *                            cleared on every call) and rounds it into O with
- *                            a second kernel; it needs the tensor-core path
- *                            with d = 128 and a GDPA activation: other
- *                            combinations (d = 64, float32 inputs, the
- *                            softmax variant) return UNSUPPORTED.  The
- *                            backward does not use the forward tiles and
- *                            takes split plans on the tensor-core path.
+ *                            a second kernel: on the tensor cores for d =
+ *                            128, on the CUDA-core kernels otherwise (float32
+ *                            inputs, other head dims; with GDPA_KERNEL_AUTO
+ *                            also bf16 d = 64, which GDPA_KERNEL_TCGEN05
+ *                            refuses with UNSUPPORTED).  The softmax
+ *                            variant's forward refuses split plans
+ *                            (UNSUPPORTED: its chunks would need a max/sum
+ *                            merge).  The backward takes split plans on
+ *                            every path (the CUDA-core dQ kernel then adds
+ *                            each chunk's share atomically into a cleared
+ *                            dQ).
  *                            GDPA_KV_SPLIT_AUTO (-1): the planner picks
  *                            chunks of 2 key blocks when some query tile
  *                            reaches 8 or more key blocks (the fastest
@@ -197,9 +202,8 @@ gdpa_status gdpa_plan_set_kernel(gdpa_plan plan, gdpa_kernel kernel);
  * O, dO and lse keep their per-token layout.  The backward's dq is then
  * [n_seeds][H][d] float32, each seed's gradient summed over the samples
  * (cleared by the call, then accumulated with atomic adds).  INVALID_ARG if
- * some sample has more than n_seeds queries; forward and backward calls
- * return UNSUPPORTED off the tensor-core path (float32 inputs, head dims
- * other than 64 and 128).  n_seeds = 0 restores per-token queries.
+ * some sample has more than n_seeds queries.  Every kernel path supports
+ * it.  n_seeds = 0 restores per-token queries.
  * gdpa_fwd_noalloc has no such mode.
  */
 gdpa_status gdpa_plan_set_shared_q(gdpa_plan plan, int n_seeds);

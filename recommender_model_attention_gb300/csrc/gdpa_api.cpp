@@ -234,10 +234,13 @@ gdpa_status fwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const vo
     if (p.n_fwd == 0) return GDPA_OK;
     cudaStream_t st = (cudaStream_t)stream;
     if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
-    // key-split tiles: tensor-core path with d = 128 only (partial sums of O);
-    // shared seed queries: tensor-core path
-    if ((p.fwd_split || p.shared_q) && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
-    if (use_tc(p, dtype)) return gdpa::launch_tc_fwd(p, q, k, v, o, lse, alpha, act, st);
+    // key-split tiles: the softmax variant's chunks would need a max/sum
+    // merge; the tensor-core forward splits only d = 128 (AUTO runs other
+    // head dims' split plans on the CUDA-core kernels)
+    if (p.fwd_split && act == GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
+    const bool tc =
+        use_tc(p, dtype) && !(p.fwd_split && p.d != 128 && p.kernel == GDPA_KERNEL_AUTO);
+    if (tc) return gdpa::launch_tc_fwd(p, q, k, v, o, lse, alpha, act, st);
     return gdpa::launch_simt_fwd(p, dtype, q, k, v, o, lse, alpha, act, st);
 }
 
@@ -258,9 +261,6 @@ gdpa_status bwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const vo
         return GDPA_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
-    // the CUDA-core dQ kernel walks the forward tiles and owns each row: no
-    // key-split plans there (the tensor-core backward has its own units)
-    if ((p.fwd_split || p.shared_q) && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
     const float* delta = nullptr;
     if (sm && p.Tq > 0) {
         // D = dO . O per row, in the plan's workspace (allocated once)

@@ -6,8 +6,13 @@
 // One CTA of four warps per tile; one warp per row; lane c holds elements
 // c, c + 32, c + 64, c + 96 of the row (d <= 128).  Scores are warp
 // reductions.  The key loop of a row is limited to its valid keys, so no
-// masking is needed inside it.
+// masking is needed inside it.  Key-split plans add each tile's partial O
+// into a float32 workspace (rounded into O afterwards) and their dQ rows
+// with atomic adds; in shared-query mode a row's Q (and dQ) is the seed at
+// its position in the sample.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "act.cuh"
 #include "gdpa_internal.h"
@@ -59,15 +64,16 @@ __device__ __forceinline__ void key_range(int i, int kb0, int kb1, int lkv, int 
 template <int ACT, typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 simt_fwd_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__ Q, const T* __restrict__ K,
-                const T* __restrict__ V, T* __restrict__ O, int H, int d, float alpha, int mask,
-                int window) {
+                const T* __restrict__ V, T* __restrict__ O, float* __restrict__ W, int H, int d,
+                float alpha, int mask, int window, int shared_q) {
     const FwdTile t = tiles[blockIdx.x];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)H * d;
     for (int r = warp; r < t.nq; r += kWarps) {
         const int64_t qrow = (int64_t)(t.qt0 + r) * row + (int64_t)t.h * d;
+        const int64_t qin = (int64_t)((shared_q ? t.i0 : t.qt0) + r) * row + (int64_t)t.h * d;
         float q[kPer], o[kPer] = {0.f, 0.f, 0.f, 0.f};
-        load_row(q, Q + qrow, d, lane);
+        load_row(q, Q + qin, d, lane);
         int lo, hi;
         key_range(t.i0 + r, t.kb0, t.kb1, t.lkv, mask, window, lo, hi);
         for (int j = lo; j < hi; ++j) {
@@ -82,7 +88,12 @@ simt_fwd_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__ Q, cons
 #pragma unroll
         for (int c = 0; c < kPer; ++c) {
             const int e = lane + 32 * c;
-            if (e < d) stf(O + qrow + e, o[c]);
+            if (e < d) {
+                if (W)
+                    atomicAdd(W + qrow + e, o[c]);   // one key chunk of a split plan
+                else
+                    stf(O + qrow + e, o[c]);
+            }
         }
     }
 }
@@ -95,14 +106,16 @@ template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 simt_softmax_fwd_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__ Q,
                         const T* __restrict__ K, const T* __restrict__ V, T* __restrict__ O,
-                        float* __restrict__ lse, int H, int d, float alpha, int mask, int window) {
+                        float* __restrict__ lse, int H, int d, float alpha, int mask, int window,
+                        int shared_q) {
     const FwdTile t = tiles[blockIdx.x];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)H * d;
     for (int r = warp; r < t.nq; r += kWarps) {
         const int64_t qrow = (int64_t)(t.qt0 + r) * row + (int64_t)t.h * d;
+        const int64_t qin = (int64_t)((shared_q ? t.i0 : t.qt0) + r) * row + (int64_t)t.h * d;
         float q[kPer], o[kPer] = {0.f, 0.f, 0.f, 0.f};
-        load_row(q, Q + qrow, d, lane);
+        load_row(q, Q + qin, d, lane);
         int lo, hi;
         key_range(t.i0 + r, t.kb0, t.kb1, t.lkv, mask, window, lo, hi);
         float m = -INFINITY, l = 0.0f;
@@ -136,14 +149,16 @@ __global__ void __launch_bounds__(kWarps * 32)
 simt_bwd_dq_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__ Q,
                    const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
                    float* __restrict__ dQ, int H, int d, float alpha, int mask, int window,
-                   const float* __restrict__ lse, const float* __restrict__ delta) {
+                   const float* __restrict__ lse, const float* __restrict__ delta, int shared_q,
+                   int accumulate) {
     const FwdTile t = tiles[blockIdx.x];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t row = (int64_t)H * d;
     for (int r = warp; r < t.nq; r += kWarps) {
         const int64_t qrow = (int64_t)(t.qt0 + r) * row + (int64_t)t.h * d;
+        const int64_t qin = (int64_t)((shared_q ? t.i0 : t.qt0) + r) * row + (int64_t)t.h * d;
         float q[kPer], go[kPer], acc[kPer] = {0.f, 0.f, 0.f, 0.f};
-        load_row(q, Q + qrow, d, lane);
+        load_row(q, Q + qin, d, lane);
         load_row(go, dO + qrow, d, lane);
         int lo, hi;
         key_range(t.i0 + r, t.kb0, t.kb1, t.lkv, mask, window, lo, hi);
@@ -169,7 +184,12 @@ simt_bwd_dq_kernel(const FwdTile* __restrict__ tiles, const T* __restrict__ Q,
 #pragma unroll
         for (int c = 0; c < kPer; ++c) {
             const int e = lane + 32 * c;
-            if (e < d) dQ[qrow + e] = alpha * acc[c];
+            if (e < d) {
+                if (accumulate)   // several key chunks or samples add into this row
+                    atomicAdd(dQ + qin + e, alpha * acc[c]);
+                else
+                    dQ[qin + e] = alpha * acc[c];
+            }
         }
     }
 }
@@ -181,7 +201,7 @@ simt_bwd_dkdv_kernel(const BwdUnit* __restrict__ units, const T* __restrict__ Q,
                      const T* __restrict__ K, const T* __restrict__ V, const T* __restrict__ dO,
                      float* __restrict__ dK, float* __restrict__ dV, int H, int d, float alpha,
                      int mask, int window, const float* __restrict__ lse,
-                     const float* __restrict__ delta) {
+                     const float* __restrict__ delta, int shared_q) {
     const BwdUnit u = units[blockIdx.x];
     const int h = u.hf & 0xffff;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -199,8 +219,9 @@ simt_bwd_dkdv_kernel(const BwdUnit* __restrict__ units, const T* __restrict__ Q,
         }
         for (int i = lo; i < hi; ++i) {
             const int64_t qrow = (int64_t)(u.qt0 + i) * row + (int64_t)h * d;
+            const int64_t qin = (int64_t)(shared_q ? i : u.qt0 + i) * row + (int64_t)h * d;
             float q[kPer], go[kPer];
-            load_row(q, Q + qrow, d, lane);
+            load_row(q, Q + qin, d, lane);
             load_row(go, dO + qrow, d, lane);
             const float x = alpha * dot_row(q, kx);
             float a, g;
@@ -230,22 +251,48 @@ simt_bwd_dkdv_kernel(const BwdUnit* __restrict__ units, const T* __restrict__ Q,
     }
 }
 
+// key-split plans: O = W rounded to the output type
+template <typename T>
+__global__ void __launch_bounds__(256) split_round_kernel(const float* __restrict__ w,
+                                                          T* __restrict__ o, int64_t n) {
+    for (int64_t i = blockIdx.x * 256LL + threadIdx.x; i < n; i += (int64_t)gridDim.x * 256)
+        stf(o + i, w[i]);
+}
+
 template <typename T>
 gdpa_status fwd_impl(Plan& p, const void* q, const void* k, const void* v, void* o, float* lse,
                      float alpha, int act, cudaStream_t st) {
     const unsigned grid = (unsigned)p.n_fwd;
+    const int sq = p.shared_q > 0;
     if (act == kSoftmax) {
+        if (p.fwd_split) return GDPA_ERR_UNSUPPORTED;   // chunks would need a max/sum merge
         simt_softmax_fwd_kernel<T><<<grid, kWarps * 32, 0, st>>>(
             p.d_fwd, (const T*)q, (const T*)k, (const T*)v, (T*)o, lse, p.H, p.d, alpha, p.mask,
-            p.window);
+            p.window, sq);
         p.launches += 1;
         return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
     }
+    float* w = nullptr;
+    const int64_t n = p.Tq * p.H * p.d;
+    if (p.fwd_split) {
+        const size_t bytes = (size_t)n * sizeof(float);
+        if (!p.d_wsplit && cudaMalloc((void**)&p.d_wsplit, bytes) != cudaSuccess) {
+            p.d_wsplit = nullptr;
+            return GDPA_ERR_ALLOC;
+        }
+        if (cudaMemsetAsync(p.d_wsplit, 0, bytes, st) != cudaSuccess) return GDPA_ERR_CUDA;
+        w = p.d_wsplit;
+    }
     GDPA_DISPATCH_ACT(act, A,
         simt_fwd_kernel<A, T><<<grid, kWarps * 32, 0, st>>>(
-            p.d_fwd, (const T*)q, (const T*)k, (const T*)v, (T*)o, p.H, p.d, alpha, p.mask,
-            p.window))
+            p.d_fwd, (const T*)q, (const T*)k, (const T*)v, (T*)o, w, p.H, p.d, alpha, p.mask,
+            p.window, sq))
     p.launches += 1;
+    if (w && n > 0) {
+        const unsigned blocks = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 8);
+        split_round_kernel<T><<<blocks, 256, 0, st>>>(w, (T*)o, n);
+        p.launches += 1;
+    }
     return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
@@ -253,36 +300,44 @@ template <typename T>
 gdpa_status bwd_impl(Plan& p, const void* q, const void* k, const void* v, const void* d_o,
                      float* dq, float* dk, float* dv, float alpha, int act, const float* lse,
                      const float* delta, cudaStream_t st) {
+    // dQ rows receive adds from several tiles (key-split plans) or samples
+    // (shared queries): clear first
+    const int sq = p.shared_q > 0;
+    const int acc = sq || p.fwd_split;
+    const int64_t dq_rows = sq ? p.shared_q : p.Tq;
+    if (acc && dq_rows > 0 &&
+        cudaMemsetAsync(dq, 0, (size_t)dq_rows * p.H * p.d * sizeof(float), st) != cudaSuccess)
+        return GDPA_ERR_CUDA;
     if (act == kSoftmax) {
         if (p.n_fwd > 0) {
             simt_bwd_dq_kernel<kSoftmax, T><<<(unsigned)p.n_fwd, kWarps * 32, 0, st>>>(
                 p.d_fwd, (const T*)q, (const T*)k, (const T*)v, (const T*)d_o, dq, p.H, p.d,
-                alpha, p.mask, p.window, lse, delta);
+                alpha, p.mask, p.window, lse, delta, sq, acc);
             p.launches += 1;
         }
         if (p.n_bwd > 0) {
             simt_bwd_dkdv_kernel<kSoftmax, T><<<(unsigned)p.n_bwd, kWarps * 32, 0, st>>>(
                 p.d_bwd, (const T*)q, (const T*)k, (const T*)v, (const T*)d_o, dk, dv, p.H, p.d,
-                alpha, p.mask, p.window, lse, delta);
+                alpha, p.mask, p.window, lse, delta, sq);
             p.launches += 1;
         }
         return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
     }
-    // The forward tiles (zero tiles included) cover every query row once and
-    // the backward units every key row once, so both kernels store their
-    // rows directly and nothing needs clearing first.
+    // Otherwise the forward tiles (zero tiles included) cover every query row
+    // once and the backward units every key row once, so both kernels store
+    // their rows directly.
     if (p.n_fwd > 0) {
         GDPA_DISPATCH_ACT(act, A,
             simt_bwd_dq_kernel<A, T><<<(unsigned)p.n_fwd, kWarps * 32, 0, st>>>(
                 p.d_fwd, (const T*)q, (const T*)k, (const T*)v, (const T*)d_o, dq, p.H, p.d,
-                alpha, p.mask, p.window, nullptr, nullptr))
+                alpha, p.mask, p.window, nullptr, nullptr, sq, acc))
         p.launches += 1;
     }
     if (p.n_bwd > 0) {
         GDPA_DISPATCH_ACT(act, A,
             simt_bwd_dkdv_kernel<A, T><<<(unsigned)p.n_bwd, kWarps * 32, 0, st>>>(
                 p.d_bwd, (const T*)q, (const T*)k, (const T*)v, (const T*)d_o, dk, dv, p.H, p.d,
-                alpha, p.mask, p.window, nullptr, nullptr))
+                alpha, p.mask, p.window, nullptr, nullptr, sq))
         p.launches += 1;
     }
     return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;

@@ -109,12 +109,23 @@ def test_shared_q_with_key_split_and_repeat(gd):
     plan.destroy()
 
 
-def test_shared_q_refused_off_the_tensor_core_path(gd):
+@pytest.mark.parametrize("dtype,d", [("f32", 128), ("f32", 40), ("bf16", 32)])
+@pytest.mark.parametrize("act", ["gelu_tanh", "softmax"])
+def test_shared_q_on_cuda_cores(gd, dtype, d, act):
     import torch
-    x = _case([4, 4], [30, 10], 4, 1, 32, 3, dtype="f32")
-    plan = gd.Plan(x["q_off"], x["kv_off"], 1, 32)
-    plan.set_shared_q(4)
-    with pytest.raises(gd.GdpaError):
-        gd.gdpa_fwd(plan, x["q"], x["k"], x["v"])
-    plan.destroy()
+    x = _case([4, 4, 0, 2], [30, 10, 5, 200], 6, 2, d, 3 + d, dtype=dtype)
+    alpha = d ** -0.5
+    plan = gd.Plan(x["q_off"], x["kv_off"], 2, d)
+    plan.set_shared_q(6)
+    if act == "softmax":
+        o, lse = gd.gdpa_softmax_fwd(plan, x["q"], x["k"], x["v"], alpha=alpha)
+        dq, dk, dv = gd.gdpa_softmax_bwd(plan, x["q"], x["k"], x["v"], o, x["do"], lse, alpha=alpha)
+    else:
+        o = gd.gdpa_fwd(plan, x["q"], x["k"], x["v"], alpha=alpha, act=act)
+        dq, dk, dv = gd.gdpa_bwd(plan, x["q"], x["k"], x["v"], x["do"], alpha=alpha, act=act)
+    plan.check()
     torch.cuda.synchronize()
+    ro, rdq, rdk, rdv = _oracle(x, 6, alpha, act)
+    _assert({"o": max_rel(ref.to_f64(o), ro), "dq": max_rel(ref.to_f64(dq), rdq),
+             "dk": max_rel(ref.to_f64(dk), rdk), "dv": max_rel(ref.to_f64(dv), rdv)}, TOL[dtype])
+    plan.destroy()

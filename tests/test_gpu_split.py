@@ -7,9 +7,12 @@ shape) spreads over many SMs.  Each chunk adds its float32 partial sum of O
 into a zeroed workspace and a second kernel rounds it to bf16.  Since
 O = act(alpha Q K^T) V is a plain sum over keys for GDPA, the result must
 match the oracle to the same bf16 tolerance as an unsplit plan; the backward
-pass (which has its own per-key-block units) must be unaffected.  The
-tensor-core path with d = 128 supports it; d = 64, float32 inputs and the
-softmax variant (whose normalisation couples the chunks) refuse it.
+pass must be unaffected (the tensor-core backward has its own per-key-block
+units; the CUDA-core dQ kernel adds each chunk's share atomically).  The
+tensor-core forward splits d = 128; float32 inputs and other head dims
+(bf16 d = 64 included, under the automatic kernel choice) split on the
+CUDA-core kernels, checked to 1e-5 for float32; the softmax variant's
+forward, whose normalisation couples the chunks, refuses split plans.
 """
 
 import numpy as np
@@ -107,19 +110,33 @@ def test_split_repeat_is_stable_and_close_to_whole(gd):
     whole.destroy()
 
 
-@pytest.mark.parametrize("what", ["d64", "f32", "softmax"])
-def test_split_refused_where_unsupported(gd, what):
+@pytest.mark.parametrize("what", ["bf16_d64", "f32_d128", "f32_d40"])
+@pytest.mark.parametrize("act", ["gelu_erf", "silu"])
+def test_split_on_cuda_cores(gd, what, act):
+    dtype, d = what.split("_d")[0], int(what.split("_d")[1])
+    x = _case([8, 130, 1], [600, 300, 0], 2, d, 3 + d, dtype=dtype)
+    errs = compare_full(gd, x, 2, d, d ** -0.5, act, dtype, max_kv_blocks=1)
+    _assert(errs, TOL[dtype])
+
+
+def test_split_softmax_forward_refused_backward_runs(gd):
     import torch
-    d = 64 if what == "d64" else 128
-    x = _case([8], [600], 1, d, 3, dtype="f32" if what == "f32" else "bf16")
-    plan = gd.Plan(x["q_off"], x["kv_off"], 1, d, max_kv_blocks=1)
+    x = _case([8, 40], [600, 300], 1, 128, 3)
+    split = gd.Plan(x["q_off"], x["kv_off"], 1, 128, max_kv_blocks=1)
+    whole = gd.Plan(x["q_off"], x["kv_off"], 1, 128)
     with pytest.raises(gd.GdpaError):
-        if what == "softmax":
-            gd.gdpa_softmax_fwd(plan, x["q"], x["k"], x["v"])
-        else:
-            gd.gdpa_fwd(plan, x["q"], x["k"], x["v"])
-    plan.destroy()
+        gd.gdpa_softmax_fwd(split, x["q"], x["k"], x["v"])
+    # the statistics of an unsplit forward feed the split plan's backward
+    o, lse = gd.gdpa_softmax_fwd(whole, x["q"], x["k"], x["v"])
+    got = gd.gdpa_softmax_bwd(split, x["q"], x["k"], x["v"], o, x["do"], lse)
+    want = gd.gdpa_softmax_bwd(whole, x["q"], x["k"], x["v"], o, x["do"], lse)
+    split.check()
+    whole.check()
     torch.cuda.synchronize()
+    for g, w in zip(got, want):
+        assert max_rel(ref.to_f64(g), ref.to_f64(w)) <= 1e-5
+    split.destroy()
+    whole.destroy()
 
 
 def test_automatic_split_matches_oracle(gd):
