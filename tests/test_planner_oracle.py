@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 from oracle import planner
-from workloads import CONFIGS, draw_lengths, offsets_from_lengths, small_case
+from workloads import draw_lengths, get_config, offsets_from_lengths, small_case
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -129,7 +129,7 @@ def test_dealing_invariants(policy, S):
 
 
 def test_plan_export_layout():
-    w = CONFIGS[1]
+    w = get_config("jagged_selfattn_window256")
     lq, lkv = draw_lengths(w)
     qo, ko = offsets_from_lengths(lq), offsets_from_lengths(lkv)
     p = planner.plan(qo, ko, w.H, 152, mask=w.mask, window=w.window)
