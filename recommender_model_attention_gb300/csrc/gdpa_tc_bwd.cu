@@ -21,10 +21,13 @@
 // d columns [64j, 64j + 64)), dV (j = 0) and dK (j = 1) from TMEM.  Per
 // query tile:
 //     S  = Q K^T   -> TMEM [0, 128)      dP = dO V^T -> TMEM [128, 256)
-//     dS           -> the 32 KB shared [query x key] buffer
-//     dQ  = dS K   -> TMEM [128, 256) (dP's columns, already read)
-//     dK += dS^T Q -> TMEM [384, 512)
-//     P            -> the same buffer, once dQ and dK have read dS
+//     dS           -> the 32 KB shared [query x key] buffer, and packed into
+//                     the first half of each 16-column step of S's own
+//                     columns (already read)
+//     dK += dS^T Q -> TMEM [384, 512), dS^T from the buffer
+//     dQ  = dS K   -> TMEM [128, 256) (dP's columns, already read), dS from
+//                     TMEM
+//     P            -> the same buffer, once dK has read dS
 //     dV += P^T dO -> TMEM [256, 384), while the warpgroups drain dQ through
 //                     the tile's Q buffer (its MMAs are done)
 // The next tile's S is issued as soon as both warpgroups have read S, its dP
@@ -62,7 +65,7 @@ struct BwdCfg {
     enum {
         kKVFull = 0, kKVEmpty, kQFull, kQFull1, kQEmpty, kQEmpty1, kDOFull, kDOFull1, kDOEmpty,
         kDOEmpty1, kSDFull, kSFree, kDQFree, kPFull, kPVDone, kDSFull, kDKDone, kAccFull,
-        kAccFree, kStage, kStage1, kPSFree, kMmaDone, kNumBars
+        kAccFree, kStage, kStage1, kPSFree, kMmaDone, kDQDone, kNumBars
     };
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
 };
@@ -204,19 +207,21 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             const uint32_t nq32 = (uint32_t)((nq + 31) & ~31);
             const uint32_t qb = smem_u32(smem + C::kOffQ + s * C::kTileBytes);
             const uint32_t dob = smem_u32(smem + C::kOffDO + s * C::kTileBytes);
-            // dQ = dS K (into dP's columns, already read) and dK += dS^T Q
+            // dK += dS^T Q (dS^T from the shared buffer), then dQ = dS K into
+            // dP's columns (already read), dS from TMEM: the warpgroups may
+            // replace dS by P in the buffer as soon as dK is done
             if (!wg_wait(&bars[C::kDSFull], i & 1, ab, 38)) goto drain;
             if (first && !wg_wait(&bars[C::kAccFree], (nu & 1) ^ 1, ab, 37)) goto drain;
             tc_fence_after();
-            for (uint32_t k = 0; k < nkv16 / 16; ++k)
-                mma_ss(tmem + kColDP,
-                       smem_desc_sw128(psbase + (k >> 2) * kHalfBytes + (k & 3) * 32, 16, 1024),
-                       smem_desc_sw128(kbase + k * 2048, kHalfBytes, 1024), idesc_dq, k > 0);
             for (uint32_t k = 0; k < nq32 / 16; ++k)
                 mma_ss(tmem + kColDK, smem_desc_sw128(psbase + k * 2048, kHalfBytes, 1024),
                        smem_desc_sw128(qb + k * 2048, kHalfBytes, 1024), idesc_acc,
                        (first && k == 0) ? 0u : 1u);
             mma_commit(&bars[C::kDKDone]);
+            for (uint32_t k = 0; k < nkv16 / 16; ++k)
+                mma_ts(tmem + kColDP, tmem + kColS + k * 16,
+                       smem_desc_sw128(kbase + k * 2048, kHalfBytes, 1024), idesc_dq, k > 0);
+            mma_commit(&bars[C::kDQDone]);
             // the next tile's scores (the warpgroups have read this tile's S)
             if (!last && !issue_s(i + 1)) goto drain;
             // dV += P^T dO once P has replaced dS in shared memory
@@ -397,14 +402,18 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                             }
                         }
                         store_half_chunk(ps, sidx >> 1, sidx & 1, r, pd);
+                        // and packed into the step's own S columns (already
+                        // read), the A operand of dQ = dS K
+                        tmem_st8(trow + kColS + col0, pd);
                     }
                 }
+                tmem_st_wait();
             }
             tc_fence_before();
             mbar_arrive(&bars[C::kSFree]);
             fence_proxy_async_smem();
             mbar_arrive(&bars[C::kDSFull]);
-            // P -> shared once dQ = dS K and dK += dS^T Q have read dS
+            // P -> shared once dK += dS^T Q has read dS
             if (!wg_wait(&bars[C::kDKDone], i & 1, ab, 45)) return;
             if (warp_rows) {
 #pragma unroll
@@ -417,6 +426,7 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             mbar_arrive(&bars[C::kPFull]);
             // dQ tile, d columns [64 wg, 64 wg + 64): TMEM -> this warpgroup's
             // half of the tile's Q buffer (its MMAs are done) -> global
+            if (!wg_wait(&bars[C::kDQDone], i & 1, ab, 48)) return;
             tc_fence_after();
             float* dq = prm.dQ + (int64_t)(dq_row0 + m * kBM) * rs + h * D;
             uint8_t* dq_stage = smem + C::kOffQ + (i & 1) * C::kTileBytes + wg * kHalfBytes;
@@ -474,7 +484,8 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             1, 256, 256,          // sd full, s free, dq free
             256, 1, 256, 1,       // p full, pv done, ds full, dk done
             1, 256, 128, 128,     // acc full, acc free, stage x2
-            256, 1                // ps free, mma done
+            256, 1,               // ps free, mma done
+            1                     // dq done
         };
         for (int b = 0; b < C::kNumBars; ++b) mbar_init(&bars[b], counts[b]);
         *abort_flag = 0;
