@@ -41,7 +41,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
     "gdpa_fwd": ("6058eb4427101988", 0.9644),
-    "gdpa_bwd": ("a24f15ff534237b6", 1.0206),
+    "gdpa_bwd": ("1a629a4e0115a790", 1.0207),
 }
 KERNEL_SOURCES = {
     "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh"),
