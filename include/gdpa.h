@@ -149,6 +149,11 @@ typedef struct gdpa_plan_s* gdpa_plan;   /* opaque, owned by the library */
  * Errors: INVALID_ARG for NULL pointers, negative sizes, offsets that do not
  * start at 0 or decrease, window < 1 with the window mask; UNSUPPORTED for
  * d > 128 or d % 4 != 0; ALLOC / CUDA for allocation or copy failures.
+ *
+ * Concurrency: calls on one plan may be enqueued on different streams only
+ * if their GPU work does not overlap when they use a plan-owned workspace
+ * (the forward of a key-split plan, the softmax variant's backward) or the
+ * plan's device error word; use one plan per concurrent stream otherwise.
  */
 gdpa_status gdpa_plan_create(const int32_t* q_off_host, const int32_t* kv_off_host, int B,
                              int H, int d, gdpa_mask mask, int window, gdpa_sched sched,
