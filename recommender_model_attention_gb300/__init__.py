@@ -18,6 +18,7 @@ from .gdpa import (  # noqa: F401
     MASK,
     Plan,
     STATUS,
+    allreduce_seed_grad,
     act_eval,
     gdpa_bwd,
     gdpa_fwd,

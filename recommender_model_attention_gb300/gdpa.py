@@ -281,6 +281,17 @@ def gdpa_bwd(plan: Plan, q, k, v, do, dq=None, dk=None, dv=None, alpha=None,
     return dq, dk, dv
 
 
+def allreduce_seed_grad(dq, group=None):
+    """Shared-query mode over several ranks, each with its own samples: each
+    rank's ``dq`` ([n_seeds, H, d] float32 from gdpa_bwd) holds its samples'
+    share of the seeds' gradient, and the sum over ranks, one all-reduce of
+    that small tensor, is the gradient of the whole batch (the only exchange
+    the sharded path has).  In place; returns ``dq``."""
+    import torch.distributed as dist
+    dist.all_reduce(dq, op=dist.ReduceOp.SUM, group=group)
+    return dq
+
+
 def gdpa_fwd_noalloc(q_off, kv_off, q, k, v, o, alpha=None, act: str = "gelu_erf",
                      mask: str = "none", window: int = 0, stream=None):
     """Forward into a caller-provided ``o`` with no allocation by the library.

@@ -3,7 +3,10 @@
 Each rank draws its own batch of the same shape (seeded by rank), plans it on
 the host with the C++ planner (no GPU), and the job's time is the maximum
 over ranks while its work is the sum: the only cross-rank steps of the path,
-which otherwise has no data exchange.
+which otherwise has no data exchange.  The one exchange of the sharded
+path, the shared seeds' gradient of pooling attention, is checked too: each
+rank's share (from the oracle) summed by the library's all-reduce equals the
+gradient of the whole batch.
 """
 
 import json
@@ -64,3 +67,59 @@ def test_two_ranks_gloo(tmp_path):
     for k in range(2):
         assert r[k]["ms"] == 15.0
         assert r[k]["flops"] == pytest.approx(2 * 12.0 * 128 * 8 * r[0]["pairs"])
+
+
+def _seed_worker(rank, world, port, outdir):
+    # shared-query pooling sharded by sample: every rank holds the same seeds
+    # and its own samples; the oracle gives each rank's share of the seeds'
+    # gradient, summed over ranks by the library's one all-reduce
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    import torch
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    import recommender_model_attention_gb300 as gd
+    from oracle import ref
+    seeds, ks, vs, dos, qos, kos = _seed_batches(world)
+    qt = ref.shared_q_tokens(seeds, qos[rank])
+    dq, _, _ = ref.bwd(qos[rank], kos[rank], qt, ks[rank], vs[rank], dos[rank], 0.3, "gelu_erf")
+    g = torch.from_numpy(ref.shared_q_grad(dq, qos[rank], seeds.shape[0])).float()
+    gd.allreduce_seed_grad(g)
+    np.save(os.path.join(outdir, "seed%d.npy" % rank), g.numpy())
+    dist.destroy_process_group()
+
+
+def _seed_batches(world):
+    from workloads import offsets_from_lengths
+    g = np.random.default_rng(17)
+    seeds = g.standard_normal((4, 2, 8))
+    out = ([], [], [], [], [])
+    for r in range(world):
+        lq = np.array([4, 2, 3]) if r == 0 else np.array([1, 4])
+        lkv = np.array([5, 9, 1]) if r == 0 else np.array([7, 3])
+        qo, ko = offsets_from_lengths(lq), offsets_from_lengths(lkv)
+        for lst, t in zip(out, (g.standard_normal((ko[-1], 2, 8)), g.standard_normal((ko[-1], 2, 8)),
+                                g.standard_normal((qo[-1], 2, 8)), qo, ko)):
+            lst.append(t)
+    return (seeds,) + out
+
+
+def test_shared_seed_gradient_all_reduce_gloo(tmp_path):
+    torch = pytest.importorskip("torch")
+    import torch.multiprocessing as mp
+    from oracle import ref
+    from workloads import offsets_from_lengths
+    port = _free_port()
+    mp.spawn(_seed_worker, args=(2, port, str(tmp_path)), nprocs=2, join=True)
+    got = [np.load(tmp_path / ("seed%d.npy" % k)) for k in range(2)]
+    assert np.array_equal(got[0], got[1])
+    # the whole batch on one process
+    seeds, ks, vs, dos, qos, kos = _seed_batches(2)
+    lq = np.concatenate([np.diff(q) for q in qos])
+    lkv = np.concatenate([np.diff(k) for k in kos])
+    qo, ko = offsets_from_lengths(lq), offsets_from_lengths(lkv)
+    dq, _, _ = ref.bwd(qo, ko, ref.shared_q_tokens(seeds, qo), np.concatenate(ks),
+                       np.concatenate(vs), np.concatenate(dos), 0.3, "gelu_erf")
+    want = ref.shared_q_grad(dq, qo, seeds.shape[0])
+    assert np.allclose(got[0], want, rtol=1e-5, atol=1e-6)
