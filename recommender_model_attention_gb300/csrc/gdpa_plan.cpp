@@ -45,9 +45,20 @@ void deal(const std::vector<Item>& items, int S, int sched, std::vector<int64_t>
     order.resize(n);
     std::iota(order.begin(), order.end(), 0);
     if (sched == GDPA_SCHED_ZIGZAG) {
-        std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
-            return items[a].cost > items[b].cost;
-        });
+        // stable sort by cost, descending: a counting sort when the costs
+        // span a small range (they count blocks or tiles), else a merge sort
+        int64_t cmax = 0;
+        for (const Item& it : items) cmax = std::max(cmax, it.cost);
+        if (cmax < (int64_t)1 << 16) {
+            std::vector<int64_t> start(cmax + 2, 0);
+            for (const Item& it : items) start[cmax - it.cost + 1]++;
+            for (int64_t c = 0; c <= cmax; ++c) start[c + 1] += start[c];
+            for (int64_t i = 0; i < n; ++i) order[start[cmax - items[i].cost]++] = i;
+        } else {
+            std::stable_sort(order.begin(), order.end(), [&](int64_t a, int64_t b) {
+                return items[a].cost > items[b].cost;
+            });
+        }
     }
     sm.resize(n);
     for (int64_t r = 0; r < n; ++r) {
@@ -123,6 +134,18 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
     // forward tiles, enumerated b -> h -> m (-> chunk)
     std::vector<Item> ft;
     std::vector<FwdTile> ft_dev;
+    {
+        // an upper bound of the tile count (key chunks counted over the
+        // sample's whole key range), so that the vectors never reallocate
+        int64_t bound = 0;
+        for (int b = 0; b < B; ++b) {
+            const int64_t nkb = cdiv(kv_off[b + 1] - kv_off[b], kBN);
+            const int64_t chunks = p.max_kvb > 0 ? std::max<int64_t>(1, cdiv(nkb, p.max_kvb)) : 1;
+            bound += H * cdiv(q_off[b + 1] - q_off[b], kBM) * chunks;
+        }
+        ft.reserve(bound);
+        ft_dev.reserve(bound);
+    }
     p.max_fwd_kvb = 0;
     p.fwd_split = 0;
     for (int b = 0; b < B; ++b) {
@@ -159,6 +182,12 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
     // backward units, enumerated b -> h -> j
     std::vector<Item> bu;
     std::vector<BwdUnit> bu_dev;
+    {
+        int64_t units = 0;
+        for (int b = 0; b < B; ++b) units += H * cdiv(kv_off[b + 1] - kv_off[b], kBN);
+        bu.reserve(units);
+        bu_dev.reserve(units);
+    }
     p.zero_dq = 0;
     for (int b = 0; b < B; ++b) {
         const int64_t lq = q_off[b + 1] - q_off[b], lkv = kv_off[b + 1] - kv_off[b];
