@@ -110,7 +110,7 @@ def useful_pairs(q_off, kv_off, mask, window):
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
 
-    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -122,12 +122,24 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
 
-    def stop(self):
+    @staticmethod
+    def _epoch(stamp):
+        # nvidia-smi's local-time stamp, "YYYY/MM/DD HH:MM:SS.mmm"
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
+    def stop(self, region=None):
+        """Summary of the samples; with region = (t0, t1) (time.time() around
+        the timed region) only the samples taken inside it, when there are
+        any (else all, and "in_region" says so)."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -136,24 +148,26 @@ class Clocks:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
-        sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        rows = []
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 8:
+            if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[0]))
-                mx.append(float(f[1]))
+                rows.append((self._epoch(f[0]), float(f[1]), float(f[2]),
+                             {n for n, v in zip(names, f[5:9]) if v.lower() == "active"}))
             except ValueError:
                 continue
-            for n, v in zip(names, f[4:8]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        if not rows:
             return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        inside = [r for r in rows if region and r[0] is not None and
+                  region[0] - 0.03 <= r[0] <= region[1] + 0.03]
+        use = inside or rows
+        return {"sm_mhz": float(np.median([r[1] for r in use])),
+                "sm_max_mhz": float(max(r[2] for r in use)),
+                "reasons": sorted(set().union(*[r[3] for r in use])), "samples": len(use),
+                "in_region": bool(inside)}
 
 
 def cpu_baseline(w, x, budget_s=15.0):
@@ -370,6 +384,7 @@ def main():
     clocks.start()
     time.sleep(0.3)
     launches0 = plan.launches
+    t_region0 = time.time()
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -384,7 +399,8 @@ def main():
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    clk = clocks.stop()
+    t_region1 = time.time()
+    clk = clocks.stop((t_region0, t_region1))
     launches = plan.launches - launches0
     plan.check()
     elapsed_ms, job_flops = reduce_across_ranks(start.elapsed_time(end),
