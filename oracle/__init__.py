@@ -10,6 +10,8 @@ does, and this package imports nothing from the library.
 * ``brute``   dense padded NumPy float64 formulation of the same maths.
 * ``planner`` the host tile plan (valid tiles, costs, zigzag / round-robin
               dealing) restated in plain Python.
+* ``mx``      MXFP8 quantisation (E4M3 elements, E8M0 scales per 32 values)
+              in float64, for the block-scaled variant.
 
 The method follows the GDPA page ("범용 내적 어텐션(GDPA): 실제 추천 시스템
 학습 부하를 위한 커널 최적화", aitrends.kr): its summary and first detailed
