@@ -9,8 +9,9 @@ dK and dV separately.  Plans must match the oracle's planner bit for bit.
 import numpy as np
 import pytest
 
-from gpu_util import TOL, compare_full, compare_sampled, pick_samples, small_case, to_dev
+from gpu_util import TOL, compare_full, compare_sampled, max_rel, pick_samples, small_case, to_dev
 from oracle import planner as ref_planner
+from oracle import ref
 from workloads import CONFIGS, get_config, make_inputs
 
 pytestmark = pytest.mark.gpu
@@ -158,4 +159,27 @@ def test_launch_counter_and_timing(gd):
     torch.cuda.synchronize()
     se, sm = plan.sm_times("fwd")
     assert np.all(se[:, 1] >= se[:, 0])
+    plan.destroy()
+
+
+def test_pma_workload_as_benchmarked_sampled(gd):
+    # the pooling workload in the launch configuration the benchmark times:
+    # the seed rows passed once (shared-query mode) and the planner's key
+    # split; sampled outputs against the oracle on the materialised queries
+    import torch
+    w = get_config("pma_pooling")
+    x = make_inputs(w, device="cuda")
+    plan = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window,
+                   max_kv_blocks="auto")
+    plan.set_shared_q(w.shared_q)
+    o = gd.gdpa_fwd(plan, x["q_seeds"], x["k"], x["v"], alpha=w.alpha, act=w.act)
+    plan.check()
+    torch.cuda.synchronize()
+    samples = pick_samples(x["q_off"], x["kv_off"], seed=3)
+    sq, skv, qi, kvi = ref.sub_batch(x["q_off"], x["kv_off"], samples)
+    qi_t = torch.from_numpy(qi).to(o.device)
+    kvi_t = torch.from_numpy(kvi).to(o.device)
+    want = ref.fwd(sq, skv, x["q"].index_select(0, qi_t), x["k"].index_select(0, kvi_t),
+                   x["v"].index_select(0, kvi_t), w.alpha, w.act, w.mask, w.window)
+    _assert({"o": max_rel(ref.to_f64(o.index_select(0, qi_t)), want)}, TOL["bf16"])
     plan.destroy()
