@@ -12,6 +12,8 @@ does, and this package imports nothing from the library.
               dealing) restated in plain Python.
 * ``mx``      MXFP8 quantisation (E4M3 elements, E8M0 scales per 32 values)
               in float64, for the block-scaled variant.
+* ``rmsnorm`` the RMSNorm prologue on Q and K and its gradient, composed
+              with the GDPA loops.
 
 The method follows the GDPA page ("범용 내적 어텐션(GDPA): 실제 추천 시스템
 학습 부하를 위한 커널 최적화", aitrends.kr): its summary and first detailed
