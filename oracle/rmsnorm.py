@@ -7,8 +7,8 @@ for recommendation models) counts the normalisation layers among the
 memory-bound operations; the GDPA page (the caption of its chart comparing
 tanh GELU with the 6th-order Taylor form) has RMSNorm keep the activation's
 inputs in the polynomial's accurate range.  A fused prologue applies the
-norm to Q and K inside the attention instead of in a separate pass.  Per (token, head) row of d values, with a scalar gain g
-and eps:
+norm to Q and K inside the attention instead of in a separate pass.  Per
+(token, head) row of d values, with a scalar gain g and eps:
 
     r = sqrt(mean(x^2) + eps),   y = g x / r,
 
