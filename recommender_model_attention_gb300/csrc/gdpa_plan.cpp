@@ -61,17 +61,23 @@ void deal(const std::vector<Item>& items, int S, int sched, std::vector<int64_t>
         }
     }
     sm.resize(n);
+    int32_t col = 0;
+    bool odd = false;   // odd dealing round: the snake runs back
     for (int64_t r = 0; r < n; ++r) {
-        int32_t pos = (int32_t)(r % S);
-        if (sched == GDPA_SCHED_ZIGZAG && ((r / S) & 1)) pos = S - 1 - pos;
-        sm[r] = pos;
+        sm[r] = (sched == GDPA_SCHED_ZIGZAG && odd) ? S - 1 - col : col;
+        if (++col == S) {
+            col = 0;
+            odd = !odd;
+        }
     }
 }
 
-// Group dealt items by SM (stable within an SM) and emit export rows.
-template <int W>
+// Group dealt items by SM (stable within an SM), emit export rows and call
+// record(q, item) for the item at queue position q.
+template <int W, typename Record>
 void emit(const std::vector<Item>& items, int S, int sched, std::vector<int32_t>& rows,
-          std::vector<int32_t>& seg, std::vector<int64_t>& queue_order) {
+          std::vector<int32_t>& seg, Record record) {
+    std::vector<int64_t> queue_order;
     std::vector<int64_t> order;
     std::vector<int32_t> sm;
     deal(items, S, sched, order, sm);
@@ -83,11 +89,14 @@ void emit(const std::vector<Item>& items, int S, int sched, std::vector<int32_t>
     std::vector<int64_t> fill(count.begin(), count.end() - 1);
     for (int64_t r = 0; r < (int64_t)order.size(); ++r) queue_order[fill[sm[r]]++] = order[r];
     rows.assign(order.size() * W, 0);
+    const int64_t n = (int64_t)queue_order.size();
     for (int s = 0; s < S; ++s) {
         for (int64_t q = count[s]; q < count[s + 1]; ++q) {
+            if (q + 8 < n) __builtin_prefetch(&items[queue_order[q + 8]]);
             const Item& it = items[queue_order[q]];
             for (int c = 0; c < W - 1; ++c) rows[q * W + c] = it.f[c];
             rows[q * W + W - 1] = s;
+            record(q, it);
         }
     }
 }
@@ -133,7 +142,6 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
 
     // forward tiles, enumerated b -> h -> m (-> chunk)
     std::vector<Item> ft;
-    std::vector<FwdTile> ft_dev;
     {
         // an upper bound of the tile count (key chunks counted over the
         // sample's whole key range), so that the vectors never reallocate
@@ -144,33 +152,20 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
             bound += H * cdiv(q_off[b + 1] - q_off[b], kBM) * chunks;
         }
         ft.reserve(bound);
-        ft_dev.reserve(bound);
     }
     p.max_fwd_kvb = 0;
     p.fwd_split = 0;
     for (int b = 0; b < B; ++b) {
-        const int64_t lq = q_off[b + 1] - q_off[b], lkv = kv_off[b + 1] - kv_off[b];
+        const int64_t lq = q_off[b + 1] - q_off[b];
         for (int h = 0; h < H; ++h) {
             for (int64_t m = 0; m < cdiv(lq, kBM); ++m) {
-                const int64_t r0 = m * kBM, r1 = std::min<int64_t>(r0 + kBM, lq);
                 int64_t k0, k1;
                 kv_hull(b, m, k0, k1);
                 const int64_t step = (p.max_kvb > 0 && k1 > k0) ? p.max_kvb : std::max<int64_t>(1, k1 - k0);
                 int64_t s = k0;
                 do {
                     const int64_t e = std::min(k1, s + step);
-                    Item it{{b, h, (int32_t)m, (int32_t)s, (int32_t)e, 0}, e - s};
-                    ft.push_back(it);
-                    FwdTile t;
-                    t.qt0 = (int32_t)(q_off[b] + r0);
-                    t.nq = (int32_t)(r1 - r0);
-                    t.kvt0 = kv_off[b];
-                    t.lkv = (int32_t)lkv;
-                    t.h = h;
-                    t.kb0 = (int32_t)s;
-                    t.kb1 = (int32_t)e;
-                    t.i0 = (int32_t)r0;
-                    ft_dev.push_back(t);
+                    ft.push_back(Item{{b, h, (int32_t)m, (int32_t)s, (int32_t)e, 0}, e - s});
                     p.max_fwd_kvb = std::max<int64_t>(p.max_fwd_kvb, e - s);
                     if (e - s < k1 - k0) p.fwd_split = 1;
                     s = e;
@@ -181,12 +176,10 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
 
     // backward units, enumerated b -> h -> j
     std::vector<Item> bu;
-    std::vector<BwdUnit> bu_dev;
     {
         int64_t units = 0;
         for (int b = 0; b < B; ++b) units += H * cdiv(kv_off[b + 1] - kv_off[b], kBN);
         bu.reserve(units);
-        bu_dev.reserve(units);
     }
     p.zero_dq = 0;
     for (int b = 0; b < B; ++b) {
@@ -216,40 +209,46 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
         if (atomic || hole) p.zero_dq = 1;
         const int32_t flags = atomic ? kUnitAtomicDQ : 0;
         for (int h = 0; h < H; ++h) {
-            for (int64_t j = 0; j < nkb; ++j) {
-                const int64_t c0 = j * kBN, c1 = std::min<int64_t>(c0 + kBN, lkv);
-                Item it{{b, h, (int32_t)j, (int32_t)m0s[j], (int32_t)m1s[j], flags}, m1s[j] - m0s[j]};
-                bu.push_back(it);
-                BwdUnit u;
-                u.kvt0 = (int32_t)(kv_off[b] + c0);
-                u.nkv = (int32_t)(c1 - c0);
-                u.qt0 = q_off[b];
-                u.lq = (int32_t)lq;
-                u.hf = h | (flags << 16);
-                u.m0 = (int32_t)m0s[j];
-                u.m1 = (int32_t)m1s[j];
-                u.c0 = (int32_t)c0;
-                bu_dev.push_back(u);
-            }
+            for (int64_t j = 0; j < nkb; ++j)
+                bu.push_back(Item{{b, h, (int32_t)j, (int32_t)m0s[j], (int32_t)m1s[j], flags},
+                                  m1s[j] - m0s[j]});
         }
     }
 
-    std::vector<int64_t> qorder;
-    emit<6>(ft, S, p.sched, p.fwd_export, p.fwd_seg, qorder);
+    // kernel-layout records in queue order (uploaded by the ABI layer),
+    // written as the items are grouped by SM
+    std::vector<FwdTile> fdev(ft.size());
+    emit<6>(ft, S, p.sched, p.fwd_export, p.fwd_seg, [&](int64_t q, const Item& it) {
+        const int b = it.f[0];
+        const int64_t lq = q_off[b + 1] - q_off[b], r0 = (int64_t)it.f[2] * kBM;
+        FwdTile& t = fdev[q];
+        t.qt0 = (int32_t)(q_off[b] + r0);
+        t.nq = (int32_t)(std::min<int64_t>(r0 + kBM, lq) - r0);
+        t.kvt0 = kv_off[b];
+        t.lkv = kv_off[b + 1] - kv_off[b];
+        t.h = it.f[1];
+        t.kb0 = it.f[3];
+        t.kb1 = it.f[4];
+        t.i0 = (int32_t)r0;
+    });
     p.n_fwd = (int64_t)ft.size();
-    {
-        std::vector<FwdTile> sorted(ft_dev.size());
-        for (size_t i = 0; i < qorder.size(); ++i) sorted[i] = ft_dev[qorder[i]];
-        ft_dev.swap(sorted);
-    }
-    emit<7>(bu, S, p.sched, p.bwd_export, p.bwd_seg, qorder);
+    std::vector<BwdUnit> bdev(bu.size());
+    emit<7>(bu, S, p.sched, p.bwd_export, p.bwd_seg, [&](int64_t q, const Item& it) {
+        const int b = it.f[0];
+        const int64_t lkv = kv_off[b + 1] - kv_off[b], c0 = (int64_t)it.f[2] * kBN;
+        BwdUnit& u = bdev[q];
+        u.kvt0 = (int32_t)(kv_off[b] + c0);
+        u.nkv = (int32_t)(std::min<int64_t>(c0 + kBN, lkv) - c0);
+        u.qt0 = q_off[b];
+        u.lq = q_off[b + 1] - q_off[b];
+        u.hf = it.f[1] | (it.f[5] << 16);
+        u.m0 = it.f[3];
+        u.m1 = it.f[4];
+        u.c0 = (int32_t)c0;
+    });
     p.n_bwd = (int64_t)bu.size();
-    std::vector<BwdUnit> bsorted(bu_dev.size());
-    for (size_t i = 0; i < qorder.size(); ++i) bsorted[i] = bu_dev[qorder[i]];
-
-    // kernel-layout records in queue order, uploaded by the ABI layer
-    p.fwd_dev_host.swap(ft_dev);
-    p.bwd_dev_host.swap(bsorted);
+    p.fwd_dev_host.swap(fdev);
+    p.bwd_dev_host.swap(bdev);
     return GDPA_OK;
 }
 
