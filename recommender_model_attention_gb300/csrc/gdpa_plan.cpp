@@ -73,7 +73,7 @@ void deal(const std::vector<Item>& items, int S, int sched, std::vector<int64_t>
 }
 
 // Group dealt items by SM (stable within an SM), emit export rows and call
-// record(q, item) for the item at queue position q.
+// record(q, item) for the items at queue positions q = 0, 1, 2, ... in turn.
 template <int W, typename Record>
 void emit(const std::vector<Item>& items, int S, int sched, std::vector<int32_t>& rows,
           std::vector<int32_t>& seg, Record record) {
@@ -88,14 +88,16 @@ void emit(const std::vector<Item>& items, int S, int sched, std::vector<int32_t>
     queue_order.assign(order.size(), 0);
     std::vector<int64_t> fill(count.begin(), count.end() - 1);
     for (int64_t r = 0; r < (int64_t)order.size(); ++r) queue_order[fill[sm[r]]++] = order[r];
-    rows.assign(order.size() * W, 0);
+    // queue positions run 0, 1, 2, ... in this loop: append, no zero fill
     const int64_t n = (int64_t)queue_order.size();
+    rows.clear();
+    rows.reserve(n * W);
     for (int s = 0; s < S; ++s) {
         for (int64_t q = count[s]; q < count[s + 1]; ++q) {
             if (q + 8 < n) __builtin_prefetch(&items[queue_order[q + 8]]);
             const Item& it = items[queue_order[q]];
-            for (int c = 0; c < W - 1; ++c) rows[q * W + c] = it.f[c];
-            rows[q * W + W - 1] = s;
+            for (int c = 0; c < W - 1; ++c) rows.push_back(it.f[c]);
+            rows.push_back(s);
             record(q, it);
         }
     }
@@ -217,11 +219,12 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
 
     // kernel-layout records in queue order (uploaded by the ABI layer),
     // written as the items are grouped by SM
-    std::vector<FwdTile> fdev(ft.size());
-    emit<6>(ft, S, p.sched, p.fwd_export, p.fwd_seg, [&](int64_t q, const Item& it) {
+    std::vector<FwdTile> fdev;
+    fdev.reserve(ft.size());
+    emit<6>(ft, S, p.sched, p.fwd_export, p.fwd_seg, [&](int64_t, const Item& it) {
         const int b = it.f[0];
         const int64_t lq = q_off[b + 1] - q_off[b], r0 = (int64_t)it.f[2] * kBM;
-        FwdTile& t = fdev[q];
+        FwdTile& t = fdev.emplace_back();
         t.qt0 = (int32_t)(q_off[b] + r0);
         t.nq = (int32_t)(std::min<int64_t>(r0 + kBM, lq) - r0);
         t.kvt0 = kv_off[b];
@@ -232,11 +235,12 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
         t.i0 = (int32_t)r0;
     });
     p.n_fwd = (int64_t)ft.size();
-    std::vector<BwdUnit> bdev(bu.size());
-    emit<7>(bu, S, p.sched, p.bwd_export, p.bwd_seg, [&](int64_t q, const Item& it) {
+    std::vector<BwdUnit> bdev;
+    bdev.reserve(bu.size());
+    emit<7>(bu, S, p.sched, p.bwd_export, p.bwd_seg, [&](int64_t, const Item& it) {
         const int b = it.f[0];
         const int64_t lkv = kv_off[b + 1] - kv_off[b], c0 = (int64_t)it.f[2] * kBN;
-        BwdUnit& u = bdev[q];
+        BwdUnit& u = bdev.emplace_back();
         u.kvt0 = (int32_t)(kv_off[b] + c0);
         u.nkv = (int32_t)(std::min<int64_t>(c0 + kBN, lkv) - c0);
         u.qt0 = q_off[b];
