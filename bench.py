@@ -240,7 +240,8 @@ def run_reference(args, w):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded, same shapes as the GPU arm)",
-            "config": {"workload": w.name, "B": w.B, "H": w.H, "d": w.d},
+            "config": {"workload": w.name, "B": w.B, "H": w.H, "d": w.d, "act": w.act,
+                       "mask": w.mask, "window": w.window},
             "cpu_baseline": base,
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
