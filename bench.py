@@ -107,6 +107,84 @@ def useful_pairs(q_off, kv_off, mask, window):
     return n
 
 
+DEFAULT_WORKLOAD = "training_cross_fwd_bwd"
+OTHER_WORKLOADS = ("jagged_selfattn_window256", "user_ad_cross", "pma_pooling")
+
+
+def busy_spread(start_end):
+    """Max/min and (max - min)/mean of the per-CTA busy times."""
+    busy = (start_end[:, 1] - start_end[:, 0]).astype(np.float64)
+    return {"max_over_min": float(busy.max() / max(busy.min(), 1.0)),
+            "max_minus_min_over_mean": float((busy.max() - busy.min()) / busy.mean())}
+
+
+def forward_workload(name, gd, pk, pk_kind, reps=20, warmup=3):
+    """One forward-only workload at its full size, timed launch by launch
+    with CUDA events on the launching stream, L2 flushed (a 256 MB write)
+    before each timed launch; planner's key split, shared seeds for pooling.
+    Returns its line: ms, useful TFLOP/s, % of bf16 peak, GB/s, HBM fraction,
+    the attainable roofline and the SM spread of both dealing policies."""
+    import torch
+    from workloads import get_config, make_inputs
+    w = get_config(name)
+    x = make_inputs(w, device="cuda", seed=rank_seed(w, 0))
+    n_seeds = w.shared_q
+    q_in = x["q_seeds"] if n_seeds else x["q"]
+
+    def plan_for(sched):
+        p = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window,
+                    sched=sched, max_kv_blocks="auto")
+        if n_seeds:
+            p.set_shared_q(n_seeds)
+        return p
+
+    plan = plan_for("zigzag")
+    o = torch.empty_like(x["q"])
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for _ in range(warmup):
+        gd.gdpa_fwd(plan, q_in, x["k"], x["v"], o=o, alpha=w.alpha, act=w.act)
+    plan.check()
+    evs = []
+    for _ in range(reps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        gd.gdpa_fwd(plan, q_in, x["k"], x["v"], o=o, alpha=w.alpha, act=w.act)
+        b.record(stream)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    plan.check()
+    times = [a.elapsed_time(b) for a, b in evs]
+    ms = float(np.median(times))
+    Tq, Tkv = int(x["q_off"][-1]), int(x["kv_off"][-1])
+    pairs = useful_pairs(x["q_off"], x["kv_off"], w.mask, w.window)
+    flops = 4.0 * w.d * w.H * pairs
+    row = w.H * w.d
+    nbytes = (int(q_in.shape[0]) + Tq + 2 * Tkv) * row * 2
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    attainable = min(pk["bf16_tflops"], flops / nbytes * pk["hbm_gbs"] / 1e3)
+    spread = {}
+    for pol in ("zigzag", "round_robin"):
+        pp = plan_for(pol)
+        pp.set_timing(True)
+        gd.gdpa_fwd(pp, q_in, x["k"], x["v"], o=o, alpha=w.alpha, act=w.act)
+        pp.check()
+        spread[pol] = busy_spread(pp.sm_times("fwd")[0])
+        pp.destroy()
+    n_tiles = plan.sizes()[0]
+    plan.destroy()
+    return {"ms": ms, "ms_min": float(min(times)), "tflops": tflops,
+            "pct_of_bf16_peak": 100.0 * tflops / pk["bf16_tflops"], "gbs": gbs,
+            "hbm_frac": gbs / pk["hbm_gbs"], "peak_kind": pk_kind,
+            "attainable_tflops": attainable, "pct_of_attainable": 100.0 * tflops / attainable,
+            "algorithmic_bytes": nbytes, "useful_pairs": pairs, "fwd_tiles": int(n_tiles),
+            "B": w.B, "H": w.H, "act": w.act, "mask": w.mask, "window": w.window,
+            "shared_q": n_seeds, "timing": "median of %d launches, L2 flushed before each" % reps,
+            "sm_spread": spread}
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
 
@@ -254,11 +332,13 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="training_cross_fwd_bwd")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--samples", type=int, default=0,
                     help="use only the first N sequences of the workload (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the forward-only lines of the other jagged workloads")
     ap.add_argument("--max-kv-blocks", default="auto",
                     help="key-split plans: at most this many 128-row key blocks per forward "
                          "tile (0 = whole key range per tile; 'auto' = the planner's choice, "
@@ -529,21 +609,36 @@ def main():
                "pipelining": "inputs up, compute, results down on three streams, "
                              "two buffer sets"}
 
-    # SM busy-time spread of each policy (separate, untimed launches)
-    spread = {}
+    # SM busy-time spread of each policy, forward and backward (separate,
+    # untimed launches)
+    spread, spread_bwd = {}, {}
     try:
         for pol in ("zigzag", "round_robin"):
             pp = make_plan(sched=pol)
             pp.set_timing(True)
             fwd_call(pp, q_in, x["k"], x["v"], o)
+            if backward:
+                bwd_call(pp, q_in, x["k"], x["v"], o, x["do"], dq, dk, dv)
             pp.check()
-            se, _ = pp.sm_times("fwd")
-            busy = (se[:, 1] - se[:, 0]).astype(np.float64)
-            spread[pol] = {"max_over_min": float(busy.max() / max(busy.min(), 1.0)),
-                           "max_minus_min_over_mean": float((busy.max() - busy.min()) / busy.mean())}
+            spread[pol] = busy_spread(pp.sm_times("fwd")[0])
+            if backward:
+                spread_bwd[pol] = busy_spread(pp.sm_times("bwd")[0])
             pp.destroy()
     except Exception as e:  # timing is a report, not the measurement
         spread["error"] = str(e)
+
+    # the other jagged workloads, forward only, in the same run
+    others = None
+    if rank == 0 and world == 1 and not args.no_workloads and args.workload == DEFAULT_WORKLOAD \
+            and not args.samples and not args.act:
+        others = {}
+        for name in OTHER_WORKLOADS:
+            try:
+                others[name] = forward_workload(name, gd, pk, pk_kind)
+            except Exception as e:  # a report beside the headline
+                others[name] = {"error": str(e)}
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -572,6 +667,8 @@ def main():
             "clocks": clk,
             "e2e": e2e,
             "sm_spread_fwd": spread,
+            "sm_spread_bwd": spread_bwd if backward else None,
+            "workloads": others,
             "plan": {"host_ms_median": float(np.median(plan_times)), "fwd_tiles": int(n_fwd_tiles),
                      "bwd_units": int(n_bwd_units)},
             "cpu_baseline": cpu,

@@ -32,6 +32,11 @@
  *     failures (an expired wait in a kernel) are reported by gdpa_check.
  *   - The caller owns all tensors and streams; a plan owns its host and
  *     device buffers and is freed by gdpa_plan_destroy.
+ *   - A plan belongs to the device that was current when it was created;
+ *     every call that launches work on it or reads its device state
+ *     (gdpa_fwd, gdpa_bwd, gdpa_softmax_fwd, gdpa_softmax_bwd, gdpa_check,
+ *     gdpa_sm_times) must be made with that device current and returns
+ *     INVALID_ARG, before touching the device, otherwise.
  */
 #ifndef GDPA_H
 #define GDPA_H
@@ -150,6 +155,10 @@ typedef struct gdpa_plan_s* gdpa_plan;   /* opaque, owned by the library */
  * start at 0 or decrease, window < 1 with the window mask; UNSUPPORTED for
  * d > 128 or d % 4 != 0; ALLOC / CUDA for allocation or copy failures.
  *
+ * The plan's device buffers come from the stream-ordered allocator and its
+ * upload is enqueued on `stream`; the call does not wait for it.  Launches on
+ * the plan, on any stream, are ordered after the upload by an event.
+ *
  * Concurrency: calls on one plan may be enqueued on different streams only
  * if their GPU work does not overlap when they use a plan-owned workspace
  * (the forward of a key-split plan, the softmax variant's backward) or the
@@ -240,26 +249,51 @@ gdpa_status gdpa_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void
                      float alpha, gdpa_act act, void* stream);
 
 /*
- * Synchronise `stream` and report device-side failures of this plan's
- * launches since the last check: TIMEOUT if a kernel abandoned a barrier
- * wait (its outputs are then incomplete), DEVICE for other flagged errors,
- * CUDA for an asynchronous CUDA error.  Clears the flags.
+ * Wait for this plan's launches (on every stream they were enqueued on) and
+ * for `stream`, and report device-side failures of the plan's launches since
+ * the last check: TIMEOUT if a kernel abandoned a barrier wait (its outputs
+ * are then incomplete; the kernel has returned and the device stays usable),
+ * DEVICE for other flagged errors, CUDA for an asynchronous CUDA error.
+ * Clears the flags.
  */
 gdpa_status gdpa_check(gdpa_plan plan, void* stream);
 
 /*
- * Per-CTA timing of the last timed launch (which = 0 forward, 1 backward):
- * start_end: uint64 [S][2] globaltimer ns; smid: int32 [S].  Synchronous.
- * INVALID_ARG if timing was not enabled or nothing was recorded.
+ * Per-CTA timing of the last timed tensor-core launch (which = 0 forward,
+ * 1 backward): start_end: uint64 [S][2] globaltimer ns; smid: int32 [S].
+ * Waits for this plan's launches only (not the whole device) and reads on the
+ * stream of the timed launch, which must still exist.  INVALID_ARG if timing
+ * was not enabled or nothing was recorded.
  */
 gdpa_status gdpa_sm_times(gdpa_plan plan, int which, uint64_t* start_end, int32_t* smid);
 
 /* Number of kernel launches this plan has issued since creation. */
 int64_t gdpa_plan_launches(gdpa_plan plan);
 
-/* Frees the plan (NULL is a no-op).  Synchronous: first waits for the work
- * queued on the plan's device, which may still read the plan's buffers. */
+/* Frees the plan (NULL is a no-op).  Does not wait on the host: the plan's
+ * device buffers are returned to the stream-ordered allocator on a private
+ * stream that first waits (on the device) for every launch made on the plan,
+ * so work still queued may keep reading them until it has run.  Other work
+ * on the device is not waited for. */
 void gdpa_plan_destroy(gdpa_plan plan);
+
+/*
+ * Failure-path test hook (the pages have no counterpart; it exists so that
+ * tests can exercise the kernels' bounded waits without a GPU fault).
+ *
+ *   limit_us   > 0: the tensor-core kernels' barrier waits on this plan give
+ *              up after limit_us microseconds instead of 2 s; 0 restores the
+ *              default.
+ *   stall      != 0: on the next tensor-core launches, CTA 0's loader skips
+ *              its first query-tile load, so a wait for it expires: the
+ *              kernel records a timeout, every role unwinds (waits, bounded,
+ *              for its own copies and MMAs in flight, frees TMEM) and returns.
+ *              gdpa_check then reports GDPA_ERR_TIMEOUT and the outputs of
+ *              that launch are incomplete.  0 restores normal launches.
+ *
+ * INVALID_ARG for a NULL plan or limit_us < 0.  Host-side only.
+ */
+gdpa_status gdpa_plan_set_wait_test(gdpa_plan plan, int limit_us, int stall);
 
 /*
  * Forward pass that allocates nothing (the GDPA page has no counterpart of
@@ -269,7 +303,7 @@ void gdpa_plan_destroy(gdpa_plan plan);
  * allocator or memory pool (which would recurse into itself), plugins that
  * are handed one fixed device arena, and processes that must reserve all of
  * their device memory up front.  They cannot create a gdpa_plan, whose tile
- * queue and error word are cudaMalloc'd.  This call computes the same
+ * queue and error word are allocated on the device.  This call computes the same
  * O = act(alpha Q K^T) V as gdpa_fwd with a zigzag plan over the current
  * device's SMs, on the tensor-core kernel (bf16, d = 64 or 128), without
  * allocating: the plan is built in static host buffers and its tile queue

@@ -13,34 +13,96 @@ namespace {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// Plan buffers come from the stream-ordered allocator on the creation
+// stream and go back to it on a stream that has waited for the plan's work,
+// so neither creating nor destroying a plan synchronises the device.
 template <typename T>
 gdpa_status upload(T** dst, const void* src, size_t bytes, cudaStream_t st) {
     if (bytes == 0) return GDPA_OK;
-    if (cudaMalloc((void**)dst, bytes) != cudaSuccess) return GDPA_ERR_ALLOC;
+    if (cudaMallocAsync((void**)dst, bytes, st) != cudaSuccess) {
+        *dst = nullptr;
+        return GDPA_ERR_ALLOC;
+    }
     if (cudaMemcpyAsync(*dst, src, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
         return GDPA_ERR_CUDA;
+    return GDPA_OK;
+}
+
+template <typename T>
+gdpa_status alloc_dev(T** dst, size_t bytes, cudaStream_t st) {
+    if (cudaMallocAsync((void**)dst, bytes, st) != cudaSuccess) {
+        *dst = nullptr;
+        return GDPA_ERR_ALLOC;
+    }
+    return GDPA_OK;
+}
+
+// Host wait for every launch this plan has enqueued (its own events only).
+gdpa_status wait_plan_work(const Plan& p) {
+    for (const gdpa::StreamEvent& w : p.work)
+        if (cudaEventSynchronize(w.event) != cudaSuccess) return GDPA_ERR_CUDA;
     return GDPA_OK;
 }
 
 void free_plan(Plan* p) {
     if (!p) return;
     if (!p->host_only) {
-        // work still queued on the device may read the plan's buffers
         int cur = -1;
         if (cudaGetDevice(&cur) == cudaSuccess && cur != p->device) cudaSetDevice(p->device);
-        cudaDeviceSynchronize();
-        cudaFree(p->d_fwd);
-        cudaFree(p->d_fwd_seg);
-        cudaFree(p->d_bwd);
-        cudaFree(p->d_bwd_seg);
-        cudaFree(p->d_err);
-        cudaFree(p->d_times);
-        cudaFree(p->d_smid);
-        cudaFree(p->d_delta);
-        cudaFree(p->d_wsplit);
+        // A private stream waits (on the device) for every stream the plan
+        // has launched on and for the upload, then returns the buffers; the
+        // host does not wait.  If the stream cannot be made, fall back to a
+        // host wait on the plan's own events.
+        cudaStream_t fs = nullptr;
+        if (cudaStreamCreateWithFlags(&fs, cudaStreamNonBlocking) != cudaSuccess) {
+            fs = nullptr;
+            wait_plan_work(*p);
+            if (p->ready) cudaEventSynchronize(p->ready);
+        } else {
+            if (p->ready) cudaStreamWaitEvent(fs, p->ready, 0);
+            for (const gdpa::StreamEvent& w : p->work) cudaStreamWaitEvent(fs, w.event, 0);
+        }
+        void* bufs[] = {p->d_fwd, p->d_fwd_seg, p->d_bwd, p->d_bwd_seg, p->d_err,
+                        p->d_times, p->d_smid, p->d_delta, p->d_wsplit};
+        for (void* b : bufs)
+            if (b) cudaFreeAsync(b, fs);
+        for (const gdpa::StreamEvent& w : p->work) cudaEventDestroy(w.event);
+        if (p->ready) cudaEventDestroy(p->ready);
+        if (fs) cudaStreamDestroy(fs);   // released once its work has run
         if (cur >= 0 && cur != p->device) cudaSetDevice(cur);
     }
     delete p;
+}
+
+// Calls that touch a plan's device buffers must run with the plan's device
+// current (the buffers live there).
+gdpa_status check_device(const Plan& p) {
+    int cur = -1;
+    if (cudaGetDevice(&cur) != cudaSuccess) return GDPA_ERR_CUDA;
+    return cur == p.device ? GDPA_OK : GDPA_ERR_INVALID_ARG;
+}
+
+// Order a launch on `st` after the plan's upload, and remember `st` so that
+// the plan's destruction and timing reads wait for this work.
+gdpa_status begin_work(Plan& p, cudaStream_t st) {
+    if (p.ready && cudaStreamWaitEvent(st, p.ready, 0) != cudaSuccess) return GDPA_ERR_CUDA;
+    return GDPA_OK;
+}
+
+void end_work(Plan& p, cudaStream_t st) {
+    for (gdpa::StreamEvent& w : p.work)
+        if (w.stream == st) {
+            cudaEventRecord(w.event, st);
+            return;
+        }
+    gdpa::StreamEvent w{st, nullptr};
+    if (cudaEventCreateWithFlags(&w.event, cudaEventDisableTiming) != cudaSuccess) {
+        // no event: fall back to waiting for this stream now
+        cudaStreamSynchronize(st);
+        return;
+    }
+    cudaEventRecord(w.event, st);
+    p.work.push_back(w);
 }
 
 bool valid_act(int a) { return a >= GDPA_ACT_GELU_ERF && a <= GDPA_ACT_SOFTMAX; }
@@ -120,26 +182,27 @@ gdpa_status create_common(const int32_t* q_off_host, const int32_t* kv_off_host,
             (st = upload(&p->d_fwd_seg, p->fwd_seg.data(), S1 * sizeof(int32_t), s)) ||
             (st = upload(&p->d_bwd, p->bwd_dev_host.data(),
                          p->bwd_dev_host.size() * sizeof(gdpa::BwdUnit), s)) ||
-            (st = upload(&p->d_bwd_seg, p->bwd_seg.data(), S1 * sizeof(int32_t), s))) {
+            (st = upload(&p->d_bwd_seg, p->bwd_seg.data(), S1 * sizeof(int32_t), s)) ||
+            (st = alloc_dev(&p->d_err, 4 * sizeof(int32_t), s)) ||
+            (st = alloc_dev(&p->d_times, 2 * (size_t)p->S * 2 * sizeof(unsigned long long), s)) ||
+            (st = alloc_dev(&p->d_smid, 2 * (size_t)p->S * sizeof(int32_t), s))) {
             cudaStreamSynchronize(s);
             free_plan(p);
             return st;
         }
-        if (cudaMalloc((void**)&p->d_err, 4 * sizeof(int32_t)) != cudaSuccess ||
-            cudaMalloc((void**)&p->d_times, 2 * (size_t)p->S * 2 * sizeof(unsigned long long)) !=
-                cudaSuccess ||
-            cudaMalloc((void**)&p->d_smid, 2 * (size_t)p->S * sizeof(int32_t)) != cudaSuccess) {
-            cudaStreamSynchronize(s);
-            free_plan(p);
-            return GDPA_ERR_ALLOC;
-        }
-        // the synchronisation also keeps the host staging vectors alive
-        // until their asynchronous copies have finished
+        // the upload is ordered on `s`; launches on any stream wait for this
+        // event instead of the host waiting here
         if (cudaMemsetAsync(p->d_err, 0, 4 * sizeof(int32_t), s) != cudaSuccess ||
-            cudaStreamSynchronize(s) != cudaSuccess) {
+            cudaEventCreateWithFlags(&p->ready, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventRecord(p->ready, s) != cudaSuccess) {
+            cudaStreamSynchronize(s);
             free_plan(p);
             return GDPA_ERR_CUDA;
         }
+        // the kernel-layout records stay with the plan (host memory) until it
+        // is destroyed, so their copies never read freed memory
+        *out = (gdpa_plan)p;
+        return GDPA_OK;
     }
     std::vector<gdpa::FwdTile>().swap(p->fwd_dev_host);
     std::vector<gdpa::BwdUnit>().swap(p->bwd_dev_host);
@@ -231,6 +294,7 @@ gdpa_status fwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const vo
     if (p.Tq > 0 && (!q || !o)) return GDPA_ERR_INVALID_ARG;
     if (p.Tkv > 0 && (!k || !v)) return GDPA_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return GDPA_ERR_INVALID_ARG;
+    if (gdpa_status ds = check_device(p)) return ds;
     if (p.n_fwd == 0) return GDPA_OK;
     cudaStream_t st = (cudaStream_t)stream;
     if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
@@ -240,8 +304,12 @@ gdpa_status fwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const vo
     if (p.fwd_split && act == GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
     const bool tc =
         use_tc(p, dtype) && !(p.fwd_split && p.d != 128 && p.kernel == GDPA_KERNEL_AUTO);
-    if (tc) return gdpa::launch_tc_fwd(p, q, k, v, o, lse, alpha, act, st);
-    return gdpa::launch_simt_fwd(p, dtype, q, k, v, o, lse, alpha, act, st);
+    if (gdpa_status bs = begin_work(p, st)) return bs;
+    const gdpa_status s = tc ? gdpa::launch_tc_fwd(p, q, k, v, o, lse, alpha, act, st)
+                             : gdpa::launch_simt_fwd(p, dtype, q, k, v, o, lse, alpha, act, st);
+    if (tc && p.timing) p.timed_stream[0] = st;
+    end_work(p, st);
+    return s;
 }
 
 gdpa_status bwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k,
@@ -259,23 +327,35 @@ gdpa_status bwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const vo
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(d_o) || !aligned16(dq) ||
         !aligned16(dk) || !aligned16(dv))
         return GDPA_ERR_INVALID_ARG;
+    if (gdpa_status ds = check_device(p)) return ds;
     cudaStream_t st = (cudaStream_t)stream;
     if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
+    if (gdpa_status bs = begin_work(p, st)) return bs;
     const float* delta = nullptr;
+    gdpa_status s = GDPA_OK;
     if (sm && p.Tq > 0) {
-        // D = dO . O per row, in the plan's workspace (allocated once)
+        // D = dO . O per row, in the plan's workspace (allocated once, stream
+        // ordered on this call's stream)
         if (!p.d_delta &&
-            cudaMalloc((void**)&p.d_delta, (size_t)p.Tq * p.H * sizeof(float)) != cudaSuccess) {
+            cudaMallocAsync((void**)&p.d_delta, (size_t)p.Tq * p.H * sizeof(float), st) !=
+                cudaSuccess) {
             p.d_delta = nullptr;
-            return GDPA_ERR_ALLOC;
+            s = GDPA_ERR_ALLOC;
         }
-        const gdpa_status s = gdpa::launch_row_dot(p, dtype, d_o, o, p.d_delta, st);
-        if (s != GDPA_OK) return s;
+        if (s == GDPA_OK) s = gdpa::launch_row_dot(p, dtype, d_o, o, p.d_delta, st);
         delta = p.d_delta;
     }
-    if (use_tc(p, dtype))
-        return gdpa::launch_tc_bwd(p, q, k, v, d_o, dq, dk, dv, alpha, act, lse, delta, st);
-    return gdpa::launch_simt_bwd(p, dtype, q, k, v, d_o, dq, dk, dv, alpha, act, lse, delta, st);
+    if (s == GDPA_OK) {
+        if (use_tc(p, dtype)) {
+            s = gdpa::launch_tc_bwd(p, q, k, v, d_o, dq, dk, dv, alpha, act, lse, delta, st);
+            if (p.timing) p.timed_stream[1] = st;
+        } else {
+            s = gdpa::launch_simt_bwd(p, dtype, q, k, v, d_o, dq, dk, dv, alpha, act, lse, delta,
+                                      st);
+        }
+    }
+    end_work(p, st);
+    return s;
 }
 
 }  // namespace
@@ -309,13 +389,19 @@ gdpa_status gdpa_softmax_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, co
 gdpa_status gdpa_check(gdpa_plan plan, void* stream) {
     if (!plan || ((Plan*)plan)->host_only) return GDPA_ERR_INVALID_ARG;
     Plan& p = *(Plan*)plan;
+    if (gdpa_status ds = check_device(p)) return ds;
     cudaStream_t st = (cudaStream_t)stream;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return GDPA_ERR_CUDA;
+    // the plan's own launches (on whatever streams), then `stream`
+    if (wait_plan_work(p) != GDPA_OK || cudaStreamSynchronize(st) != cudaSuccess)
+        return GDPA_ERR_CUDA;
     int32_t err[4] = {0, 0, 0, 0};
-    if (cudaMemcpy(err, p.d_err, sizeof(err), cudaMemcpyDeviceToHost) != cudaSuccess)
+    if (cudaMemcpyAsync(err, p.d_err, sizeof(err), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
         return GDPA_ERR_CUDA;
     if (err[0] == gdpa::kDevOk) return GDPA_OK;
-    if (cudaMemset(p.d_err, 0, sizeof(err)) != cudaSuccess) return GDPA_ERR_CUDA;
+    if (cudaMemsetAsync(p.d_err, 0, sizeof(err), st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+        return GDPA_ERR_CUDA;
     return err[0] == gdpa::kDevTimeout ? GDPA_ERR_TIMEOUT : GDPA_ERR_DEVICE;
 }
 
@@ -324,12 +410,26 @@ gdpa_status gdpa_sm_times(gdpa_plan plan, int which, uint64_t* start_end, int32_
         return GDPA_ERR_INVALID_ARG;
     Plan& p = *(Plan*)plan;
     if (!p.timed[which]) return GDPA_ERR_INVALID_ARG;
-    if (cudaDeviceSynchronize() != cudaSuccess) return GDPA_ERR_CUDA;
-    if (cudaMemcpy(start_end, p.d_times + (size_t)which * p.S * 2, (size_t)p.S * 2 * sizeof(uint64_t),
-                   cudaMemcpyDeviceToHost) != cudaSuccess ||
-        cudaMemcpy(smid, p.d_smid + (size_t)which * p.S, (size_t)p.S * sizeof(int32_t),
-                   cudaMemcpyDeviceToHost) != cudaSuccess)
+    if (gdpa_status ds = check_device(p)) return ds;
+    // waits for this plan's launches only, and reads on the stream of the
+    // timed launch
+    cudaStream_t st = p.timed_stream[which];
+    if (wait_plan_work(p) != GDPA_OK ||
+        cudaMemcpyAsync(start_end, p.d_times + (size_t)which * p.S * 2,
+                        (size_t)p.S * 2 * sizeof(uint64_t), cudaMemcpyDeviceToHost, st) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(smid, p.d_smid + (size_t)which * p.S, (size_t)p.S * sizeof(int32_t),
+                        cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
         return GDPA_ERR_CUDA;
+    return GDPA_OK;
+}
+
+gdpa_status gdpa_plan_set_wait_test(gdpa_plan plan, int limit_us, int stall) {
+    if (!plan || limit_us < 0) return GDPA_ERR_INVALID_ARG;
+    Plan& p = *(Plan*)plan;
+    p.wait_limit_us = (uint32_t)limit_us;
+    p.stall = stall ? 1 : 0;
     return GDPA_OK;
 }
 

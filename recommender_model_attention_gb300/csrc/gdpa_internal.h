@@ -35,6 +35,14 @@ constexpr int kUnitAtomicDQ = 1;
 // Device error word layout (int32[4]): code, where, cta, detail.
 enum DevErr : int32_t { kDevOk = 0, kDevTimeout = 1, kDevBad = 2 };
 
+// Stream-ordered bookkeeping of a plan's device work: one event per stream
+// the plan has launched on, recorded after each call, so that destroying the
+// plan or reading its timings waits for this plan's work only.
+struct StreamEvent {
+    cudaStream_t stream;
+    cudaEvent_t event;
+};
+
 struct Plan {
     int device = 0;
     bool host_only = false;
@@ -62,7 +70,17 @@ struct Plan {
     unsigned long long* d_times = nullptr;   // [2][S][2]
     int32_t* d_smid = nullptr;               // [2][S]
     int timed[2] = {0, 0};
+    cudaStream_t timed_stream[2] = {nullptr, nullptr};
     int64_t launches = 0;
+    // the upload of the plan (recorded on the creation stream); every launch
+    // waits for it on its own stream
+    cudaEvent_t ready = nullptr;
+    std::vector<StreamEvent> work;
+    // failure-path test hook: bounded-wait limit in microseconds (0 = the
+    // kernels' default) and whether CTA 0's loader skips its first query-tile
+    // load so that a wait expires
+    uint32_t wait_limit_us = 0;
+    int stall = 0;
     // softmax-variant backward: dO_t . O_t per row and head, [Tq][H] float,
     // allocated on first use
     float* d_delta = nullptr;
@@ -95,7 +113,8 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
                               unsigned long long* times, int32_t* smid, int H, int d, int64_t Tq,
                               int64_t Tkv, int mask, int window, const void* q, int64_t q_rows,
                               int shared_q, const void* k, const void* v, void* o, float* lse,
-                              float* w, float alpha, int act, cudaStream_t st);
+                              float* w, float alpha, int act, cudaStream_t st,
+                              uint32_t wait_limit_us = 0, int stall = 0);
 gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, const void* d_o,
                           float* dq, float* dk, float* dv, float alpha, int act, const float* lse,
                           const float* delta, cudaStream_t st);

@@ -5,7 +5,7 @@
 // custom allocator or a memory pool's own bookkeeping, plugins handed a fixed
 // device arena, or processes whose allocations must all be reserved up front.
 // They cannot create a gdpa_plan (its tile queue and error word are
-// cudaMalloc'd).  This entry point plans on the host into static host
+// allocated on the device).  This entry point plans on the host into static host
 // buffers, uploads the tile queue into a file-scope static device array, and
 // launches the same forward kernel.  It calls no cudaMalloc, cudaFree or
 // other allocating routine and keeps its host state in static buffers; the
@@ -181,11 +181,14 @@ extern "C" gdpa_status gdpa_fwd_noalloc(const int32_t* q_off_host, const int32_t
     DeviceSlot* slot = nullptr;
     gdpa_status s = setup_device(dev, &slot);
     if (s != GDPA_OK) return s;
-    // the staging buffers may still feed the previous call's upload
+    // the staging buffers may still feed the previous call's upload (on any
+    // device: the host staging is shared); a failed wait is reported once and
+    // does not hold back later calls
     for (int i = 0; i < kMaxDevices; ++i) {
         if (g_slots[i].pending) {
-            if (cudaEventSynchronize(g_slots[i].uploaded) != cudaSuccess) return GDPA_ERR_CUDA;
+            const cudaError_t e = cudaEventSynchronize(g_slots[i].uploaded);
             g_slots[i].pending = false;
+            if (e != cudaSuccess) return GDPA_ERR_CUDA;
         }
     }
     const int n = plan_static(q_off_host, kv_off_host, B, H, mask, window, S);

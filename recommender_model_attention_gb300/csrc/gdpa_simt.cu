@@ -276,7 +276,7 @@ gdpa_status fwd_impl(Plan& p, const void* q, const void* k, const void* v, void*
     const int64_t n = p.Tq * p.H * p.d;
     if (p.fwd_split) {
         const size_t bytes = (size_t)n * sizeof(float);
-        if (!p.d_wsplit && cudaMalloc((void**)&p.d_wsplit, bytes) != cudaSuccess) {
+        if (!p.d_wsplit && cudaMallocAsync((void**)&p.d_wsplit, bytes, st) != cudaSuccess) {
             p.d_wsplit = nullptr;
             return GDPA_ERR_ALLOC;
         }

@@ -87,6 +87,8 @@ struct BwdParams {
     unsigned long long* times;
     int32_t* smid;
     int timing;
+    uint64_t wait_ns;     // bounded-wait limit
+    int stall;            // test hook: CTA 0 skips its first Q load
 };
 
 __device__ __forceinline__ BwdUnit load_unit(const BwdUnit* p) {
@@ -126,13 +128,17 @@ __device__ void bwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
             const int y = u.qt0 + m * kBM;   // dO rows
             const int yq = prm.shared_q ? m * kBM : y;
             if (!mbar_wait(&bars[C::kQEmpty + s], ph ^ 1, ab, 22)) goto unwind;
-            mbar_arrive_expect_tx(&bars[C::kQFull + s], C::kTileBytes);
-            q_armed[s] = (int32_t)ph;
+            // failure-path test hook: CTA 0 never loads its first Q tile, so
+            // the MMA warp's bounded wait for it expires
+            if (!(prm.stall && blockIdx.x == 0 && i == 0)) {
+                mbar_arrive_expect_tx(&bars[C::kQFull + s], C::kTileBytes);
+                q_armed[s] = (int32_t)ph;
 #pragma unroll
-            for (int hf = 0; hf < C::kHalves; ++hf)
-                tma_load_2d(tmQ, &bars[C::kQFull + s],
-                            smem + C::kOffQ + s * C::kTileBytes + hf * kHalfBytes, h * D + hf * 64,
-                            yq, pol_stream);
+                for (int hf = 0; hf < C::kHalves; ++hf)
+                    tma_load_2d(tmQ, &bars[C::kQFull + s],
+                                smem + C::kOffQ + s * C::kTileBytes + hf * kHalfBytes,
+                                h * D + hf * 64, yq, pol_stream);
+            }
             if (!mbar_wait(&bars[C::kDOEmpty + s], ph ^ 1, ab, 23)) goto unwind;
             mbar_arrive_expect_tx(&bars[C::kDOFull + s], C::kTileBytes);
             do_armed[s] = (int32_t)ph;
@@ -502,7 +508,7 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const Abort ab{abort_flag, prm.err};
+    const Abort ab{abort_flag, prm.err, prm.wait_ns};
 
     if (warp == 0) {
         if (lane == 0) bwd_producer<D>(&tmQ, &tmK, &tmV, &tmDO, prm, smem, bars, seg0, seg1, ab);
@@ -588,6 +594,8 @@ gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, 
     prm.times = p.d_times;
     prm.smid = p.d_smid;
     prm.timing = p.timing;
+    prm.wait_ns = tc::wait_limit_ns(p.wait_limit_us);
+    prm.stall = p.stall;
     if (p.timing) p.timed[1] = 1;
     gdpa_status s = GDPA_OK;
     if (p.d == 128) {

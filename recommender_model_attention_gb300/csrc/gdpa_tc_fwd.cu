@@ -99,6 +99,8 @@ struct FwdParams {
     unsigned long long* times;
     int32_t* smid;
     int timing;
+    uint64_t wait_ns;   // bounded-wait limit
+    int stall;          // test hook: CTA 0 skips its first Q load
 };
 
 __device__ __forceinline__ FwdTile load_tile(const FwdTile* p) {
@@ -148,13 +150,17 @@ __device__ void fwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
         if (tile.kb1 <= tile.kb0) continue;
         const uint32_t qs = a % C::kNQ, qph = (a / C::kNQ) & 1;
         if (!mbar_wait(&bars[C::kBarQEmpty + qs], qph ^ 1, ab, 1)) goto unwind;
-        mbar_arrive_expect_tx(&bars[C::kBarQFull + qs], C::kTileBytes);
-        q_armed[qs] = (int32_t)qph;
+        // failure-path test hook: CTA 0 never loads its first Q tile, so the
+        // S issuer's bounded wait for it expires
+        if (!(prm.stall && blockIdx.x == 0 && a == 0)) {
+            mbar_arrive_expect_tx(&bars[C::kBarQFull + qs], C::kTileBytes);
+            q_armed[qs] = (int32_t)qph;
 #pragma unroll
-        for (int hf = 0; hf < C::kHalves; ++hf)
-            tma_load_2d(tmQ, &bars[C::kBarQFull + qs],
-                        smem + C::kOffQ + qs * C::kTileBytes + hf * kHalfBytes,
-                        tile.h * D + hf * 64, prm.shared_q ? tile.i0 : tile.qt0, pol_q);
+            for (int hf = 0; hf < C::kHalves; ++hf)
+                tma_load_2d(tmQ, &bars[C::kBarQFull + qs],
+                            smem + C::kOffQ + qs * C::kTileBytes + hf * kHalfBytes,
+                            tile.h * D + hf * 64, prm.shared_q ? tile.i0 : tile.qt0, pol_q);
+        }
         const int nit = tile_items<SM>(tile);
         for (int it = 0; it < nit; ++it, ++i) {
             const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
@@ -685,7 +691,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const Abort ab{abort_flag, prm.err};
+    const Abort ab{abort_flag, prm.err, prm.wait_ns};
 
     if (warp == 0) {
         if (lane == 0) fwd_producer<D, ACT == kSoftmax>(&tmQ, &tmK, &tmV, prm, smem, bars, seg0, seg1, ab);
@@ -743,7 +749,8 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
                               unsigned long long* times, int32_t* smid, int H, int d, int64_t Tq,
                               int64_t Tkv, int mask, int window, const void* q, int64_t q_rows,
                               int shared_q, const void* k, const void* v, void* o, float* lse,
-                              float* w, float alpha, int act, cudaStream_t st) {
+                              float* w, float alpha, int act, cudaStream_t st,
+                              uint32_t wait_limit_us, int stall) {
     if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
     if (w && (d != 128 || act == kSoftmax)) return GDPA_ERR_UNSUPPORTED;
     if (Tq == 0) return GDPA_OK;
@@ -778,6 +785,8 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
     prm.times = times;
     prm.smid = smid;
     prm.timing = times != nullptr && smid != nullptr;
+    prm.wait_ns = tc::wait_limit_ns(wait_limit_us);
+    prm.stall = stall;
     gdpa_status s = GDPA_OK;
     if (w) {
         GDPA_DISPATCH_ACT(act, A, s = launch<128, A, true>(S, mq, mk, mv, mo, mw, prm, st))
@@ -804,7 +813,7 @@ gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, 
         // into a zeroed workspace; a second kernel rounds it into O
         if (p.d != 128 || act == kSoftmax) return GDPA_ERR_UNSUPPORTED;
         const size_t bytes = (size_t)p.Tq * p.H * p.d * sizeof(float);
-        if (!p.d_wsplit && cudaMalloc((void**)&p.d_wsplit, bytes) != cudaSuccess) {
+        if (!p.d_wsplit && cudaMallocAsync((void**)&p.d_wsplit, bytes, st) != cudaSuccess) {
             p.d_wsplit = nullptr;
             return GDPA_ERR_ALLOC;
         }
@@ -816,7 +825,7 @@ gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, 
         p.d_fwd, p.d_fwd_seg, p.S, p.d_err, p.timing ? p.d_times : nullptr,
         p.timing ? p.d_smid : nullptr, p.H, p.d, p.Tq, p.Tkv, p.mask, p.window, q,
         p.shared_q > 0 ? (int64_t)p.shared_q : p.Tq, p.shared_q > 0, k, v, o, lse, w, alpha, act,
-        st);
+        st, p.wait_limit_us, p.stall);
     if (s == GDPA_OK) p.launches += 1;
     if (s == GDPA_OK && w) {
         const int64_t n4 = p.Tq * p.H * p.d / 4;

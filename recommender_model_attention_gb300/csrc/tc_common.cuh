@@ -61,8 +61,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Every wait of the tensor-core kernels is bounded: after kWaitLimitNs (or
-// kWaitLimitIters polls) it records a timeout in the plan's error word,
+// Every wait of the tensor-core kernels is bounded: after the CTA's limit
+// (kWaitLimitNs unless the plan's failure-path test hook set a shorter one)
+// or kWaitLimitIters polls it records a timeout in the plan's error word,
 // raises the CTA's abort flag and returns false; the caller then unwinds.
 // A raised abort flag (another role gave up) also ends the wait.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
@@ -71,7 +72,14 @@ constexpr uint32_t kWaitLimitIters = 1u << 30;
 struct Abort {
     volatile int* flag;   // shared memory, per CTA
     int32_t* err;         // global error word (code, where, cta, detail)
+    uint64_t limit_ns;    // wait limit
 };
+
+// The wait limit of a launch: `limit_us` > 0 from the test hook, else the
+// default.
+__host__ __device__ constexpr uint64_t wait_limit_ns(uint32_t limit_us) {
+    return limit_us > 0 ? (uint64_t)limit_us * 1000ull : kWaitLimitNs;
+}
 
 __device__ __forceinline__ void raise_error(const Abort& ab, int32_t code, int32_t where) {
     if (atomicCAS(ab.err, 0, code) == 0) {
@@ -81,14 +89,14 @@ __device__ __forceinline__ void raise_error(const Abort& ab, int32_t code, int32
     *ab.flag = 1;
 }
 
-static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const Abort& ab,
-                                            int32_t where) {
+__device__ __forceinline__ bool mbar_wait_slow_inl(uint64_t* bar, uint32_t parity, const Abort& ab,
+                                                  int32_t where) {
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0) {
             if (*ab.flag) return false;
-            if (globaltimer() - t0 > kWaitLimitNs || it > kWaitLimitIters) {
+            if (globaltimer() - t0 > ab.limit_ns || it > kWaitLimitIters) {
                 raise_error(ab, kDevTimeout, where);
                 return false;
             }
@@ -96,10 +104,22 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
     }
 }
 
+// Out-of-line form: smaller code where registers are not scarce.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, const Abort& ab,
+                                                   int32_t where) {
+    return mbar_wait_slow_inl(bar, parity, ab, where);
+}
+
+// kInline: the slow path inlined (no call, so no registers saved around it;
+// for kernels that hold many live values across their waits).
+template <bool kInline = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Abort& ab,
                                           int32_t where) {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, ab, where);
+    if constexpr (kInline)
+        return mbar_wait_slow_inl(bar, parity, ab, where);
+    else
+        return mbar_wait_slow(bar, parity, ab, where);
 }
 
 // bounded wait used while unwinding (ignores the abort flag)
@@ -358,9 +378,10 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N, bool a
 
 // A wait taken by every thread of a warp(group); warp-uniform result so
 // that the .sync.aligned tcgen05 instructions after it run with whole warps.
+template <bool kInline = false>
 __device__ __forceinline__ bool wg_wait(uint64_t* bar, uint32_t parity, const Abort& ab,
                                         int32_t where) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, where));
+    return __all_sync(0xffffffffu, mbar_wait<kInline>(bar, parity, ab, where));
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -62,6 +62,7 @@ def lib():
             "gdpa_plan_set_kernel": [vp, st],
             "gdpa_plan_set_timing": [vp, st],
             "gdpa_plan_set_shared_q": [vp, st],
+            "gdpa_plan_set_wait_test": [vp, st, st],
             "gdpa_fwd": [vp, st, vp, vp, vp, vp, ctypes.c_float, st, vp],
             "gdpa_bwd": [vp, st, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, st, vp],
             "gdpa_check": [vp, vp],
@@ -189,6 +190,13 @@ class Plan:
 
     def set_timing(self, enable: bool):
         _ok(lib().gdpa_plan_set_timing(self.handle, 1 if enable else 0), "gdpa_plan_set_timing")
+
+    def set_wait_test(self, limit_us: int = 0, stall: bool = False):
+        """Failure-path test hook: bounded-wait limit (microseconds, 0 = the
+        default) and whether CTA 0's loader skips its first query-tile load on
+        the next tensor-core launches, so that a wait expires."""
+        _ok(lib().gdpa_plan_set_wait_test(self.handle, int(limit_us), 1 if stall else 0),
+            "gdpa_plan_set_wait_test")
 
     def sm_times(self, which: str = "fwd"):
         """(start_end uint64 [S, 2] in ns, smid int32 [S]) of the last timed launch."""
