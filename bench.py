@@ -108,6 +108,7 @@ def useful_pairs(q_off, kv_off, mask, window):
 
 
 DEFAULT_WORKLOAD = "training_cross_fwd_bwd"
+POLICIES = ("zigzag", "round_robin", "zigzag_timed")
 OTHER_WORKLOADS = ("jagged_selfattn_window256", "user_ad_cross", "pma_pooling")
 
 
@@ -118,7 +119,7 @@ def busy_spread(start_end):
             "max_minus_min_over_mean": float((busy.max() - busy.min()) / busy.mean())}
 
 
-def forward_workload(name, gd, pk, pk_kind, reps=20, warmup=3):
+def forward_workload(name, gd, pk, pk_kind, sched="zigzag_timed", reps=20, warmup=3):
     """One forward-only workload at its full size, timed launch by launch
     with CUDA events on the launching stream, L2 flushed (a 256 MB write)
     before each timed launch; planner's key split, shared seeds for pooling.
@@ -131,14 +132,14 @@ def forward_workload(name, gd, pk, pk_kind, reps=20, warmup=3):
     n_seeds = w.shared_q
     q_in = x["q_seeds"] if n_seeds else x["q"]
 
-    def plan_for(sched):
+    def plan_for(pol):
         p = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window,
-                    sched=sched, max_kv_blocks="auto")
+                    sched=pol, max_kv_blocks="auto")
         if n_seeds:
             p.set_shared_q(n_seeds)
         return p
 
-    plan = plan_for("zigzag")
+    plan = plan_for(sched)
     o = torch.empty_like(x["q"])
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
@@ -166,7 +167,7 @@ def forward_workload(name, gd, pk, pk_kind, reps=20, warmup=3):
     gbs = nbytes / (ms * 1e-3) / 1e9
     attainable = min(pk["bf16_tflops"], flops / nbytes * pk["hbm_gbs"] / 1e3)
     spread = {}
-    for pol in ("zigzag", "round_robin"):
+    for pol in POLICIES:
         pp = plan_for(pol)
         pp.set_timing(True)
         gd.gdpa_fwd(pp, q_in, x["k"], x["v"], o=o, alpha=w.alpha, act=w.act)
@@ -181,7 +182,8 @@ def forward_workload(name, gd, pk, pk_kind, reps=20, warmup=3):
             "attainable_tflops": attainable, "pct_of_attainable": 100.0 * tflops / attainable,
             "algorithmic_bytes": nbytes, "useful_pairs": pairs, "fwd_tiles": int(n_tiles),
             "B": w.B, "H": w.H, "act": w.act, "mask": w.mask, "window": w.window,
-            "shared_q": n_seeds, "timing": "median of %d launches, L2 flushed before each" % reps,
+            "shared_q": n_seeds, "sched": sched,
+            "timing": "median of %d launches, L2 flushed before each" % reps,
             "sm_spread": spread}
 
 
@@ -337,6 +339,8 @@ def main():
                     help="use only the first N sequences of the workload (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sched", default="zigzag_timed", choices=list(POLICIES),
+                    help="dealing policy of the timed plans")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the forward-only lines of the other jagged workloads")
     ap.add_argument("--max-kv-blocks", default="auto",
@@ -388,6 +392,7 @@ def main():
     q_in = x["q_seeds"] if n_seeds else x["q"]
 
     def make_plan(**kw):
+        kw.setdefault("sched", args.sched)
         p = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, mask=w.mask, window=w.window,
                     max_kv_blocks=mkb, **kw)
         if n_seeds:
@@ -613,7 +618,7 @@ def main():
     # untimed launches)
     spread, spread_bwd = {}, {}
     try:
-        for pol in ("zigzag", "round_robin"):
+        for pol in POLICIES:
             pp = make_plan(sched=pol)
             pp.set_timing(True)
             fwd_call(pp, q_in, x["k"], x["v"], o)
@@ -634,7 +639,7 @@ def main():
         others = {}
         for name in OTHER_WORKLOADS:
             try:
-                others[name] = forward_workload(name, gd, pk, pk_kind)
+                others[name] = forward_workload(name, gd, pk, pk_kind, sched=args.sched)
             except Exception as e:  # a report beside the headline
                 others[name] = {"error": str(e)}
             torch.cuda.synchronize()
@@ -651,7 +656,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded lengths and RMSNorm'd N(0,1) inputs, random dO)",
             "config": {"workload": w.name, "B": len(x["q_off"]) - 1, "H": w.H, "d": w.d,
-                       "act": w.act, "max_kv_blocks": mkb,
+                       "act": w.act, "max_kv_blocks": mkb, "sched": args.sched,
                        "key_split": key_split, "shared_q": n_seeds,
                        "Tq": Tq, "Tkv": Tkv, "useful_pairs": pairs,
                        "l2": "inputs larger than L2 (%.1f GB resident)" % (input_bytes / 1e9),

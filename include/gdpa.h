@@ -82,10 +82,26 @@ typedef enum {
     GDPA_MASK_CAUSAL_WINDOW = 1    /* i - window < j <= i */
 } gdpa_mask;
 
-/* Tile-to-SM assignment (GDPA page, zigzag scheduling paragraph and diagram). */
+/* Tile-to-SM assignment (GDPA page, zigzag scheduling paragraph and diagram).
+ *
+ * ZIGZAG costs a forward tile by its key blocks and a backward unit by its
+ * query tiles.  ZIGZAG_TIMED deals the same way (stable sort by cost, snake
+ * order) but costs a backward unit with an integer time model, in units of
+ * 50 ns, fitted to the tensor-core backward's measured times on GB300:
+ *   36 + 22 nkv16 / 128 + sum over its query tiles of
+ *   (40 + 34 nq32 / 128 + 24 nkv16 / 128)          (a zero unit: 1)
+ * where nq32 is a query tile's rows rounded up to 32 and nkv16 the unit's
+ * keys rounded up to 16 (integer divisions): a unit carries a fixed cost
+ * (loading its K and V, storing dK and dV) and each query tile a cost that
+ * grows with the keys, which counting query tiles alone does not see.
+ * Forward tiles keep the key-block cost: equal-cost tiles keep their
+ * enumeration order, so the tiles of one sample run at the same time and
+ * share its K and V in L2 (costing them by time scattered them and was
+ * measured slower). */
 typedef enum {
     GDPA_SCHED_ZIGZAG = 0,       /* sort by cost, deal in snake order */
-    GDPA_SCHED_ROUND_ROBIN = 1   /* enumeration order, tile r to SM r % S */
+    GDPA_SCHED_ROUND_ROBIN = 1,  /* enumeration order, tile r to SM r % S */
+    GDPA_SCHED_ZIGZAG_TIMED = 2  /* sort by the time model, deal in snake order */
 } gdpa_sched;
 
 typedef enum { GDPA_BF16 = 0, GDPA_F32 = 1 } gdpa_dtype;

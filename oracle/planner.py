@@ -27,6 +27,13 @@ backward).  Zigzag: stable sort by w descending, the r-th tile goes to round
 r // S, position p = r % S, SM p on even rounds and S - 1 - p on odd ones.
 Round robin: the r-th tile in enumeration order goes to SM r % S.  Each SM's
 queue keeps the dealing order.
+
+Timed zigzag (the library's GDPA_SCHED_ZIGZAG_TIMED) deals like zigzag, with
+the backward units' w from an integer time model (50 ns units) of the
+tensor-core backward: 36 + 22 K/128 plus 40 + 34 q/128 + 24 K/128 for each of
+the unit's query tiles, where q is a query tile's rows rounded up to 32 and K
+the unit's keys rounded up to 16, every division an integer one; an empty
+unit costs 1.  Forward tiles keep w = key blocks.
 """
 
 from __future__ import annotations
@@ -94,10 +101,29 @@ def bwd_units(q_off, kv_off, H, BM=128, BN=128, mask="none", window=0):
     return out, zero_dq
 
 
+def _round_up(a, m):
+    return _cdiv(a, m) * m
+
+
+def bwd_time(unit, q_off, kv_off, BM=128, BN=128):
+    """Timed-zigzag cost of a backward unit (b, h, j, m0, m1, flags)."""
+    b, _, j, m0, m1 = unit[:5]
+    if m1 <= m0:
+        return 1
+    lq = int(q_off[b + 1]) - int(q_off[b])
+    lkv = int(kv_off[b + 1]) - int(kv_off[b])
+    keys = _round_up(min(BN, lkv - j * BN), 16)
+    cost = 36 + (22 * keys) // 128
+    for m in range(m0, m1):
+        rows = _round_up(min(BM, lq - m * BM), 32)
+        cost += 40 + (34 * rows) // 128 + (24 * keys) // 128
+    return cost
+
+
 def deal(costs, S, policy="zigzag"):
     """SM of every item (by item index) and the per-SM queues (lists of item indices)."""
     n = len(costs)
-    if policy == "zigzag":
+    if policy in ("zigzag", "zigzag_timed"):
         order = sorted(range(n), key=lambda i: (-costs[i], i))
     elif policy == "round_robin":
         order = list(range(n))
@@ -107,7 +133,7 @@ def deal(costs, S, policy="zigzag"):
     queues = [[] for _ in range(S)]
     for r, i in enumerate(order):
         p = r % S
-        if policy == "zigzag" and (r // S) % 2 == 1:
+        if policy in ("zigzag", "zigzag_timed") and (r // S) % 2 == 1:
             p = S - 1 - p
         sm[i] = p
         queues[p].append(i)
@@ -125,8 +151,12 @@ def plan(q_off, kv_off, H, S, BM=128, BN=128, mask="none", window=0,
     ft = fwd_tiles(q_off, kv_off, H, BM, BN, mask, window, max_kv_blocks)
     bu, zero_dq = bwd_units(q_off, kv_off, H, BM, BN, mask, window)
     res = {"zero_dq": zero_dq}
-    for name, items, cost_of in (("fwd", ft, lambda t: t[4] - t[3]),
-                                 ("bwd", bu, lambda u: u[4] - u[3])):
+    fcost = lambda t: t[4] - t[3]  # noqa: E731
+    if policy == "zigzag_timed":
+        bcost = lambda u: bwd_time(u, q_off, kv_off, BM, BN)  # noqa: E731
+    else:
+        bcost = lambda u: u[4] - u[3]  # noqa: E731
+    for name, items, cost_of in (("fwd", ft, fcost), ("bwd", bu, bcost)):
         costs = [cost_of(t) for t in items]
         sm, queues = deal(costs, S, policy)
         rows, seg = [], [0]

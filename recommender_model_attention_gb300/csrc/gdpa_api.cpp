@@ -142,7 +142,9 @@ gdpa_status create_common(const int32_t* q_off_host, const int32_t* kv_off_host,
     if (!q_off_host || !kv_off_host || B < 0 || H < 1 || d < 1) return GDPA_ERR_INVALID_ARG;
     if (mask != GDPA_MASK_NONE && mask != GDPA_MASK_CAUSAL_WINDOW) return GDPA_ERR_INVALID_ARG;
     if (mask == GDPA_MASK_CAUSAL_WINDOW && window < 1) return GDPA_ERR_INVALID_ARG;
-    if (sched != GDPA_SCHED_ZIGZAG && sched != GDPA_SCHED_ROUND_ROBIN) return GDPA_ERR_INVALID_ARG;
+    if (sched != GDPA_SCHED_ZIGZAG && sched != GDPA_SCHED_ROUND_ROBIN &&
+        sched != GDPA_SCHED_ZIGZAG_TIMED)
+        return GDPA_ERR_INVALID_ARG;
     if (num_sms < 0 || max_kv_blocks_per_tile < GDPA_KV_SPLIT_AUTO) return GDPA_ERR_INVALID_ARG;
     if (host_only && num_sms == 0) return GDPA_ERR_INVALID_ARG;
     if (d > 128 || d % 4 != 0) return GDPA_ERR_UNSUPPORTED;

@@ -22,7 +22,9 @@
 //    fastest at 16, 64 and 1024 samples).
 //  * cost = blocks on the inner loop; zigzag = stable sort by cost,
 //    descending, then snake dealing over the S SMs; round robin = tile r to
-//    SM r % S in enumeration order.
+//    SM r % S in enumeration order.  Timed zigzag deals the same way but
+//    costs backward units with the integer time model of include/gdpa.h
+//    (GDPA_SCHED_ZIGZAG_TIMED).
 #include <algorithm>
 #include <numeric>
 
@@ -32,6 +34,18 @@ namespace gdpa {
 namespace {
 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t up(int64_t a, int64_t m) { return cdiv(a, m) * m; }
+
+// The time model of GDPA_SCHED_ZIGZAG_TIMED (units of 50 ns).
+// Backward unit: nkv keys, query tiles [m0, m1) of a sample with lq queries.
+int64_t bwd_time_cost(int64_t nkv, int64_t m0, int64_t m1, int64_t lq) {
+    if (m1 <= m0) return 1;
+    const int64_t k16 = up(nkv, 16);
+    int64_t c = 36 + 22 * k16 / 128;
+    for (int64_t m = m0; m < m1; ++m)
+        c += 40 + 34 * up(std::min<int64_t>(kBM, lq - m * kBM), 32) / 128 + 24 * k16 / 128;
+    return c;
+}
 
 struct Item {
     int32_t f[6];  // forward: b h m kb0 kb1 -; backward: b h j m0 m1 flags
@@ -44,7 +58,8 @@ void deal(const std::vector<Item>& items, int S, int sched, std::vector<int64_t>
     const int64_t n = (int64_t)items.size();
     order.resize(n);
     std::iota(order.begin(), order.end(), 0);
-    if (sched == GDPA_SCHED_ZIGZAG) {
+    const bool zz = sched == GDPA_SCHED_ZIGZAG || sched == GDPA_SCHED_ZIGZAG_TIMED;
+    if (zz) {
         // stable sort by cost, descending: a counting sort when the costs
         // span a small range (they count blocks or tiles), else a merge sort
         int64_t cmax = 0;
@@ -64,7 +79,7 @@ void deal(const std::vector<Item>& items, int S, int sched, std::vector<int64_t>
     int32_t col = 0;
     bool odd = false;   // odd dealing round: the snake runs back
     for (int64_t r = 0; r < n; ++r) {
-        sm[r] = (sched == GDPA_SCHED_ZIGZAG && odd) ? S - 1 - col : col;
+        sm[r] = (zz && odd) ? S - 1 - col : col;
         if (++col == S) {
             col = 0;
             odd = !odd;
@@ -115,6 +130,7 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
     p.max_lq = 0;
     for (int b = 0; b < B; ++b) p.max_lq = std::max<int64_t>(p.max_lq, q_off[b + 1] - q_off[b]);
     const bool win = p.mask == GDPA_MASK_CAUSAL_WINDOW;
+    const bool timed = p.sched == GDPA_SCHED_ZIGZAG_TIMED;
     const int64_t W = p.window;
     // key-block hull of query tile m of sample b (empty: k0 = k1 = 0)
     auto kv_hull = [&](int b, int64_t m, int64_t& k0, int64_t& k1) {
@@ -211,9 +227,13 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
         if (atomic || hole) p.zero_dq = 1;
         const int32_t flags = atomic ? kUnitAtomicDQ : 0;
         for (int h = 0; h < H; ++h) {
-            for (int64_t j = 0; j < nkb; ++j)
+            for (int64_t j = 0; j < nkb; ++j) {
+                const int64_t cost =
+                    timed ? bwd_time_cost(std::min<int64_t>(kBN, lkv - j * kBN), m0s[j], m1s[j], lq)
+                          : m1s[j] - m0s[j];
                 bu.push_back(Item{{b, h, (int32_t)j, (int32_t)m0s[j], (int32_t)m1s[j], flags},
-                                  m1s[j] - m0s[j]});
+                                  cost});
+            }
         }
     }
 

@@ -18,7 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libgdpa_gb300.so")
 ACT = {"gelu_erf": 0, "gelu_tanh": 1, "silu": 2, "gelu_taylor6": 3, "identity": 4,
        "softmax": 5}
 MASK = {"none": 0, "causal_window": 1}
-SCHED = {"zigzag": 0, "round_robin": 1}
+SCHED = {"zigzag": 0, "round_robin": 1, "zigzag_timed": 2}
 KERNEL = {"auto": 0, "tcgen05": 1, "simt": 2}
 KV_SPLIT_AUTO = -1   # max_kv_blocks_per_tile: the planner chooses
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration", 3: "CUDA error",

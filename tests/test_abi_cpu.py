@@ -57,7 +57,7 @@ def _compare(gd, qo, ko, H, S, mask, window, sched, max_kvb=0):
 
 
 @pytest.mark.parametrize("cfg", CONFIGS, ids=[c.name for c in CONFIGS])
-@pytest.mark.parametrize("sched", ["zigzag", "round_robin"])
+@pytest.mark.parametrize("sched", ["zigzag", "round_robin", "zigzag_timed"])
 def test_planner_matches_oracle_on_workloads(gd, cfg, sched):
     lq, lkv = draw_lengths(cfg)
     qo, ko = offsets_from_lengths(lq), offsets_from_lengths(lkv)
@@ -72,7 +72,7 @@ def test_planner_matches_oracle_random(gd, seed, S):
     mask = "causal_window" if seed % 2 else "none"
     c = small_case(seed, B=9, H=1, d=1, q_range=(0, 700),
                    kv_range=None if mask == "causal_window" else (0, 400), zero_lengths=True)
-    for sched in ("zigzag", "round_robin"):
+    for sched in ("zigzag", "round_robin", "zigzag_timed"):
         _compare(gd, c["q_off"], c["kv_off"], 3, S, mask, 1 + 37 * seed, sched,
                  max_kvb=(seed % 3))
 

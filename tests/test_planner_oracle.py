@@ -109,7 +109,27 @@ def test_kv_split_chunks():
     assert tiles == [(0, 0, 0, 0, 3), (0, 0, 0, 3, 6), (0, 0, 0, 6, 8), (1, 0, 0, 0, 2)]
 
 
-@pytest.mark.parametrize("policy", ["zigzag", "round_robin"])
+def test_timed_costs_hand_worked_example():
+    g = _read("timed_costs_worked_example.txt")
+    qo, ko = offsets_from_lengths(g["q_lengths"]), offsets_from_lengths(g["kv_lengths"])
+    units, _ = planner.bwd_units(qo, ko, 1)
+    assert [planner.bwd_time(u, qo, ko) for u in units] == g["bwd_costs"]
+
+
+def test_timed_costs_grow_with_work():
+    # more keys or more query rows never cost less, and a unit of one query
+    # tile costs more than the tile alone (its fixed part)
+    for lq in (1, 100, 128, 129, 1000):
+        for lkv in (1, 16, 17, 64, 112):
+            qo = offsets_from_lengths([lq, lq, lq + 32])
+            ko = offsets_from_lengths([lkv, lkv + 16, lkv])
+            u, _ = planner.bwd_units(qo, ko, 1)
+            c = [planner.bwd_time(x, qo, ko) for x in u]
+            assert c[1] >= c[0] and c[2] >= c[0]
+            assert c[0] > 40 * len(range(u[0][3], u[0][4]))
+
+
+@pytest.mark.parametrize("policy", ["zigzag", "round_robin", "zigzag_timed"])
 @pytest.mark.parametrize("S", [1, 7, 152])
 def test_dealing_invariants(policy, S):
     rng = np.random.Generator(np.random.PCG64(S))
@@ -120,10 +140,11 @@ def test_dealing_invariants(policy, S):
         assert flat == list(range(len(costs)))
         for s, q in enumerate(queues):
             assert all(sm[i] == s for i in q)
-            assert q == sorted(q, key=lambda i: (-costs[i], i)) if policy == "zigzag" else q == sorted(q)
+            assert (q == sorted(q, key=lambda i: (-costs[i], i)) if policy != "round_robin"
+                    else q == sorted(q))
         work = [sum(costs[i] for i in q) for q in queues]
         assert sum(work) == sum(costs)
-        if policy == "zigzag" and costs:
+        if policy != "round_robin" and costs:
             # snake dealing of a descending list: spread at most the largest item
             assert max(work) - min(work) <= max(costs)
 
