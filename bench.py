@@ -7,7 +7,10 @@ GELU-erf, dO ~ N(0, 1)), inputs resident in HBM.  Prints one JSON line.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 Under torchrun each rank runs its own batch of the same shape (different
-seed): the work shards by sample with no exchange, so scaling is weak.
+seed): the work shards by sample with no exchange, so scaling is weak.  With
+``--scaling strong`` every rank draws the same batch and runs the samples that
+gdpa_shard_batch deals to it (by work, zigzag order), so the total work is
+fixed as the rank count grows.
 ``--impl reference`` times the float64 CPU oracle on a bounded sample.
 """
 
@@ -339,6 +342,9 @@ def main():
                     help="use only the first N sequences of the workload (profiling runs)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--scaling", default="weak", choices=["weak", "strong"],
+                    help="N > 1: each rank its own batch (weak) or one batch sharded over "
+                         "the ranks by gdpa_shard_batch (strong)")
     ap.add_argument("--sched", default="zigzag_timed", choices=list(POLICIES),
                     help="dealing policy of the timed plans")
     ap.add_argument("--no-workloads", action="store_true",
@@ -380,7 +386,23 @@ def main():
         from workloads import draw_lengths
         lq, lkv = draw_lengths(w)
         lengths = (lq[:args.samples], lkv[:args.samples])
-    x = make_inputs(w, device="cuda", seed=rank_seed(w, rank), lengths=lengths)
+    strong = args.scaling == "strong" and world > 1
+    if strong:
+        # one batch for the whole job; this rank keeps the samples dealt to it
+        full = make_inputs(w, device="cuda", seed=rank_seed(w, 0), lengths=lengths)
+        owner, _ = gd.shard_batch(full["q_off"], full["kv_off"], w.H, world, w.mask, w.window)
+        lo, lk, qi, ki, _ = gd.shard_rows(full["q_off"], full["kv_off"], owner, rank)
+        qi_t = torch.from_numpy(qi).cuda()
+        ki_t = torch.from_numpy(ki).cuda()
+        x = dict(full)
+        x["q_off"], x["kv_off"] = lo, lk
+        for n, idx in (("q", qi_t), ("k", ki_t), ("v", ki_t), ("do", qi_t)):
+            if full.get(n) is not None:
+                x[n] = full[n].index_select(0, idx).contiguous()
+        del full
+        torch.cuda.empty_cache()
+    else:
+        x = make_inputs(w, device="cuda", seed=rank_seed(w, rank), lengths=lengths)
     stream = torch.cuda.current_stream()
     mkb = args.max_kv_blocks if args.max_kv_blocks == "auto" else int(args.max_kv_blocks)
     if w.act == "softmax" and mkb == "auto":
@@ -653,14 +675,17 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "higher_is_better": True, "scaling": "strong" if strong else "weak",
+            "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded lengths and RMSNorm'd N(0,1) inputs, random dO)",
             "config": {"workload": w.name, "B": len(x["q_off"]) - 1, "H": w.H, "d": w.d,
                        "act": w.act, "max_kv_blocks": mkb, "sched": args.sched,
                        "key_split": key_split, "shared_q": n_seeds,
                        "Tq": Tq, "Tkv": Tkv, "useful_pairs": pairs,
                        "l2": "inputs larger than L2 (%.1f GB resident)" % (input_bytes / 1e9),
-                       "parallelism": "samples sharded by rank, no exchange" if world > 1
+                       "parallelism": ("one batch's samples dealt to ranks by gdpa_shard_batch, "
+                                       "no exchange" if strong else
+                                       "each rank its own batch, no exchange") if world > 1
                        else "single GPU"},
             "pct_of_bf16_peak": 100.0 * value / world / pk["bf16_tflops"],
             "fwd": {"ms": fwd_ms, "tflops": fwd_flops / (fwd_ms * 1e-3) / 1e12,

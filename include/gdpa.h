@@ -216,6 +216,30 @@ gdpa_status gdpa_plan_export(gdpa_plan plan, int32_t* tiles_out, int64_t cap, in
 gdpa_status gdpa_plan_export_bwd(gdpa_plan plan, int32_t* units_out, int64_t cap,
                                  int64_t* n_out, int32_t* seg_start_out, int* zero_dq_out);
 
+/*
+ * Deal the samples of one batch to num_ranks GPUs (one process per GPU), so
+ * that each rank runs the samples given to it as a batch of its own with no
+ * exchange (samples and heads are independent; GDPA page, the jagged-input
+ * and zigzag-scheduling paragraph, applied one level up; GEM page "GEM
+ * 트레이닝: Meta가 LLM 규모의 광고 파운데이션 모델 효율성을 두 배로 높인 방법",
+ * techlist.io, section on scaling to thousands of GPUs: variable lengths
+ * make stragglers).  A sample's work is H times the key blocks of its
+ * 128-row query tiles (with the causal window: of the window's hull), the
+ * forward tile cost of gdpa_plan_create summed over the sample.  Samples are
+ * sorted by work, descending and stable, and dealt in snake order: the r-th
+ * goes to rank r % R on even rounds r / R and R - 1 - r % R on odd ones.
+ *
+ *   q_off, kv_off  host int32 [B+1] offsets (as gdpa_plan_create).
+ *   rank_out       host int32 [B]: the rank of each sample.
+ *   work_out       host int64 [num_ranks] (may be NULL): each rank's work.
+ *
+ * INVALID_ARG for NULL pointers, B < 0, H < 1, num_ranks < 1, bad offsets
+ * or a window < 1 with the window mask.  Host only; no device is touched.
+ */
+gdpa_status gdpa_shard_batch(const int32_t* q_off, const int32_t* kv_off, int B, int H,
+                             gdpa_mask mask, int window, int num_ranks, int32_t* rank_out,
+                             int64_t* work_out);
+
 /* Choose the kernel family (default AUTO); INVALID_ARG for unknown values. */
 gdpa_status gdpa_plan_set_kernel(gdpa_plan plan, gdpa_kernel kernel);
 

@@ -170,3 +170,18 @@ def plan(q_off, kv_off, H, S, BM=128, BN=128, mask="none", window=0,
         res[name + "_work"] = np.array([sum(costs[i] for i in queues[s]) for s in range(S)],
                                        dtype=np.int64)
     return res
+
+
+def shard_samples(q_off, kv_off, H, R, BM=128, BN=128, mask="none", window=0):
+    """Samples of one batch dealt to R ranks (the library's gdpa_shard_batch):
+    a sample's work is H times the key blocks of its forward tiles (the
+    forward tile cost, summed over the sample); stable sort by work,
+    descending, then snake dealing over the ranks.  Returns (rank of each
+    sample, work of each rank)."""
+    q_off = [int(x) for x in q_off]
+    B = len(q_off) - 1
+    work = [0] * B
+    for t in fwd_tiles(q_off, kv_off, 1, BM, BN, mask, window):
+        work[t[0]] += (t[4] - t[3]) * H
+    rank, queues = deal(work, R, "zigzag")
+    return rank, [sum(work[b] for b in q) for q in queues]

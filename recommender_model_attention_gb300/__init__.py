@@ -26,6 +26,8 @@ from .gdpa import (  # noqa: F401
     gdpa_softmax_bwd,
     gdpa_softmax_fwd,
     lib,
+    shard_batch,
+    shard_rows,
 )
 
 

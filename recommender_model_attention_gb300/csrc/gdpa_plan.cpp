@@ -276,4 +276,47 @@ gdpa_status build_plan_host(Plan& p, const int32_t* q_off, const int32_t* kv_off
     return GDPA_OK;
 }
 
+
+// ---------------------------------------------------------------- sharding
+
+extern "C" gdpa_status gdpa_shard_batch(const int32_t* q_off, const int32_t* kv_off, int B, int H,
+                                        gdpa_mask mask, int window, int num_ranks,
+                                        int32_t* rank_out, int64_t* work_out) {
+    if (!q_off || !kv_off || B < 0 || H < 1 || num_ranks < 1 || (B > 0 && !rank_out))
+        return GDPA_ERR_INVALID_ARG;
+    if (mask != GDPA_MASK_NONE && mask != GDPA_MASK_CAUSAL_WINDOW) return GDPA_ERR_INVALID_ARG;
+    if (mask == GDPA_MASK_CAUSAL_WINDOW && window < 1) return GDPA_ERR_INVALID_ARG;
+    if (q_off[0] != 0 || kv_off[0] != 0) return GDPA_ERR_INVALID_ARG;
+    for (int b = 0; b < B; ++b)
+        if (q_off[b + 1] < q_off[b] || kv_off[b + 1] < kv_off[b]) return GDPA_ERR_INVALID_ARG;
+    const bool win = mask == GDPA_MASK_CAUSAL_WINDOW;
+    // a sample's work: H x the key blocks of its query tiles (the forward
+    // tile cost of gdpa_plan_create, summed over the sample)
+    std::vector<Item> items(B);
+    for (int b = 0; b < B; ++b) {
+        const int64_t lq = q_off[b + 1] - q_off[b], lkv = kv_off[b + 1] - kv_off[b];
+        int64_t w = 0;
+        for (int64_t m = 0; m < cdiv(lq, kBM); ++m) {
+            const int64_t r0 = m * kBM, r1 = std::min<int64_t>(r0 + kBM, lq);
+            int64_t lo = 0, hi = lkv;
+            if (win) {
+                lo = std::max<int64_t>(0, r0 - window + 1);
+                hi = std::min<int64_t>(lkv, r1);
+            }
+            if (lo < hi) w += cdiv(hi, kBN) - lo / kBN;
+        }
+        items[b] = Item{{b, 0, 0, 0, 0, 0}, w * H};
+    }
+    std::vector<int64_t> order;
+    std::vector<int32_t> rank;
+    deal(items, num_ranks, GDPA_SCHED_ZIGZAG, order, rank);
+    if (work_out)
+        for (int r = 0; r < num_ranks; ++r) work_out[r] = 0;
+    for (int64_t k = 0; k < (int64_t)order.size(); ++k) {
+        rank_out[order[k]] = rank[k];
+        if (work_out) work_out[rank[k]] += items[order[k]].cost;
+    }
+    return GDPA_OK;
+}
+
 }  // namespace gdpa

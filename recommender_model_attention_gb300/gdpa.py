@@ -70,6 +70,7 @@ def lib():
             "gdpa_fwd_noalloc": [i32p, i32p, st, st, st, st, st, vp, vp, vp, vp, ctypes.c_float,
                                  st, vp],
             "gdpa_act_eval": [st, st, vp, vp, vp, ctypes.c_int64, vp],
+            "gdpa_shard_batch": [i32p, i32p, st, st, st, st, st, i32p, i64p],
             "gdpa_softmax_fwd": [vp, st, vp, vp, vp, vp, vp, ctypes.c_float, vp],
             "gdpa_softmax_bwd": [vp, st, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp],
         }
@@ -287,6 +288,41 @@ def gdpa_bwd(plan: Plan, q, k, v, do, dq=None, dk=None, dv=None, alpha=None,
                        _ptr(dk), _ptr(dv), ctypes.c_float(alpha), ACT[act], _stream_ptr(stream)),
         "gdpa_bwd")
     return dq, dk, dv
+
+
+def shard_batch(q_off, kv_off, H: int, num_ranks: int, mask: str = "none", window: int = 0):
+    """(rank of each sample int32 [B], work of each rank int64 [R]): the
+    samples of one batch dealt to ranks by work in zigzag order
+    (gdpa_shard_batch)."""
+    qo, qp = _i32(q_off)
+    ko, kp = _i32(kv_off)
+    if len(qo) != len(ko) or len(qo) < 1:
+        raise ValueError("offset arrays must both have B + 1 entries")
+    B = len(qo) - 1
+    rank = np.zeros(max(B, 1), dtype=np.int32)
+    work = np.zeros(int(num_ranks), dtype=np.int64)
+    _ok(lib().gdpa_shard_batch(qp, kp, B, int(H), MASK[mask], int(window), int(num_ranks),
+                               rank.ctypes.data_as(ctypes.POINTER(ctypes.c_int32)),
+                               work.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))),
+        "gdpa_shard_batch")
+    return rank[:B], work
+
+
+def shard_rows(q_off, kv_off, rank_of_sample, rank: int):
+    """The local batch of one rank: (local q_off, local kv_off, query row
+    indices, key row indices, sample indices) of the samples dealt to
+    ``rank``, in their batch order; the index arrays gather the rank's rows
+    from (or scatter its results to) the whole batch's token-major tensors."""
+    q_off = np.asarray(q_off, dtype=np.int64)
+    kv_off = np.asarray(kv_off, dtype=np.int64)
+    mine = np.nonzero(np.asarray(rank_of_sample) == rank)[0]
+    lq = q_off[mine + 1] - q_off[mine]
+    lkv = kv_off[mine + 1] - kv_off[mine]
+    qi = np.concatenate([np.arange(q_off[b], q_off[b + 1]) for b in mine] or [np.zeros(0, np.int64)])
+    ki = np.concatenate([np.arange(kv_off[b], kv_off[b + 1]) for b in mine] or [np.zeros(0, np.int64)])
+    lo = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    lk = np.concatenate([[0], np.cumsum(lkv)]).astype(np.int32)
+    return lo, lk, qi.astype(np.int64), ki.astype(np.int64), mine
 
 
 def allreduce_seed_grad(dq, group=None):

@@ -159,3 +159,57 @@ def test_empty_batch_plan(gd):
     tiles, seg = p.export()
     assert tiles.shape == (0, 6) and np.all(seg == 0)
     p.destroy()
+
+
+def test_shard_batch_hand_worked(gd):
+    # worked by hand from the rule in include/gdpa.h (H = 2, two ranks):
+    # sample 0: Lq 300 -> 3 query tiles x 1 key block (Lkv 100), work 3 x 2 = 6
+    # sample 1: Lq 5 -> 1 tile x 3 key blocks (Lkv 300), work 3 x 2 = 6
+    # sample 2: Lq 0 -> no tile, work 0
+    # sample 3: Lq 129 -> 2 tiles x 1 block, work 2 x 2 = 4
+    # sorted (stable, descending): 0, 1, 3, 2; ranks 0, 1 (round 0), then 1, 0
+    qo = offsets_from_lengths([300, 5, 0, 129])
+    ko = offsets_from_lengths([100, 300, 10, 1])
+    rank, work = gd.shard_batch(qo, ko, 2, 2)
+    assert list(rank) == [0, 1, 0, 1]
+    assert list(work) == [6, 10]
+
+
+@pytest.mark.parametrize("cfg", CONFIGS, ids=[c.name for c in CONFIGS])
+@pytest.mark.parametrize("R", [1, 2, 3, 8])
+def test_shard_batch_matches_oracle(gd, cfg, R):
+    lq, lkv = draw_lengths(cfg)
+    qo, ko = offsets_from_lengths(lq), offsets_from_lengths(lkv)
+    rank, work = gd.shard_batch(qo, ko, cfg.H, R, cfg.mask, cfg.window)
+    want_rank, want_work = ref_planner.shard_samples(qo, ko, cfg.H, R, mask=cfg.mask,
+                                                     window=cfg.window)
+    assert list(rank) == list(want_rank)
+    assert list(work) == list(want_work)
+    # every sample's work lands on some rank, and every rank gets work when
+    # there are enough samples
+    assert work.sum() == sum(want_work)
+    if len(lq) >= R:
+        assert work.min() > 0
+
+
+def test_shard_rows_partition(gd):
+    c = small_case(5, B=11, H=1, d=1, q_range=(0, 90), kv_range=(0, 70), zero_lengths=True)
+    rank, _ = gd.shard_batch(c["q_off"], c["kv_off"], 1, 3)
+    seen_q, seen_k = [], []
+    for r in range(3):
+        lo, lk, qi, ki, mine = gd.shard_rows(c["q_off"], c["kv_off"], rank, r)
+        assert list(np.diff(lo)) == [int(c["q_off"][b + 1] - c["q_off"][b]) for b in mine]
+        assert list(np.diff(lk)) == [int(c["kv_off"][b + 1] - c["kv_off"][b]) for b in mine]
+        assert len(qi) == lo[-1] and len(ki) == lk[-1]
+        seen_q += list(qi)
+        seen_k += list(ki)
+    assert sorted(seen_q) == list(range(int(c["q_off"][-1])))
+    assert sorted(seen_k) == list(range(int(c["kv_off"][-1])))
+
+
+def test_shard_batch_refuses_bad_arguments(gd):
+    qo = offsets_from_lengths([3, 4])
+    with pytest.raises(gd.GdpaError):
+        gd.shard_batch(qo, qo, 1, 0)
+    with pytest.raises(gd.GdpaError):
+        gd.shard_batch(np.array([1, 2, 3]), qo, 1, 2)

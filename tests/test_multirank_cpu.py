@@ -1,18 +1,22 @@
-"""The benchmark's multi-rank logic on CPU with gloo, world size 2.
+"""The multi-rank path on CPU with gloo, world size 2.
 
-Each rank draws its own batch of the same shape (seeded by rank), plans it on
-the host with the C++ planner (no GPU), and the job's time is the maximum
-over ranks while its work is the sum: the only cross-rank steps of the path,
-which otherwise has no data exchange.  The one exchange of the sharded
-path, the shared seeds' gradient of pooling attention, is checked too: each
-rank's share (from the oracle) summed by the library's all-reduce equals the
-gradient of the whole batch.
+One batch is sharded over the ranks by the library's gdpa_shard_batch (its
+samples dealt by work in zigzag order); each rank runs its own samples as a
+batch of their own (here through the float64 oracle, the GPU kernels' stand-
+in on a CPU machine) and the outputs and gradients gathered from the ranks equal
+those of the whole batch exactly, because samples share nothing.  The job's
+time is the slowest rank's measured time and its work the sum of the ranks'
+(the benchmark's reduction).  The one exchange of the sharded path, the
+shared seeds' gradient of pooling attention, is checked too: each rank's share
+(from the oracle) summed by the library's all-reduce equals the gradient of
+the whole batch.
 """
 
 import json
 import os
 import socket
 import sys
+import time
 
 import numpy as np
 import pytest
@@ -26,47 +30,84 @@ def _free_port():
         return s.getsockname()[1]
 
 
-def _worker(rank, world, port, outdir):
+def _batch():
+    """A jagged batch with the training workload's length mix, small enough
+    for the float64 oracle."""
+    from workloads import draw_lengths, get_config, make_inputs
+    w = get_config("training_cross_fwd_bwd")
+    lq, lkv = draw_lengths(w)
+    lq, lkv = np.minimum(lq[:24], 300), lkv[:24]
+    x = make_inputs(w, device="cpu", seed=77, lengths=(lq, lkv))
+    return w, x
+
+
+def _shard_worker(rank, world, port, outdir):
     sys.path.insert(0, ROOT)
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
                       WORLD_SIZE=str(world))
+    import torch
     import torch.distributed as dist
     dist.init_process_group("gloo", rank=rank, world_size=world)
     import bench
     import recommender_model_attention_gb300 as gd
-    from workloads import draw_lengths, get_config, make_inputs
-    w = get_config("training_cross_fwd_bwd")
-    lq, lkv = draw_lengths(w)
-    lq, lkv = np.minimum(lq[:6], 300), lkv[:6]
-    x = make_inputs(w, device="cpu", seed=bench.rank_seed(w, rank), lengths=(lq, lkv))
-    plan = gd.Plan(x["q_off"], x["kv_off"], w.H, w.d, num_sms=152, host_only=True)
-    n_fwd, n_bwd, _ = plan.sizes()
-    pairs = bench.useful_pairs(x["q_off"], x["kv_off"], w.mask, w.window)
-    ms, flops = bench.reduce_across_ranks(10.0 + 5.0 * rank, 12.0 * w.d * w.H * pairs, "cpu")
-    sums = [None] * world
-    dist.all_gather_object(sums, float(x["q"].float().sum()))
+    from oracle import ref
+    w, x = _batch()
+    owner, work = gd.shard_batch(x["q_off"], x["kv_off"], w.H, world)
+    lo, lk, qi, ki, mine = gd.shard_rows(x["q_off"], x["kv_off"], owner, rank)
+    sub = [x[n].index_select(0, torch.from_numpy(idx)) for n, idx in
+           (("q", qi), ("k", ki), ("v", ki), ("do", qi))]
+    t0 = time.perf_counter()
+    o = ref.fwd(lo, lk, sub[0], sub[1], sub[2], w.alpha, w.act)
+    dq, dk, dv = ref.bwd(lo, lk, sub[0], sub[1], sub[2], sub[3], w.alpha, w.act)
+    ms = (time.perf_counter() - t0) * 1e3
+    flops = 12.0 * w.d * w.H * bench.useful_pairs(lo, lk, w.mask, w.window)
+    job_ms, job_flops = bench.reduce_across_ranks(ms, flops, "cpu")
+    times = [None] * world
+    dist.all_gather_object(times, (ms, flops))
+    np.savez(os.path.join(outdir, "shard%d.npz" % rank), o=o, dq=dq, dk=dk, dv=dv, qi=qi, ki=ki,
+             mine=mine)
     with open(os.path.join(outdir, "rank%d.json" % rank), "w") as f:
-        json.dump({"ms": ms, "flops": flops, "n_fwd": n_fwd, "n_bwd": n_bwd, "pairs": pairs,
-                   "q_sums": sums}, f)
+        json.dump({"job_ms": job_ms, "job_flops": job_flops, "times": times,
+                   "work": [int(v) for v in work]}, f)
     dist.destroy_process_group()
 
 
-def test_two_ranks_gloo(tmp_path):
+def test_sharded_batch_equals_whole_batch_gloo(tmp_path):
     torch = pytest.importorskip("torch")
     import torch.multiprocessing as mp
     pytest.importorskip("torch.distributed")
     import recommender_model_attention_gb300 as gd
+    from oracle import planner, ref
     gd.build()
     port = _free_port()
-    mp.spawn(_worker, args=(2, port, str(tmp_path)), nprocs=2, join=True)
-    r = [json.load(open(tmp_path / ("rank%d.json" % k))) for k in range(2)]
-    # same shape on both ranks (same plan sizes and work), different data
-    assert r[0]["n_fwd"] == r[1]["n_fwd"] and r[0]["n_bwd"] == r[1]["n_bwd"]
-    assert r[0]["q_sums"][0] != r[0]["q_sums"][1]
-    # job time = slowest rank, job work = sum over ranks, identical on every rank
-    for k in range(2):
-        assert r[k]["ms"] == 15.0
-        assert r[k]["flops"] == pytest.approx(2 * 12.0 * 128 * 8 * r[0]["pairs"])
+    mp.spawn(_shard_worker, args=(2, port, str(tmp_path)), nprocs=2, join=True)
+    w, x = _batch()
+    args = (x["q_off"], x["kv_off"], x["q"], x["k"], x["v"])
+    want_o = ref.fwd(*args, w.alpha, w.act)
+    want = ref.bwd(*args, x["do"], w.alpha, w.act)
+    got = {n: np.full_like(t, np.nan) for n, t in zip(("o", "dq", "dk", "dv"), (want_o,) + want)}
+    owners = []
+    for r in range(2):
+        z = np.load(tmp_path / ("shard%d.npz" % r))
+        owners.append(z["mine"])
+        for n, idx in (("o", "qi"), ("dq", "qi"), ("dk", "ki"), ("dv", "ki")):
+            got[n][z[idx]] = z[n]
+    # every sample on exactly one rank, both ranks busy, as the oracle deals
+    allb = np.sort(np.concatenate(owners))
+    assert np.array_equal(allb, np.arange(len(x["q_off"]) - 1))
+    assert all(len(o) > 0 for o in owners)
+    rank_ref, work_ref = planner.shard_samples(x["q_off"], x["kv_off"], w.H, 2)
+    assert all(rank_ref[b] == r for r in range(2) for b in owners[r])
+    # the gathered shards are the whole batch's result, bit for bit
+    for n, ref_t in zip(("o", "dq", "dk", "dv"), (want_o,) + want):
+        assert np.array_equal(got[n], ref_t), n
+    # job time = slowest rank, job work = sum of the ranks', on every rank
+    meta = [json.load(open(tmp_path / ("rank%d.json" % r))) for r in range(2)]
+    times = meta[0]["times"]
+    for m in meta:
+        assert m["job_ms"] == max(t[0] for t in times)
+        assert m["job_flops"] == pytest.approx(sum(t[1] for t in times))
+        assert m["work"] == work_ref
 
 
 def _seed_worker(rank, world, port, outdir):
