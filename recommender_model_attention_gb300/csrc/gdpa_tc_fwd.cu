@@ -518,7 +518,20 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
                             uint32_t sv[16], pk[8];
                             tmem_ld16(s_tmem + col0, sv);
                             tmem_ld_wait();
-                            if (prm.mask != GDPA_MASK_CAUSAL_WINDOW && col0 + 16 <= nvalid) {
+                            // the chunk's keys against the window of this
+                            // warp's 32 rows (warp-uniform): all valid, none
+                            // valid, or mixed (per-pair masks)
+                            const int jlo = jbase + col0, jhi = jlo + 15;
+                            bool all_valid = col0 + 16 <= nvalid, none_valid = false;
+                            if (prm.mask == GDPA_MASK_CAUSAL_WINDOW) {
+                                const int ilo = tile.i0 + quarter * 32, ihi = ilo + 31;
+                                all_valid = all_valid && jhi <= ilo && jlo > ihi - prm.window;
+                                none_valid = jlo > ihi || jhi <= ilo - prm.window;
+                            }
+                            if (none_valid) {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) pk[e] = 0u;
+                            } else if (all_valid) {
 #pragma unroll
                                 for (int e = 0; e < 16; e += 2)
                                     pk[e >> 1] = pack_bf16x2(act_s<ACT>(__uint_as_float(sv[e]), ksc),

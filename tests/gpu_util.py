@@ -3,12 +3,32 @@ and compare with the float64 oracle on the same inputs."""
 
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 from oracle import ref
 from workloads import make_inputs, small_case
 
 TOL = {"f32": 1e-5, "bf16": 1e-2}
+
+# Every checked error with its tolerance, for the end-of-run margin summary
+# (tests/conftest.py): (test id, quantity, max relative error, tolerance).
+MARGINS = []
+
+
+def record(errs, tol):
+    """Note each error of `errs` ({name: max relative error}) against `tol`."""
+    test = os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0]
+    for name, e in errs.items():
+        MARGINS.append((test, name, float(e), float(tol)))
+
+
+def check(errs, tol):
+    """Record, then assert every error is within `tol`."""
+    record(errs, tol)
+    for name, e in errs.items():
+        assert e <= tol, "%s: max rel err %.3e > %.1e (%s)" % (name, e, tol, errs)
 
 
 def max_rel(got, want) -> float:
@@ -96,5 +116,5 @@ def pick_samples(q_off, kv_off, n_random=4, seed=0):
     return sorted(set(picks))
 
 
-__all__ = ["TOL", "compare_full", "compare_sampled", "make_inputs", "max_rel", "pick_samples",
+__all__ = ["MARGINS", "TOL", "check", "compare_full", "record", "compare_sampled", "make_inputs", "max_rel", "pick_samples",
            "small_case", "to_dev"]

@@ -11,7 +11,7 @@ a side stream.
 import numpy as np
 import pytest
 
-from gpu_util import TOL, compare_full, to_dev
+from gpu_util import TOL, check, compare_full, to_dev
 from workloads import offsets_from_lengths
 
 pytestmark = pytest.mark.gpu
@@ -38,8 +38,7 @@ def _case(lq, lkv, H, d, seed):
 
 
 def _assert(errs, tol=TOL["bf16"]):
-    for name, e in errs.items():
-        assert e <= tol, "%s: max rel err %.3e > %.1e (%s)" % (name, e, tol, errs)
+    check(errs, tol)
 
 
 def test_zero_samples(gd):

@@ -14,7 +14,7 @@ import time
 import numpy as np
 import pytest
 
-from gpu_util import TOL, max_rel, small_case, to_dev
+from gpu_util import TOL, check, max_rel, small_case, to_dev
 from oracle import ref
 
 pytestmark = pytest.mark.gpu
@@ -66,15 +66,13 @@ def test_expired_wait_reports_timeout_and_plan_recovers(gd, which, d):
     if which == "fwd":
         o = gd.gdpa_fwd(plan, c["q"], c["k"], c["v"], alpha=alpha, act="gelu_erf")
         plan.check()
-        err = max_rel(ref.to_f64(o), ref.fwd(*args, alpha, "gelu_erf"))
-        assert err <= TOL["bf16"], err
+        check({"o": max_rel(ref.to_f64(o), ref.fwd(*args, alpha, "gelu_erf"))}, TOL["bf16"])
     else:
         grads = gd.gdpa_bwd(plan, c["q"], c["k"], c["v"], c["do"], alpha=alpha, act="gelu_erf")
         plan.check()
         want = ref.bwd(*args, c["do"], alpha, "gelu_erf")
-        for name, g, w in zip(("dq", "dk", "dv"), grads, want):
-            err = max_rel(ref.to_f64(g), w)
-            assert err <= TOL["bf16"], (name, err)
+        check({name: max_rel(ref.to_f64(g), w) for name, g, w in zip(("dq", "dk", "dv"), grads, want)},
+              TOL["bf16"])
     plan.check()
     plan.destroy()
     torch.cuda.synchronize()
@@ -104,9 +102,8 @@ def test_destroy_does_not_wait_for_other_streams(gd):
     o = gd.gdpa_fwd(plan, c["q"], c["k"], c["v"], alpha=alpha, act="silu")
     plan.destroy()   # returns at once; the forward still reads the plan
     torch.cuda.synchronize()
-    err = max_rel(ref.to_f64(o), ref.fwd(c["q_off"], c["kv_off"], c["q"], c["k"], c["v"], alpha,
-                                         "silu"))
-    assert err <= TOL["bf16"], err
+    check({"o": max_rel(ref.to_f64(o), ref.fwd(c["q_off"], c["kv_off"], c["q"], c["k"], c["v"],
+                                                 alpha, "silu"))}, TOL["bf16"])
     side = torch.cuda.Stream()
     big = torch.randn(4096, 4096, device="cuda")
     torch.cuda.synchronize()

@@ -11,7 +11,7 @@ the tensor-core kernel and the CUDA-core path.
 import numpy as np
 import pytest
 
-from gpu_util import TOL, compare_full, compare_sampled, pick_samples, small_case, to_dev
+from gpu_util import TOL, check, compare_full, compare_sampled, pick_samples, small_case, to_dev
 from workloads import get_config, make_inputs, offsets_from_lengths
 
 pytestmark = pytest.mark.gpu
@@ -28,8 +28,7 @@ def gd():
 
 
 def _assert(errs, tol):
-    for name, e in errs.items():
-        assert e <= tol, "%s: max rel err %.3e > %.1e (%s)" % (name, e, tol, errs)
+    check(errs, tol)
 
 
 def _case(lq, lkv, H, d, seed, dtype="bf16", scale=1.0):

@@ -9,7 +9,7 @@ dK and dV separately.  Plans must match the oracle's planner bit for bit.
 import numpy as np
 import pytest
 
-from gpu_util import TOL, compare_full, compare_sampled, max_rel, pick_samples, small_case, to_dev
+from gpu_util import TOL, check, compare_full, compare_sampled, max_rel, pick_samples, small_case, to_dev
 from oracle import planner as ref_planner
 from oracle import ref
 from workloads import CONFIGS, get_config, make_inputs
@@ -31,8 +31,7 @@ def gd():
 
 
 def _assert(errs, tol):
-    for name, e in errs.items():
-        assert e <= tol, "%s: max rel err %.3e > %.1e (%s)" % (name, e, tol, errs)
+    check(errs, tol)
 
 
 def test_device_plan_matches_oracle(gd):

@@ -11,7 +11,7 @@ bf16 tolerance as everywhere: 1e-2 of max|ref| per output.
 import numpy as np
 import pytest
 
-from gpu_util import TOL, max_rel, to_dev
+from gpu_util import TOL, check, max_rel, to_dev
 from oracle import ref
 from workloads import offsets_from_lengths
 
@@ -47,8 +47,7 @@ def _oracle(x, n_seeds, alpha, act):
 
 
 def _assert(errs, tol=TOL["bf16"]):
-    for name, e in errs.items():
-        assert e <= tol, "%s: max rel err %.3e > %.1e (%s)" % (name, e, tol, errs)
+    check(errs, tol)
 
 
 # 32 seeds; samples of 32 queries (the pooling shape), shorter ones, an

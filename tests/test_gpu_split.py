@@ -18,7 +18,7 @@ forward, whose normalisation couples the chunks, refuses split plans.
 import numpy as np
 import pytest
 
-from gpu_util import TOL, compare_full, max_rel, to_dev
+from gpu_util import TOL, check, compare_full, max_rel, to_dev
 from oracle import ref
 from workloads import offsets_from_lengths
 
@@ -47,8 +47,7 @@ def _case(lq, lkv, H, d, seed, dtype="bf16"):
 
 
 def _assert(errs, tol=TOL["bf16"]):
-    for name, e in errs.items():
-        assert e <= tol, "%s: max rel err %.3e > %.1e (%s)" % (name, e, tol, errs)
+    check(errs, tol)
 
 
 # few query rows against long key sequences (the pooling-attention shape),

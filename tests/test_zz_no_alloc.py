@@ -13,7 +13,7 @@ import ctypes
 import numpy as np
 import pytest
 
-from gpu_util import TOL, max_rel, small_case, to_dev
+from gpu_util import TOL, check, max_rel, small_case, to_dev
 from oracle import ref
 
 pytestmark = pytest.mark.gpu
@@ -75,7 +75,7 @@ def test_noalloc_matches_planned_forward_on_consecutive_calls(gd):
         ref_err = max_rel(want.double().cpu().numpy(),
                           ref.fwd(c["q_off"], c["kv_off"], c["q"], c["k"], c["v"],
                                   case["d"] ** -0.5, case["act"], case["mask"], case["window"]))
-        assert ref_err <= TOL["bf16"], ref_err
+        check({"o": ref_err}, TOL["bf16"])
         for _ in range(2):
             o = torch.full_like(c["q"], float("nan"))
             st = _call(gd, c, case["H"], case["d"], case["act"], case["mask"], case["window"], o)
