@@ -43,8 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the unsplit softmax-free kernels; otherwise reported null.
 TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
-    "gdpa_fwd": ("6058eb4427101988", 0.9644),
-    "gdpa_bwd": ("1a629a4e0115a790", 1.0207),
+    "gdpa_fwd": ("e11c01230c7efa3b", 0.9673),
+    "gdpa_bwd": ("30888e988d692ae0", 1.0268),
 }
 KERNEL_SOURCES = {
     "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh"),
