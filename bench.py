@@ -356,6 +356,9 @@ def main():
     ap.add_argument("--materialise-q", action="store_true",
                     help="shared-query workloads: pass Q replicated per sample instead of "
                          "the seed rows (shared-query mode)")
+    ap.add_argument("--qk-norm", type=float, default=0.0,
+                    help="fused RMSNorm of the Q and K rows inside the kernels with this gain "
+                         "(eps 1e-6); 0 = off")
     ap.add_argument("--act", default=None,
                     help="override the workload's activation; 'softmax' times the softmax "
                          "variant (Jagged Flash Attention) on the same batch")
@@ -419,6 +422,8 @@ def main():
                     max_kv_blocks=mkb, **kw)
         if n_seeds:
             p.set_shared_q(n_seeds)
+        if args.qk_norm > 0:
+            p.set_qk_norm(args.qk_norm, 1e-6)
         return p
 
     plan = make_plan()
@@ -680,6 +685,7 @@ def main():
             "data": "synthetic (seeded lengths and RMSNorm'd N(0,1) inputs, random dO)",
             "config": {"workload": w.name, "B": len(x["q_off"]) - 1, "H": w.H, "d": w.d,
                        "act": w.act, "max_kv_blocks": mkb, "sched": args.sched,
+                       "qk_norm": args.qk_norm,
                        "key_split": key_split, "shared_q": n_seeds,
                        "Tq": Tq, "Tkv": Tkv, "useful_pairs": pairs,
                        "l2": "inputs larger than L2 (%.1f GB resident)" % (input_bytes / 1e9),

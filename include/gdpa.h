@@ -262,6 +262,29 @@ gdpa_status gdpa_plan_set_kernel(gdpa_plan plan, gdpa_kernel kernel);
  */
 gdpa_status gdpa_plan_set_shared_q(gdpa_plan plan, int n_seeds);
 
+/*
+ * Fused RMSNorm prologue (the GDPA page: RMSNorm keeps the activation's
+ * inputs in range, the caption under its Taylor code; GEM page, section on
+ * why GPU utilisation is hard for recommendation models: normalisation is a
+ * memory-bound pass of its own).  gain > 0: the q and k given to gdpa_fwd,
+ * gdpa_bwd, gdpa_softmax_fwd and gdpa_softmax_bwd on this plan are the raw
+ * rows, and every (token, head) row of Q and K is normalised inside the
+ * kernels,
+ *     y = gain x / sqrt(mean(x^2) + eps),
+ * before it enters the attention; V is used as given.  The backward's dq and
+ * dk are then the gradients with respect to the raw rows,
+ *     dL/dx = (gain / r) (dy - x (x . dy) / (d r^2)),  r = sqrt(mean(x^2) + eps).
+ * The kernels never write the normalised rows: they scale the scores of the
+ * raw rows by c_i c_j (c = gain / r of the query and key row), and the
+ * gradients likewise.  Each launch first computes the keys' c (one pass over
+ * K into a plan-owned [H][Tkv + 128] float workspace, allocated on first
+ * use).  Tensor-core kernels only (bf16, d = 64 or 128): the CUDA-core path
+ * returns UNSUPPORTED while it is on; gdpa_fwd_noalloc has no such mode.
+ * gain = 0 turns it off.  INVALID_ARG for a negative or NaN gain or eps, or
+ * eps = 0 with gain > 0 (an all-zero row would divide by zero).
+ */
+gdpa_status gdpa_plan_set_qk_norm(gdpa_plan plan, float gain, float eps);
+
 /* Record per-CTA start/end times (%globaltimer, ns) and SM ids on the next
  * launches (enable != 0), readable with gdpa_sm_times. */
 gdpa_status gdpa_plan_set_timing(gdpa_plan plan, int enable);

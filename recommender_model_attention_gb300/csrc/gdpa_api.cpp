@@ -63,7 +63,7 @@ void free_plan(Plan* p) {
             for (const gdpa::StreamEvent& w : p->work) cudaStreamWaitEvent(fs, w.event, 0);
         }
         void* bufs[] = {p->d_fwd, p->d_fwd_seg, p->d_bwd, p->d_bwd_seg, p->d_err,
-                        p->d_times, p->d_smid, p->d_delta, p->d_wsplit};
+                        p->d_times, p->d_smid, p->d_delta, p->d_wsplit, p->d_kscale};
         for (void* b : bufs)
             if (b) cudaFreeAsync(b, fs);
         for (const gdpa::StreamEvent& w : p->work) cudaEventDestroy(w.event);
@@ -276,6 +276,15 @@ gdpa_status gdpa_plan_set_shared_q(gdpa_plan plan, int n_seeds) {
     return GDPA_OK;
 }
 
+gdpa_status gdpa_plan_set_qk_norm(gdpa_plan plan, float gain, float eps) {
+    if (!plan || !(gain >= 0.0f) || !(eps >= 0.0f)) return GDPA_ERR_INVALID_ARG;
+    Plan& p = *(Plan*)plan;
+    if (gain > 0.0f && eps == 0.0f) return GDPA_ERR_INVALID_ARG;   // rows of zeros
+    p.qk_gain = gain;
+    p.qk_eps = eps;
+    return GDPA_OK;
+}
+
 gdpa_status gdpa_plan_set_timing(gdpa_plan plan, int enable) {
     if (!plan) return GDPA_ERR_INVALID_ARG;
     ((Plan*)plan)->timing = enable ? 1 : 0;
@@ -306,6 +315,8 @@ gdpa_status fwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const vo
     if (p.fwd_split && act == GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
     const bool tc =
         use_tc(p, dtype) && !(p.fwd_split && p.d != 128 && p.kernel == GDPA_KERNEL_AUTO);
+    // the fused RMSNorm runs in the tensor-core kernels only
+    if (p.qk_gain > 0.0f && !tc) return GDPA_ERR_UNSUPPORTED;
     if (gdpa_status bs = begin_work(p, st)) return bs;
     const gdpa_status s = tc ? gdpa::launch_tc_fwd(p, q, k, v, o, lse, alpha, act, st)
                              : gdpa::launch_simt_fwd(p, dtype, q, k, v, o, lse, alpha, act, st);
@@ -332,6 +343,7 @@ gdpa_status bwd_common(gdpa_plan plan, gdpa_dtype dtype, const void* q, const vo
     if (gdpa_status ds = check_device(p)) return ds;
     cudaStream_t st = (cudaStream_t)stream;
     if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
+    if (p.qk_gain > 0.0f && !use_tc(p, dtype)) return GDPA_ERR_UNSUPPORTED;
     if (gdpa_status bs = begin_work(p, st)) return bs;
     const float* delta = nullptr;
     gdpa_status s = GDPA_OK;

@@ -81,6 +81,10 @@ struct Plan {
     // load so that a wait expires
     uint32_t wait_limit_us = 0;
     int stall = 0;
+    // fused RMSNorm of Q and K rows (gain > 0 enables): the keys' g / rms in
+    // a [H][Tkv + 128] float workspace, refreshed by every launch
+    float qk_gain = 0.0f, qk_eps = 0.0f;
+    float* d_kscale = nullptr;
     // softmax-variant backward: dO_t . O_t per row and head, [Tq][H] float,
     // allocated on first use
     float* d_delta = nullptr;
@@ -114,10 +118,20 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
                               int64_t Tkv, int mask, int window, const void* q, int64_t q_rows,
                               int shared_q, const void* k, const void* v, void* o, float* lse,
                               float* w, float alpha, int act, cudaStream_t st,
-                              uint32_t wait_limit_us = 0, int stall = 0);
+                              uint32_t wait_limit_us = 0, int stall = 0,
+                              const float* kscale = nullptr, int64_t kscale_ld = 0,
+                              float qk_gain = 0.0f, float qk_eps = 0.0f);
 gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, const void* d_o,
                           float* dq, float* dk, float* dv, float alpha, int act, const float* lse,
                           const float* delta, cudaStream_t st);
+// Fused RMSNorm: out[h][t] = gain / sqrt(mean(x[t][h][:]^2) + eps) for rows
+// t < rows of a bf16 [rows][H][d] tensor (the plan's key-scale workspace,
+// leading dimension ld).
+gdpa_status launch_row_scale(const Plan& p, const void* x, int64_t rows, float* out, int64_t ld,
+                             cudaStream_t st);
+// The plan's key scales for `k` (workspace allocated on first use, stream
+// ordered); returns the workspace or NULL (status in *s).
+float* plan_key_scales(Plan& p, const void* k, cudaStream_t st, gdpa_status* s);
 // delta[t][h] = dO[t][h][:] . O[t][h][:] over rows t < Tq (softmax variant)
 gdpa_status launch_row_dot(Plan& p, gdpa_dtype dt, const void* d_o, const void* o, float* delta,
                            cudaStream_t st);

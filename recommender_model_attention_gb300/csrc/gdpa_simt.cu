@@ -393,4 +393,59 @@ gdpa_status launch_row_dot(Plan& p, gdpa_dtype dt, const void* d_o, const void* 
     return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
 }
 
+namespace {
+
+// one warp per (token, head) row: gain / rms of the row
+__global__ void __launch_bounds__(256)
+row_scale_kernel(const __nv_bfloat16* __restrict__ x, float* __restrict__ out, int64_t rows,
+                 int H, int d, int64_t ld, float gain, float eps) {
+    const int64_t rw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (rw >= rows * H) return;
+    const __nv_bfloat16* p = x + rw * d;
+    float ss = 0.0f;
+    for (int c = lane; c < d; c += 32) {
+        const float v = __bfloat162float(p[c]);
+        ss = fmaf(v, v, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) {
+        const int64_t t = rw / H, h = rw % H;
+        out[h * ld + t] = gain / sqrtf(ss / (float)d + eps);
+    }
+}
+
+}  // namespace
+
+gdpa_status launch_row_scale(const Plan& p, const void* x, int64_t rows, float* out, int64_t ld,
+                             cudaStream_t st) {
+    if (rows == 0) return GDPA_OK;
+    const int64_t n = rows * p.H;
+    row_scale_kernel<<<(unsigned)((n + 7) / 8), 256, 0, st>>>((const __nv_bfloat16*)x, out, rows,
+                                                              p.H, p.d, ld, p.qk_gain, p.qk_eps);
+    return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+float* plan_key_scales(Plan& p, const void* k, cudaStream_t st, gdpa_status* s) {
+    const int64_t ld = p.Tkv + 128;   // padding read (masked) past a sample's last key
+    const size_t bytes = (size_t)p.H * ld * sizeof(float);
+    *s = GDPA_OK;
+    if (!p.d_kscale) {
+        if (cudaMallocAsync((void**)&p.d_kscale, bytes, st) != cudaSuccess) {
+            p.d_kscale = nullptr;
+            *s = GDPA_ERR_ALLOC;
+            return nullptr;
+        }
+        if (cudaMemsetAsync(p.d_kscale, 0, bytes, st) != cudaSuccess) {
+            *s = GDPA_ERR_CUDA;
+            return nullptr;
+        }
+    }
+    *s = launch_row_scale(p, k, p.Tkv, p.d_kscale, ld, st);
+    if (*s != GDPA_OK) return nullptr;
+    p.launches += 1;
+    return p.d_kscale;
+}
+
 }  // namespace gdpa

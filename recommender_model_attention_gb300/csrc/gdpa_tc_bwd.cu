@@ -61,7 +61,8 @@ struct BwdCfg {
     static constexpr int kOffQ = kOffV + kTileBytes;          // 2 stages
     static constexpr int kOffDO = kOffQ + 2 * kTileBytes;     // 2 stages
     static constexpr int kOffPS = kOffDO + 2 * kTileBytes;    // P / dS / staging
-    static constexpr int kOffBar = kOffPS + 128 * 128 * 2;
+    static constexpr int kOffDot = kOffPS + 128 * 128 * 2;    // fused RMSNorm: [2][128] f32
+    static constexpr int kOffBar = kOffDot + 2 * 128 * 4;
     enum {
         kKVFull = 0, kKVEmpty, kQFull, kQFull1, kQEmpty, kQEmpty1, kDOFull, kDOFull1, kDOEmpty,
         kDOEmpty1, kSDFull, kSFree, kDQFree, kPFull, kPVDone, kDSFull, kDKDone, kAccFull,
@@ -89,6 +90,11 @@ struct BwdParams {
     int timing;
     uint64_t wait_ns;     // bounded-wait limit
     int stall;            // test hook: CTA 0 skips its first Q load
+    // fused RMSNorm of Q and K (or NULL): g / rms of every key row, [H][ld]
+    // floats; gain and eps for the query rows computed in the kernel
+    const float* kscale;
+    int64_t kscale_ld;
+    float qk_gain, qk_eps;
 };
 
 __device__ __forceinline__ BwdUnit load_unit(const BwdUnit* p) {
@@ -241,7 +247,9 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             mma_commit(&bars[C::kDOEmpty + s]);
             if (last) {
                 mma_commit(&bars[C::kAccFull]);
-                mma_commit(&bars[C::kKVEmpty]);
+                // the fused RMSNorm's dK drain still reads K: warpgroup 1
+                // hands the stage back then
+                if (!prm.kscale) mma_commit(&bars[C::kKVEmpty]);
             } else if (!issue_dp(i + 1)) {   // once this tile's dQ is drained
                 goto drain;
             }
@@ -275,6 +283,137 @@ __device__ __forceinline__ void store_half_chunk(uint8_t* ps, int c, int hh, int
     }
 }
 
+// Fused RMSNorm: the drain of a row's gradient with respect to the
+// normalised row, dy = TMEM value (times alpha for dQ and dK), into the
+// gradient with respect to the raw row x,
+//     dx = c (dy - x (x . dy) c^2 / (d g^2)),   c = g / rms(x),
+// i.e. out = sc (v - kappa x) with sc = alpha c and kappa = (x . v) c^2 /
+// (d g^2).  Columns [col, col + 32 P) of this warp's 32 lanes; x holds the
+// thread's row's raw values of those columns (packed bf16 pairs, read before
+// the staging may overwrite them); staging and stores as drain_warp.
+template <int P>
+static __device__ __noinline__ void drain_warp_norm(uint32_t trow, uint32_t col, uint8_t* stage,
+                                                    const CUtensorMap* map, int x0, int y0,
+                                                    float* dst, int64_t rs, int nrows, bool atomic,
+                                                    float sc, float kappa,
+                                                    const uint32_t (&x)[16 * P], int quarter,
+                                                    int lane, uint64_t* release) {
+    const int row0 = quarter * 32;
+    const bool any = row0 < nrows;
+    const bool full = row0 + 32 <= nrows;
+    uint8_t* wst = stage + quarter * 4096;
+#pragma unroll
+    for (int pass = 0; pass < P; ++pass) {
+        uint32_t v[32];
+        if (any) {
+            tmem_ld32(trow + col + pass * 32, v);
+            tmem_ld_wait();
+        }
+        if (pass == P - 1 && release) {
+            tc_fence_before();
+            mbar_arrive(release);
+        }
+        if (!any) continue;
+        float o[32];
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            const uint32_t w = x[16 * pass + e / 2];
+            o[e] = sc * fmaf(-kappa, bf16_lo(w), __uint_as_float(v[e]));
+            o[e + 1] = sc * fmaf(-kappa, bf16_hi(w), __uint_as_float(v[e + 1]));
+        }
+        if (full) {
+            if (pass > 0) {
+                if (lane == 0) bulk_wait_read_all();
+                __syncwarp();
+            }
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<float4*>(wst + lane * 128 + ((c ^ (lane & 7)) << 4)) =
+                    make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                if (atomic)
+                    tma_reduce_add_2d(map, wst, x0 + pass * 32, y0 + row0);
+                else
+                    tma_store_2d(map, wst, x0 + pass * 32, y0 + row0);
+                bulk_commit();
+            }
+        } else if (row0 + lane < nrows) {
+            float* d = dst + (int64_t)(row0 + lane) * rs + pass * 32;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float4 w = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                if (atomic)
+                    atomicAdd(reinterpret_cast<float4*>(d + 4 * c), w);
+                else
+                    *reinterpret_cast<float4*>(d + 4 * c) = w;
+            }
+        }
+    }
+}
+
+// x . v over columns [col, col + 32 P) of this warp's lanes (TMEM) and the
+// row's raw values x (packed bf16 pairs).
+template <int P>
+__device__ __forceinline__ float row_dot_tmem(uint32_t trow, uint32_t col, const uint32_t (&x)[16 * P]) {
+    float dot = 0.0f;
+#pragma unroll
+    for (int pass = 0; pass < P; ++pass) {
+        uint32_t v[32];
+        tmem_ld32(trow + col + pass * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+            const uint32_t w = x[16 * pass + e / 2];
+            dot = fmaf(bf16_lo(w), __uint_as_float(v[e]), dot);
+            dot = fmaf(bf16_hi(w), __uint_as_float(v[e + 1]), dot);
+        }
+    }
+    return dot;
+}
+
+// The dQ tile's drain with the RMSNorm Jacobian: the row dot x . dQ over all
+// d columns (each warpgroup's 64, exchanged through `dotx`, [2][128] floats,
+// when d = 128), then the transformed drain.  x: the tile's raw Q (its
+// consumed stage, which the drain then uses as staging).
+template <int D>
+static __device__ __noinline__ void drain_dq_norm(uint32_t trow, int wg, int r, const uint8_t* qtile,
+                                                  float* dotx, uint8_t* stage, const CUtensorMap* map,
+                                                  int x0, int y0, float* dst, int64_t rs, int nrows,
+                                                  bool atomic, float alpha, float ci, float gain,
+                                                  int quarter, int lane, uint64_t* release) {
+    uint32_t xq[32];
+    load_row_bf16<2>(qtile, r, 64 * wg, xq);
+    float dot = row_dot_tmem<2>(trow, kColDP + 64 * wg, xq);
+    if (D == 128) {
+        dotx[wg * 128 + r] = dot;
+        named_bar_sync(1, 256);
+        dot += dotx[(1 - wg) * 128 + r];
+    }
+    const float kappa = dot * ci * ci / ((float)D * gain * gain);
+    drain_warp_norm<2>(trow, kColDP + 64 * wg, stage, map, x0, y0, dst, rs, nrows, atomic, alpha * ci,
+                       kappa, xq, quarter, lane, release);
+}
+
+// The unit's dK drain with the RMSNorm Jacobian (warpgroup 1): the key row's
+// raw values from the K stage, which then goes back to the producer
+// (`kv_empty`), the row dot, the transformed drain.
+template <int D>
+static __device__ __noinline__ void drain_dk_norm(uint32_t trow, int r, const uint8_t* ktile,
+                                                  uint8_t* stage, const CUtensorMap* map, int x0,
+                                                  int y0, float* dst, int64_t rs, int nrows,
+                                                  float alpha, float cj, float gain, int quarter,
+                                                  int lane, uint64_t* kv_empty, uint64_t* release) {
+    uint32_t xk[D / 2];
+    load_row_bf16<D / 32>(ktile, r, 0, xk);
+    mbar_arrive(kv_empty);
+    const float dot = row_dot_tmem<D / 32>(trow, kColDK, xk);
+    const float kappa = dot * cj * cj / ((float)D * gain * gain);
+    drain_warp_norm<D / 32>(trow, kColDK, stage, map, x0, y0, dst, rs, nrows, false, alpha * cj,
+                            kappa, xk, quarter, lane, release);
+}
+
 // P and dS of one pair from its score s and dP: GDPA, P = act(alpha s) and
 // dS = dP act'(alpha s); the softmax variant, P = exp(alpha s - lse) (in base
 // 2 with lse2 = lse log2 e) and dS = P (dP - D), lse2 and D being the row's.
@@ -291,7 +430,7 @@ __device__ __forceinline__ void bwd_p_ds(float s, float dp, const ActScale& k, f
     }
 }
 
-template <int D, int ACT>
+template <int D, int ACT, bool NORM>
 __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const CUtensorMap* tmDK,
                             const CUtensorMap* tmDV, uint8_t* smem, uint64_t* bars, uint32_t tmem,
                             int seg0, int seg1, const Abort& ab) {
@@ -360,6 +499,15 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             if (m == u.m0 && nu > 0 && !wg_wait(&bars[C::kPSFree], (nu - 1) & 1, ab, 47)) return;
             if (!wg_wait(&bars[C::kPVDone], (i & 1) ^ 1, ab, 44)) return;
             tc_fence_after();
+            // fused RMSNorm: this row's scale from the tile's raw Q
+            float ci = 1.0f;
+            const float* kscale = nullptr;
+            if constexpr (NORM) {
+                if (!wg_wait(&bars[C::kQFull + (i & 1)], (i >> 1) & 1, ab, 42)) return;
+                ci = row_scale<D>(smem + C::kOffQ + (i & 1) * C::kTileBytes, r, prm.qk_gain,
+                                  prm.qk_eps);
+                kscale = prm.kscale + (int64_t)h * prm.kscale_ld + u.kvt0;
+            }
             uint32_t pp[4][8];
             if (warp_rows) {
 #pragma unroll
@@ -371,6 +519,7 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                         tmem_ld16(trow + kColS + col0, sv);
                         tmem_ld16(trow + kColDP + col0, dv);
                         tmem_ld_wait();
+                        if constexpr (NORM) scale_step(sv, ci, kscale + col0);
                         const bool full = !windowed && col0 + 16 <= u.nkv;
                         if (!row_ok) {
 #pragma unroll
@@ -407,10 +556,26 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                                 pd[e >> 1] = pack_bf16x2(d2[0], d2[1]);
                             }
                         }
-                        store_half_chunk(ps, sidx >> 1, sidx & 1, r, pd);
-                        // and packed into the step's own S columns (already
-                        // read), the A operand of dQ = dS K
-                        tmem_st8(trow + kColS + col0, pd);
+                        if constexpr (NORM) {
+                            // dK = dS^T Q of the normalised Q rows: dS times
+                            // the row's c into shared memory; dQ = dS K of the
+                            // normalised keys: dS times each key's c into TMEM
+                            uint32_t pdk[8];
+#pragma unroll
+                            for (int e = 0; e < 16; e += 2) {
+                                const float d0 = bf16_lo(pd[e >> 1]), d1 = bf16_hi(pd[e >> 1]);
+                                pdk[e >> 1] = pack_bf16x2(d0 * __ldg(kscale + col0 + e),
+                                                          d1 * __ldg(kscale + col0 + e + 1));
+                                pd[e >> 1] = pack_bf16x2(d0 * ci, d1 * ci);
+                            }
+                            store_half_chunk(ps, sidx >> 1, sidx & 1, r, pd);
+                            tmem_st8(trow + kColS + col0, pdk);
+                        } else {
+                            store_half_chunk(ps, sidx >> 1, sidx & 1, r, pd);
+                            // and packed into the step's own S columns
+                            // (already read), the A operand of dQ = dS K
+                            tmem_st8(trow + kColS + col0, pd);
+                        }
                     }
                 }
                 tmem_st_wait();
@@ -436,7 +601,18 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             tc_fence_after();
             float* dq = prm.dQ + (int64_t)(dq_row0 + m * kBM) * rs + h * D;
             uint8_t* dq_stage = smem + C::kOffQ + (i & 1) * C::kTileBytes + wg * kHalfBytes;
-            if (D == 128 || wg == 0) {
+            if constexpr (NORM) {
+                if (D == 128 || wg == 0) {
+                    drain_dq_norm<D>(trow, wg, r, smem + C::kOffQ + (i & 1) * C::kTileBytes,
+                                     reinterpret_cast<float*>(smem + C::kOffDot), dq_stage, tmDQ,
+                                     h * D + 64 * wg, dq_row0 + m * kBM, dq + 64 * wg, rs, nq,
+                                     atomic_dq, prm.alpha, ci, prm.qk_gain, quarter, lane,
+                                     &bars[C::kDQFree]);
+                } else {
+                    tc_fence_before();
+                    mbar_arrive(&bars[C::kDQFree]);
+                }
+            } else if (D == 128 || wg == 0) {
                 drain_warp(trow, kColDP + 64 * wg, 64, dq_stage, tmDQ, h * D + 64 * wg,
                            dq_row0 + m * kBM, dq + 64 * wg, rs, nq, atomic_dq, prm.alpha, quarter,
                            lane, &bars[C::kDQFree]);
@@ -456,9 +632,17 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
         }
         {
             float* dst = (wg == 0 ? prm.dV : prm.dK) + (int64_t)u.kvt0 * rs + h * D;
-            drain_warp(trow, wg == 0 ? kColDV : kColDK, D, stage, wg == 0 ? tmDV : tmDK, h * D,
-                       u.kvt0, dst, rs, u.nkv, false, wg == 0 ? 1.0f : prm.alpha, quarter, lane,
-                       &bars[C::kAccFree]);
+            if (NORM && wg == 1) {
+                const float cj = r < u.nkv ? __ldg(prm.kscale + (int64_t)h * prm.kscale_ld + u.kvt0 + r)
+                                           : 0.0f;
+                drain_dk_norm<D>(trow, r, smem + C::kOffK, stage, tmDK, h * D, u.kvt0, dst, rs,
+                                 u.nkv, prm.alpha, cj, prm.qk_gain, quarter, lane,
+                                 &bars[C::kKVEmpty], &bars[C::kAccFree]);
+            } else {
+                drain_warp(trow, wg == 0 ? kColDV : kColDK, D, stage, wg == 0 ? tmDV : tmDK, h * D,
+                           u.kvt0, dst, rs, u.nkv, false, wg == 0 ? 1.0f : prm.alpha, quarter,
+                           lane, &bars[C::kAccFree]);
+            }
             staging_release_wait(lane);
             mbar_arrive(&bars[C::kPSFree]);
         }
@@ -466,7 +650,7 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
     }
 }
 
-template <int D, int ACT>
+template <int D, int ACT, bool NORM>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -484,7 +668,7 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     if (threadIdx.x == 0) {
         t_start = globaltimer();
         const uint32_t counts[C::kNumBars] = {
-            1, 1,                 // kv full / empty
+            1, NORM ? 128u : 1u,  // kv full / empty (fused RMSNorm: warpgroup 1 after dK)
             1, 1, 256, 256,       // q full x2, q empty x2 (warpgroups, after dQ staging)
             1, 1, 1, 1,           // dO full x2, dO empty x2
             1, 256, 256,          // sd full, s free, dq free
@@ -517,7 +701,7 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         bwd_mma<D>(prm, smem, bars, tmem, seg0, seg1, ab);   // the whole warp
         __syncwarp();
     } else {
-        bwd_compute<D, ACT>(prm, &tmDQ, &tmDK, &tmDV, smem, bars, tmem, seg0, seg1, ab);
+        bwd_compute<D, ACT, NORM>(prm, &tmDQ, &tmDK, &tmDV, smem, bars, tmem, seg0, seg1, ab);
         // every bulk store of this warp has landed before the CTA retires
         if (lane == 0) bulk_wait_all();
         __syncwarp();
@@ -536,10 +720,10 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
 }
 
-template <int D, int ACT>
-gdpa_status launch(Plan& p, const CUtensorMap* maps, const BwdParams& prm, cudaStream_t st) {
+template <int D, int ACT, bool NORM>
+gdpa_status launch1(Plan& p, const CUtensorMap* maps, const BwdParams& prm, cudaStream_t st) {
     using C = BwdCfg<D>;
-    auto kern = tc_bwd_kernel<D, ACT>;
+    auto kern = tc_bwd_kernel<D, ACT, NORM>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return GDPA_ERR_CUDA;
@@ -547,6 +731,12 @@ gdpa_status launch(Plan& p, const CUtensorMap* maps, const BwdParams& prm, cudaS
                                                 maps[5], maps[6], prm);
     p.launches += 1;
     return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+template <int D, int ACT>
+gdpa_status launch(Plan& p, const CUtensorMap* maps, const BwdParams& prm, cudaStream_t st) {
+    return prm.kscale ? launch1<D, ACT, true>(p, maps, prm, st)
+                      : launch1<D, ACT, false>(p, maps, prm, st);
 }
 
 }  // namespace
@@ -596,6 +786,15 @@ gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, 
     prm.timing = p.timing;
     prm.wait_ns = tc::wait_limit_ns(p.wait_limit_us);
     prm.stall = p.stall;
+    prm.kscale = nullptr;
+    prm.kscale_ld = p.Tkv + 128;
+    prm.qk_gain = p.qk_gain;
+    prm.qk_eps = p.qk_eps;
+    if (p.qk_gain > 0.0f) {   // fused RMSNorm: the keys' scales first
+        gdpa_status ks;
+        prm.kscale = plan_key_scales(p, k, st, &ks);
+        if (ks != GDPA_OK) return ks;
+    }
     if (p.timing) p.timed[1] = 1;
     gdpa_status s = GDPA_OK;
     if (p.d == 128) {

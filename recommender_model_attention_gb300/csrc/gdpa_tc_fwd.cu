@@ -101,6 +101,11 @@ struct FwdParams {
     int timing;
     uint64_t wait_ns;   // bounded-wait limit
     int stall;          // test hook: CTA 0 skips its first Q load
+    // fused RMSNorm of Q and K (or NULL): g / rms of every key row, [H][ld]
+    // floats, and the gain and eps applied to the query rows in the kernel
+    const float* kscale;
+    int64_t kscale_ld;
+    float qk_gain, qk_eps;
 };
 
 __device__ __forceinline__ FwdTile load_tile(const FwdTile* p) {
@@ -344,7 +349,7 @@ template <int D>
 __device__ float softmax_tile(const FwdTile& tile, const FwdParams& prm, uint64_t* bars,
                               uint32_t& s_use, uint32_t& x_use, uint32_t s_tmem,
                               uint32_t o_tmem_part0, int wg, int part, int r, bool warp_rows,
-                              const Abort& ab) {
+                              float ci, const float* kscale, const Abort& ab) {
     using C = FwdCfg<D>;
     const float c2 = prm.alpha * 1.44269504088896340736f;   // alpha log2(e)
     const int ipos = tile.i0 + r;
@@ -393,6 +398,7 @@ __device__ float softmax_tile(const FwdTile& tile, const FwdParams& prm, uint64_
                             uint32_t sv[16];
                             tmem_ld16(s_tmem + col0, sv);
                             tmem_ld_wait();
+                            if (kscale) scale_step(sv, ci, kscale + jbase + col0);
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const float t = c2 * __uint_as_float(sv[e]);
@@ -424,6 +430,7 @@ __device__ float softmax_tile(const FwdTile& tile, const FwdParams& prm, uint64_
                             uint32_t sv[16], pk[8];
                             tmem_ld16(s_tmem + col0, sv);
                             tmem_ld_wait();
+                            if (kscale) scale_step(sv, ci, kscale + jbase + col0);
 #pragma unroll
                             for (int e = 0; e < 16; e += 2) {
                                 float pv2[2];
@@ -488,11 +495,19 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
         const uint32_t qs = a % C::kNQ;
         const bool warp_rows = quarter * 32 < tile.nq;
         const int ipos = tile.i0 + r;
+        // fused RMSNorm: this row's scale from the tile's raw Q
+        float ci = 1.0f;
+        const float* kscale = nullptr;
+        if (prm.kscale) {
+            if (!wg_wait(&bars[C::kBarQFull + qs], (a / C::kNQ) & 1, ab, 15)) return;
+            ci = row_scale<D>(smem + C::kOffQ + qs * C::kTileBytes, r, prm.qk_gain, prm.qk_eps);
+            kscale = prm.kscale + (int64_t)tile.h * prm.kscale_ld + tile.kvt0;
+        }
         float oscale = 1.0f;   // the softmax variant's 1 / (row sum)
         if constexpr (ACT == kSoftmax) {
             oscale = softmax_tile<D>(tile, prm, bars, s_use, x_use, s_tmem,
                                      tmem + wg * 256 + 128 + lane_addr, (int)wg, part, r, warp_rows,
-                                     ab);
+                                     ci, kscale, ab);
             if (__any_sync(0xffffffffu, oscale < 0.0f)) return;
         } else
         for (int kb = tile.kb0; kb < tile.kb1; ++kb) {
@@ -518,6 +533,7 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
                             uint32_t sv[16], pk[8];
                             tmem_ld16(s_tmem + col0, sv);
                             tmem_ld_wait();
+                            if (kscale) scale_step(sv, ci, kscale + jbase + col0);
                             // the chunk's keys against the window of this
                             // warp's 32 rows (warp-uniform): all valid, none
                             // valid, or mixed (per-pair masks)
@@ -763,7 +779,8 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
                               int64_t Tkv, int mask, int window, const void* q, int64_t q_rows,
                               int shared_q, const void* k, const void* v, void* o, float* lse,
                               float* w, float alpha, int act, cudaStream_t st,
-                              uint32_t wait_limit_us, int stall) {
+                              uint32_t wait_limit_us, int stall, const float* kscale,
+                              int64_t kscale_ld, float qk_gain, float qk_eps) {
     if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
     if (w && (d != 128 || act == kSoftmax)) return GDPA_ERR_UNSUPPORTED;
     if (Tq == 0) return GDPA_OK;
@@ -800,6 +817,10 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
     prm.timing = times != nullptr && smid != nullptr;
     prm.wait_ns = tc::wait_limit_ns(wait_limit_us);
     prm.stall = stall;
+    prm.kscale = kscale;
+    prm.kscale_ld = kscale_ld;
+    prm.qk_gain = qk_gain;
+    prm.qk_eps = qk_eps;
     gdpa_status s = GDPA_OK;
     if (w) {
         GDPA_DISPATCH_ACT(act, A, s = launch<128, A, true>(S, mq, mk, mv, mo, mw, prm, st))
@@ -834,11 +855,17 @@ gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, 
         w = p.d_wsplit;
     }
     if (p.timing) p.timed[0] = 1;
+    const float* kscale = nullptr;
+    if (p.qk_gain > 0.0f) {   // fused RMSNorm: the keys' scales first
+        gdpa_status ks;
+        kscale = plan_key_scales(p, k, st, &ks);
+        if (ks != GDPA_OK) return ks;
+    }
     gdpa_status s = launch_tc_fwd_raw(
         p.d_fwd, p.d_fwd_seg, p.S, p.d_err, p.timing ? p.d_times : nullptr,
         p.timing ? p.d_smid : nullptr, p.H, p.d, p.Tq, p.Tkv, p.mask, p.window, q,
         p.shared_q > 0 ? (int64_t)p.shared_q : p.Tq, p.shared_q > 0, k, v, o, lse, w, alpha, act,
-        st, p.wait_limit_us, p.stall);
+        st, p.wait_limit_us, p.stall, kscale, p.Tkv + 128, p.qk_gain, p.qk_eps);
     if (s == GDPA_OK) p.launches += 1;
     if (s == GDPA_OK && w) {
         const int64_t n4 = p.Tq * p.H * p.d / 4;

@@ -390,6 +390,60 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// ---------------------------------------------------------------- fused RMSNorm
+
+// Fused RMSNorm: the scores of the raw rows are scaled by c_i c'_j, c = g /
+// rms of the row, so that x = alpha c_i c'_j q_i . k_j is the score of the
+// normalised rows.  c of row r of a [128 x D] bf16 tile of raw rows in shared
+// memory (128-byte-swizzled halves of 64 columns, 16 KB each).
+template <int D>
+__device__ __forceinline__ float row_scale(const uint8_t* tile, int r, float gain, float eps) {
+    float ss = 0.0f;
+#pragma unroll
+    for (int hf = 0; hf < D / 64; ++hf) {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            const uint4 v =
+                *reinterpret_cast<const uint4*>(tile + hf * 16384 + r * 128 + ((c ^ (r & 7)) << 4));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float lo = __uint_as_float(w[u] << 16), hi = __uint_as_float(w[u] & 0xffff0000u);
+                ss = fmaf(lo, lo, ss);
+                ss = fmaf(hi, hi, ss);
+            }
+        }
+    }
+    return gain / sqrtf(ss / (float)D + eps);
+}
+
+// The 16 scores of a step, scaled by c_i and the keys' c'_j (j = j0 ..).
+__device__ __forceinline__ void scale_step(uint32_t (&sv)[16], float ci, const float* kscale_j0) {
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        sv[e] = __float_as_uint(__uint_as_float(sv[e]) * (ci * __ldg(kscale_j0 + e)));
+}
+
+// Columns [c0, c0 + 32 n) of row r of the same tile layout, as packed bf16
+// pairs (16 n words).
+template <int N>
+__device__ __forceinline__ void load_row_bf16(const uint8_t* tile, int r, int c0, uint32_t (&x)[16 * N]) {
+#pragma unroll
+    for (int q = 0; q < 4 * N; ++q) {
+        const int c = c0 / 8 + q;   // 16-byte chunk (8 columns) within the row
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + (c >> 3) * 16384 + r * 128 +
+                                                        (((c & 7) ^ (r & 7)) << 4));
+        x[4 * q] = v.x;
+        x[4 * q + 1] = v.y;
+        x[4 * q + 2] = v.z;
+        x[4 * q + 3] = v.w;
+    }
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+
 // ---------------------------------------------------------------- host side
 
 // Build a 2-D bf16 tensor map over a [rows][row_elems] row-major tensor with

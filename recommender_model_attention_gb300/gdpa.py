@@ -63,6 +63,7 @@ def lib():
             "gdpa_plan_set_timing": [vp, st],
             "gdpa_plan_set_shared_q": [vp, st],
             "gdpa_plan_set_wait_test": [vp, st, st],
+            "gdpa_plan_set_qk_norm": [vp, ctypes.c_float, ctypes.c_float],
             "gdpa_fwd": [vp, st, vp, vp, vp, vp, ctypes.c_float, st, vp],
             "gdpa_bwd": [vp, st, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, st, vp],
             "gdpa_check": [vp, vp],
@@ -191,6 +192,12 @@ class Plan:
 
     def set_timing(self, enable: bool):
         _ok(lib().gdpa_plan_set_timing(self.handle, 1 if enable else 0), "gdpa_plan_set_timing")
+
+    def set_qk_norm(self, gain: float = 1.0, eps: float = 1e-6):
+        """Fused RMSNorm of the Q and K rows inside the kernels (gain > 0);
+        gain = 0 turns it off."""
+        _ok(lib().gdpa_plan_set_qk_norm(self.handle, ctypes.c_float(gain), ctypes.c_float(eps)),
+            "gdpa_plan_set_qk_norm")
 
     def set_wait_test(self, limit_us: int = 0, stall: bool = False):
         """Failure-path test hook: bounded-wait limit (microseconds, 0 = the

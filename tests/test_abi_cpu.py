@@ -213,3 +213,14 @@ def test_shard_batch_refuses_bad_arguments(gd):
         gd.shard_batch(qo, qo, 1, 0)
     with pytest.raises(gd.GdpaError):
         gd.shard_batch(np.array([1, 2, 3]), qo, 1, 2)
+
+
+def test_qk_norm_argument_checks(gd):
+    qo = offsets_from_lengths([3, 4])
+    p = gd.Plan(qo, qo, 2, 64, num_sms=4, host_only=True)
+    p.set_qk_norm(1.0, 1e-6)
+    p.set_qk_norm(0.0, 0.0)          # off
+    for gain, eps in ((-1.0, 1e-6), (1.0, 0.0), (1.0, -1e-3), (float("nan"), 1e-6)):
+        with pytest.raises(gd.GdpaError):
+            p.set_qk_norm(gain, eps)
+    p.destroy()
