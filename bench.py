@@ -563,15 +563,23 @@ def main():
         metric_d = [torch.empty(n_out, dtype=f32, device="cuda") for _ in range(2)]
         metric_h = torch.empty(n_out, dtype=f32, pin_memory=True)
 
-        def e2e_run(n, replan=False, full=False):
+        def bf16_compute(p, ins, outs):
+            q_d, k_d, v_d, do_d = ins
+            fwd_call(p, q_d, k_d, v_d, outs[0])
+            if backward:
+                bwd_call(p, q_d, k_d, v_d, outs[0], do_d, *outs[1:])
+
+        def e2e_run(n, replan=False, full=False, hosts=None, dsets=None, compute=bf16_compute):
+            hosts = (hq, hk, hv, hdo) if hosts is None else hosts
+            dsets = sets if dsets is None else dsets
             plans = []
             for k in range(n):
                 sl = k % 2
-                (q_d, k_d, v_d, do_d), outs = sets[sl]
+                ins, outs = dsets[sl]
                 if k >= 2:
                     up.wait_event(ev["done"][sl])      # step k-2 has read this set
                 with torch.cuda.stream(up):
-                    for dst, src in zip((q_d, k_d, v_d, do_d), (hq, hk, hv, hdo)):
+                    for dst, src in zip(ins, hosts):
                         if dst is not None:
                             dst.copy_(src, non_blocking=True)
                     ev["in"][sl].record(up)
@@ -582,9 +590,7 @@ def main():
                 stream.wait_event(ev["in"][sl])
                 if k >= 2:
                     stream.wait_event(ev["out"][sl])   # step k-2's results are down
-                fwd_call(p, q_d, k_d, v_d, outs[0])
-                if backward:
-                    bwd_call(p, q_d, k_d, v_d, outs[0], do_d, *outs[1:])
+                compute(p, ins, outs)
                 if not full:
                     for j, t in enumerate(outs):
                         metric_d[sl][j] = torch.linalg.vector_norm(t, dtype=f32)
@@ -640,6 +646,65 @@ def main():
                                  "ms_per_step": full_total / n_e2e},
                "pipelining": "inputs up, compute, results down on three streams, "
                              "two buffer sets"}
+
+    # the same step with Q and K arriving in MXFP8 (E4M3 elements, one E8M0
+    # scale per 32 values along d): gdpa_fwd_mx / gdpa_bwd_mx expand them to
+    # bf16 on the device, then run the bf16 kernels; on device and end to end
+    mxfp8 = None
+    if rank == 0 and world == 1 and not args.no_workloads and not softmax and not args.samples:
+        qm, km = gd.mx_quantise(q_in), gd.mx_quantise(x["k"])
+
+        def mx_step(p, q_m, k_m, v_, do_, o_, dq_, dk_, dv_):
+            gd.gdpa_fwd_mx(p, q_m, k_m, v_, o=o_, alpha=w.alpha, act=w.act)
+            if backward:   # reuses the forward's expansion of Q and K
+                gd.gdpa_bwd_mx(p, None, None, v_, do_, dq_, dk_, dv_, alpha=w.alpha, act=w.act)
+
+        for _ in range(args.warmup):
+            mx_step(plan, qm, km, x["v"], x["do"], o, dq, dk, dv)
+        torch.cuda.synchronize()
+        mev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+        for s in range(args.steps):
+            mev[s][0].record(stream)
+            gd.gdpa_fwd_mx(plan, qm, km, x["v"], o=o, alpha=w.alpha, act=w.act)
+            mev[s][1].record(stream)
+            if backward:
+                gd.gdpa_bwd_mx(plan, None, None, x["v"], x["do"], dq, dk, dv, alpha=w.alpha,
+                               act=w.act)
+            mev[s][2].record(stream)
+        torch.cuda.synchronize()
+        plan.check()
+        m_fwd = float(np.mean([a.elapsed_time(b) for a, b, _ in mev]))
+        m_bwd = float(np.mean([b.elapsed_time(c) for _, b, c in mev])) if backward else 0.0
+        m_ms = float(np.mean([a.elapsed_time(c) for a, _, c in mev]))
+        mx_in = (qm.elements, qm.scales, km.elements, km.scales, x["v"], x["do"])
+        mx_bytes = sum(t.numel() * t.element_size() for t in mx_in if t is not None)
+        mxfp8 = {"ms_per_step": m_ms, "fwd_ms": m_fwd, "bwd_ms": m_bwd,
+                 "tflops": (fwd_flops + bwd_flops) / (m_ms * 1e-3) / 1e12,
+                 "input_bytes": int(mx_bytes), "input_bytes_bf16": int(input_bytes),
+                 "what": "Q and K in MXFP8, expanded to bf16 on the device by the forward "
+                         "(two launches) and reused by the backward; V, dO, O bf16, "
+                         "gradients float32"}
+        if e2e is not None:
+            h_mx = [t.cpu().pin_memory() if t is not None else None for t in mx_in]
+            mx_sets = [([torch.empty_like(t) if t is not None else None for t in mx_in], outs)
+                       for _, outs in sets]
+
+            def mx_compute(p, ins, outs):
+                mx_step(p, gd.MX(ins[0], ins[1]), gd.MX(ins[2], ins[3]), ins[4], ins[5], *outs)
+
+            e2e_run(2, hosts=h_mx, dsets=mx_sets, compute=mx_compute)
+            torch.cuda.synchronize()
+            a.record(stream)
+            e2e_run(n_e2e, hosts=h_mx, dsets=mx_sets, compute=mx_compute)
+            b.record(stream)
+            torch.cuda.synchronize()
+            mx_e2e_ms = a.elapsed_time(b) / n_e2e
+            mxfp8["e2e"] = {"value": (fwd_flops + bwd_flops) / (mx_e2e_ms * 1e-3) / 1e12,
+                            "unit": UNIT, "ms_per_step": mx_e2e_ms,
+                            "h2d_bytes_per_step": int(mx_bytes), "d2h_bytes_per_step": int(d2h)}
+            del h_mx, mx_sets
+        del qm, km
+        torch.cuda.empty_cache()
 
     # SM busy-time spread of each policy, forward and backward (separate,
     # untimed launches)
@@ -702,6 +767,7 @@ def main():
             "gpu_launches": int(launches),
             "clocks": clk,
             "e2e": e2e,
+            "mxfp8": mxfp8,
             "sm_spread_fwd": spread,
             "sm_spread_bwd": spread_bwd if backward else None,
             "workloads": others,

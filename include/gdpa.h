@@ -34,8 +34,9 @@
  *     device buffers and is freed by gdpa_plan_destroy.
  *   - A plan belongs to the device that was current when it was created;
  *     every call that launches work on it or reads its device state
- *     (gdpa_fwd, gdpa_bwd, gdpa_softmax_fwd, gdpa_softmax_bwd, gdpa_check,
- *     gdpa_sm_times) must be made with that device current and returns
+ *     (gdpa_fwd, gdpa_bwd, gdpa_softmax_fwd, gdpa_softmax_bwd, gdpa_fwd_mx,
+ *     gdpa_bwd_mx, gdpa_check, gdpa_sm_times) must be made with that device
+ *     current and returns
  *     INVALID_ARG, before touching the device, otherwise.
  */
 #ifndef GDPA_H
@@ -274,11 +275,14 @@ gdpa_status gdpa_plan_set_shared_q(gdpa_plan plan, int n_seeds);
  * before it enters the attention; V is used as given.  The backward's dq and
  * dk are then the gradients with respect to the raw rows,
  *     dL/dx = (gain / r) (dy - x (x . dy) / (d r^2)),  r = sqrt(mean(x^2) + eps).
- * The kernels never write the normalised rows: they scale the scores of the
- * raw rows by c_i c_j (c = gain / r of the query and key row), and the
- * gradients likewise.  Each launch first computes the keys' c (one pass over
- * K into a plan-owned [H][Tkv + 128] float workspace, allocated on first
- * use).  Tensor-core kernels only (bf16, d = 64 or 128): the CUDA-core path
+ * Each launch first normalises the keys in one pass over K (c = gain / r of
+ * every key row into a plan-owned [H][Tkv + 128] float workspace, the rows
+ * c k rounded to bf16 into a plan-owned [Tkv][H][d] workspace; both
+ * allocated on first use and kept until gdpa_plan_destroy); the attention
+ * kernels read those keys, compute each query row's c from its tile and
+ * fold it into alpha (x = alpha c_i q_i . k_hat_j), and apply the norm's
+ * Jacobian to dq and dk as they drain them.  The queries are never written
+ * normalised.  Tensor-core kernels only (bf16, d = 64 or 128): the CUDA-core path
  * returns UNSUPPORTED while it is on; gdpa_fwd_noalloc has no such mode.
  * gain = 0 turns it off.  INVALID_ARG for a negative or NaN gain or eps, or
  * eps = 0 with gain > 0 (an all-zero row would divide by zero).
@@ -420,6 +424,63 @@ gdpa_status gdpa_softmax_fwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, co
 gdpa_status gdpa_softmax_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void* k,
                              const void* v, const void* o, const void* d_o, const float* lse,
                              float* dq, float* dk, float* dv, float alpha, void* stream);
+
+/*
+ * MXFP8 encoding of Q and K.  The GEM page ("GEM 트레이닝: Meta가 LLM 규모의
+ * 광고 파운데이션 모델 효율성을 두 배로 높인 방법", techlist.io, section "GPU
+ * 연산 효율을 높인 맞춤형 커널과 정밀도") trains attention in mixed precision
+ * that includes MXFP8; the format is OCP Microscaling: blocks of 32
+ * consecutive values share one power-of-two scale 2^E (E8M0), and each value
+ * is an FP8 E4M3 element (bias 7, largest finite 448, subnormals, no
+ * infinities).  For a block whose largest magnitude is a > 0,
+ * E = floor(log2 a) - 8, clamped to [-127, 127]; an all-zero block has
+ * E = -127.  Element = x / 2^E rounded to the nearest E4M3 value, ties to
+ * the even mantissa, saturated at +-448.  The block stands for element * 2^E.
+ *
+ * Storage: `elements` holds one E4M3 code per value in the value's position
+ * (uint8, 16-byte aligned device memory); `scales` holds E + 127 as one byte
+ * per block, block i covering values [32 i, 32 i + 32).  For a [T][H][d]
+ * tensor (d a multiple of 32) that is elements [T][H][d] and scales
+ * [T][H][d / 32].
+ */
+
+/* x: n bf16 values (device, 16-byte aligned) -> elements [n], scales [n / 32].
+ * INVALID_ARG for n < 0, n not a multiple of 32, NULL or misaligned
+ * pointers; CUDA if the launch fails.  Asynchronous on `stream`. */
+gdpa_status gdpa_mx_quantise(const void* x, int64_t n, uint8_t* elements, uint8_t* scales,
+                             void* stream);
+
+/* elements [n], scales [n / 32] -> x: n bf16 values, each element * 2^E
+ * rounded to bf16 (exact unless the value is below bf16's smallest
+ * subnormal).  Errors and stream as gdpa_mx_quantise. */
+gdpa_status gdpa_mx_dequantise(const uint8_t* elements, const uint8_t* scales, int64_t n, void* x,
+                               void* stream);
+
+/*
+ * GDPA with Q and K given in MXFP8 (blocks along d; d = 32, 64 or 128), V in
+ * bf16: the forward and backward of gdpa_fwd / gdpa_bwd (and the softmax
+ * variant's forward with act = GDPA_ACT_SOFTMAX) on the values the MXFP8
+ * tensors stand for.  The gradients dq, dk are with respect to those values
+ * (float32, as gdpa_bwd).  q_el / q_sc hold Q's rows (Tq rows, or the seed
+ * rows in shared-query mode), k_el / k_sc K's Tkv rows.  The call expands Q
+ * and K to bf16 in a plan-owned device workspace ((Q rows + Tkv) H d bf16,
+ * allocated on the stream on first use, kept until gdpa_plan_destroy; ALLOC
+ * on failure) and runs the bf16 kernels the plan selects; the fused
+ * RMSNorm, when on, normalises the expanded rows.  With all four of q_el,
+ * q_sc, k_el, k_sc NULL the call reuses the expansion the plan's previous
+ * gdpa_fwd_mx / gdpa_bwd_mx made (e.g. the backward of a forward on the same
+ * Q and K, saving the second expansion); the caller orders the two calls
+ * (same stream, or an event) and INVALID_ARG is returned if there is no
+ * such expansion.  Errors as gdpa_fwd / gdpa_bwd, plus INVALID_ARG for NULL
+ * or misaligned element pointers (other than the reuse form) or
+ * d % 32 != 0.
+ */
+gdpa_status gdpa_fwd_mx(gdpa_plan plan, const uint8_t* q_el, const uint8_t* q_sc,
+                        const uint8_t* k_el, const uint8_t* k_sc, const void* v, void* o,
+                        float alpha, gdpa_act act, void* stream);
+gdpa_status gdpa_bwd_mx(gdpa_plan plan, const uint8_t* q_el, const uint8_t* q_sc,
+                        const uint8_t* k_el, const uint8_t* k_sc, const void* v, const void* d_o,
+                        float* dq, float* dk, float* dv, float alpha, gdpa_act act, void* stream);
 
 /* Activation test hook.
  *

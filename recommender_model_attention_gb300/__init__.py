@@ -16,16 +16,21 @@ from .gdpa import (  # noqa: F401
     GdpaError,
     LIB_PATH,
     MASK,
+    MX,
     Plan,
     STATUS,
     allreduce_seed_grad,
     act_eval,
     gdpa_bwd,
+    gdpa_bwd_mx,
     gdpa_fwd,
+    gdpa_fwd_mx,
     gdpa_fwd_noalloc,
     gdpa_softmax_bwd,
     gdpa_softmax_fwd,
     lib,
+    mx_dequantise,
+    mx_quantise,
     shard_batch,
     shard_rows,
 )

@@ -63,7 +63,8 @@ void free_plan(Plan* p) {
             for (const gdpa::StreamEvent& w : p->work) cudaStreamWaitEvent(fs, w.event, 0);
         }
         void* bufs[] = {p->d_fwd, p->d_fwd_seg, p->d_bwd, p->d_bwd_seg, p->d_err,
-                        p->d_times, p->d_smid, p->d_delta, p->d_wsplit, p->d_kscale};
+                        p->d_times, p->d_smid, p->d_delta, p->d_wsplit, p->d_kscale, p->d_mxqk,
+                        p->d_khat};
         for (void* b : bufs)
             if (b) cudaFreeAsync(b, fs);
         for (const gdpa::StreamEvent& w : p->work) cudaEventDestroy(w.event);
@@ -397,6 +398,119 @@ gdpa_status gdpa_softmax_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, co
                              const void* v, const void* o, const void* d_o, const float* lse,
                              float* dq, float* dk, float* dv, float alpha, void* stream) {
     return bwd_common(plan, dtype, q, k, v, o, d_o, lse, dq, dk, dv, alpha, GDPA_ACT_SOFTMAX,
+                      stream);
+}
+
+gdpa_status gdpa_mx_quantise(const void* x, int64_t n, uint8_t* elements, uint8_t* scales,
+                             void* stream) {
+    if (n < 0 || n % 32) return GDPA_ERR_INVALID_ARG;
+    if (n == 0) return GDPA_OK;
+    if (!x || !elements || !scales || !aligned16(x) || !aligned16(elements))
+        return GDPA_ERR_INVALID_ARG;
+    return gdpa::launch_mx_quantise(x, n, elements, scales, (cudaStream_t)stream);
+}
+
+gdpa_status gdpa_mx_dequantise(const uint8_t* elements, const uint8_t* scales, int64_t n, void* x,
+                               void* stream) {
+    if (n < 0 || n % 32) return GDPA_ERR_INVALID_ARG;
+    if (n == 0) return GDPA_OK;
+    if (!x || !elements || !scales || !aligned16(x) || !aligned16(elements))
+        return GDPA_ERR_INVALID_ARG;
+    return gdpa::launch_mx_dequantise(elements, scales, n, x, (cudaStream_t)stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Expands MXFP8 Q and K into the plan's bf16 workspace (allocated on the
+// stream on first use) and returns where the expansions start.
+gdpa_status mx_expand(Plan& p, const uint8_t* q_el, const uint8_t* q_sc, const uint8_t* k_el,
+                      const uint8_t* k_sc, cudaStream_t st, const void** q, const void** k) {
+    if (p.d % 32) return GDPA_ERR_INVALID_ARG;
+    const int64_t q_rows = p.shared_q > 0 ? p.shared_q : p.Tq;
+    const int64_t row = (int64_t)p.H * p.d;
+    if (!q_el && !q_sc && !k_el && !k_sc && (q_rows > 0 || p.Tkv > 0)) {
+        // reuse the expansion of the plan's previous MXFP8 call
+        if (!p.mx_ready || (size_t)(q_rows + p.Tkv) * row * 2 > p.mxqk_bytes)
+            return GDPA_ERR_INVALID_ARG;
+        if (gdpa_status ds = check_device(p)) return ds;
+        *q = p.d_mxqk;
+        *k = (uint8_t*)p.d_mxqk + (size_t)q_rows * row * 2;
+        return GDPA_OK;
+    }
+    if (q_rows > 0 && (!q_el || !q_sc || !aligned16(q_el))) return GDPA_ERR_INVALID_ARG;
+    if (p.Tkv > 0 && (!k_el || !k_sc || !aligned16(k_el))) return GDPA_ERR_INVALID_ARG;
+    if (gdpa_status ds = check_device(p)) return ds;
+    const size_t bytes = (size_t)(q_rows + p.Tkv) * row * 2;
+    if (p.d_mxqk && bytes > p.mxqk_bytes) {
+        // the shared-query mode changed Q's row count: replace the workspace
+        // once the plan's earlier work has run
+        for (const gdpa::StreamEvent& w : p.work) cudaStreamWaitEvent(st, w.event, 0);
+        cudaFreeAsync(p.d_mxqk, st);
+        p.d_mxqk = nullptr;
+        p.mx_ready = false;
+    }
+    if (!p.d_mxqk && bytes > 0) {
+        if (cudaMallocAsync(&p.d_mxqk, bytes, st) != cudaSuccess) {
+            p.d_mxqk = nullptr;
+            return GDPA_ERR_ALLOC;
+        }
+        p.mxqk_bytes = bytes;
+    }
+    uint8_t* base = (uint8_t*)p.d_mxqk;
+    *q = base;
+    *k = base + (size_t)q_rows * row * 2;
+    gdpa_status s = GDPA_OK;
+    if (q_rows > 0) {
+        s = gdpa::launch_mx_dequantise(q_el, q_sc, q_rows * row, (void*)*q, st);
+        if (s == GDPA_OK) p.launches += 1;
+    }
+    if (s == GDPA_OK && p.Tkv > 0) {
+        s = gdpa::launch_mx_dequantise(k_el, k_sc, p.Tkv * row, (void*)*k, st);
+        if (s == GDPA_OK) p.launches += 1;
+    }
+    end_work(p, st);   // the workspace is in use until these have run
+    p.mx_ready = s == GDPA_OK;
+    return s;
+}
+
+}  // namespace
+
+extern "C" {
+
+gdpa_status gdpa_fwd_mx(gdpa_plan plan, const uint8_t* q_el, const uint8_t* q_sc,
+                        const uint8_t* k_el, const uint8_t* k_sc, const void* v, void* o,
+                        float alpha, gdpa_act act, void* stream) {
+    if (!plan || ((Plan*)plan)->host_only) return GDPA_ERR_INVALID_ARG;
+    Plan& p = *(Plan*)plan;
+    if (!valid_act(act)) return GDPA_ERR_INVALID_ARG;
+    if (p.Tq > 0 && !o) return GDPA_ERR_INVALID_ARG;
+    if (p.Tkv > 0 && !v) return GDPA_ERR_INVALID_ARG;
+    if (!aligned16(v) || !aligned16(o)) return GDPA_ERR_INVALID_ARG;
+    if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, GDPA_BF16)) return GDPA_ERR_UNSUPPORTED;
+    const void *q = nullptr, *k = nullptr;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (gdpa_status s = mx_expand(p, q_el, q_sc, k_el, k_sc, st, &q, &k)) return s;
+    return fwd_common(plan, GDPA_BF16, q, k, v, o, nullptr, alpha, act, stream);
+}
+
+gdpa_status gdpa_bwd_mx(gdpa_plan plan, const uint8_t* q_el, const uint8_t* q_sc,
+                        const uint8_t* k_el, const uint8_t* k_sc, const void* v, const void* d_o,
+                        float* dq, float* dk, float* dv, float alpha, gdpa_act act, void* stream) {
+    if (!plan || ((Plan*)plan)->host_only) return GDPA_ERR_INVALID_ARG;
+    Plan& p = *(Plan*)plan;
+    if (!valid_act(act)) return GDPA_ERR_INVALID_ARG;
+    if (act == GDPA_ACT_SOFTMAX) return GDPA_ERR_UNSUPPORTED;
+    if (p.Tq > 0 && (!d_o || !dq)) return GDPA_ERR_INVALID_ARG;
+    if (p.Tkv > 0 && (!v || !dk || !dv)) return GDPA_ERR_INVALID_ARG;
+    if (!aligned16(v) || !aligned16(d_o) || !aligned16(dq) || !aligned16(dk) || !aligned16(dv))
+        return GDPA_ERR_INVALID_ARG;
+    if (p.kernel == GDPA_KERNEL_TCGEN05 && !use_tc(p, GDPA_BF16)) return GDPA_ERR_UNSUPPORTED;
+    const void *q = nullptr, *k = nullptr;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (gdpa_status s = mx_expand(p, q_el, q_sc, k_el, k_sc, st, &q, &k)) return s;
+    return bwd_common(plan, GDPA_BF16, q, k, v, nullptr, d_o, nullptr, dq, dk, dv, alpha, act,
                       stream);
 }
 

@@ -82,9 +82,16 @@ struct Plan {
     uint32_t wait_limit_us = 0;
     int stall = 0;
     // fused RMSNorm of Q and K rows (gain > 0 enables): the keys' g / rms in
-    // a [H][Tkv + 128] float workspace, refreshed by every launch
+    // a [H][Tkv + 128] float workspace and the normalised keys (bf16,
+    // [Tkv][H][d]), refreshed by every launch
     float qk_gain = 0.0f, qk_eps = 0.0f;
     float* d_kscale = nullptr;
+    void* d_khat = nullptr;
+    // MXFP8 entry points: bf16 expansion of Q's rows then K's rows,
+    // [q_rows + Tkv][H][d], allocated on first use
+    void* d_mxqk = nullptr;
+    size_t mxqk_bytes = 0;
+    bool mx_ready = false;   // it holds the last MXFP8 call's Q and K
     // softmax-variant backward: dO_t . O_t per row and head, [Tq][H] float,
     // allocated on first use
     float* d_delta = nullptr;
@@ -113,25 +120,29 @@ gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, 
                           float* lse, float alpha, int act, cudaStream_t st);
 // Forward tensor-core launch on explicit device buffers (tile queue, queue
 // starts, error word; times/smid may be NULL to skip per-CTA timing).
+// qk_gain > 0: fused RMSNorm, with k already normalised (plan_key_norm).
 gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, int32_t* err,
                               unsigned long long* times, int32_t* smid, int H, int d, int64_t Tq,
                               int64_t Tkv, int mask, int window, const void* q, int64_t q_rows,
                               int shared_q, const void* k, const void* v, void* o, float* lse,
                               float* w, float alpha, int act, cudaStream_t st,
                               uint32_t wait_limit_us = 0, int stall = 0,
-                              const float* kscale = nullptr, int64_t kscale_ld = 0,
                               float qk_gain = 0.0f, float qk_eps = 0.0f);
 gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, const void* d_o,
                           float* dq, float* dk, float* dv, float alpha, int act, const float* lse,
                           const float* delta, cudaStream_t st);
-// Fused RMSNorm: out[h][t] = gain / sqrt(mean(x[t][h][:]^2) + eps) for rows
-// t < rows of a bf16 [rows][H][d] tensor (the plan's key-scale workspace,
-// leading dimension ld).
-gdpa_status launch_row_scale(const Plan& p, const void* x, int64_t rows, float* out, int64_t ld,
-                             cudaStream_t st);
-// The plan's key scales for `k` (workspace allocated on first use, stream
-// ordered); returns the workspace or NULL (status in *s).
-float* plan_key_scales(Plan& p, const void* k, cudaStream_t st, gdpa_status* s);
+// Fused RMSNorm of the keys (d = 64 or 128): c = gain / sqrt(mean(k^2) +
+// eps) of every (token, head) row of `k` into the plan's d_kscale
+// ([H][Tkv + 128] floats) and the normalised rows c k (bf16) into d_khat
+// ([Tkv][H][d]); both allocated on first use, stream ordered.  Returns
+// d_khat (k itself when Tkv = 0) or NULL (status in *s).
+const void* plan_key_norm(Plan& p, const void* k, cudaStream_t st, gdpa_status* s);
+// MXFP8 (32-value blocks): bf16 x[n] <-> E4M3 codes el[n] + scale bytes
+// sc[n / 32]; n a multiple of 32
+gdpa_status launch_mx_quantise(const void* x, int64_t n_values, uint8_t* el, uint8_t* sc,
+                               cudaStream_t st);
+gdpa_status launch_mx_dequantise(const uint8_t* el, const uint8_t* sc, int64_t n_values, void* x,
+                                 cudaStream_t st);
 // delta[t][h] = dO[t][h][:] . O[t][h][:] over rows t < Tq (softmax variant)
 gdpa_status launch_row_dot(Plan& p, gdpa_dtype dt, const void* d_o, const void* o, float* delta,
                            cudaStream_t st);

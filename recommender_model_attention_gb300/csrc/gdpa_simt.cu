@@ -395,43 +395,63 @@ gdpa_status launch_row_dot(Plan& p, gdpa_dtype dt, const void* d_o, const void* 
 
 namespace {
 
-// one warp per (token, head) row: gain / rms of the row
+// Fused RMSNorm of the keys, one warp per (token, head) row of a bf16
+// [rows][H][d] tensor: c = gain / sqrt(mean(k^2) + eps) into
+// scale[h][t] (leading dimension ld) and the normalised row c k, rounded to
+// bf16, into khat.  V = d / 32 values per lane (d = 64 or 128).
+template <int V>
 __global__ void __launch_bounds__(256)
-row_scale_kernel(const __nv_bfloat16* __restrict__ x, float* __restrict__ out, int64_t rows,
-                 int H, int d, int64_t ld, float gain, float eps) {
+key_norm_kernel(const __nv_bfloat16* __restrict__ k, __nv_bfloat16* __restrict__ khat,
+                float* __restrict__ scale, int64_t rows, int H, int64_t ld, float gain, float eps) {
     const int64_t rw = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (rw >= rows * H) return;
-    const __nv_bfloat16* p = x + rw * d;
-    float ss = 0.0f;
-    for (int c = lane; c < d; c += 32) {
-        const float v = __bfloat162float(p[c]);
-        ss = fmaf(v, v, ss);
+    constexpr int d = 32 * V;
+    const __nv_bfloat16* src = k + rw * d + lane * V;
+    float x[V];
+    if constexpr (V == 4) {
+        const uint2 w = *reinterpret_cast<const uint2*>(src);
+        x[0] = __uint_as_float(w.x << 16);
+        x[1] = __uint_as_float(w.x & 0xffff0000u);
+        x[2] = __uint_as_float(w.y << 16);
+        x[3] = __uint_as_float(w.y & 0xffff0000u);
+    } else {
+        const uint32_t w = *reinterpret_cast<const uint32_t*>(src);
+        x[0] = __uint_as_float(w << 16);
+        x[1] = __uint_as_float(w & 0xffff0000u);
     }
+    float ss = 0.0f;
+#pragma unroll
+    for (int e = 0; e < V; ++e) ss = fmaf(x[e], x[e], ss);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float c = gain / sqrtf(ss / (float)d + eps);
+    __nv_bfloat16* dst = khat + rw * d + lane * V;
+    const __nv_bfloat162 p0 = __floats2bfloat162_rn(c * x[0], c * x[1]);
+    if constexpr (V == 4) {
+        const __nv_bfloat162 p1 = __floats2bfloat162_rn(c * x[2], c * x[3]);
+        *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<const uint32_t*>(&p0),
+                                                    *reinterpret_cast<const uint32_t*>(&p1));
+    } else {
+        *reinterpret_cast<__nv_bfloat162*>(dst) = p0;
+    }
     if (lane == 0) {
         const int64_t t = rw / H, h = rw % H;
-        out[h * ld + t] = gain / sqrtf(ss / (float)d + eps);
+        scale[h * ld + t] = c;
     }
 }
 
 }  // namespace
 
-gdpa_status launch_row_scale(const Plan& p, const void* x, int64_t rows, float* out, int64_t ld,
-                             cudaStream_t st) {
-    if (rows == 0) return GDPA_OK;
-    const int64_t n = rows * p.H;
-    row_scale_kernel<<<(unsigned)((n + 7) / 8), 256, 0, st>>>((const __nv_bfloat16*)x, out, rows,
-                                                              p.H, p.d, ld, p.qk_gain, p.qk_eps);
-    return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
-}
-
-float* plan_key_scales(Plan& p, const void* k, cudaStream_t st, gdpa_status* s) {
-    const int64_t ld = p.Tkv + 128;   // padding read (masked) past a sample's last key
-    const size_t bytes = (size_t)p.H * ld * sizeof(float);
+const void* plan_key_norm(Plan& p, const void* k, cudaStream_t st, gdpa_status* s) {
     *s = GDPA_OK;
+    if (p.d != 64 && p.d != 128) {
+        *s = GDPA_ERR_UNSUPPORTED;
+        return nullptr;
+    }
+    const int64_t ld = p.Tkv + 128;
     if (!p.d_kscale) {
+        const size_t bytes = (size_t)p.H * ld * sizeof(float);
         if (cudaMallocAsync((void**)&p.d_kscale, bytes, st) != cudaSuccess) {
             p.d_kscale = nullptr;
             *s = GDPA_ERR_ALLOC;
@@ -442,10 +462,27 @@ float* plan_key_scales(Plan& p, const void* k, cudaStream_t st, gdpa_status* s) 
             return nullptr;
         }
     }
-    *s = launch_row_scale(p, k, p.Tkv, p.d_kscale, ld, st);
-    if (*s != GDPA_OK) return nullptr;
+    const int64_t n = p.Tkv * p.H;
+    if (!p.d_khat && n > 0 &&
+        cudaMallocAsync(&p.d_khat, (size_t)n * p.d * sizeof(__nv_bfloat16), st) != cudaSuccess) {
+        p.d_khat = nullptr;
+        *s = GDPA_ERR_ALLOC;
+        return nullptr;
+    }
+    if (n == 0) return k;
+    const unsigned grid = (unsigned)((n + 7) / 8);
+    if (p.d == 128)
+        key_norm_kernel<4><<<grid, 256, 0, st>>>((const __nv_bfloat16*)k, (__nv_bfloat16*)p.d_khat,
+                                                 p.d_kscale, p.Tkv, p.H, ld, p.qk_gain, p.qk_eps);
+    else
+        key_norm_kernel<2><<<grid, 256, 0, st>>>((const __nv_bfloat16*)k, (__nv_bfloat16*)p.d_khat,
+                                                 p.d_kscale, p.Tkv, p.H, ld, p.qk_gain, p.qk_eps);
+    if (cudaGetLastError() != cudaSuccess) {
+        *s = GDPA_ERR_CUDA;
+        return nullptr;
+    }
     p.launches += 1;
-    return p.d_kscale;
+    return p.d_khat;
 }
 
 }  // namespace gdpa

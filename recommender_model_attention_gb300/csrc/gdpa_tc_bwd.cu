@@ -66,7 +66,7 @@ struct BwdCfg {
     enum {
         kKVFull = 0, kKVEmpty, kQFull, kQFull1, kQEmpty, kQEmpty1, kDOFull, kDOFull1, kDOEmpty,
         kDOEmpty1, kSDFull, kSFree, kDQFree, kPFull, kPVDone, kDSFull, kDKDone, kAccFull,
-        kAccFree, kStage, kStage1, kPSFree, kMmaDone, kDQDone, kNumBars
+        kAccFree, kStage, kStage1, kPSFree, kMmaDone, kDQDone, kDotFull, kNumBars
     };
     static constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 16 + 1024;
 };
@@ -90,8 +90,9 @@ struct BwdParams {
     int timing;
     uint64_t wait_ns;     // bounded-wait limit
     int stall;            // test hook: CTA 0 skips its first Q load
-    // fused RMSNorm of Q and K (or NULL): g / rms of every key row, [H][ld]
-    // floats; gain and eps for the query rows computed in the kernel
+    // fused RMSNorm (or NULL): the keys arrive normalised and kscale holds
+    // each key row's g / rms, [H][ld] floats; each query row's scale is
+    // computed from its tile (gain, eps) and folded into alpha
     const float* kscale;
     int64_t kscale_ld;
     float qk_gain, qk_eps;
@@ -288,48 +289,65 @@ __device__ __forceinline__ void store_half_chunk(uint8_t* ps, int c, int hh, int
 // gradient with respect to the raw row x,
 //     dx = c (dy - x (x . dy) c^2 / (d g^2)),   c = g / rms(x),
 // i.e. out = sc (v - kappa x) with sc = alpha c and kappa = (x . v) c^2 /
-// (d g^2).  Columns [col, col + 32 P) of this warp's 32 lanes; x holds the
-// thread's row's raw values of those columns (packed bf16 pairs, read before
-// the staging may overwrite them); staging and stores as drain_warp.
-template <int P>
-static __device__ __noinline__ void drain_warp_norm(uint32_t trow, uint32_t col, uint8_t* stage,
-                                                    const CUtensorMap* map, int x0, int y0,
-                                                    float* dst, int64_t rs, int nrows, bool atomic,
-                                                    float sc, float kappa,
-                                                    const uint32_t (&x)[16 * P], int quarter,
-                                                    int lane, uint64_t* release) {
+// (d g^2) (or, in terms of the normalised row x_hat = c x, kappa = (x_hat .
+// v) / (d g^2) with x_hat in place of x).  Columns [col, col + 32 P) of this
+// warp's 32 lanes, 16 at a time; xw(pass, half, x8) gives the 8 packed bf16
+// words of x for columns col + 32 pass + 16 half ..; staging and stores as
+// drain_warp.
+template <int P, typename XW>
+__device__ __forceinline__ void drain_warp_norm(uint32_t trow, uint32_t col, uint8_t* stage,
+                                                const CUtensorMap* map, int x0, int y0, float* dst,
+                                                int64_t rs, int nrows, bool atomic, float sc,
+                                                float kappa, XW xw, int quarter, int lane,
+                                                uint64_t* release) {
     const int row0 = quarter * 32;
     const bool any = row0 < nrows;
     const bool full = row0 + 32 <= nrows;
     uint8_t* wst = stage + quarter * 4096;
 #pragma unroll
     for (int pass = 0; pass < P; ++pass) {
-        uint32_t v[32];
-        if (any) {
-            tmem_ld32(trow + col + pass * 32, v);
-            tmem_ld_wait();
+        if (full && pass > 0) {
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
         }
-        if (pass == P - 1 && release) {
-            tc_fence_before();
-            mbar_arrive(release);
-        }
-        if (!any) continue;
-        float o[32];
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-            const uint32_t w = x[16 * pass + e / 2];
-            o[e] = sc * fmaf(-kappa, bf16_lo(w), __uint_as_float(v[e]));
-            o[e + 1] = sc * fmaf(-kappa, bf16_hi(w), __uint_as_float(v[e + 1]));
+        for (int hf = 0; hf < 2; ++hf) {
+            uint32_t v[16];
+            if (any) {
+                tmem_ld16(trow + col + pass * 32 + hf * 16, v);
+                tmem_ld_wait();
+            }
+            if (pass == P - 1 && hf == 1 && release) {
+                tc_fence_before();
+                mbar_arrive(release);
+            }
+            if (!any) continue;
+            uint32_t x8[8];
+            xw(pass, hf, x8);
+            float o[16];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                o[2 * e] = sc * fmaf(-kappa, bf16_lo(x8[e]), __uint_as_float(v[2 * e]));
+                o[2 * e + 1] = sc * fmaf(-kappa, bf16_hi(x8[e]), __uint_as_float(v[2 * e + 1]));
+            }
+            if (full) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<float4*>(wst + lane * 128 + (((4 * hf + c) ^ (lane & 7)) << 4)) =
+                        make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+            } else if (row0 + lane < nrows) {
+                float* d = dst + (int64_t)(row0 + lane) * rs + pass * 32 + hf * 16;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float4 w = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                    if (atomic)
+                        atomicAdd(reinterpret_cast<float4*>(d + 4 * c), w);
+                    else
+                        *reinterpret_cast<float4*>(d + 4 * c) = w;
+                }
+            }
         }
         if (full) {
-            if (pass > 0) {
-                if (lane == 0) bulk_wait_read_all();
-                __syncwarp();
-            }
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-                *reinterpret_cast<float4*>(wst + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                    make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -339,79 +357,82 @@ static __device__ __noinline__ void drain_warp_norm(uint32_t trow, uint32_t col,
                     tma_store_2d(map, wst, x0 + pass * 32, y0 + row0);
                 bulk_commit();
             }
-        } else if (row0 + lane < nrows) {
-            float* d = dst + (int64_t)(row0 + lane) * rs + pass * 32;
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 w = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-                if (atomic)
-                    atomicAdd(reinterpret_cast<float4*>(d + 4 * c), w);
-                else
-                    *reinterpret_cast<float4*>(d + 4 * c) = w;
-            }
         }
     }
 }
 
-// x . v over columns [col, col + 32 P) of this warp's lanes (TMEM) and the
-// row's raw values x (packed bf16 pairs).
-template <int P>
-__device__ __forceinline__ float row_dot_tmem(uint32_t trow, uint32_t col, const uint32_t (&x)[16 * P]) {
-    float dot = 0.0f;
+// 8 packed bf16 words: columns [c0, c0 + 16) of row r of a [128 x D] bf16
+// tile in shared memory (128-byte-swizzled halves of 64 columns)
+__device__ __forceinline__ void load_row16(const uint8_t* tile, int r, int c0, uint32_t (&x)[8]) {
 #pragma unroll
-    for (int pass = 0; pass < P; ++pass) {
-        uint32_t v[32];
-        tmem_ld32(trow + col + pass * 32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-            const uint32_t w = x[16 * pass + e / 2];
-            dot = fmaf(bf16_lo(w), __uint_as_float(v[e]), dot);
-            dot = fmaf(bf16_hi(w), __uint_as_float(v[e + 1]), dot);
-        }
+    for (int q = 0; q < 2; ++q) {
+        const int c = c0 / 8 + q;
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + (c >> 3) * 16384 + r * 128 +
+                                                        (((c & 7) ^ (r & 7)) << 4));
+        x[4 * q] = v.x;
+        x[4 * q + 1] = v.y;
+        x[4 * q + 2] = v.z;
+        x[4 * q + 3] = v.w;
     }
-    return dot;
 }
 
-// The dQ tile's drain with the RMSNorm Jacobian: the row dot x . dQ over all
-// d columns (each warpgroup's 64, exchanged through `dotx`, [2][128] floats,
-// when d = 128), then the transformed drain.  x: the tile's raw Q (its
-// consumed stage, which the drain then uses as staging).
+// The dQ tile's drain with the RMSNorm Jacobian.  The keys are normalised
+// (k_hat) and x = alpha c q . k_hat, so the TMEM tile T = dS K_hat gives the
+// gradient alpha T for the normalised row, and its dot with the raw row is
+// q . (alpha T) = alpha sum_j dS_j s_j, the row's `dot` over all keys (the
+// warpgroups' shares added): dq = alpha c (T - q dot c^2 / (d g^2)).  The
+// raw row's columns [64 wg, 64 wg + 64) come from the tile's Q stage, all
+// read before the drain's first staging write goes over them.
 template <int D>
 static __device__ __noinline__ void drain_dq_norm(uint32_t trow, int wg, int r, const uint8_t* qtile,
-                                                  float* dotx, uint8_t* stage, const CUtensorMap* map,
+                                                  float dot, uint8_t* stage, const CUtensorMap* map,
                                                   int x0, int y0, float* dst, int64_t rs, int nrows,
                                                   bool atomic, float alpha, float ci, float gain,
                                                   int quarter, int lane, uint64_t* release) {
     uint32_t xq[32];
     load_row_bf16<2>(qtile, r, 64 * wg, xq);
-    float dot = row_dot_tmem<2>(trow, kColDP + 64 * wg, xq);
-    if (D == 128) {
-        dotx[wg * 128 + r] = dot;
-        named_bar_sync(1, 256);
-        dot += dotx[(1 - wg) * 128 + r];
-    }
     const float kappa = dot * ci * ci / ((float)D * gain * gain);
-    drain_warp_norm<2>(trow, kColDP + 64 * wg, stage, map, x0, y0, dst, rs, nrows, atomic, alpha * ci,
-                       kappa, xq, quarter, lane, release);
+    drain_warp_norm<2>(
+        trow, kColDP + 64 * wg, stage, map, x0, y0, dst, rs, nrows, atomic, alpha * ci, kappa,
+        [&](int pass, int hf, uint32_t (&x8)[8]) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x8[e] = xq[16 * pass + 8 * hf + e];
+        },
+        quarter, lane, release);
 }
 
-// The unit's dK drain with the RMSNorm Jacobian (warpgroup 1): the key row's
-// raw values from the K stage, which then goes back to the producer
-// (`kv_empty`), the row dot, the transformed drain.
+// The unit's dK drain with the RMSNorm Jacobian (warpgroup 1).  In terms of
+// the normalised key row k_hat (the K stage holds it) and the TMEM row U
+// (the gradient for k_hat is alpha U): dk = alpha c (U - k_hat (k_hat . U)
+// / (d g^2)).  The K stage goes back to the producer (`kv_empty`) after the
+// drain's last read of it.
 template <int D>
 static __device__ __noinline__ void drain_dk_norm(uint32_t trow, int r, const uint8_t* ktile,
                                                   uint8_t* stage, const CUtensorMap* map, int x0,
                                                   int y0, float* dst, int64_t rs, int nrows,
                                                   float alpha, float cj, float gain, int quarter,
                                                   int lane, uint64_t* kv_empty, uint64_t* release) {
-    uint32_t xk[D / 2];
-    load_row_bf16<D / 32>(ktile, r, 0, xk);
+    float dot = 0.0f;
+    if (quarter * 32 < nrows) {
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t v[16], x8[8];
+            tmem_ld16(trow + kColDK + c0, v);
+            load_row16(ktile, r, c0, x8);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                dot = fmaf(bf16_lo(x8[e]), __uint_as_float(v[2 * e]), dot);
+                dot = fmaf(bf16_hi(x8[e]), __uint_as_float(v[2 * e + 1]), dot);
+            }
+        }
+    }
+    const float kappa = dot / ((float)D * gain * gain);
+    drain_warp_norm<D / 32>(
+        trow, kColDK, stage, map, x0, y0, dst, rs, nrows, false, alpha * cj, kappa,
+        [&](int pass, int hf, uint32_t (&x8)[8]) { load_row16(ktile, r, 32 * pass + 16 * hf, x8); },
+        quarter, lane, release);
     mbar_arrive(kv_empty);
-    const float dot = row_dot_tmem<D / 32>(trow, kColDK, xk);
-    const float kappa = dot * cj * cj / ((float)D * gain * gain);
-    drain_warp_norm<D / 32>(trow, kColDK, stage, map, x0, y0, dst, rs, nrows, false, alpha * cj,
-                            kappa, xk, quarter, lane, release);
 }
 
 // P and dS of one pair from its score s and dP: GDPA, P = act(alpha s) and
@@ -444,7 +465,7 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
     uint8_t* ps = smem + C::kOffPS;
     uint8_t* stage = ps + wg * kHalfBytes;
     const int64_t rs = (int64_t)prm.H * D;
-    const ActScale ksc = act_scale<ACT>(prm.alpha);
+    ActScale ksc = act_scale<ACT>(prm.alpha);
     uint32_t nu = 0, i = 0;
     int pending_q = -1;   // Q stage still read by this warp's last dQ stores
     for (int t = seg0; t < seg1; ++t) {
@@ -499,14 +520,15 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             if (m == u.m0 && nu > 0 && !wg_wait(&bars[C::kPSFree], (nu - 1) & 1, ab, 47)) return;
             if (!wg_wait(&bars[C::kPVDone], (i & 1) ^ 1, ab, 44)) return;
             tc_fence_after();
-            // fused RMSNorm: this row's scale from the tile's raw Q
+            // fused RMSNorm: the keys are normalised; this row's scale c,
+            // from the tile's raw Q, joins alpha (x = alpha c q . k_hat)
             float ci = 1.0f;
-            const float* kscale = nullptr;
+            float gdot = 0.0f;   // sum_j dS_j s_j over this warpgroup's keys
             if constexpr (NORM) {
                 if (!wg_wait(&bars[C::kQFull + (i & 1)], (i >> 1) & 1, ab, 42)) return;
                 ci = row_scale<D>(smem + C::kOffQ + (i & 1) * C::kTileBytes, r, prm.qk_gain,
                                   prm.qk_eps);
-                kscale = prm.kscale + (int64_t)h * prm.kscale_ld + u.kvt0;
+                ksc = act_scale<ACT>(prm.alpha * ci);
             }
             uint32_t pp[4][8];
             if (warp_rows) {
@@ -515,15 +537,17 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                     const int sidx = wg + 2 * k;
                     if (sidx < nh) {
                         const int col0 = sidx * 16;
-                        uint32_t sv[16], dv[16], pd[8];
+                        // pd: dS (TMEM, the A operand of dQ = dS K); pq:
+                        // dS for dK = dS^T Q, times the row's c when fused
+                        // RMSNorm gives dK for the normalised keys
+                        uint32_t sv[16], dv[16], pd[8], pq[8];
                         tmem_ld16(trow + kColS + col0, sv);
                         tmem_ld16(trow + kColDP + col0, dv);
                         tmem_ld_wait();
-                        if constexpr (NORM) scale_step(sv, ci, kscale + col0);
                         const bool full = !windowed && col0 + 16 <= u.nkv;
                         if (!row_ok) {
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) pp[k][e] = pd[e] = 0u;
+                            for (int e = 0; e < 8; ++e) pp[k][e] = pd[e] = pq[e] = 0u;
                         } else if (full) {
 #pragma unroll
                             for (int e = 0; e < 16; e += 2) {
@@ -534,6 +558,11 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                                               ksc, lse2, drow, a1, d1);
                                 pp[k][e >> 1] = pack_bf16x2(a0, a1);
                                 pd[e >> 1] = pack_bf16x2(d0, d1);
+                                if constexpr (NORM) {
+                                    pq[e >> 1] = pack_bf16x2(d0 * ci, d1 * ci);
+                                    gdot = fmaf(d0, __uint_as_float(sv[e]), gdot);
+                                    gdot = fmaf(d1, __uint_as_float(sv[e + 1]), gdot);
+                                }
                             }
                         } else {
 #pragma unroll
@@ -551,25 +580,17 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                                                   ksc, lse2, drow, a, ds);
                                     p2[w] = valid ? a : 0.0f;
                                     d2[w] = valid ? ds : 0.0f;
+                                    if constexpr (NORM)
+                                        gdot = fmaf(d2[w], __uint_as_float(sv[e + w]), gdot);
                                 }
                                 pp[k][e >> 1] = pack_bf16x2(p2[0], p2[1]);
                                 pd[e >> 1] = pack_bf16x2(d2[0], d2[1]);
+                                if constexpr (NORM) pq[e >> 1] = pack_bf16x2(d2[0] * ci, d2[1] * ci);
                             }
                         }
                         if constexpr (NORM) {
-                            // dK = dS^T Q of the normalised Q rows: dS times
-                            // the row's c into shared memory; dQ = dS K of the
-                            // normalised keys: dS times each key's c into TMEM
-                            uint32_t pdk[8];
-#pragma unroll
-                            for (int e = 0; e < 16; e += 2) {
-                                const float d0 = bf16_lo(pd[e >> 1]), d1 = bf16_hi(pd[e >> 1]);
-                                pdk[e >> 1] = pack_bf16x2(d0 * __ldg(kscale + col0 + e),
-                                                          d1 * __ldg(kscale + col0 + e + 1));
-                                pd[e >> 1] = pack_bf16x2(d0 * ci, d1 * ci);
-                            }
-                            store_half_chunk(ps, sidx >> 1, sidx & 1, r, pd);
-                            tmem_st8(trow + kColS + col0, pdk);
+                            store_half_chunk(ps, sidx >> 1, sidx & 1, r, pq);
+                            tmem_st8(trow + kColS + col0, pd);
                         } else {
                             store_half_chunk(ps, sidx >> 1, sidx & 1, r, pd);
                             // and packed into the step's own S columns
@@ -579,6 +600,10 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                     }
                 }
                 tmem_st_wait();
+            }
+            if constexpr (NORM) {   // this warpgroup's share of the row dot
+                reinterpret_cast<float*>(smem + C::kOffDot)[wg * 128 + r] = gdot;
+                mbar_arrive(&bars[C::kDotFull]);
             }
             tc_fence_before();
             mbar_arrive(&bars[C::kSFree]);
@@ -603,8 +628,10 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             uint8_t* dq_stage = smem + C::kOffQ + (i & 1) * C::kTileBytes + wg * kHalfBytes;
             if constexpr (NORM) {
                 if (D == 128 || wg == 0) {
+                    if (!wg_wait(&bars[C::kDotFull], i & 1, ab, 49)) return;
+                    const float* dotx = reinterpret_cast<const float*>(smem + C::kOffDot);
                     drain_dq_norm<D>(trow, wg, r, smem + C::kOffQ + (i & 1) * C::kTileBytes,
-                                     reinterpret_cast<float*>(smem + C::kOffDot), dq_stage, tmDQ,
+                                     dotx[r] + dotx[128 + r], dq_stage, tmDQ,
                                      h * D + 64 * wg, dq_row0 + m * kBM, dq + 64 * wg, rs, nq,
                                      atomic_dq, prm.alpha, ci, prm.qk_gain, quarter, lane,
                                      &bars[C::kDQFree]);
@@ -675,7 +702,7 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             256, 1, 256, 1,       // p full, pv done, ds full, dk done
             1, 256, 128, 128,     // acc full, acc free, stage x2
             256, 1,               // ps free, mma done
-            1                     // dq done
+            1, 256                // dq done, row dots written (fused RMSNorm)
         };
         for (int b = 0; b < C::kNumBars; ++b) mbar_init(&bars[b], counts[b]);
         *abort_flag = 0;
@@ -754,6 +781,11 @@ gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, 
             return GDPA_ERR_CUDA;
     }
     if (p.n_bwd == 0) return GDPA_OK;
+    if (p.qk_gain > 0.0f) {   // fused RMSNorm: the normalised keys first
+        gdpa_status ks;
+        k = plan_key_norm(p, k, st, &ks);
+        if (ks != GDPA_OK) return ks;
+    }
     CUtensorMap maps[7];
     const uint64_t q_rows = p.Tq > 0 ? (uint64_t)p.Tq : 1;
     const uint64_t qt_rows = dq_rows > 0 ? (uint64_t)dq_rows : 1;   // Q and dQ tensors
@@ -786,15 +818,10 @@ gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, 
     prm.timing = p.timing;
     prm.wait_ns = tc::wait_limit_ns(p.wait_limit_us);
     prm.stall = p.stall;
-    prm.kscale = nullptr;
+    prm.kscale = p.qk_gain > 0.0f ? p.d_kscale : nullptr;
     prm.kscale_ld = p.Tkv + 128;
     prm.qk_gain = p.qk_gain;
     prm.qk_eps = p.qk_eps;
-    if (p.qk_gain > 0.0f) {   // fused RMSNorm: the keys' scales first
-        gdpa_status ks;
-        prm.kscale = plan_key_scales(p, k, st, &ks);
-        if (ks != GDPA_OK) return ks;
-    }
     if (p.timing) p.timed[1] = 1;
     gdpa_status s = GDPA_OK;
     if (p.d == 128) {

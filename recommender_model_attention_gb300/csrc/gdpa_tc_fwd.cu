@@ -101,10 +101,8 @@ struct FwdParams {
     int timing;
     uint64_t wait_ns;   // bounded-wait limit
     int stall;          // test hook: CTA 0 skips its first Q load
-    // fused RMSNorm of Q and K (or NULL): g / rms of every key row, [H][ld]
-    // floats, and the gain and eps applied to the query rows in the kernel
-    const float* kscale;
-    int64_t kscale_ld;
+    // fused RMSNorm (qk_gain > 0): the keys arrive normalised; each query
+    // row's scale g / rms is computed from its tile and folded into alpha
     float qk_gain, qk_eps;
 };
 
@@ -349,9 +347,9 @@ template <int D>
 __device__ float softmax_tile(const FwdTile& tile, const FwdParams& prm, uint64_t* bars,
                               uint32_t& s_use, uint32_t& x_use, uint32_t s_tmem,
                               uint32_t o_tmem_part0, int wg, int part, int r, bool warp_rows,
-                              float ci, const float* kscale, const Abort& ab) {
+                              float alpha, const Abort& ab) {
     using C = FwdCfg<D>;
-    const float c2 = prm.alpha * 1.44269504088896340736f;   // alpha log2(e)
+    const float c2 = alpha * 1.44269504088896340736f;   // alpha log2(e)
     const int ipos = tile.i0 + r;
     const int nit = tile_items<true>(tile);
     float m = -INFINITY, l = 0.0f;
@@ -398,7 +396,6 @@ __device__ float softmax_tile(const FwdTile& tile, const FwdParams& prm, uint64_
                             uint32_t sv[16];
                             tmem_ld16(s_tmem + col0, sv);
                             tmem_ld_wait();
-                            if (kscale) scale_step(sv, ci, kscale + jbase + col0);
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const float t = c2 * __uint_as_float(sv[e]);
@@ -430,7 +427,6 @@ __device__ float softmax_tile(const FwdTile& tile, const FwdParams& prm, uint64_
                             uint32_t sv[16], pk[8];
                             tmem_ld16(s_tmem + col0, sv);
                             tmem_ld_wait();
-                            if (kscale) scale_step(sv, ci, kscale + jbase + col0);
 #pragma unroll
                             for (int e = 0; e < 16; e += 2) {
                                 float pv2[2];
@@ -465,7 +461,7 @@ __device__ float softmax_tile(const FwdTile& tile, const FwdParams& prm, uint64_
     return l > 0.0f ? 1.0f / l : 0.0f;
 }
 
-template <int D, int ACT, bool SPLIT>
+template <int D, int ACT, bool SPLIT, bool NORM>
 __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const CUtensorMap* tmW,
                             uint8_t* smem,
                             uint64_t* bars, uint32_t tmem, int seg0, int seg1, const Abort& ab) {
@@ -480,7 +476,7 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const uint32_t s_tmem = tmem + wg * 256 + lane_addr;
     const uint32_t o_tmem = tmem + wg * 256 + 128 + lane_addr + part * (D / 2);
-    const ActScale ksc = act_scale<ACT>(prm.alpha);
+    ActScale ksc = act_scale<ACT>(prm.alpha);
     uint32_t a = 0, s_use = 0, o_use = 0, x_use = 0;
     for (int t = seg0; t < seg1; ++t) {
         const FwdTile tile = load_tile(prm.tiles + t);
@@ -495,19 +491,20 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
         const uint32_t qs = a % C::kNQ;
         const bool warp_rows = quarter * 32 < tile.nq;
         const int ipos = tile.i0 + r;
-        // fused RMSNorm: this row's scale from the tile's raw Q
-        float ci = 1.0f;
-        const float* kscale = nullptr;
-        if (prm.kscale) {
+        // fused RMSNorm: the keys are normalised; this row's scale c, from
+        // the tile's raw Q, joins alpha (x = alpha c q . k_hat)
+        float alpha_row = prm.alpha;
+        if constexpr (NORM) {
             if (!wg_wait(&bars[C::kBarQFull + qs], (a / C::kNQ) & 1, ab, 15)) return;
-            ci = row_scale<D>(smem + C::kOffQ + qs * C::kTileBytes, r, prm.qk_gain, prm.qk_eps);
-            kscale = prm.kscale + (int64_t)tile.h * prm.kscale_ld + tile.kvt0;
+            alpha_row *= row_scale<D>(smem + C::kOffQ + qs * C::kTileBytes, r, prm.qk_gain,
+                                      prm.qk_eps);
+            ksc = act_scale<ACT>(alpha_row);
         }
         float oscale = 1.0f;   // the softmax variant's 1 / (row sum)
         if constexpr (ACT == kSoftmax) {
             oscale = softmax_tile<D>(tile, prm, bars, s_use, x_use, s_tmem,
                                      tmem + wg * 256 + 128 + lane_addr, (int)wg, part, r, warp_rows,
-                                     ci, kscale, ab);
+                                     alpha_row, ab);
             if (__any_sync(0xffffffffu, oscale < 0.0f)) return;
         } else
         for (int kb = tile.kb0; kb < tile.kb1; ++kb) {
@@ -533,7 +530,6 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
                             uint32_t sv[16], pk[8];
                             tmem_ld16(s_tmem + col0, sv);
                             tmem_ld_wait();
-                            if (kscale) scale_step(sv, ci, kscale + jbase + col0);
                             // the chunk's keys against the window of this
                             // warp's 32 rows (warp-uniform): all valid, none
                             // valid, or mixed (per-pair masks)
@@ -670,7 +666,7 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
     }
 }
 
-template <int D, int ACT, bool SPLIT>
+template <int D, int ACT, bool SPLIT, bool NORM>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -732,7 +728,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         fwd_mma_pv<D, ACT == kSoftmax>(prm, smem, bars, tmem, seg0, seg1, ab);
         __syncwarp();
     } else {
-        fwd_compute<D, ACT, SPLIT>(prm, &tmO, &tmW, smem, bars, tmem, seg0, seg1, ab);
+        fwd_compute<D, ACT, SPLIT, NORM>(prm, &tmO, &tmW, smem, bars, tmem, seg0, seg1, ab);
         if (lane == 0) bulk_wait_all();
         __syncwarp();
     }
@@ -750,17 +746,27 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     }
 }
 
-template <int D, int ACT, bool SPLIT = false>
-gdpa_status launch(int S, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                   const CUtensorMap& mo, const CUtensorMap& mw, const FwdParams& prm,
-                   cudaStream_t st) {
+template <int D, int ACT, bool SPLIT, bool NORM>
+gdpa_status launch1(int S, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                    const CUtensorMap& mo, const CUtensorMap& mw, const FwdParams& prm,
+                    cudaStream_t st) {
     using C = FwdCfg<D>;
-    auto kern = tc_fwd_kernel<D, ACT, SPLIT>;
+    auto kern = tc_fwd_kernel<D, ACT, SPLIT, NORM>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) !=
         cudaSuccess)
         return GDPA_ERR_CUDA;
     kern<<<S, kThreads, C::kSmemBytes, st>>>(mq, mk, mv, mo, mw, prm);
     return cudaGetLastError() == cudaSuccess ? GDPA_OK : GDPA_ERR_CUDA;
+}
+
+// the fused RMSNorm is a separate instantiation, so that the plain kernels
+// carry none of its work
+template <int D, int ACT, bool SPLIT = false>
+gdpa_status launch(int S, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                   const CUtensorMap& mo, const CUtensorMap& mw, const FwdParams& prm,
+                   cudaStream_t st) {
+    return prm.qk_gain > 0.0f ? launch1<D, ACT, SPLIT, true>(S, mq, mk, mv, mo, mw, prm, st)
+                              : launch1<D, ACT, SPLIT, false>(S, mq, mk, mv, mo, mw, prm, st);
 }
 
 // Key-split plans: O = bf16(W), four elements per thread and step.
@@ -779,8 +785,7 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
                               int64_t Tkv, int mask, int window, const void* q, int64_t q_rows,
                               int shared_q, const void* k, const void* v, void* o, float* lse,
                               float* w, float alpha, int act, cudaStream_t st,
-                              uint32_t wait_limit_us, int stall, const float* kscale,
-                              int64_t kscale_ld, float qk_gain, float qk_eps) {
+                              uint32_t wait_limit_us, int stall, float qk_gain, float qk_eps) {
     if (d != 64 && d != 128) return GDPA_ERR_UNSUPPORTED;
     if (w && (d != 128 || act == kSoftmax)) return GDPA_ERR_UNSUPPORTED;
     if (Tq == 0) return GDPA_OK;
@@ -817,8 +822,6 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
     prm.timing = times != nullptr && smid != nullptr;
     prm.wait_ns = tc::wait_limit_ns(wait_limit_us);
     prm.stall = stall;
-    prm.kscale = kscale;
-    prm.kscale_ld = kscale_ld;
     prm.qk_gain = qk_gain;
     prm.qk_eps = qk_eps;
     gdpa_status s = GDPA_OK;
@@ -855,17 +858,16 @@ gdpa_status launch_tc_fwd(Plan& p, const void* q, const void* k, const void* v, 
         w = p.d_wsplit;
     }
     if (p.timing) p.timed[0] = 1;
-    const float* kscale = nullptr;
-    if (p.qk_gain > 0.0f) {   // fused RMSNorm: the keys' scales first
+    if (p.qk_gain > 0.0f) {   // fused RMSNorm: the normalised keys first
         gdpa_status ks;
-        kscale = plan_key_scales(p, k, st, &ks);
+        k = plan_key_norm(p, k, st, &ks);
         if (ks != GDPA_OK) return ks;
     }
     gdpa_status s = launch_tc_fwd_raw(
         p.d_fwd, p.d_fwd_seg, p.S, p.d_err, p.timing ? p.d_times : nullptr,
         p.timing ? p.d_smid : nullptr, p.H, p.d, p.Tq, p.Tkv, p.mask, p.window, q,
         p.shared_q > 0 ? (int64_t)p.shared_q : p.Tq, p.shared_q > 0, k, v, o, lse, w, alpha, act,
-        st, p.wait_limit_us, p.stall, kscale, p.Tkv + 128, p.qk_gain, p.qk_eps);
+        st, p.wait_limit_us, p.stall, p.qk_gain, p.qk_eps);
     if (s == GDPA_OK) p.launches += 1;
     if (s == GDPA_OK && w) {
         const int64_t n4 = p.Tq * p.H * p.d / 4;

@@ -146,10 +146,6 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 // ---------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -392,10 +388,9 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // ---------------------------------------------------------------- fused RMSNorm
 
-// Fused RMSNorm: the scores of the raw rows are scaled by c_i c'_j, c = g /
-// rms of the row, so that x = alpha c_i c'_j q_i . k_j is the score of the
-// normalised rows.  c of row r of a [128 x D] bf16 tile of raw rows in shared
-// memory (128-byte-swizzled halves of 64 columns, 16 KB each).
+// Fused RMSNorm: c = g / rms of row r of a [128 x D] bf16 tile of raw rows
+// in shared memory (128-byte-swizzled halves of 64 columns, 16 KB each); the
+// kernels fold it into alpha, x = alpha c q . k_hat with normalised keys.
 template <int D>
 __device__ __forceinline__ float row_scale(const uint8_t* tile, int r, float gain, float eps) {
     float ss = 0.0f;
@@ -415,13 +410,6 @@ __device__ __forceinline__ float row_scale(const uint8_t* tile, int r, float gai
         }
     }
     return gain / sqrtf(ss / (float)D + eps);
-}
-
-// The 16 scores of a step, scaled by c_i and the keys' c'_j (j = j0 ..).
-__device__ __forceinline__ void scale_step(uint32_t (&sv)[16], float ci, const float* kscale_j0) {
-#pragma unroll
-    for (int e = 0; e < 16; ++e)
-        sv[e] = __float_as_uint(__uint_as_float(sv[e]) * (ci * __ldg(kscale_j0 + e)));
 }
 
 // Columns [c0, c0 + 32 n) of row r of the same tile layout, as packed bf16

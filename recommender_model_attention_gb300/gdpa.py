@@ -9,6 +9,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+from typing import NamedTuple
 
 import numpy as np
 
@@ -74,6 +75,10 @@ def lib():
             "gdpa_shard_batch": [i32p, i32p, st, st, st, st, st, i32p, i64p],
             "gdpa_softmax_fwd": [vp, st, vp, vp, vp, vp, vp, ctypes.c_float, vp],
             "gdpa_softmax_bwd": [vp, st, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, vp],
+            "gdpa_mx_quantise": [vp, ctypes.c_int64, vp, vp, vp],
+            "gdpa_mx_dequantise": [vp, vp, ctypes.c_int64, vp, vp],
+            "gdpa_fwd_mx": [vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, st, vp],
+            "gdpa_bwd_mx": [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, st, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -294,6 +299,95 @@ def gdpa_bwd(plan: Plan, q, k, v, do, dq=None, dk=None, dv=None, alpha=None,
     _ok(lib().gdpa_bwd(plan.handle, _dtype_id(q), _ptr(q), _ptr(k), _ptr(v), _ptr(do), _ptr(dq),
                        _ptr(dk), _ptr(dv), ctypes.c_float(alpha), ACT[act], _stream_ptr(stream)),
         "gdpa_bwd")
+    return dq, dk, dv
+
+
+class MX(NamedTuple):
+    """An MXFP8 tensor: E4M3 codes (uint8, the values' shape) and one E8M0
+    scale byte (exponent + 127) per 32 values along the last axis."""
+    elements: "object"
+    scales: "object"
+
+
+def mx_quantise(x, stream=None) -> MX:
+    """bf16 CUDA tensor (last axis a multiple of 32) -> its MXFP8 encoding."""
+    import torch
+    if not x.is_cuda or not x.is_contiguous() or x.dtype != torch.bfloat16:
+        raise ValueError("mx_quantise takes a contiguous bfloat16 CUDA tensor")
+    if x.shape[-1] % 32:
+        raise ValueError("the last axis must be a multiple of 32")
+    el = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    sc = torch.empty(x.shape[:-1] + (x.shape[-1] // 32,), dtype=torch.uint8, device=x.device)
+    _ok(lib().gdpa_mx_quantise(_ptr(x), x.numel(), _ptr(el), _ptr(sc), _stream_ptr(stream)),
+        "gdpa_mx_quantise")
+    return MX(el, sc)
+
+
+def mx_dequantise(m: MX, stream=None):
+    """The bf16 values an MXFP8 tensor stands for."""
+    import torch
+    el, sc = m
+    _mx_check(el, sc, 0, None, "x")
+    x = torch.empty(el.shape, dtype=torch.bfloat16, device=el.device)
+    _ok(lib().gdpa_mx_dequantise(_ptr(el), _ptr(sc), el.numel(), _ptr(x), _stream_ptr(stream)),
+        "gdpa_mx_dequantise")
+    return x
+
+
+def _mx_check(el, sc, rows, plan, name):
+    import torch
+    for t, what in ((el, "elements"), (sc, "scales")):
+        if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.uint8:
+            raise ValueError("%s %s must be a contiguous uint8 CUDA tensor" % (name, what))
+    if tuple(sc.shape) != tuple(el.shape[:-1]) + (el.shape[-1] // 32,) or el.shape[-1] % 32:
+        raise ValueError("%s: scales must have one byte per 32 elements" % name)
+    if plan is not None and tuple(el.shape) != (rows, plan.H, plan.d):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(el.shape),
+                                                           (rows, plan.H, plan.d)))
+
+
+def gdpa_fwd_mx(plan: Plan, q: MX, k: MX, v, o=None, alpha=None, act: str = "gelu_erf",
+                stream=None):
+    """gdpa_fwd with Q and K in MXFP8 (``mx_quantise``); V and O bf16."""
+    import torch
+    _mx_check(q.elements, q.scales, plan.q_rows, plan, "q")
+    _mx_check(k.elements, k.scales, plan.Tkv, plan, "k")
+    _check(v, plan.Tkv, plan, "v", torch.bfloat16)
+    if o is None:
+        o = torch.empty((plan.Tq, plan.H, plan.d), dtype=torch.bfloat16, device=v.device)
+    _check(o, plan.Tq, plan, "o", torch.bfloat16)
+    alpha = plan.d ** -0.5 if alpha is None else float(alpha)
+    _ok(lib().gdpa_fwd_mx(plan.handle, _ptr(q.elements), _ptr(q.scales), _ptr(k.elements),
+                          _ptr(k.scales), _ptr(v), _ptr(o), ctypes.c_float(alpha), ACT[act],
+                          _stream_ptr(stream)), "gdpa_fwd_mx")
+    return o
+
+
+def gdpa_bwd_mx(plan: Plan, q, k, v, do, dq=None, dk=None, dv=None, alpha=None,
+                act: str = "gelu_erf", stream=None):
+    """gdpa_bwd with Q and K in MXFP8: float32 (dQ, dK, dV) with respect to the
+    values the MXFP8 tensors stand for.  q = k = None reuses the bf16
+    expansion of the plan's previous MXFP8 call (the forward's)."""
+    import torch
+    reuse = q is None and k is None
+    if not reuse:
+        _mx_check(q.elements, q.scales, plan.q_rows, plan, "q")
+        _mx_check(k.elements, k.scales, plan.Tkv, plan, "k")
+        ptrs = [_ptr(q.elements), _ptr(q.scales), _ptr(k.elements), _ptr(k.scales)]
+    else:
+        ptrs = [ctypes.c_void_p(0)] * 4
+    _check(v, plan.Tkv, plan, "v", torch.bfloat16)
+    _check(do, plan.Tq, plan, "do", torch.bfloat16)
+    f32 = torch.float32
+    dq = torch.empty((plan.q_rows, plan.H, plan.d), dtype=f32, device=v.device) if dq is None else dq
+    dk = torch.empty(v.shape, dtype=f32, device=v.device) if dk is None else dk
+    dv = torch.empty(v.shape, dtype=f32, device=v.device) if dv is None else dv
+    _check(dq, plan.q_rows, plan, "dq", f32)
+    _check(dk, plan.Tkv, plan, "dk", f32)
+    _check(dv, plan.Tkv, plan, "dv", f32)
+    alpha = plan.d ** -0.5 if alpha is None else float(alpha)
+    _ok(lib().gdpa_bwd_mx(plan.handle, *ptrs, _ptr(v), _ptr(do), _ptr(dq), _ptr(dk), _ptr(dv),
+                          ctypes.c_float(alpha), ACT[act], _stream_ptr(stream)), "gdpa_bwd_mx")
     return dq, dk, dv
 
 
