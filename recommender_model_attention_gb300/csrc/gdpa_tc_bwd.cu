@@ -290,10 +290,9 @@ __device__ __forceinline__ void store_half_chunk(uint8_t* ps, int c, int hh, int
 //     dx = c (dy - x (x . dy) c^2 / (d g^2)),   c = g / rms(x),
 // i.e. out = sc (v - kappa x) with sc = alpha c and kappa = (x . v) c^2 /
 // (d g^2) (or, in terms of the normalised row x_hat = c x, kappa = (x_hat .
-// v) / (d g^2) with x_hat in place of x).  Columns [col, col + 32 P) of this
-// warp's 32 lanes, 16 at a time; xw(pass, half, x8) gives the 8 packed bf16
-// words of x for columns col + 32 pass + 16 half ..; staging and stores as
-// drain_warp.
+// v) / (d g^2) with x_hat in place of x).  Columns [col, col + 16 P) of this
+// warp's 32 lanes, 16 at a time; xw(step, x8) gives the 8 packed bf16 words
+// of x for columns col + 16 step ..; staging and stores as drain_warp.
 template <int P, typename XW>
 __device__ __forceinline__ void drain_warp_norm(uint32_t trow, uint32_t col, uint8_t* stage,
                                                 const CUtensorMap* map, int x0, int y0, float* dst,
@@ -306,56 +305,56 @@ __device__ __forceinline__ void drain_warp_norm(uint32_t trow, uint32_t col, uin
     uint8_t* wst = stage + quarter * 4096;
 #pragma unroll
     for (int pass = 0; pass < P; ++pass) {
-        if (full && pass > 0) {
-            if (lane == 0) bulk_wait_read_all();
-            __syncwarp();
+        uint32_t v[16];
+        if (any) {
+            tmem_ld16(trow + col + pass * 16, v);
+            tmem_ld_wait();
         }
+        if (pass == P - 1 && release) {
+            tc_fence_before();
+            mbar_arrive(release);
+        }
+        if (!any) continue;
+        uint32_t x8[8];
+        xw(pass, x8);
+        float o[16];
+        const uint64_t nk2 = f2_make(-kappa, -kappa), sc2 = f2_make(sc, sc);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-            uint32_t v[16];
-            if (any) {
-                tmem_ld16(trow + col + pass * 32 + hf * 16, v);
-                tmem_ld_wait();
-            }
-            if (pass == P - 1 && hf == 1 && release) {
-                tc_fence_before();
-                mbar_arrive(release);
-            }
-            if (!any) continue;
-            uint32_t x8[8];
-            xw(pass, hf, x8);
-            float o[16];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                o[2 * e] = sc * fmaf(-kappa, bf16_lo(x8[e]), __uint_as_float(v[2 * e]));
-                o[2 * e + 1] = sc * fmaf(-kappa, bf16_hi(x8[e]), __uint_as_float(v[2 * e + 1]));
-            }
-            if (full) {
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<float4*>(wst + lane * 128 + (((4 * hf + c) ^ (lane & 7)) << 4)) =
-                        make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-            } else if (row0 + lane < nrows) {
-                float* d = dst + (int64_t)(row0 + lane) * rs + pass * 32 + hf * 16;
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const float4 w = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-                    if (atomic)
-                        atomicAdd(reinterpret_cast<float4*>(d + 4 * c), w);
-                    else
-                        *reinterpret_cast<float4*>(d + 4 * c) = w;
-                }
-            }
+        for (int e = 0; e < 8; ++e) {
+            const float2 r2 = f2_split(f2_mul(
+                sc2, f2_fma(nk2, f2_bf16x2(x8[e]),
+                            f2_make(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1])))));
+            o[2 * e] = r2.x;
+            o[2 * e + 1] = r2.y;
         }
         if (full) {
+            uint8_t* buf = wst + (pass & 1) * 2048;
+            if (pass >= 2) {
+                if (lane == 0) bulk_wait_read_but1();
+                __syncwarp();
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                *reinterpret_cast<float4*>(buf + stage_off64(lane, c)) =
+                    make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 if (atomic)
-                    tma_reduce_add_2d(map, wst, x0 + pass * 32, y0 + row0);
+                    tma_reduce_add_2d(map, buf, x0 + pass * 16, y0 + row0);
                 else
-                    tma_store_2d(map, wst, x0 + pass * 32, y0 + row0);
+                    tma_store_2d(map, buf, x0 + pass * 16, y0 + row0);
                 bulk_commit();
+            }
+        } else if (row0 + lane < nrows) {
+            float* d = dst + (int64_t)(row0 + lane) * rs + pass * 16;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const float4 w = make_float4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+                if (atomic)
+                    atomicAdd(reinterpret_cast<float4*>(d + 4 * c), w);
+                else
+                    *reinterpret_cast<float4*>(d + 4 * c) = w;
             }
         }
     }
@@ -391,12 +390,13 @@ static __device__ __noinline__ void drain_dq_norm(uint32_t trow, int wg, int r, 
                                                   int quarter, int lane, uint64_t* release) {
     uint32_t xq[32];
     load_row_bf16<2>(qtile, r, 64 * wg, xq);
+    __syncwarp();   // every lane's row is read before any staging write lands on it
     const float kappa = dot * ci * ci / ((float)D * gain * gain);
-    drain_warp_norm<2>(
+    drain_warp_norm<4>(
         trow, kColDP + 64 * wg, stage, map, x0, y0, dst, rs, nrows, atomic, alpha * ci, kappa,
-        [&](int pass, int hf, uint32_t (&x8)[8]) {
+        [&](int step, uint32_t (&x8)[8]) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x8[e] = xq[16 * pass + 8 * hf + e];
+            for (int e = 0; e < 8; ++e) x8[e] = xq[8 * step + e];
         },
         quarter, lane, release);
 }
@@ -428,9 +428,9 @@ static __device__ __noinline__ void drain_dk_norm(uint32_t trow, int r, const ui
         }
     }
     const float kappa = dot / ((float)D * gain * gain);
-    drain_warp_norm<D / 32>(
+    drain_warp_norm<D / 16>(
         trow, kColDK, stage, map, x0, y0, dst, rs, nrows, false, alpha * cj, kappa,
-        [&](int pass, int hf, uint32_t (&x8)[8]) { load_row16(ktile, r, 32 * pass + 16 * hf, x8); },
+        [&](int step, uint32_t (&x8)[8]) { load_row16(ktile, r, 16 * step, x8); },
         quarter, lane, release);
     mbar_arrive(kv_empty);
 }
@@ -523,7 +523,7 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             // fused RMSNorm: the keys are normalised; this row's scale c,
             // from the tile's raw Q, joins alpha (x = alpha c q . k_hat)
             float ci = 1.0f;
-            float gdot = 0.0f;   // sum_j dS_j s_j over this warpgroup's keys
+            uint64_t gdot2 = f2_make(0.0f, 0.0f);   // sum_j dS_j s_j over this warpgroup's keys
             if constexpr (NORM) {
                 if (!wg_wait(&bars[C::kQFull + (i & 1)], (i >> 1) & 1, ab, 42)) return;
                 ci = row_scale<D>(smem + C::kOffQ + (i & 1) * C::kTileBytes, r, prm.qk_gain,
@@ -559,9 +559,13 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                                 pp[k][e >> 1] = pack_bf16x2(a0, a1);
                                 pd[e >> 1] = pack_bf16x2(d0, d1);
                                 if constexpr (NORM) {
-                                    pq[e >> 1] = pack_bf16x2(d0 * ci, d1 * ci);
-                                    gdot = fmaf(d0, __uint_as_float(sv[e]), gdot);
-                                    gdot = fmaf(d1, __uint_as_float(sv[e + 1]), gdot);
+                                    const uint64_t d2 = f2_make(d0, d1);
+                                    const float2 q2 = f2_split(f2_mul(d2, f2_make(ci, ci)));
+                                    pq[e >> 1] = pack_bf16x2(q2.x, q2.y);
+                                    gdot2 = f2_fma(d2,
+                                                   f2_make(__uint_as_float(sv[e]),
+                                                           __uint_as_float(sv[e + 1])),
+                                                   gdot2);
                                 }
                             }
                         } else {
@@ -580,12 +584,18 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                                                   ksc, lse2, drow, a, ds);
                                     p2[w] = valid ? a : 0.0f;
                                     d2[w] = valid ? ds : 0.0f;
-                                    if constexpr (NORM)
-                                        gdot = fmaf(d2[w], __uint_as_float(sv[e + w]), gdot);
                                 }
                                 pp[k][e >> 1] = pack_bf16x2(p2[0], p2[1]);
                                 pd[e >> 1] = pack_bf16x2(d2[0], d2[1]);
-                                if constexpr (NORM) pq[e >> 1] = pack_bf16x2(d2[0] * ci, d2[1] * ci);
+                                if constexpr (NORM) {
+                                    const uint64_t dd = f2_make(d2[0], d2[1]);
+                                    const float2 q2 = f2_split(f2_mul(dd, f2_make(ci, ci)));
+                                    pq[e >> 1] = pack_bf16x2(q2.x, q2.y);
+                                    gdot2 = f2_fma(dd,
+                                                   f2_make(__uint_as_float(sv[e]),
+                                                           __uint_as_float(sv[e + 1])),
+                                                   gdot2);
+                                }
                             }
                         }
                         if constexpr (NORM) {
@@ -602,7 +612,8 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                 tmem_st_wait();
             }
             if constexpr (NORM) {   // this warpgroup's share of the row dot
-                reinterpret_cast<float*>(smem + C::kOffDot)[wg * 128 + r] = gdot;
+                const float2 g2 = f2_split(gdot2);
+                reinterpret_cast<float*>(smem + C::kOffDot)[wg * 128 + r] = g2.x + g2.y;
                 mbar_arrive(&bars[C::kDotFull]);
             }
             tc_fence_before();
@@ -665,6 +676,9 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                 drain_dk_norm<D>(trow, r, smem + C::kOffK, stage, tmDK, h * D, u.kvt0, dst, rs,
                                  u.nkv, prm.alpha, cj, prm.qk_gain, quarter, lane,
                                  &bars[C::kKVEmpty], &bars[C::kAccFree]);
+            } else if (NORM) {   // dV, with the norm's 16-column tensor maps
+                drain_warp16(trow, kColDV, D, stage, tmDV, h * D, u.kvt0, dst, rs, u.nkv, false,
+                             1.0f, quarter, lane, &bars[C::kAccFree]);
             } else {
                 drain_warp(trow, wg == 0 ? kColDV : kColDK, D, stage, wg == 0 ? tmDV : tmDK, h * D,
                            u.kvt0, dst, rs, u.nkv, false, wg == 0 ? 1.0f : prm.alpha, quarter,
@@ -787,6 +801,8 @@ gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, 
         if (ks != GDPA_OK) return ks;
     }
     CUtensorMap maps[7];
+    // the fused RMSNorm's drains stage 16 columns at a time
+    const uint32_t norm_cols = p.qk_gain > 0.0f ? 16 : 32;
     const uint64_t q_rows = p.Tq > 0 ? (uint64_t)p.Tq : 1;
     const uint64_t qt_rows = dq_rows > 0 ? (uint64_t)dq_rows : 1;   // Q and dQ tensors
     const void* qp = p.Tq > 0 ? q : k;
@@ -795,9 +811,10 @@ gdpa_status launch_tc_bwd(Plan& p, const void* q, const void* k, const void* v, 
         !tc::make_tmap_bf16(&maps[1], k, (uint64_t)p.Tkv, row, 128) ||
         !tc::make_tmap_bf16(&maps[2], v, (uint64_t)p.Tkv, row, 128) ||
         !tc::make_tmap_bf16(&maps[3], dop, q_rows, row, 128) ||
-        !tc::make_tmap_f32(&maps[4], p.Tq > 0 ? (const void*)dq : (const void*)dk, qt_rows, row, 32) ||
-        !tc::make_tmap_f32(&maps[5], dk, (uint64_t)p.Tkv, row, 32) ||
-        !tc::make_tmap_f32(&maps[6], dv, (uint64_t)p.Tkv, row, 32))
+        !tc::make_tmap_f32(&maps[4], p.Tq > 0 ? (const void*)dq : (const void*)dk, qt_rows, row, 32,
+                           norm_cols) ||
+        !tc::make_tmap_f32(&maps[5], dk, (uint64_t)p.Tkv, row, 32, norm_cols) ||
+        !tc::make_tmap_f32(&maps[6], dv, (uint64_t)p.Tkv, row, 32, norm_cols))
         return GDPA_ERR_CUDA;
     BwdParams prm;
     prm.units = p.d_bwd;

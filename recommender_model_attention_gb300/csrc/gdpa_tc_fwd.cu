@@ -586,7 +586,7 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
                 // a second kernel converts once every tile has landed
                 static_assert(D == 128 && ACT != kSoftmax, "key split: d = 128 GDPA only");
                 const int64_t rs = (int64_t)prm.H * D;
-                drain_warp_inl(tmem + wg * 256 + lane_addr, 128 + part * (D / 2), D / 2,
+                drain_warp16_inl(tmem + wg * 256 + lane_addr, 128 + part * (D / 2), D / 2,
                            smem + C::kOffQ + qs * C::kTileBytes + part * (C::kTileBytes / 2), tmW,
                            tile.h * D + part * (D / 2), tile.qt0,
                            prm.W + (int64_t)tile.qt0 * rs + tile.h * D + part * (D / 2), rs,
@@ -801,7 +801,7 @@ gdpa_status launch_tc_fwd_raw(const FwdTile* tiles, const int32_t* seg, int S, i
         !tc::make_tmap_bf16(&mo, o, (uint64_t)Tq, row, 32))
         return GDPA_ERR_CUDA;
     if (w) {
-        if (!tc::make_tmap_f32(&mw, w, (uint64_t)Tq, row, 32)) return GDPA_ERR_CUDA;
+        if (!tc::make_tmap_f32(&mw, w, (uint64_t)Tq, row, 32, 16)) return GDPA_ERR_CUDA;
     } else {
         mw = mo;   // not read
     }

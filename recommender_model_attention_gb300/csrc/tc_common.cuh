@@ -193,6 +193,11 @@ __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// ... all but the most recent group
+__device__ __forceinline__ void bulk_wait_read_but1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 // this thread's bulk stores have completed
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -386,6 +391,35 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// ---------------------------------------------------------------- packed float pairs
+
+// Two floats in one 64-bit register for the f32x2 arithmetic of sm_100 and
+// later (two results per instruction).
+__device__ __forceinline__ uint64_t f2_make(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 f2_split(uint64_t v) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+    return r;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// the two bf16 values of a packed word (low half first) as a float pair
+__device__ __forceinline__ uint64_t f2_bf16x2(uint32_t w) {
+    return f2_make(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 // ---------------------------------------------------------------- fused RMSNorm
 
 // Fused RMSNorm: c = g / rms of row r of a [128 x D] bf16 tile of raw rows
@@ -393,7 +427,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // kernels fold it into alpha, x = alpha c q . k_hat with normalised keys.
 template <int D>
 __device__ __forceinline__ float row_scale(const uint8_t* tile, int r, float gain, float eps) {
-    float ss = 0.0f;
+    uint64_t ss2 = f2_make(0.0f, 0.0f);
 #pragma unroll
     for (int hf = 0; hf < D / 64; ++hf) {
 #pragma unroll
@@ -403,13 +437,13 @@ __device__ __forceinline__ float row_scale(const uint8_t* tile, int r, float gai
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-                const float lo = __uint_as_float(w[u] << 16), hi = __uint_as_float(w[u] & 0xffff0000u);
-                ss = fmaf(lo, lo, ss);
-                ss = fmaf(hi, hi, ss);
+                const uint64_t x2 = f2_bf16x2(w[u]);
+                ss2 = f2_fma(x2, x2, ss2);
             }
         }
     }
-    return gain / sqrtf(ss / (float)D + eps);
+    const float2 ss = f2_split(ss2);
+    return gain / sqrtf((ss.x + ss.y) / (float)D + eps);
 }
 
 // Columns [c0, c0 + 32 n) of row r of the same tile layout, as packed bf16
@@ -439,9 +473,12 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
                     uint32_t box_rows);
 
-// Same for fp32 with a [box_rows][32] box (128-byte rows, 128-byte swizzle).
+// Same for fp32 with a [box_rows][box_cols] box: box_cols = 32 (128-byte
+// rows, 128-byte swizzle: 16-byte chunk c of row r at position c ^ (r & 7))
+// or 16 (64-byte rows, 64-byte swizzle: chunk c of row r at position
+// c ^ ((r >> 1) & 3)); staging buffers 1024-byte aligned.
 bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
-                   uint32_t box_rows);
+                   uint32_t box_rows, uint32_t box_cols);
 
 }  // namespace tc
 }  // namespace gdpa

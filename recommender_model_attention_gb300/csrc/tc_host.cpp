@@ -47,15 +47,17 @@ bool make_tmap_bf16(CUtensorMap* map, const void* base, uint64_t rows, uint64_t 
 }
 
 bool make_tmap_f32(CUtensorMap* map, const void* base, uint64_t rows, uint64_t row_elems,
-                   uint32_t box_rows) {
+                   uint32_t box_rows, uint32_t box_cols) {
+    if (box_cols != 16 && box_cols != 32) return false;
     EncodeTiledFn fn = encode_fn();
     if (!fn || !base || rows == 0) return false;
     const cuuint64_t dims[2] = {row_elems, rows};
     const cuuint64_t strides[1] = {row_elems * 4};
-    const cuuint32_t box[2] = {32, box_rows};
+    const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              box_cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
