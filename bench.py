@@ -43,8 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the unsplit softmax-free kernels; otherwise reported null.
 TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
-    "gdpa_fwd": ("e11c01230c7efa3b", 0.9673),
-    "gdpa_bwd": ("30888e988d692ae0", 1.0268),
+    "gdpa_fwd": ("45e360c415c1d12e", 0.9668),
+    "gdpa_bwd": ("d40c27880e9a7c5c", 1.0266),
 }
 KERNEL_SOURCES = {
     "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh"),
@@ -205,7 +205,7 @@ class Clocks:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "50"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
