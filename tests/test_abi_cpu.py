@@ -224,3 +224,28 @@ def test_qk_norm_argument_checks(gd):
         with pytest.raises(gd.GdpaError):
             p.set_qk_norm(gain, eps)
     p.destroy()
+
+
+def test_mx_argument_checks_on_the_host(gd):
+    # the MXFP8 entry points refuse bad sizes and pointers before touching a
+    # device: counts that are not a multiple of the 32-value block, NULL or
+    # misaligned buffers; n = 0 is a no-op
+    import ctypes
+    L = gd.lib()
+    vp = ctypes.c_void_p
+    a = vp(1 << 20)   # an aligned address that is never dereferenced
+    assert L.gdpa_mx_quantise(a, 48, a, a, None) == 1
+    assert L.gdpa_mx_quantise(a, -32, a, a, None) == 1
+    assert L.gdpa_mx_quantise(None, 32, a, a, None) == 1
+    assert L.gdpa_mx_quantise(vp((1 << 20) + 8), 32, a, a, None) == 1
+    assert L.gdpa_mx_dequantise(a, a, 31, a, None) == 1
+    assert L.gdpa_mx_dequantise(vp((1 << 20) + 4), a, 32, a, None) == 1
+    assert L.gdpa_mx_quantise(None, 0, None, None, None) == 0
+    assert L.gdpa_mx_dequantise(None, None, 0, None, None) == 0
+    # the plan forms: a NULL plan, and a host-only plan, are refused
+    assert L.gdpa_fwd_mx(None, a, a, a, a, a, a, ctypes.c_float(1.0), 0, None) == 1
+    qo = offsets_from_lengths([3, 4])
+    p = gd.Plan(qo, qo, 2, 64, num_sms=4, host_only=True)
+    assert L.gdpa_fwd_mx(p.handle, a, a, a, a, a, a, ctypes.c_float(1.0), 0, None) == 1
+    assert L.gdpa_bwd_mx(p.handle, a, a, a, a, a, a, a, a, a, ctypes.c_float(1.0), 0, None) == 1
+    p.destroy()
