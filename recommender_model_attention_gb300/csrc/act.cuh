@@ -22,6 +22,8 @@
 
 #include <cuda_runtime.h>
 
+#include "f2.cuh"
+
 namespace gdpa {
 
 // kSoftmax is not element-wise: it selects the softmax variant (Jagged Flash
@@ -227,6 +229,62 @@ __device__ __forceinline__ void act_dact_s(float s, const ActScale& k, float& a,
         da = fmaf(hx * fmaf(-t, t, 1.0f), fmaf(k.d1, s2, k.d0), fmaf(0.5f, t, 0.5f));
     } else {
         act_dact_f<ACT, true>(k.alpha * s, a, da);
+    }
+}
+
+// act_s of two scores at once: the same operations lane by lane in f32x2
+// form (half the instructions; the same results, bit for bit).  The
+// derivative's 1 - t^2 is formed as t^2 - 1 and the sign carried by -u'
+// (both exact negations under round-to-nearest).
+template <int ACT>
+__device__ __forceinline__ void act_s2(float s0, float s1, const ActScale& k, float& a0, float& a1) {
+    if constexpr (tanh_form<ACT>()) {
+        const uint64_t s = f2_make(s0, s1);
+        const uint64_t hx = f2_mul(f2_make(k.h, k.h), s);
+        float2 u;
+        if constexpr (ACT == kSilu) {
+            u = f2_split(hx);
+        } else {
+            u = f2_split(f2_mul(s, f2_fma(f2_make(k.c1, k.c1), f2_mul(s, s), f2_make(k.c0, k.c0))));
+        }
+        const float2 a = f2_split(f2_fma(hx, f2_make(tanh_approx(u.x), tanh_approx(u.y)), hx));
+        a0 = a.x;
+        a1 = a.y;
+    } else {
+        a0 = act_s<ACT>(s0, k);
+        a1 = act_s<ACT>(s1, k);
+    }
+}
+
+// act_dact_s of two scores at once (f32x2 form of the same operations).
+template <int ACT>
+__device__ __forceinline__ void act_dact_s2(float s0, float s1, const ActScale& k, float& a0,
+                                            float& a1, float& da0, float& da1) {
+    if constexpr (tanh_form<ACT>()) {
+        const uint64_t s = f2_make(s0, s1);
+        const uint64_t hx = f2_mul(f2_make(k.h, k.h), s);
+        uint64_t nup;   // -u'(x)
+        float2 u;
+        if constexpr (ACT == kSilu) {
+            u = f2_split(hx);
+            nup = f2_make(-0.5f, -0.5f);
+        } else {
+            const uint64_t s2 = f2_mul(s, s);
+            u = f2_split(f2_mul(s, f2_fma(f2_make(k.c1, k.c1), s2, f2_make(k.c0, k.c0))));
+            nup = f2_fma(f2_make(-k.d1, -k.d1), s2, f2_make(-k.d0, -k.d0));
+        }
+        const uint64_t t = f2_make(tanh_approx(u.x), tanh_approx(u.y));
+        const float2 a = f2_split(f2_fma(hx, t, hx));
+        const uint64_t y = f2_mul(hx, f2_fma(t, t, f2_make(-1.0f, -1.0f)));   // -x/2 (1 - t^2)
+        const uint64_t half_t = f2_fma(f2_make(0.5f, 0.5f), t, f2_make(0.5f, 0.5f));
+        const float2 da = f2_split(f2_fma(y, nup, half_t));
+        a0 = a.x;
+        a1 = a.y;
+        da0 = da.x;
+        da1 = da.y;
+    } else {
+        act_dact_s<ACT>(s0, k, a0, da0);
+        act_dact_s<ACT>(s1, k, a1, da1);
     }
 }
 

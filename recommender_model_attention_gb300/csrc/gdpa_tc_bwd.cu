@@ -451,6 +451,24 @@ __device__ __forceinline__ void bwd_p_ds(float s, float dp, const ActScale& k, f
     }
 }
 
+// bwd_p_ds of two pairs at once (f32x2 arithmetic for the GDPA activations;
+// the same results)
+template <int ACT>
+__device__ __forceinline__ void bwd_p_ds2(float s0, float s1, float dp0, float dp1,
+                                          const ActScale& k, float lse2, float drow, float& p0,
+                                          float& p1, float& ds0, float& ds1) {
+    if constexpr (ACT == kSoftmax) {
+        bwd_p_ds<ACT>(s0, dp0, k, lse2, drow, p0, ds0);
+        bwd_p_ds<ACT>(s1, dp1, k, lse2, drow, p1, ds1);
+    } else {
+        float da0, da1;
+        act_dact_s2<ACT>(s0, s1, k, p0, p1, da0, da1);
+        const float2 d = f2_split(f2_mul(f2_make(dp0, dp1), f2_make(da0, da1)));
+        ds0 = d.x;
+        ds1 = d.y;
+    }
+}
+
 template <int D, int ACT, bool NORM>
 __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const CUtensorMap* tmDK,
                             const CUtensorMap* tmDV, uint8_t* smem, uint64_t* bars, uint32_t tmem,
@@ -552,10 +570,9 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
 #pragma unroll
                             for (int e = 0; e < 16; e += 2) {
                                 float a0, d0, a1, d1;
-                                bwd_p_ds<ACT>(__uint_as_float(sv[e]), __uint_as_float(dv[e]), ksc,
-                                              lse2, drow, a0, d0);
-                                bwd_p_ds<ACT>(__uint_as_float(sv[e + 1]), __uint_as_float(dv[e + 1]),
-                                              ksc, lse2, drow, a1, d1);
+                                bwd_p_ds2<ACT>(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]),
+                                               __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]),
+                                               ksc, lse2, drow, a0, a1, d0, d1);
                                 pp[k][e >> 1] = pack_bf16x2(a0, a1);
                                 pd[e >> 1] = pack_bf16x2(d0, d1);
                                 if constexpr (NORM) {

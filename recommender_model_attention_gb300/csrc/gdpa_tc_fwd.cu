@@ -545,9 +545,12 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
                                 for (int e = 0; e < 8; ++e) pk[e] = 0u;
                             } else if (all_valid) {
 #pragma unroll
-                                for (int e = 0; e < 16; e += 2)
-                                    pk[e >> 1] = pack_bf16x2(act_s<ACT>(__uint_as_float(sv[e]), ksc),
-                                                             act_s<ACT>(__uint_as_float(sv[e + 1]), ksc));
+                                for (int e = 0; e < 16; e += 2) {
+                                    float a0, a1;
+                                    act_s2<ACT>(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]),
+                                                ksc, a0, a1);
+                                    pk[e >> 1] = pack_bf16x2(a0, a1);
+                                }
                             } else {
 #pragma unroll
                                 for (int e = 0; e < 16; e += 2) {
