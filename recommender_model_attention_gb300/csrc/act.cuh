@@ -250,6 +250,15 @@ __device__ __forceinline__ void act_s2(float s0, float s1, const ActScale& k, fl
         const float2 a = f2_split(f2_fma(hx, f2_make(tanh_approx(u.x), tanh_approx(u.y)), hx));
         a0 = a.x;
         a1 = a.y;
+    } else if constexpr (ACT == kTaylor6) {   // taylor6 of x = alpha s, lane by lane
+        const uint64_t x = f2_mul(f2_make(k.alpha, k.alpha), f2_make(s0, s1));
+        const uint64_t x2 = f2_mul(x, x);
+        uint64_t t = f2_fma(f2_make(kT6c6, kT6c6), x2, f2_make(kT6c4, kT6c4));
+        t = f2_fma(t, x2, f2_make(kT6c2, kT6c2));
+        t = f2_fma(t, x, f2_make(0.5f, 0.5f));
+        const float2 a = f2_split(f2_mul(t, x));
+        a0 = a.x;
+        a1 = a.y;
     } else {
         a0 = act_s<ACT>(s0, k);
         a1 = act_s<ACT>(s1, k);
@@ -278,6 +287,21 @@ __device__ __forceinline__ void act_dact_s2(float s0, float s1, const ActScale& 
         const uint64_t y = f2_mul(hx, f2_fma(t, t, f2_make(-1.0f, -1.0f)));   // -x/2 (1 - t^2)
         const uint64_t half_t = f2_fma(f2_make(0.5f, 0.5f), t, f2_make(0.5f, 0.5f));
         const float2 da = f2_split(f2_fma(y, nup, half_t));
+        a0 = a.x;
+        a1 = a.y;
+        da0 = da.x;
+        da1 = da.y;
+    } else if constexpr (ACT == kTaylor6) {   // taylor6 and dtaylor6 of x = alpha s
+        const uint64_t x = f2_mul(f2_make(k.alpha, k.alpha), f2_make(s0, s1));
+        const uint64_t x2 = f2_mul(x, x);
+        uint64_t t = f2_fma(f2_make(kT6c6, kT6c6), x2, f2_make(kT6c4, kT6c4));
+        t = f2_fma(t, x2, f2_make(kT6c2, kT6c2));
+        t = f2_fma(t, x, f2_make(0.5f, 0.5f));
+        const float2 a = f2_split(f2_mul(t, x));
+        constexpr float e6 = 6.0f * kT6c6, e4 = 4.0f * kT6c4, e2 = 2.0f * kT6c2;
+        uint64_t g = f2_fma(f2_make(e6, e6), x2, f2_make(e4, e4));
+        g = f2_fma(g, x2, f2_make(e2, e2));
+        const float2 da = f2_split(f2_fma(g, x, f2_make(0.5f, 0.5f)));
         a0 = a.x;
         a1 = a.y;
         da0 = da.x;

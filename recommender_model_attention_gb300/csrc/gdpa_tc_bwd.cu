@@ -589,6 +589,9 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
 #pragma unroll
                             for (int e = 0; e < 16; e += 2) {
                                 float p2[2], d2[2];
+                                bwd_p_ds2<ACT>(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]),
+                                               __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]),
+                                               ksc, lse2, drow, p2[0], p2[1], d2[0], d2[1]);
 #pragma unroll
                                 for (int w = 0; w < 2; ++w) {
                                     const int col = col0 + e + w;
@@ -596,11 +599,8 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                                     bool valid = col < u.nkv;
                                     if (windowed)
                                         valid = valid && jpos <= ipos && jpos > ipos - prm.window;
-                                    float a, ds;
-                                    bwd_p_ds<ACT>(__uint_as_float(sv[e + w]), __uint_as_float(dv[e + w]),
-                                                  ksc, lse2, drow, a, ds);
-                                    p2[w] = valid ? a : 0.0f;
-                                    d2[w] = valid ? ds : 0.0f;
+                                    p2[w] = valid ? p2[w] : 0.0f;
+                                    d2[w] = valid ? d2[w] : 0.0f;
                                 }
                                 pp[k][e >> 1] = pack_bf16x2(p2[0], p2[1]);
                                 pd[e >> 1] = pack_bf16x2(d2[0], d2[1]);

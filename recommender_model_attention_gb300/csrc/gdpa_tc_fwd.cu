@@ -22,11 +22,12 @@
 //  * warps 2-17: four activation/epilogue warpgroups.  Tiles alternate
 //    between two slots, each with its own TMEM S (128 columns) and O (128
 //    columns) accumulators, and two warpgroups share a slot: part h takes
-//    the 32-column key chunks h and h + 2 of S and the O columns
-//    [h d/2, (h + 1) d/2).  They read S with tcgen05.ld, apply alpha, the
-//    activation and the jagged / window mask (masked pairs become exactly 0
-//    after the activation), and write P as packed bf16 into the first half of
-//    each 32-column S chunk they have read (tcgen05.st); P V then takes P
+//    the 16-column key steps h, h + 2, ... of S (the softmax variant the
+//    32-column chunks h and h + 2) and the O columns [h d/2, (h + 1) d/2).
+//    They read S with tcgen05.ld, apply alpha, the activation and the
+//    jagged / window mask (masked pairs become exactly 0 after the
+//    activation), and write P as packed bf16 into the first half of each
+//    S step (chunk) they have read (tcgen05.st); P V then takes P
 //    straight from TMEM (A operand in TMEM, one address per K = 16 step).
 //    After the last key block they read O from TMEM and stage it (bf16) in
 //    the tile's consumed Q buffer; each warp writes its 32 rows with one TMA
@@ -259,8 +260,9 @@ drain:
 // every item in queue order as soon as the warpgroups have put P in TMEM, so
 // it never waits for the next tile's loads; then S of the tile's next item,
 // which overwrites the P just read (in issue order on this thread).  P comes
-// from the slot's S columns (keys [16k, 16k + 16) in 32-column chunk k/2's
-// first 16 columns, half k%2), V MN-major from shared memory.
+// from the slot's S columns (keys [16k, 16k + 16) in the first 8 columns of
+// step k; softmax variant: in 32-column chunk k/2's first 16 columns, half
+// k%2), V MN-major from shared memory.
 template <int D, bool SM>
 __device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
                            int seg0, int seg1, const Abort& ab) {
@@ -298,8 +300,8 @@ __device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, 
 #pragma unroll
                 for (int k = 0; k < 8; ++k)
                     if (k < nsteps)
-                        mma_ts(d_o, p_tmem + (k >> 1) * 32 + (k & 1) * 8, vdesc + mnmajor_step(k),
-                               idesc, (first && k == 0) ? 0u : 1u);
+                        mma_ts(d_o, p_tmem + (SM ? (k >> 1) * 32 + (k & 1) * 8 : k * 16),
+                               vdesc + mnmajor_step(k), idesc, (first && k == 0) ? 0u : 1u);
             }
             mma_commit(&bars[C::kBarKVEmpty + ks]);
             if (last) {
@@ -514,63 +516,58 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
             s_use++;
             tc_fence_after();
             // S -> registers 16 columns at a time; alpha, activation and mask;
-            // P (bf16 pairs) back into the first 16 columns of the same
-            // 32-column chunk, which only this warpgroup reads and has read
-            // (P column 32c + 8h + k holds keys 32c + 16h + 2k, +1)
+            // P (bf16 pairs) back into the first 8 columns of the same
+            // 16-column step, which only this warpgroup reads and has read.
+            // Part h takes the steps h, h + 2, ...
             if (warp_rows) {
                 const int jbase = kb * kBN;
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c = part + 2 * cc;
-                    if (c < nch) {
 #pragma unroll 1
-                        for (int hh = 0; hh < 2; ++hh) {
-                            const int col0 = c * 32 + hh * 16;
-                            if (col0 >= nvalid) break;   // GEMMs stop at 16-column granularity
-                            uint32_t sv[16], pk[8];
-                            tmem_ld16(s_tmem + col0, sv);
-                            tmem_ld_wait();
-                            // the chunk's keys against the window of this
-                            // warp's 32 rows (warp-uniform): all valid, none
-                            // valid, or mixed (per-pair masks)
-                            const int jlo = jbase + col0, jhi = jlo + 15;
-                            bool all_valid = col0 + 16 <= nvalid, none_valid = false;
-                            if (prm.mask == GDPA_MASK_CAUSAL_WINDOW) {
-                                const int ilo = tile.i0 + quarter * 32, ihi = ilo + 31;
-                                all_valid = all_valid && jhi <= ilo && jlo > ihi - prm.window;
-                                none_valid = jlo > ihi || jhi <= ilo - prm.window;
+                for (int k = 0; k < 4; ++k) {
+                    const int col0 = (part + 2 * k) * 16;
+                    if (col0 >= nvalid) break;   // GEMMs stop at 16-column granularity
+                    uint32_t sv[16], pk[8];
+                    tmem_ld16(s_tmem + col0, sv);
+                    tmem_ld_wait();
+                    // the step's keys against the window of this warp's 32
+                    // rows (warp-uniform): all valid, none valid, or mixed
+                    // (per-pair masks)
+                    const int jlo = jbase + col0, jhi = jlo + 15;
+                    bool all_valid = col0 + 16 <= nvalid, none_valid = false;
+                    if (prm.mask == GDPA_MASK_CAUSAL_WINDOW) {
+                        const int ilo = tile.i0 + quarter * 32, ihi = ilo + 31;
+                        all_valid = all_valid && jhi <= ilo && jlo > ihi - prm.window;
+                        none_valid = jlo > ihi || jhi <= ilo - prm.window;
+                    }
+                    if (none_valid) {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) pk[e] = 0u;
+                    } else if (all_valid) {
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            float a0, a1;
+                            act_s2<ACT>(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), ksc,
+                                        a0, a1);
+                            pk[e >> 1] = pack_bf16x2(a0, a1);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            float pv[2];
+                            act_s2<ACT>(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), ksc,
+                                        pv[0], pv[1]);
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int col = col0 + e + u;
+                                const int jpos = jbase + col;
+                                bool valid = col < nvalid;
+                                if (prm.mask == GDPA_MASK_CAUSAL_WINDOW)
+                                    valid = valid && jpos <= ipos && jpos > ipos - prm.window;
+                                pv[u] = valid ? pv[u] : 0.0f;
                             }
-                            if (none_valid) {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) pk[e] = 0u;
-                            } else if (all_valid) {
-#pragma unroll
-                                for (int e = 0; e < 16; e += 2) {
-                                    float a0, a1;
-                                    act_s2<ACT>(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]),
-                                                ksc, a0, a1);
-                                    pk[e >> 1] = pack_bf16x2(a0, a1);
-                                }
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 16; e += 2) {
-                                    float pv[2];
-#pragma unroll
-                                    for (int u = 0; u < 2; ++u) {
-                                        const int col = col0 + e + u;
-                                        const int jpos = jbase + col;
-                                        bool valid = col < nvalid;
-                                        if (prm.mask == GDPA_MASK_CAUSAL_WINDOW)
-                                            valid = valid && jpos <= ipos && jpos > ipos - prm.window;
-                                        const float a = act_s<ACT>(__uint_as_float(sv[e + u]), ksc);
-                                        pv[u] = valid ? a : 0.0f;
-                                    }
-                                    pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
-                                }
-                            }
-                            tmem_st8(s_tmem + c * 32 + hh * 8, pk);
+                            pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
                         }
                     }
+                    tmem_st8(s_tmem + col0, pk);
                 }
                 tmem_st_wait();
             }

@@ -8,6 +8,13 @@
 namespace gdpa {
 namespace tc {
 
+// four accumulator words times `sc2` (the scale in both halves), in pairs
+__device__ __forceinline__ float4 scaled4(const uint32_t* v, uint64_t sc2) {
+    const float2 lo = f2_split(f2_mul(sc2, f2_make(__uint_as_float(v[0]), __uint_as_float(v[1]))));
+    const float2 hi = f2_split(f2_mul(sc2, f2_make(__uint_as_float(v[2]), __uint_as_float(v[3]))));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
 // Drain TMEM columns [col, col + ncols) (a multiple of 32) of this warp's
 // 32 lanes (block rows 32 * quarter + lane) into rows [0, nrows) of a block
 // of a [rows][H * d] fp32 tensor whose first element has tensor-map
@@ -30,6 +37,7 @@ __device__ __forceinline__ void drain_warp_inl(uint32_t trow, uint32_t col, int 
     const bool any = row0 < nrows;
     const bool full = row0 + 32 <= nrows;
     uint8_t* wst = stage + quarter * 4096;
+    const uint64_t sc2 = f2_make(scale, scale);
     for (int pass = 0; pass < ncols / 32; ++pass) {
         uint32_t v[32];
         if (any) {
@@ -49,9 +57,7 @@ __device__ __forceinline__ void drain_warp_inl(uint32_t trow, uint32_t col, int 
 #pragma unroll
             for (int c = 0; c < 8; ++c)
                 *reinterpret_cast<float4*>(wst + lane * 128 + ((c ^ (lane & 7)) << 4)) =
-                    make_float4(scale * __uint_as_float(v[4 * c]), scale * __uint_as_float(v[4 * c + 1]),
-                                scale * __uint_as_float(v[4 * c + 2]),
-                                scale * __uint_as_float(v[4 * c + 3]));
+                    scaled4(v + 4 * c, sc2);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -65,10 +71,7 @@ __device__ __forceinline__ void drain_warp_inl(uint32_t trow, uint32_t col, int 
             float* d = dst + (int64_t)(row0 + lane) * rs + pass * 32;
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
-                const float4 w = make_float4(scale * __uint_as_float(v[4 * c]),
-                                             scale * __uint_as_float(v[4 * c + 1]),
-                                             scale * __uint_as_float(v[4 * c + 2]),
-                                             scale * __uint_as_float(v[4 * c + 3]));
+                const float4 w = scaled4(v + 4 * c, sc2);
                 if (atomic)
                     atomicAdd(reinterpret_cast<float4*>(d + 4 * c), w);
                 else
@@ -99,6 +102,7 @@ __device__ __forceinline__ void drain_warp16_inl(uint32_t trow, uint32_t col, in
     const bool any = row0 < nrows;
     const bool full = row0 + 32 <= nrows;
     uint8_t* wst = stage + quarter * 4096;
+    const uint64_t sc2 = f2_make(scale, scale);
     for (int pass = 0; pass < ncols / 16; ++pass) {
         uint32_t v[16];
         if (any) {
@@ -119,9 +123,7 @@ __device__ __forceinline__ void drain_warp16_inl(uint32_t trow, uint32_t col, in
 #pragma unroll
             for (int c = 0; c < 4; ++c)
                 *reinterpret_cast<float4*>(buf + stage_off64(lane, c)) =
-                    make_float4(scale * __uint_as_float(v[4 * c]), scale * __uint_as_float(v[4 * c + 1]),
-                                scale * __uint_as_float(v[4 * c + 2]),
-                                scale * __uint_as_float(v[4 * c + 3]));
+                    scaled4(v + 4 * c, sc2);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -135,10 +137,7 @@ __device__ __forceinline__ void drain_warp16_inl(uint32_t trow, uint32_t col, in
             float* d = dst + (int64_t)(row0 + lane) * rs + pass * 16;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
-                const float4 w = make_float4(scale * __uint_as_float(v[4 * c]),
-                                             scale * __uint_as_float(v[4 * c + 1]),
-                                             scale * __uint_as_float(v[4 * c + 2]),
-                                             scale * __uint_as_float(v[4 * c + 3]));
+                const float4 w = scaled4(v + 4 * c, sc2);
                 if (atomic)
                     atomicAdd(reinterpret_cast<float4*>(d + 4 * c), w);
                 else
