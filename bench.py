@@ -43,8 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the unsplit softmax-free kernels; otherwise reported null.
 TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
-    "gdpa_fwd": ("45e360c415c1d12e", 0.9668),
-    "gdpa_bwd": ("d40c27880e9a7c5c", 1.0266),
+    "gdpa_fwd": ("ac08e6cc36aae9b8", 0.9679),
+    "gdpa_bwd": ("da3a254577e866de", 1.0267),
 }
 KERNEL_SOURCES = {
     "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh"),

@@ -485,9 +485,12 @@ gdpa_status gdpa_bwd_mx(gdpa_plan plan, const uint8_t* q_el, const uint8_t* q_sc
 /* Activation test hook.
  *
  * Evaluates act(x) and act'(x) element-wise with the same device functions
- * the kernels use: fast != 0 selects the tensor-core kernels' flavour (the
- * one P and dS are computed with on the bf16 path), fast == 0 the CUDA-core
- * float32 path's.  The activations are those of the GDPA page ("범용 내적
+ * the kernels use: fast == 1 selects the tensor-core kernels' flavour (the
+ * one P and dS are computed with on the bf16 path) one element at a time,
+ * fast == 2 the same flavour in the two-at-a-time (f32x2) form the
+ * tensor-core kernels evaluate it in (elements 2k and 2k + 1 together; an
+ * odd last element with a copy of itself), fast == 0 the CUDA-core float32
+ * path's.  Forms 1 and 2 are meant to agree bit for bit.  The activations are those of the GDPA page ("범용 내적
  * 어텐션(GDPA)", aitrends.kr: GELU, SiLU and the Taylor-6 GELU replacing
  * softmax), plus identity.  It exists so that tests can check those
  * functions against reference values directly.
@@ -497,8 +500,8 @@ gdpa_status gdpa_bwd_mx(gdpa_plan plan, const uint8_t* q_el, const uint8_t* q_sc
  *   n          >= 0; n == 0 does nothing.
  *   stream     cudaStream_t; asynchronous.
  *
- * Errors: INVALID_ARG for an unknown act, n < 0 or NULL arrays; CUDA if the
- * launch fails.
+ * Errors: INVALID_ARG for an unknown act, fast outside 0..2, n < 0 or NULL
+ * arrays; CUDA if the launch fails.
  */
 gdpa_status gdpa_act_eval(gdpa_act act, int fast, const float* x, float* y, float* dy, int64_t n,
                           void* stream);

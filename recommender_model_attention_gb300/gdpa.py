@@ -456,16 +456,18 @@ def gdpa_fwd_noalloc(q_off, kv_off, q, k, v, o, alpha=None, act: str = "gelu_erf
     return o
 
 
-def act_eval(x, act: str = "gelu_erf", fast: bool = True, stream=None):
+def act_eval(x, act: str = "gelu_erf", fast=True, stream=None):
     """(act(x), act'(x)) element-wise with the kernels' device functions
-    (``fast``: the tensor-core flavour; else the float32 CUDA-core one).
-    ``x``: a contiguous float32 CUDA tensor."""
+    (``fast``: the tensor-core flavour, one element at a time; ``fast=2``:
+    the same in the f32x2 pair form those kernels evaluate it in; false: the
+    float32 CUDA-core one).  ``x``: a contiguous float32 CUDA tensor."""
     import torch
     if x.dtype != torch.float32 or not x.is_cuda or not x.is_contiguous():
         raise ValueError("x must be a contiguous float32 CUDA tensor")
     y = torch.empty_like(x)
     dy = torch.empty_like(x)
-    _ok(lib().gdpa_act_eval(ACT[act], 1 if fast else 0, _ptr(x), _ptr(y), _ptr(dy),
+    mode = 2 if fast == 2 else (1 if fast else 0)
+    _ok(lib().gdpa_act_eval(ACT[act], mode, _ptr(x), _ptr(y), _ptr(dy),
                             ctypes.c_int64(x.numel()), _stream_ptr(stream)), "gdpa_act_eval")
     return y, dy
 

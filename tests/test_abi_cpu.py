@@ -249,3 +249,20 @@ def test_mx_argument_checks_on_the_host(gd):
     assert L.gdpa_fwd_mx(p.handle, a, a, a, a, a, a, ctypes.c_float(1.0), 0, None) == 1
     assert L.gdpa_bwd_mx(p.handle, a, a, a, a, a, a, a, a, a, ctypes.c_float(1.0), 0, None) == 1
     p.destroy()
+
+
+def test_act_eval_argument_checks_on_the_host(gd):
+    # the activation test hook refuses an unknown activation or form, a
+    # negative count and NULL arrays before touching a device; n = 0 is a
+    # no-op
+    import ctypes
+    L = gd.lib()
+    vp = ctypes.c_void_p
+    a = vp(1 << 20)   # never dereferenced
+    n = ctypes.c_int64
+    assert L.gdpa_act_eval(0, 3, a, a, a, n(8), None) == 1
+    assert L.gdpa_act_eval(0, -1, a, a, a, n(8), None) == 1
+    assert L.gdpa_act_eval(5, 1, a, a, a, n(8), None) == 1   # softmax is a row operation
+    assert L.gdpa_act_eval(0, 2, a, a, a, n(-1), None) == 1
+    assert L.gdpa_act_eval(0, 2, None, a, a, n(8), None) == 1
+    assert L.gdpa_act_eval(0, 2, None, None, None, n(0), None) == 0

@@ -84,3 +84,30 @@ def test_fast_flavour_polynomials(gd, act):
     x, y, dy, want, dwant = _run(gd, act, True)
     assert np.max(np.abs(y - want) / np.maximum(1.0, np.abs(want))) <= 2e-6
     assert np.max(np.abs(dy - dwant) / np.maximum(1.0, np.abs(dwant))) <= 2e-6
+
+
+@pytest.mark.parametrize("act", ["gelu_erf", "gelu_tanh", "silu", "gelu_taylor6", "identity"])
+@pytest.mark.parametrize("odd", [False, True])
+def test_pair_form_is_the_scalar_form_bit_for_bit(gd, act, odd):
+    """The tensor-core kernels evaluate the activation two scores at a time
+    in f32x2 arithmetic: lane by lane the same operations as the scalar form
+    (the derivative's 1 - t^2 formed as t^2 - 1 with the sign carried by -u',
+    both exact negations), so every value and derivative must match the
+    scalar form's bits, including the tails, signed zeros and an odd last
+    element paired with itself.  The hook also checks in the kernel that the
+    value of the value-and-derivative pair form (the backward's P) has the
+    bits of the value-only pair form (the forward's), writing NaN where not."""
+    import torch
+    x = _grid()
+    rng = np.random.default_rng(7)
+    x = np.concatenate([x, rng.standard_normal(4001).astype(np.float32) * 3,
+                        np.float32([-0.0, 1e-30, -1e-30, 3e38, -3e38])])
+    if (x.size % 2 == 1) != odd:
+        x = x[:-1]
+    xt = torch.from_numpy(x).cuda()
+    y1, d1 = gd.act_eval(xt, act, True)
+    y2, d2 = gd.act_eval(xt, act, 2)
+    torch.cuda.synchronize()
+    b = lambda t: t.cpu().numpy().view(np.uint32)
+    assert np.array_equal(b(y1), b(y2)), act
+    assert np.array_equal(b(d1), b(d2)), act
