@@ -107,6 +107,11 @@ struct FwdParams {
     float qk_gain, qk_eps;
 };
 
+// Hint: bring the line holding p into L1 (no register result, no wait).
+__device__ __forceinline__ void prefetch_l1(const void* p) {
+    asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ FwdTile load_tile(const FwdTile* p) {
     const int4* q = reinterpret_cast<const int4*>(p);
     const int4 a = __ldg(q), b = __ldg(q + 1);
@@ -150,6 +155,9 @@ __device__ void fwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
     for (int s = 0; s < C::kNKV; ++s) kv_armed[s] = -1;
     uint32_t a = 0, i = 0;
     for (int t = seg0; t < seg1; ++t) {
+        // (the descriptor line 4 tiles ahead, so that this warp's next
+        // descriptor loads hit in L1)
+        if (t + 4 < seg1) prefetch_l1(prm.tiles + t + 4);
         const FwdTile tile = load_tile(prm.tiles + t);
         if (tile.kb1 <= tile.kb0) continue;
         const uint32_t qs = a % C::kNQ, qph = (a / C::kNQ) & 1;
@@ -228,6 +236,9 @@ __device__ void fwd_mma_s(const FwdParams& prm, uint8_t* smem, uint64_t* bars, u
     int64_t last0 = -1, last1 = -1;   // each slot's last item so far
     uint32_t a = 0, i = 0;
     for (int t = seg0; t < seg1; ++t) {
+        // (the descriptor line 4 tiles ahead, so that this warp's next
+        // descriptor loads hit in L1)
+        if (t + 4 < seg1) prefetch_l1(prm.tiles + t + 4);
         const FwdTile tile = load_tile(prm.tiles + t);
         if (tile.kb1 <= tile.kb0) continue;
         const uint32_t wg = a % kNumWG;
@@ -270,6 +281,9 @@ __device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, 
     uint32_t p_use0 = 0, p_use1 = 0, o_use0 = 0, o_use1 = 0;
     uint32_t a = 0, i = 0;
     for (int t = seg0; t < seg1; ++t) {
+        // (the descriptor line 4 tiles ahead, so that this warp's next
+        // descriptor loads hit in L1)
+        if (t + 4 < seg1) prefetch_l1(prm.tiles + t + 4);
         const FwdTile tile = load_tile(prm.tiles + t);
         if (tile.kb1 <= tile.kb0) continue;
         const uint32_t wg = a % kNumWG;
@@ -481,6 +495,9 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
     ActScale ksc = act_scale<ACT>(prm.alpha);
     uint32_t a = 0, s_use = 0, o_use = 0, x_use = 0;
     for (int t = seg0; t < seg1; ++t) {
+        // (the descriptor line 4 tiles ahead, so that this warp's next
+        // descriptor loads hit in L1)
+        if (t + 4 < seg1) prefetch_l1(prm.tiles + t + 4);
         const FwdTile tile = load_tile(prm.tiles + t);
         if (tile.kb1 <= tile.kb0) {
             if (!SPLIT && (t - seg0) % (kNumWG * kParts) == grp) store_zero_rows<D>(tile, prm, tid);
