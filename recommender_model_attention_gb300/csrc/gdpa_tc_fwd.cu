@@ -10,7 +10,9 @@
 //  * grid = one CTA per planned SM queue; CTA s walks tiles seg[s]..seg[s+1].
 //  * warp 0 (one lane): TMA producer.  Q tile [128 x d] per tile through a
 //    3-stage ring, K and V blocks [128 x d] per (tile, key block) item
-//    through 2-stage rings.
+//    through 2-stage rings; a K stage is handed back once its item's S has
+//    read it and a V stage once its P V has, and the producer loads K one
+//    item ahead of V, so the next items' scores never wait for a P V.
 //  * warps 1 and 18: tcgen05.mma issuers (the whole warp runs the issue
 //    code, one elected lane issues).  Warp 1 issues S = Q K^T of each tile's
 //    first item as soon as its Q and K are loaded and its slot's previous
@@ -66,14 +68,15 @@ struct FwdCfg {
     static constexpr int kOffK = kOffQ + kNQ * kTileBytes;
     static constexpr int kOffV = kOffK + kNKV * kTileBytes;
     static constexpr int kOffBar = kOffV + kNKV * kTileBytes;
-    // q_full, q_empty, k_full, v_full, kv_empty,
+    // q_full, q_empty, k_full, v_full, k_empty, v_empty,
     // s_full, p_full, o_full, o_free, stage (per warpgroup), mma_done
     static constexpr int kBarQFull = 0;
     static constexpr int kBarQEmpty = kBarQFull + kNQ;
     static constexpr int kBarKFull = kBarQEmpty + kNQ;
     static constexpr int kBarVFull = kBarKFull + kNKV;
-    static constexpr int kBarKVEmpty = kBarVFull + kNKV;
-    static constexpr int kBarSFull = kBarKVEmpty + kNKV;
+    static constexpr int kBarKEmpty = kBarVFull + kNKV;   // the item's S has read K
+    static constexpr int kBarVEmpty = kBarKEmpty + kNKV;  // the item's P V has read V
+    static constexpr int kBarSFull = kBarVEmpty + kNKV;
     static constexpr int kBarPFull = kBarSFull + kNumWG;
     static constexpr int kBarOFull = kBarPFull + kNumWG;
     static constexpr int kBarOFree = kBarOFull + kNumWG;
@@ -150,9 +153,29 @@ __device__ void fwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
     using C = FwdCfg<D>;
     const uint64_t pol_q = policy_evict_first();
     const uint64_t pol_kv = policy_evict_last();
-    int32_t q_armed[C::kNQ], kv_armed[C::kNKV];
+    int32_t q_armed[C::kNQ], k_armed[C::kNKV], v_armed[C::kNKV];
     for (int s = 0; s < C::kNQ; ++s) q_armed[s] = -1;
-    for (int s = 0; s < C::kNKV; ++s) kv_armed[s] = -1;
+    for (int s = 0; s < C::kNKV; ++s) k_armed[s] = v_armed[s] = -1;
+    // K runs ahead of V: a K stage is free once its item's S has read it, a
+    // V stage only once its P V has, so within a tile item i's K goes in as
+    // soon as item i - kNKV's S is done, and item i - 1's V after it; a
+    // tile's last V goes in before the next tile's Q (whose stage waits for
+    // an epilogue).  Either way item i's V precedes item i + 2's K.
+    int pend_y = -1, pend_h = 0;   // the item whose V is still to load
+    uint32_t pend_i = 0;
+    auto load_v = [&]() -> bool {
+        const uint32_t vs = pend_i % C::kNKV, vph = (pend_i / C::kNKV) & 1;
+        if (!mbar_wait(&bars[C::kBarVEmpty + vs], vph ^ 1, ab, 2)) return false;
+        mbar_arrive_expect_tx(&bars[C::kBarVFull + vs], C::kTileBytes);
+#pragma unroll
+        for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_2d(tmV, &bars[C::kBarVFull + vs],
+                        smem + C::kOffV + vs * C::kTileBytes + hf * kHalfBytes,
+                        pend_h * D + hf * 64, pend_y, pol_kv);
+        v_armed[vs] = (int32_t)vph;
+        pend_y = -1;
+        return true;
+    };
     uint32_t a = 0, i = 0;
     for (int t = seg0; t < seg1; ++t) {
         // (the descriptor line 4 tiles ahead, so that this warp's next
@@ -160,6 +183,7 @@ __device__ void fwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
         if (t + 4 < seg1) prefetch_l1(prm.tiles + t + 4);
         const FwdTile tile = load_tile(prm.tiles + t);
         if (tile.kb1 <= tile.kb0) continue;
+        if (pend_y >= 0 && !load_v()) goto unwind;   // the previous tile's last V
         const uint32_t qs = a % C::kNQ, qph = (a / C::kNQ) & 1;
         if (!mbar_wait(&bars[C::kBarQEmpty + qs], qph ^ 1, ab, 1)) goto unwind;
         // failure-path test hook: CTA 0 never loads its first Q tile, so the
@@ -176,7 +200,7 @@ __device__ void fwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
         const int nit = tile_items<SM>(tile);
         for (int it = 0; it < nit; ++it, ++i) {
             const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
-            if (!mbar_wait(&bars[C::kBarKVEmpty + ks], kph ^ 1, ab, 2)) goto unwind;
+            if (!mbar_wait(&bars[C::kBarKEmpty + ks], kph ^ 1, ab, 2)) goto unwind;
             const int y = tile.kvt0 + item_block<SM>(tile, it) * kBN;
             mbar_arrive_expect_tx(&bars[C::kBarKFull + ks], C::kTileBytes);
 #pragma unroll
@@ -184,25 +208,23 @@ __device__ void fwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
                 tma_load_2d(tmK, &bars[C::kBarKFull + ks],
                             smem + C::kOffK + ks * C::kTileBytes + hf * kHalfBytes,
                             tile.h * D + hf * 64, y, pol_kv);
-            mbar_arrive_expect_tx(&bars[C::kBarVFull + ks], C::kTileBytes);
-#pragma unroll
-            for (int hf = 0; hf < C::kHalves; ++hf)
-                tma_load_2d(tmV, &bars[C::kBarVFull + ks],
-                            smem + C::kOffV + ks * C::kTileBytes + hf * kHalfBytes,
-                            tile.h * D + hf * 64, y, pol_kv);
-            kv_armed[ks] = (int32_t)kph;
+            k_armed[ks] = (int32_t)kph;
+            if (pend_y >= 0 && !load_v()) goto unwind;   // the item before's V
+            pend_y = y;
+            pend_h = tile.h;
+            pend_i = i;
         }
         ++a;
     }
+    if (pend_y >= 0) load_v();
 unwind:
     // never leave the CTA with a TMA write still in flight
     for (int s = 0; s < C::kNQ; ++s)
         if (q_armed[s] >= 0) mbar_wait_teardown(&bars[C::kBarQFull + s], (uint32_t)q_armed[s]);
-    for (int s = 0; s < C::kNKV; ++s)
-        if (kv_armed[s] >= 0) {
-            mbar_wait_teardown(&bars[C::kBarKFull + s], (uint32_t)kv_armed[s]);
-            mbar_wait_teardown(&bars[C::kBarVFull + s], (uint32_t)kv_armed[s]);
-        }
+    for (int s = 0; s < C::kNKV; ++s) {
+        if (k_armed[s] >= 0) mbar_wait_teardown(&bars[C::kBarKFull + s], (uint32_t)k_armed[s]);
+        if (v_armed[s] >= 0) mbar_wait_teardown(&bars[C::kBarVFull + s], (uint32_t)v_armed[s]);
+    }
 }
 
 // S = Q K^T of one item into slot w's S columns (K-major Q and K tiles),
@@ -225,9 +247,10 @@ __device__ __forceinline__ void issue_s(uint8_t* smem, uint64_t* bars, uint32_t 
 // S issuer (warp 1, the whole warp; one elected lane issues): S of each
 // tile's first item, as soon as its Q and K are loaded and the slot's
 // previous item has had its P V complete (its S columns hold that item's P;
-// P V runs on another warp, whose commit of the item's K/V-empty arrival
-// this waits for).  S of a tile's later items follows the P V of the item
-// before it on the P V warp, in issue order.
+// P V runs on another warp, whose commit of the item's V-empty arrival this
+// waits for).  S of a tile's later items follows the P V of the item before
+// it on the P V warp, in issue order.  Each S commits its K stage's
+// K-empty arrival.
 template <int D, bool SM>
 __device__ void fwd_mma_s(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
                           int seg0, int seg1, const Abort& ab) {
@@ -245,18 +268,22 @@ __device__ void fwd_mma_s(const FwdParams& prm, uint8_t* smem, uint64_t* bars, u
         const uint32_t qs = a % C::kNQ, qph = (a / C::kNQ) & 1;
         const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
         int64_t& last = wg ? last1 : last0;
-        // (an item kNKV or more before this one has had its K/V stage
-        // refilled since, which took its P V's completion: no wait, and its
-        // K/V-empty phase would be stale)
-        if (last >= 0 && last + C::kNKV >= (int64_t)i) {
+        // (the producer loads item i's K after item i - 2's V, so once
+        // item i >= last + kNKV + 2 has its K, the V stage of `last` has been
+        // refilled, which took its P V's completion: no wait, and its
+        // V-empty phase could be stale; for i <= last + kNKV + 1 the phase
+        // after `last`'s completion can have completed once at most, as the
+        // P V of item last + 2 kNKV follows this item's)
+        if (last >= 0 && last + C::kNKV + 1 >= (int64_t)i) {
             const uint32_t ls = (uint32_t)(last % C::kNKV), lph = (uint32_t)((last / C::kNKV) & 1);
-            if (!wg_wait(&bars[C::kBarKVEmpty + ls], lph, ab, 13)) goto drain;
+            if (!wg_wait(&bars[C::kBarVEmpty + ls], lph, ab, 13)) goto drain;
         }
         if (!wg_wait(&bars[C::kBarQFull + qs], qph, ab, 3) ||
             !wg_wait(&bars[C::kBarKFull + ks], kph, ab, 4))
             goto drain;
         tc_fence_after();
         issue_s<D>(smem, bars, tmem, wg, qs, ks, min(kBN, tile.lkv - tile.kb0 * kBN));
+        mma_commit(&bars[C::kBarKEmpty + ks]);
         i += (uint32_t)tile_items<SM>(tile);
         last = (int64_t)i - 1;
         ++a;
@@ -317,7 +344,7 @@ __device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, 
                         mma_ts(d_o, p_tmem + (SM ? (k >> 1) * 32 + (k & 1) * 8 : k * 16),
                                vdesc + mnmajor_step(k), idesc, (first && k == 0) ? 0u : 1u);
             }
-            mma_commit(&bars[C::kBarKVEmpty + ks]);
+            mma_commit(&bars[C::kBarVEmpty + ks]);
             if (last) {
                 mma_commit(&bars[C::kBarOFull + wg]);
                 o_use++;
@@ -327,6 +354,7 @@ __device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, 
                 tc_fence_after();
                 issue_s<D>(smem, bars, tmem, wg, qs, ks1,
                            min(kBN, tile.lkv - item_block<SM>(tile, it + 1) * kBN));
+                mma_commit(&bars[C::kBarKEmpty + ks1]);
             }
         }
         ++a;
@@ -706,7 +734,8 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         for (int s = 0; s < C::kNKV; ++s) {
             mbar_init(&bars[C::kBarKFull + s], 1);
             mbar_init(&bars[C::kBarVFull + s], 1);
-            mbar_init(&bars[C::kBarKVEmpty + s], 1);
+            mbar_init(&bars[C::kBarKEmpty + s], 1);
+            mbar_init(&bars[C::kBarVEmpty + s], 1);
         }
         for (int w = 0; w < kNumWG; ++w) {
             mbar_init(&bars[C::kBarSFull + w], 1);
