@@ -326,6 +326,16 @@ gdpa_status gdpa_bwd(gdpa_plan plan, gdpa_dtype dtype, const void* q, const void
 gdpa_status gdpa_check(gdpa_plan plan, void* stream);
 
 /*
+ * Where the last failure that gdpa_check reported for this plan came from
+ * (host-side copy, no device access): detail = int32 [4], the device error
+ * code (1 = an abandoned barrier wait), the site (a number naming the wait
+ * in the kernel source: 1-15 forward, 21-50 backward), the CTA that gave up
+ * first, and a code-specific word.  All zero if gdpa_check has reported no
+ * failure for this plan.  Errors: INVALID_ARG for a NULL plan or detail.
+ */
+gdpa_status gdpa_error_detail(gdpa_plan plan, int32_t* detail);
+
+/*
  * Per-CTA timing of the last timed tensor-core launch (which = 0 forward,
  * 1 backward): start_end: uint64 [S][2] globaltimer ns; smid: int32 [S].
  * Waits for this plan's launches only (not the whole device) and reads on the

@@ -527,10 +527,18 @@ gdpa_status gdpa_check(gdpa_plan plan, void* stream) {
         cudaStreamSynchronize(st) != cudaSuccess)
         return GDPA_ERR_CUDA;
     if (err[0] == gdpa::kDevOk) return GDPA_OK;
+    for (int j = 0; j < 4; ++j) p.last_err[j] = err[j];
     if (cudaMemsetAsync(p.d_err, 0, sizeof(err), st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
         return GDPA_ERR_CUDA;
     return err[0] == gdpa::kDevTimeout ? GDPA_ERR_TIMEOUT : GDPA_ERR_DEVICE;
+}
+
+gdpa_status gdpa_error_detail(gdpa_plan plan, int32_t* detail) {
+    if (!plan || !detail) return GDPA_ERR_INVALID_ARG;
+    const Plan& p = *(const Plan*)plan;
+    for (int j = 0; j < 4; ++j) detail[j] = p.last_err[j];
+    return GDPA_OK;
 }
 
 gdpa_status gdpa_sm_times(gdpa_plan plan, int which, uint64_t* start_end, int32_t* smid) {

@@ -67,6 +67,7 @@ struct Plan {
     BwdUnit* d_bwd = nullptr;
     int32_t* d_bwd_seg = nullptr;
     int32_t* d_err = nullptr;                // [4]
+    int32_t last_err[4] = {0, 0, 0, 0};      // the last failure gdpa_check read
     unsigned long long* d_times = nullptr;   // [2][S][2]
     int32_t* d_smid = nullptr;               // [2][S]
     int timed[2] = {0, 0};

@@ -154,6 +154,21 @@ __device__ void bwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
                 tma_load_2d(tmDO, &bars[C::kDOFull + s],
                             smem + C::kOffDO + s * C::kTileBytes + hf * kHalfBytes, h * D + hf * 64,
                             y, pol_stream);
+            if (m == u.m0) {
+                // the next unit's K and V into L2 now, so that its loads at
+                // the unit boundary need not come from HBM
+                for (int t1 = t + 1; t1 < seg1; ++t1) {
+                    const BwdUnit u1 = load_unit(prm.units + t1);
+                    if (u1.m1 <= u1.m0) continue;
+                    const int h1 = u1.hf & 0xffff;
+#pragma unroll
+                    for (int hf = 0; hf < C::kHalves; ++hf) {
+                        tma_prefetch_2d(tmK, h1 * D + hf * 64, u1.kvt0, pol_keep);
+                        tma_prefetch_2d(tmV, h1 * D + hf * 64, u1.kvt0, pol_keep);
+                    }
+                    break;
+                }
+            }
         }
         ++nu;
     }
@@ -235,6 +250,10 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
                 mma_ts(tmem + kColDP, tmem + kColS + k * 16,
                        smem_desc_sw128(kbase + k * 2048, kHalfBytes, 1024), idesc_dq, k > 0);
             mma_commit(&bars[C::kDQDone]);
+            // the unit's last reader of K and V (dV reads P and dO): the
+            // stage goes back to the producer (the fused RMSNorm's dK drain
+            // still reads K: warpgroup 1 hands it back then)
+            if (last && !prm.kscale) mma_commit(&bars[C::kKVEmpty]);
             // the next tile's scores (the warpgroups have read this tile's S)
             if (!last && !issue_s(i + 1)) goto drain;
             // dV += P^T dO once P has replaced dS in shared memory
@@ -248,9 +267,6 @@ __device__ void bwd_mma(const BwdParams& prm, uint8_t* smem, uint64_t* bars, uin
             mma_commit(&bars[C::kDOEmpty + s]);
             if (last) {
                 mma_commit(&bars[C::kAccFull]);
-                // the fused RMSNorm's dK drain still reads K: warpgroup 1
-                // hands the stage back then
-                if (!prm.kscale) mma_commit(&bars[C::kKVEmpty]);
             } else if (!issue_dp(i + 1)) {   // once this tile's dQ is drained
                 goto drain;
             }

@@ -268,13 +268,14 @@ __device__ void fwd_mma_s(const FwdParams& prm, uint8_t* smem, uint64_t* bars, u
         const uint32_t qs = a % C::kNQ, qph = (a / C::kNQ) & 1;
         const uint32_t ks = i % C::kNKV, kph = (i / C::kNKV) & 1;
         int64_t& last = wg ? last1 : last0;
-        // (the producer loads item i's K after item i - 2's V, so once
-        // item i >= last + kNKV + 2 has its K, the V stage of `last` has been
-        // refilled, which took its P V's completion: no wait, and its
-        // V-empty phase could be stale; for i <= last + kNKV + 1 the phase
-        // after `last`'s completion can have completed once at most, as the
-        // P V of item last + 2 kNKV follows this item's)
-        if (last >= 0 && last + C::kNKV + 1 >= (int64_t)i) {
+        // (the producer loads the V of every item before a tile's first
+        // item ahead of that item's K, so once item i >= last + kNKV + 1
+        // has its K, the V stage of `last` has been refilled, which took
+        // its P V's completion: no wait, and its V-empty phase could be
+        // stale.  For i <= last + kNKV the phase after `last`'s completion,
+        // the P V of item last + kNKV, cannot have completed: that item is
+        // this one or a later one, which needs this S.)
+        if (last >= 0 && last + C::kNKV >= (int64_t)i) {
             const uint32_t ls = (uint32_t)(last % C::kNKV), lph = (uint32_t)((last / C::kNKV) & 1);
             if (!wg_wait(&bars[C::kBarVEmpty + ls], lph, ab, 13)) goto drain;
         }

@@ -164,6 +164,16 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
         : "memory");
 }
 
+// 2-D tile prefetch global -> L2 (no shared memory written, no completion to
+// wait for): a later tma_load_2d of the same box hits in L2.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y,
+                                                uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(map),
+        "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
 // 2-D tile store shared -> global (bulk-group completion); x * 4 bytes (fp32)
 // must be a multiple of 16 and no coordinate may be negative.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x,

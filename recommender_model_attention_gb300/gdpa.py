@@ -68,6 +68,7 @@ def lib():
             "gdpa_fwd": [vp, st, vp, vp, vp, vp, ctypes.c_float, st, vp],
             "gdpa_bwd": [vp, st, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float, st, vp],
             "gdpa_check": [vp, vp],
+            "gdpa_error_detail": [vp, i32p],
             "gdpa_sm_times": [vp, st, ctypes.POINTER(ctypes.c_uint64), i32p],
             "gdpa_fwd_noalloc": [i32p, i32p, st, st, st, st, st, vp, vp, vp, vp, ctypes.c_float,
                                  st, vp],
@@ -222,7 +223,18 @@ class Plan:
         return se, sm
 
     def check(self, stream=None):
-        _ok(lib().gdpa_check(self.handle, _stream_ptr(stream)), "gdpa_check")
+        status = lib().gdpa_check(self.handle, _stream_ptr(stream))
+        if status != 0:
+            code, site, cta, word = self.error_detail()
+            raise GdpaError(status, "gdpa_check (device code %d, wait site %d, CTA %d, %d)"
+                            % (code, site, cta, word))
+
+    def error_detail(self):
+        """(device code, wait site, CTA, word) of the last failure that
+        check() reported for this plan; zeros if none."""
+        d = (ctypes.c_int32 * 4)()
+        _ok(lib().gdpa_error_detail(self.handle, d), "gdpa_error_detail")
+        return tuple(int(v) for v in d)
 
     @property
     def launches(self) -> int:

@@ -266,3 +266,17 @@ def test_act_eval_argument_checks_on_the_host(gd):
     assert L.gdpa_act_eval(0, 2, a, a, a, n(-1), None) == 1
     assert L.gdpa_act_eval(0, 2, None, a, a, n(8), None) == 1
     assert L.gdpa_act_eval(0, 2, None, None, None, n(0), None) == 0
+
+
+def test_error_detail_on_the_host(gd):
+    # the last-failure record is a host-side copy: zeros before any failure,
+    # and refused for a NULL plan or output
+    import ctypes
+    L = gd.lib()
+    d = (ctypes.c_int32 * 4)(9, 9, 9, 9)
+    assert L.gdpa_error_detail(None, d) == 1
+    qo = offsets_from_lengths([3, 4])
+    p = gd.Plan(qo, qo, 2, 64, num_sms=4, host_only=True)
+    assert L.gdpa_error_detail(p.handle, None) == 1
+    assert p.error_detail() == (0, 0, 0, 0)
+    p.destroy()

@@ -120,3 +120,19 @@ def test_repeat_calls_identical_forward(gd):
     plan.check()
     assert torch.equal(o1, o2)
     plan.destroy()
+
+
+@pytest.mark.parametrize("num_sms", [1, 2, 3, 7])
+@pytest.mark.parametrize("sched", ["round_robin", "zigzag"])
+def test_multi_block_tiles_on_few_ctas(gd, sched, num_sms):
+    """Long queues of forward tiles with 1 to 4 key blocks each (keys up to
+    500), in both dealing orders, on a handful of CTAs: every CTA's two tile
+    slots take turns on the K and V rings with tiles of different lengths,
+    the case where a stage released too early or a barrier phase skipped
+    shows up as a wrong output or an abandoned wait."""
+    rng = np.random.default_rng(900 + num_sms)
+    lq = rng.integers(1, 300, 24).tolist()
+    lkv = rng.integers(1, 500, 24).tolist()
+    x = _case(lq, lkv, 2, 128, 900 + num_sms)
+    _assert(compare_full(gd, x, 2, 128, 128 ** -0.5, "gelu_erf", "bf16", sched=sched,
+                         num_sms=num_sms))

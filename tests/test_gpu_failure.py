@@ -57,6 +57,11 @@ def test_expired_wait_reports_timeout_and_plan_recovers(gd, which, d):
     with pytest.raises(gd.GdpaError) as e:
         plan.check()
     assert e.value.status == TIMEOUT
+    # where: an abandoned wait (device code 1) at one of this kernel's wait
+    # sites, first given up by the stalled CTA 0
+    code, site, cta, _ = plan.error_detail()
+    assert code == 1 and cta == 0, plan.error_detail()
+    assert (1 <= site <= 15) if which == "fwd" else (21 <= site <= 50), site
     # the kernel returned well inside the default limit (2 s per wait)
     assert time.time() - t0 < 10.0
     # the flag is cleared and the device is usable: a normal launch on the
