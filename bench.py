@@ -43,8 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the unsplit softmax-free kernels; otherwise reported null.
 TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
-    "gdpa_fwd": ("ac08e6cc36aae9b8", 0.9679),
-    "gdpa_bwd": ("da3a254577e866de", 1.0267),
+    "gdpa_fwd": ("271a642be8c09ae6", 0.9679),
+    "gdpa_bwd": ("ab378ae1722d7e27", 1.0295),
 }
 KERNEL_SOURCES = {
     "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh"),
