@@ -329,7 +329,7 @@ gdpa_status gdpa_check(gdpa_plan plan, void* stream);
  * Where the last failure that gdpa_check reported for this plan came from
  * (host-side copy, no device access): detail = int32 [4], the device error
  * code (1 = an abandoned barrier wait), the site (a number naming the wait
- * in the kernel source: 1-15 forward, 21-50 backward), the CTA that gave up
+ * in the kernel source: 1-16 forward, 21-50 backward), the CTA that gave up
  * first, and a code-specific word.  All zero if gdpa_check has reported no
  * failure for this plan.  Errors: INVALID_ARG for a NULL plan or detail.
  */

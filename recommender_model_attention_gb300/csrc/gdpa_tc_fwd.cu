@@ -110,6 +110,25 @@ struct FwdParams {
     float qk_gain, qk_eps;
 };
 
+// Bounded wait for a shared-memory counter that other warps raise to reach
+// `v` (false, with the error recorded, if it does not in time or the CTA is
+// aborting).  Every lane of the calling warp reads it.
+__device__ __forceinline__ bool counter_wait(const volatile int* c, int v, const Abort& ab,
+                                             int32_t where) {
+    if (*c >= v) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1; *c < v; ++it) {
+        if ((it & 31u) == 0) {
+            if (*ab.flag) return false;
+            if (globaltimer() - t0 > ab.limit_ns || it > kWaitLimitIters) {
+                raise_error(ab, kDevTimeout, where);
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
 // Hint: bring the line holding p into L1 (no register result, no wait).
 __device__ __forceinline__ void prefetch_l1(const void* p) {
     asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
@@ -250,10 +269,14 @@ __device__ __forceinline__ void issue_s(uint8_t* smem, uint64_t* bars, uint32_t 
 // P V runs on another warp, whose commit of the item's V-empty arrival this
 // waits for).  S of a tile's later items follows the P V of the item before
 // it on the P V warp, in issue order.  Each S commits its K stage's
-// K-empty arrival.
+// K-empty arrival.  Its waits on barriers that other warps also consume are
+// kept within one phase: a K-full only after the K kNKV items back has been
+// seen to land (a shared counter the two MMA warps raise), and the slot's
+// previous P V only while that V-empty phase is current.
 template <int D, bool SM>
 __device__ void fwd_mma_s(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
-                          int seg0, int seg1, const Abort& ab) {
+                          volatile int* k_seen, int seg0, int seg1, const Abort& ab) {
+    const int lane = threadIdx.x & 31;
     using C = FwdCfg<D>;
     static_assert(kNumWG == 2, "slot bookkeeping below is written for two slots");
     int64_t last0 = -1, last1 = -1;   // each slot's last item so far
@@ -279,9 +302,14 @@ __device__ void fwd_mma_s(const FwdParams& prm, uint8_t* smem, uint64_t* bars, u
             const uint32_t ls = (uint32_t)(last % C::kNKV), lph = (uint32_t)((last / C::kNKV) & 1);
             if (!wg_wait(&bars[C::kBarVEmpty + ls], lph, ab, 13)) goto drain;
         }
-        if (!wg_wait(&bars[C::kBarQFull + qs], qph, ab, 3) ||
+        // K-full of this stage says "item i's K is in" only once the load of
+        // item i - kNKV into it has been seen to land (by this warp or the
+        // P V warp, which raise k_seen as they see each K-full)
+        if (!__all_sync(0xffffffffu, counter_wait(k_seen, (int)i - C::kNKV, ab, 16)) ||
+            !wg_wait(&bars[C::kBarQFull + qs], qph, ab, 3) ||
             !wg_wait(&bars[C::kBarKFull + ks], kph, ab, 4))
             goto drain;
+        if (lane == 0) atomicMax((int*)k_seen, (int)i);
         tc_fence_after();
         issue_s<D>(smem, bars, tmem, wg, qs, ks, min(kBN, tile.lkv - tile.kb0 * kBN));
         mma_commit(&bars[C::kBarKEmpty + ks]);
@@ -304,7 +332,8 @@ drain:
 // k%2), V MN-major from shared memory.
 template <int D, bool SM>
 __device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, uint32_t tmem,
-                           int seg0, int seg1, const Abort& ab) {
+                           volatile int* k_seen, int seg0, int seg1, const Abort& ab) {
+    const int lane = threadIdx.x & 31;
     using C = FwdCfg<D>;
     uint32_t p_use0 = 0, p_use1 = 0, o_use0 = 0, o_use1 = 0;
     uint32_t a = 0, i = 0;
@@ -351,7 +380,10 @@ __device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, 
                 o_use++;
             } else {
                 const uint32_t ks1 = (i + 1) % C::kNKV, kph1 = ((i + 1) / C::kNKV) & 1;
+                // (item i - 1's K, kNKV back in this stage, has landed: its
+                // S preceded this item's P V)
                 if (!wg_wait(&bars[C::kBarKFull + ks1], kph1, ab, 4)) goto drain;
+                if (lane == 0) atomicMax((int*)k_seen, (int)(i + 1));
                 tc_fence_after();
                 issue_s<D>(smem, bars, tmem, wg, qs, ks1,
                            min(kBN, tile.lkv - item_block<SM>(tile, it + 1) * kBN));
@@ -723,6 +755,9 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    // the highest item whose K-full the MMA warps have seen (the S issuer's
+    // guard against reading a K-full phase two completions short)
+    volatile int* k_seen = reinterpret_cast<volatile int*>(tmem_slot + 2);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int seg0 = prm.seg[blockIdx.x], seg1 = prm.seg[blockIdx.x + 1];
     uint64_t t_start = 0;
@@ -749,6 +784,7 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         mbar_init(&bars[C::kBarMmaDone + 1], 1);
         for (int w = 0; w < kNumWG; ++w) mbar_init(&bars[C::kBarXchg + w], 128 * kParts);
         *abort_flag = 0;
+        *k_seen = -1;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -769,10 +805,10 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
         if (lane == 0) fwd_producer<D, ACT == kSoftmax>(&tmQ, &tmK, &tmV, prm, smem, bars, seg0, seg1, ab);
         __syncwarp();
     } else if (warp == 1) {
-        fwd_mma_s<D, ACT == kSoftmax>(prm, smem, bars, tmem, seg0, seg1, ab);
+        fwd_mma_s<D, ACT == kSoftmax>(prm, smem, bars, tmem, k_seen, seg0, seg1, ab);
         __syncwarp();
     } else if (warp == kPvWarp) {
-        fwd_mma_pv<D, ACT == kSoftmax>(prm, smem, bars, tmem, seg0, seg1, ab);
+        fwd_mma_pv<D, ACT == kSoftmax>(prm, smem, bars, tmem, k_seen, seg0, seg1, ab);
         __syncwarp();
     } else {
         fwd_compute<D, ACT, SPLIT, NORM>(prm, &tmO, &tmW, smem, bars, tmem, seg0, seg1, ab);

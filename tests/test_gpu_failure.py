@@ -61,7 +61,7 @@ def test_expired_wait_reports_timeout_and_plan_recovers(gd, which, d):
     # sites, first given up by the stalled CTA 0
     code, site, cta, _ = plan.error_detail()
     assert code == 1 and cta == 0, plan.error_detail()
-    assert (1 <= site <= 15) if which == "fwd" else (21 <= site <= 50), site
+    assert (1 <= site <= 16) if which == "fwd" else (21 <= site <= 50), site
     # the kernel returned well inside the default limit (2 s per wait)
     assert time.time() - t0 < 10.0
     # the flag is cleared and the device is usable: a normal launch on the
