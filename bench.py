@@ -44,11 +44,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
     "gdpa_fwd": ("271a642be8c09ae6", 0.9679),
-    "gdpa_bwd": ("ab378ae1722d7e27", 1.0295),
+    "gdpa_bwd": ("2d1f541ffe0ba14b", 1.0295),
 }
 KERNEL_SOURCES = {
-    "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh"),
-    "gdpa_bwd": ("gdpa_tc_bwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh"),
+    "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh", "f2.cuh"),
+    "gdpa_bwd": ("gdpa_tc_bwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh", "f2.cuh"),
 }
 
 
