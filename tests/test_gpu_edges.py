@@ -136,3 +136,21 @@ def test_multi_block_tiles_on_few_ctas(gd, sched, num_sms):
     x = _case(lq, lkv, 2, 128, 900 + num_sms)
     _assert(compare_full(gd, x, 2, 128, 128 ** -0.5, "gelu_erf", "bf16", sched=sched,
                          num_sms=num_sms))
+
+
+@pytest.mark.parametrize("num_sms", [2, 5])
+@pytest.mark.parametrize("act,mask,window,split", [
+    ("softmax", "none", 0, 0),            # two passes over tiles of several key blocks
+    ("silu", "causal_window", 200, 0),    # windowed tiles of 1-3 blocks
+    ("gelu_erf", "none", 0, 1),           # key-split tiles of one block, fp32 reduce
+])
+def test_forward_queues_on_few_ctas(gd, act, mask, window, split, num_sms):
+    """The forward's item queue (K, V rings and the S issuer's guards) on long
+    per-CTA queues for the softmax variant's two passes, the causal window
+    and a key-split plan."""
+    rng = np.random.default_rng(950 + num_sms)
+    lq = rng.integers(1, 400, 16).tolist()
+    lkv = lq if mask != "none" else rng.integers(1, 600, 16).tolist()
+    x = _case(lq, lkv, 2, 128, 950 + num_sms)
+    _assert(compare_full(gd, x, 2, 128, 128 ** -0.5, act, "bf16", mask, window,
+                         backward=act != "softmax", num_sms=num_sms, max_kv_blocks=split))
