@@ -43,7 +43,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the unsplit softmax-free kernels; otherwise reported null.
 TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
-    "gdpa_fwd": ("9ac70dbf988074a0", 0.9679),
+    "gdpa_fwd": ("04be62bd48cfb1e2", 0.9679),
     "gdpa_bwd": ("2d1f541ffe0ba14b", 1.0295),
 }
 KERNEL_SOURCES = {

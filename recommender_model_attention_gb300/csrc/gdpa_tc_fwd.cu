@@ -589,7 +589,6 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
         } else
         for (int kb = tile.kb0; kb < tile.kb1; ++kb) {
             const int nvalid = min(kBN, tile.lkv - kb * kBN);
-            const int nch = (nvalid + 31) >> 5;
             if (!wg_wait(&bars[C::kBarSFull + wg], s_use & 1, ab, 6)) return;
             s_use++;
             tc_fence_after();
