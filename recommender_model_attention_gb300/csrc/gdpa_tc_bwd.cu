@@ -582,41 +582,26 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                         if (!row_ok) {
 #pragma unroll
                             for (int e = 0; e < 8; ++e) pp[k][e] = pd[e] = pq[e] = 0u;
-                        } else if (full) {
-#pragma unroll
-                            for (int e = 0; e < 16; e += 2) {
-                                float a0, d0, a1, d1;
-                                bwd_p_ds2<ACT>(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]),
-                                               __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]),
-                                               ksc, lse2, drow, a0, a1, d0, d1);
-                                pp[k][e >> 1] = pack_bf16x2(a0, a1);
-                                pd[e >> 1] = pack_bf16x2(d0, d1);
-                                if constexpr (NORM) {
-                                    const uint64_t d2 = f2_make(d0, d1);
-                                    const float2 q2 = f2_split(f2_mul(d2, f2_make(ci, ci)));
-                                    pq[e >> 1] = pack_bf16x2(q2.x, q2.y);
-                                    gdot2 = f2_fma(d2,
-                                                   f2_make(__uint_as_float(sv[e]),
-                                                           __uint_as_float(sv[e + 1])),
-                                                   gdot2);
-                                }
-                            }
                         } else {
+                            // one body for whole and ragged steps: the masks
+                            // only where the step is not entirely valid
 #pragma unroll
                             for (int e = 0; e < 16; e += 2) {
                                 float p2[2], d2[2];
                                 bwd_p_ds2<ACT>(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]),
                                                __uint_as_float(dv[e]), __uint_as_float(dv[e + 1]),
                                                ksc, lse2, drow, p2[0], p2[1], d2[0], d2[1]);
+                                if (!full) {
 #pragma unroll
-                                for (int w = 0; w < 2; ++w) {
-                                    const int col = col0 + e + w;
-                                    const int jpos = u.c0 + col;
-                                    bool valid = col < u.nkv;
-                                    if (windowed)
-                                        valid = valid && jpos <= ipos && jpos > ipos - prm.window;
-                                    p2[w] = valid ? p2[w] : 0.0f;
-                                    d2[w] = valid ? d2[w] : 0.0f;
+                                    for (int w = 0; w < 2; ++w) {
+                                        const int col = col0 + e + w;
+                                        const int jpos = u.c0 + col;
+                                        bool valid = col < u.nkv;
+                                        if (windowed)
+                                            valid = valid && jpos <= ipos && jpos > ipos - prm.window;
+                                        p2[w] = valid ? p2[w] : 0.0f;
+                                        d2[w] = valid ? d2[w] : 0.0f;
+                                    }
                                 }
                                 pp[k][e >> 1] = pack_bf16x2(p2[0], p2[1]);
                                 pd[e >> 1] = pack_bf16x2(d2[0], d2[1]);
