@@ -14,7 +14,8 @@
 // a cleared dQ.
 //
 // Roles: warp 0 TMA producer (K, V once per unit; Q and dO per query tile
-// through 2-stage rings); warp 1 tcgen05.mma issuer (the whole warp runs
+// through 2-stage rings, the next tile's and the next unit's boxes
+// prefetched into L2); warp 1 tcgen05.mma issuer (the whole warp runs
 // the issue code, one elected lane issues); warps 2-9 two
 // warpgroups that turn S and dP (TMEM) into dS and P (bf16, shared memory),
 // warpgroup j taking the 16-column key steps j, j + 2, ..., and drain dQ (j:
@@ -154,6 +155,16 @@ __device__ void bwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
                 tma_load_2d(tmDO, &bars[C::kDOFull + s],
                             smem + C::kOffDO + s * C::kTileBytes + hf * kHalfBytes, h * D + hf * 64,
                             y, pol_stream);
+            if (m + 1 < u.m1) {
+                // the next query tile's Q and dO boxes into L2: their ring
+                // loads wait for this tile's stages to free and then find
+                // them there (a shared Q stays in L2 anyway)
+#pragma unroll
+                for (int hf = 0; hf < C::kHalves; ++hf) {
+                    if (!prm.shared_q) tma_prefetch_2d(tmQ, h * D + hf * 64, y + kBM, pol_stream);
+                    tma_prefetch_2d(tmDO, h * D + hf * 64, y + kBM, pol_stream);
+                }
+            }
             if (m == u.m0) {
                 // the next unit's K and V into L2 now, so that its loads at
                 // the unit boundary need not come from HBM

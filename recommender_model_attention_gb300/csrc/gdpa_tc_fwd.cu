@@ -12,7 +12,8 @@
 //    3-stage ring, K and V blocks [128 x d] per (tile, key block) item
 //    through 2-stage rings; a K stage is handed back once its item's S has
 //    read it and a V stage once its P V has, and the producer loads K one
-//    item ahead of V, so the next items' scores never wait for a P V.
+//    item ahead of V, so the next items' scores never wait for a P V.  The
+//    next tile's Q is prefetched into L2 while its stage is still busy.
 //  * warps 1 and 18: tcgen05.mma issuers (the whole warp runs the issue
 //    code, one elected lane issues).  Warp 1 issues S = Q K^T of each tile's
 //    first item as soon as its Q and K are loaded and its slot's previous
@@ -232,6 +233,18 @@ __device__ void fwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
             pend_y = y;
             pend_h = tile.h;
             pend_i = i;
+        }
+        // the next tile's Q box into L2 once this tile's loads are issued:
+        // its ring load waits for an epilogue to free a stage, and then
+        // finds Q in L2 instead of starting the HBM read (a shared Q is
+        // read by every tile and stays in L2 anyway)
+        if (!prm.shared_q && t + 1 < seg1) {
+            const FwdTile tn = load_tile(prm.tiles + t + 1);
+            if (tn.kb1 > tn.kb0) {
+#pragma unroll
+                for (int hf = 0; hf < C::kHalves; ++hf)
+                    tma_prefetch_2d(tmQ, tn.h * D + hf * 64, tn.qt0, pol_q);
+            }
         }
         ++a;
     }
