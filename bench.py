@@ -43,8 +43,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the unsplit softmax-free kernels; otherwise reported null.
 TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
-    "gdpa_fwd": ("04be62bd48cfb1e2", 0.9679),
-    "gdpa_bwd": ("a9c89d5ed5b986fe", 1.0291),
+    "gdpa_fwd": ("f3b0201820008622", 0.9609),
+    "gdpa_bwd": ("d0bd78d7bbd86bc2", 1.0461),
 }
 KERNEL_SOURCES = {
     "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh", "f2.cuh"),

@@ -155,14 +155,17 @@ __device__ void bwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
                 tma_load_2d(tmDO, &bars[C::kDOFull + s],
                             smem + C::kOffDO + s * C::kTileBytes + hf * kHalfBytes, h * D + hf * 64,
                             y, pol_stream);
-            if (m + 1 < u.m1) {
-                // the next query tile's Q and dO boxes into L2: their ring
+            if (!prm.kscale && m + 1 < u.m1) {
+                // the next query tile's Q and dO boxes into L2 (evict-last,
+                // so that they stay until their loads take them): their ring
                 // loads wait for this tile's stages to free and then find
-                // them there (a shared Q stays in L2 anyway)
+                // them there (a shared Q stays in L2 anyway).  The fused
+                // RMSNorm kernel, bound by its arithmetic, runs faster
+                // without.
 #pragma unroll
                 for (int hf = 0; hf < C::kHalves; ++hf) {
-                    if (!prm.shared_q) tma_prefetch_2d(tmQ, h * D + hf * 64, y + kBM, pol_stream);
-                    tma_prefetch_2d(tmDO, h * D + hf * 64, y + kBM, pol_stream);
+                    if (!prm.shared_q) tma_prefetch_2d(tmQ, h * D + hf * 64, y + kBM, pol_keep);
+                    tma_prefetch_2d(tmDO, h * D + hf * 64, y + kBM, pol_keep);
                 }
             }
             if (m == u.m0) {

@@ -237,13 +237,15 @@ __device__ void fwd_producer(const CUtensorMap* tmQ, const CUtensorMap* tmK, con
         // the next tile's Q box into L2 once this tile's loads are issued:
         // its ring load waits for an epilogue to free a stage, and then
         // finds Q in L2 instead of starting the HBM read (a shared Q is
-        // read by every tile and stays in L2 anyway)
+        // read by every tile and stays in L2 anyway).  Prefetched as
+        // evict-last, so that it is still there when the load (evict-first)
+        // takes it.
         if (!prm.shared_q && t + 1 < seg1) {
             const FwdTile tn = load_tile(prm.tiles + t + 1);
             if (tn.kb1 > tn.kb0) {
 #pragma unroll
                 for (int hf = 0; hf < C::kHalves; ++hf)
-                    tma_prefetch_2d(tmQ, tn.h * D + hf * 64, tn.qt0, pol_q);
+                    tma_prefetch_2d(tmQ, tn.h * D + hf * 64, tn.qt0, pol_kv);
             }
         }
         ++a;
