@@ -21,7 +21,10 @@
 //    TMEM, then S of the tile's next item.  So the tensor core computes the
 //    next tile's scores while this tile's activation runs, and a tile's P V
 //    never waits for the next tile's loads (software pipelining across tile
-//    boundaries on one flattened loop).
+//    boundaries on one flattened loop).  Within an item, S and P V run in
+//    two key halves with their own barriers: the activation starts on keys
+//    [0, 64) while the tensor core computes keys [64, 128), and their P V
+//    while the activation finishes the rest.
 //  * warps 2-17: four activation/epilogue warpgroups.  Tiles alternate
 //    between two slots, each with its own TMEM S (128 columns) and O (128
 //    columns) accumulators, and two warpgroups share a slot: part h takes
@@ -77,9 +80,9 @@ struct FwdCfg {
     static constexpr int kBarVFull = kBarKFull + kNKV;
     static constexpr int kBarKEmpty = kBarVFull + kNKV;   // the item's S has read K
     static constexpr int kBarVEmpty = kBarKEmpty + kNKV;  // the item's P V has read V
-    static constexpr int kBarSFull = kBarVEmpty + kNKV;
-    static constexpr int kBarPFull = kBarSFull + kNumWG;
-    static constexpr int kBarOFull = kBarPFull + kNumWG;
+    static constexpr int kBarSFull = kBarVEmpty + kNKV;    // per slot and key half
+    static constexpr int kBarPFull = kBarSFull + 2 * kNumWG;   // per slot and key half
+    static constexpr int kBarOFull = kBarPFull + 2 * kNumWG;
     static constexpr int kBarOFree = kBarOFull + kNumWG;
     static constexpr int kBarStage = kBarOFree + kNumWG;             // per warpgroup
     static constexpr int kBarMmaDone = kBarStage + kNumWG * kParts;   // S issuer, P V issuer
@@ -261,21 +264,36 @@ unwind:
     }
 }
 
-// S = Q K^T of one item into slot w's S columns (K-major Q and K tiles),
-// N = the item's valid keys rounded up to 16; commits the slot's S-full.
+// S = Q K^T of one item into slot w's S columns (K-major Q and K tiles) in
+// two key halves, [0, 64) and [64, 128), each N = its valid keys rounded up
+// to 16 and each committing its own S-full, so that the activation starts
+// on the first half while the tensor core computes the second.  An item of
+// at most 64 keys has no second half: nothing is issued or committed for it,
+// and no one waits for it (every role decides this from the tile alone).
 template <int D>
 __device__ __forceinline__ void issue_s(uint8_t* smem, uint64_t* bars, uint32_t tmem, uint32_t w,
                                         uint32_t qs, uint32_t ks, int nvalid) {
     using C = FwdCfg<D>;
     const uint32_t n16 = (uint32_t)((nvalid + 15) & ~15);
-    const uint32_t idesc = idesc_bf16(128, n16, false, false);
     const uint64_t qdesc = smem_desc_sw128(smem_u32(smem + C::kOffQ + qs * C::kTileBytes), 16, 1024);
     const uint64_t kdesc = smem_desc_sw128(smem_u32(smem + C::kOffK + ks * C::kTileBytes), 16, 1024);
+    const uint32_t na = n16 < 64u ? n16 : 64u;
+    const uint32_t idesc_a = idesc_bf16(128, na, false, false);
 #pragma unroll
     for (int k = 0; k < D / 16; ++k)
-        mma_ss(tmem + w * 256, qdesc + kmajor_step(k), kdesc + kmajor_step(k), idesc,
+        mma_ss(tmem + w * 256, qdesc + kmajor_step(k), kdesc + kmajor_step(k), idesc_a,
                k > 0 ? 1u : 0u);
-    mma_commit(&bars[C::kBarSFull + w]);
+    mma_commit(&bars[C::kBarSFull + 2 * w]);
+    if (n16 > 64u) {
+        // keys 64..127: K rows 64.. start 64 x 128 bytes into each 128-byte-
+        // swizzled box (a whole number of 1024-byte swizzle atoms)
+        const uint32_t idesc_b = idesc_bf16(128, n16 - 64u, false, false);
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k)
+            mma_ss(tmem + w * 256 + 64, qdesc + kmajor_step(k), kdesc + (8192 >> 4) + kmajor_step(k),
+                   idesc_b, k > 0 ? 1u : 0u);
+        mma_commit(&bars[C::kBarSFull + 2 * w + 1]);
+    }
 }
 
 // S issuer (warp 1, the whole warp; one elected lane issues): S of each
@@ -350,7 +368,7 @@ __device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, 
                            volatile int* k_seen, int seg0, int seg1, const Abort& ab) {
     const int lane = threadIdx.x & 31;
     using C = FwdCfg<D>;
-    uint32_t p_use0 = 0, p_use1 = 0, o_use0 = 0, o_use1 = 0;
+    uint32_t p_use0 = 0, p_use1 = 0, pb_use0 = 0, pb_use1 = 0, o_use0 = 0, o_use1 = 0;
     uint32_t a = 0, i = 0;
     for (int t = seg0; t < seg1; ++t) {
         // (the descriptor line 4 tiles ahead, so that this warp's next
@@ -361,6 +379,7 @@ __device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, 
         const uint32_t wg = a % kNumWG;
         const uint32_t qs = a % C::kNQ;
         uint32_t& p_use = wg ? p_use1 : p_use0;
+        uint32_t& pb_use = wg ? pb_use1 : pb_use0;   // second key halves
         uint32_t& o_use = wg ? o_use1 : o_use0;
         const int nit = tile_items<SM>(tile);
         for (int it = 0; it < nit; ++it, ++i) {
@@ -369,26 +388,37 @@ __device__ void fwd_mma_pv(const FwdParams& prm, uint8_t* smem, uint64_t* bars, 
             const bool pv = item_pv<SM>(tile, it);
             const bool first = pv && (it == 0 || !item_pv<SM>(tile, it - 1));
             const bool last = it == nit - 1;
-            if (!wg_wait(&bars[C::kBarPFull + wg], p_use & 1, ab, 11)) goto drain;
-            p_use++;
+            if (!wg_wait(&bars[C::kBarPFull + 2 * wg], p_use & 1, ab, 11)) goto drain;
             // (also for an item without P V: its V load must have landed
             // before the stage goes back to the producer)
             if (!wg_wait(&bars[C::kBarVFull + ks], kph, ab, 10)) goto drain;
             if (first && !wg_wait(&bars[C::kBarOFree + wg], (o_use & 1) ^ 1, ab, 12)) goto drain;
-            tc_fence_after();
-            if (pv) {
-                const int nsteps = (min(kBN, tile.lkv - kb * kBN) + 15) >> 4;
+            {
+                const int nvalid = min(kBN, tile.lkv - kb * kBN);
+                const int nsteps = pv ? (nvalid + 15) >> 4 : 0;
                 constexpr uint32_t idesc = idesc_bf16(128, D, false, true);
                 const uint32_t p_tmem = tmem + wg * 256;
                 const uint32_t d_o = tmem + wg * 256 + 128;
                 const uint64_t vdesc =
                     smem_desc_sw128(smem_u32(smem + C::kOffV + ks * C::kTileBytes), kHalfBytes, 1024);
+                // keys [0, 64) as soon as their P is in, keys [64, 128) once
+                // the rest is
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    if (k < nsteps)
-                        mma_ts(d_o, p_tmem + (SM ? (k >> 1) * 32 + (k & 1) * 8 : k * 16),
-                               vdesc + mnmajor_step(k), idesc, (first && k == 0) ? 0u : 1u);
+                for (int hlf = 0; hlf < 2; ++hlf) {
+                    if (hlf == 1) {
+                        if (nvalid <= 64) break;
+                        if (!wg_wait(&bars[C::kBarPFull + 2 * wg + 1], pb_use & 1, ab, 11)) goto drain;
+                        pb_use++;
+                    }
+                    tc_fence_after();
+#pragma unroll
+                    for (int k = 4 * hlf; k < 4 * hlf + 4; ++k)
+                        if (k < nsteps)
+                            mma_ts(d_o, p_tmem + (SM ? (k >> 1) * 32 + (k & 1) * 8 : k * 16),
+                                   vdesc + mnmajor_step(k), idesc, (first && k == 0) ? 0u : 1u);
+                }
             }
+            p_use++;
             mma_commit(&bars[C::kBarVEmpty + ks]);
             if (last) {
                 mma_commit(&bars[C::kBarOFull + wg]);
@@ -437,7 +467,7 @@ __device__ __forceinline__ void store_zero_rows(const FwdTile& tile, const FwdPa
 // negative value if a wait gave up.
 template <int D>
 __device__ float softmax_tile(const FwdTile& tile, const FwdParams& prm, uint64_t* bars,
-                              uint32_t& s_use, uint32_t& x_use, uint32_t s_tmem,
+                              uint32_t& s_use, uint32_t& sb_use, uint32_t& x_use, uint32_t s_tmem,
                               uint32_t o_tmem_part0, int wg, int part, int r, bool warp_rows,
                               float alpha, const Abort& ab) {
     using C = FwdCfg<D>;
@@ -465,8 +495,12 @@ __device__ float softmax_tile(const FwdTile& tile, const FwdParams& prm, uint64_
         const int nvalid = min(kBN, tile.lkv - kb * kBN);
         const int nch = (nvalid + 31) >> 5;
         const int jbase = kb * kBN;
-        if (!wg_wait(&bars[C::kBarSFull + wg], s_use & 1, ab, 6)) return -1.0f;
+        if (!wg_wait(&bars[C::kBarSFull + 2 * wg], s_use & 1, ab, 6)) return -1.0f;
         s_use++;
+        if (nvalid > 64) {
+            if (!wg_wait(&bars[C::kBarSFull + 2 * wg + 1], sb_use & 1, ab, 6)) return -1.0f;
+            sb_use++;
+        }
         tc_fence_after();
         auto valid_at = [&](int col) {
             const int jpos = jbase + col;
@@ -545,7 +579,8 @@ __device__ float softmax_tile(const FwdTile& tile, const FwdParams& prm, uint64_
             }
         }
         tc_fence_before();
-        mbar_arrive(&bars[C::kBarPFull + wg]);
+        mbar_arrive(&bars[C::kBarPFull + 2 * wg]);
+        if (nvalid > 64) mbar_arrive(&bars[C::kBarPFull + 2 * wg + 1]);
     }
     if (prm.lse && part == 0 && r < tile.nq)   // natural log of the row's sum of exp(alpha s)
         prm.lse[(int64_t)(tile.qt0 + r) * prm.H + tile.h] =
@@ -569,7 +604,7 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
     const uint32_t s_tmem = tmem + wg * 256 + lane_addr;
     const uint32_t o_tmem = tmem + wg * 256 + 128 + lane_addr + part * (D / 2);
     ActScale ksc = act_scale<ACT>(prm.alpha);
-    uint32_t a = 0, s_use = 0, o_use = 0, x_use = 0;
+    uint32_t a = 0, s_use = 0, sb_use = 0, o_use = 0, x_use = 0;
     for (int t = seg0; t < seg1; ++t) {
         // (the descriptor line 4 tiles ahead, so that this warp's next
         // descriptor loads hit in L1)
@@ -597,74 +632,81 @@ __device__ void fwd_compute(const FwdParams& prm, const CUtensorMap* tmO, const 
         }
         float oscale = 1.0f;   // the softmax variant's 1 / (row sum)
         if constexpr (ACT == kSoftmax) {
-            oscale = softmax_tile<D>(tile, prm, bars, s_use, x_use, s_tmem,
+            oscale = softmax_tile<D>(tile, prm, bars, s_use, sb_use, x_use, s_tmem,
                                      tmem + wg * 256 + 128 + lane_addr, (int)wg, part, r, warp_rows,
                                      alpha_row, ab);
             if (__any_sync(0xffffffffu, oscale < 0.0f)) return;
         } else
         for (int kb = tile.kb0; kb < tile.kb1; ++kb) {
             const int nvalid = min(kBN, tile.lkv - kb * kBN);
-            if (!wg_wait(&bars[C::kBarSFull + wg], s_use & 1, ab, 6)) return;
-            s_use++;
-            tc_fence_after();
+            const int jbase = kb * kBN;
             // S -> registers 16 columns at a time; alpha, activation and mask;
             // P (bf16 pairs) back into the first 8 columns of the same
             // 16-column step, which only this warpgroup reads and has read.
-            // Part h takes the steps h, h + 2, ...
-            if (warp_rows) {
-                const int jbase = kb * kBN;
+            // Part h takes the steps h, h + 2, ...; the keys [0, 64) as soon
+            // as their half of S is in, releasing their P to the P V issuer,
+            // then the keys [64, 128)
 #pragma unroll 1
-                for (int k = 0; k < 4; ++k) {
-                    const int col0 = (part + 2 * k) * 16;
-                    if (col0 >= nvalid) break;   // GEMMs stop at 16-column granularity
-                    uint32_t sv[16], pk[8];
-                    tmem_ld16(s_tmem + col0, sv);
-                    tmem_ld_wait();
-                    // the step's keys against the window of this warp's 32
-                    // rows (warp-uniform): all valid, none valid, or mixed
-                    // (per-pair masks)
-                    const int jlo = jbase + col0, jhi = jlo + 15;
-                    bool all_valid = col0 + 16 <= nvalid, none_valid = false;
-                    if (prm.mask == GDPA_MASK_CAUSAL_WINDOW) {
-                        const int ilo = tile.i0 + quarter * 32, ihi = ilo + 31;
-                        all_valid = all_valid && jhi <= ilo && jlo > ihi - prm.window;
-                        none_valid = jlo > ihi || jhi <= ilo - prm.window;
-                    }
-                    if (none_valid) {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) pk[e] = 0u;
-                    } else if (all_valid) {
-#pragma unroll
-                        for (int e = 0; e < 16; e += 2) {
-                            float a0, a1;
-                            act_s2<ACT>(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), ksc,
-                                        a0, a1);
-                            pk[e >> 1] = pack_bf16x2(a0, a1);
+            for (int hlf = 0; hlf < (nvalid > 64 ? 2 : 1); ++hlf) {
+                if (!wg_wait(&bars[C::kBarSFull + 2 * wg + hlf], (hlf ? sb_use : s_use) & 1, ab, 6))
+                    return;
+                tc_fence_after();
+                if (warp_rows) {
+#pragma unroll 1
+                    for (int k = 2 * hlf; k < 2 * hlf + 2; ++k) {
+                        const int col0 = (part + 2 * k) * 16;
+                        if (col0 >= nvalid) break;   // GEMMs stop at 16-column granularity
+                        uint32_t sv[16], pk[8];
+                        tmem_ld16(s_tmem + col0, sv);
+                        tmem_ld_wait();
+                        // the step's keys against the window of this warp's 32
+                        // rows (warp-uniform): all valid, none valid, or mixed
+                        // (per-pair masks)
+                        const int jlo = jbase + col0, jhi = jlo + 15;
+                        bool all_valid = col0 + 16 <= nvalid, none_valid = false;
+                        if (prm.mask == GDPA_MASK_CAUSAL_WINDOW) {
+                            const int ilo = tile.i0 + quarter * 32, ihi = ilo + 31;
+                            all_valid = all_valid && jhi <= ilo && jlo > ihi - prm.window;
+                            none_valid = jlo > ihi || jhi <= ilo - prm.window;
                         }
-                    } else {
+                        if (none_valid) {
 #pragma unroll
-                        for (int e = 0; e < 16; e += 2) {
-                            float pv[2];
-                            act_s2<ACT>(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), ksc,
-                                        pv[0], pv[1]);
+                            for (int e = 0; e < 8; ++e) pk[e] = 0u;
+                        } else if (all_valid) {
 #pragma unroll
-                            for (int u = 0; u < 2; ++u) {
-                                const int col = col0 + e + u;
-                                const int jpos = jbase + col;
-                                bool valid = col < nvalid;
-                                if (prm.mask == GDPA_MASK_CAUSAL_WINDOW)
-                                    valid = valid && jpos <= ipos && jpos > ipos - prm.window;
-                                pv[u] = valid ? pv[u] : 0.0f;
+                            for (int e = 0; e < 16; e += 2) {
+                                float a0, a1;
+                                act_s2<ACT>(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), ksc,
+                                            a0, a1);
+                                pk[e >> 1] = pack_bf16x2(a0, a1);
                             }
-                            pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 16; e += 2) {
+                                float pv[2];
+                                act_s2<ACT>(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1]), ksc,
+                                            pv[0], pv[1]);
+#pragma unroll
+                                for (int u = 0; u < 2; ++u) {
+                                    const int col = col0 + e + u;
+                                    const int jpos = jbase + col;
+                                    bool valid = col < nvalid;
+                                    if (prm.mask == GDPA_MASK_CAUSAL_WINDOW)
+                                        valid = valid && jpos <= ipos && jpos > ipos - prm.window;
+                                    pv[u] = valid ? pv[u] : 0.0f;
+                                }
+                                pk[e >> 1] = pack_bf16x2(pv[0], pv[1]);
+                            }
                         }
+                        tmem_st8(s_tmem + col0, pk);
                     }
-                    tmem_st8(s_tmem + col0, pk);
+                    tmem_st_wait();
                 }
-                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(&bars[C::kBarPFull + 2 * wg + hlf]);
             }
-            tc_fence_before();
-            mbar_arrive(&bars[C::kBarPFull + wg]);
+            s_use++;
+            if (nvalid > 64) sb_use++;
         }
         // epilogue: this part's O columns (TMEM) -> bf16 -> this part's half of
         // the tile's (consumed) Q buffer -> global
@@ -787,9 +829,11 @@ tc_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ C
             mbar_init(&bars[C::kBarKEmpty + s], 1);
             mbar_init(&bars[C::kBarVEmpty + s], 1);
         }
-        for (int w = 0; w < kNumWG; ++w) {
+        for (int w = 0; w < 2 * kNumWG; ++w) {
             mbar_init(&bars[C::kBarSFull + w], 1);
             mbar_init(&bars[C::kBarPFull + w], 128 * kParts);
+        }
+        for (int w = 0; w < kNumWG; ++w) {
             mbar_init(&bars[C::kBarOFull + w], 1);
             mbar_init(&bars[C::kBarOFree + w], 128 * kParts);
         }
