@@ -43,7 +43,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # the unsplit softmax-free kernels; otherwise reported null.
 TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
-    "gdpa_fwd": ("f3b0201820008622", 0.9609),
+    "gdpa_fwd": ("2db4b4c8e0ddc353", 0.9602),
     "gdpa_bwd": ("d0bd78d7bbd86bc2", 1.0461),
 }
 KERNEL_SOURCES = {
