@@ -40,7 +40,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # workload; traffic grows with the rows processed, so it is scaled to a full
 # launch by algorithmic bytes).  Valid only for the kernel sources they were
 # measured on (hash of the kernel's source files), the training workload and
-# the unsplit softmax-free kernels; otherwise reported null.
+# the unsplit softmax-free kernels without the fused RMSNorm; otherwise
+# reported null.
 TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
     "gdpa_fwd": ("2db4b4c8e0ddc353", 0.9602),
@@ -531,7 +532,8 @@ def main():
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     src_hash, ratio = TRAFFIC_RATIO[dom]
     traffic = (ratio * dom_bytes if kernel_source_hash(dom) == src_hash and
-               w.name == TRAFFIC_WORKLOAD and not key_split and not softmax else None)
+               w.name == TRAFFIC_WORKLOAD and not key_split and not softmax and
+               not args.qk_norm > 0 else None)
     roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
                 "algorithmic_bytes": dom_bytes, "peak_kind": pk_kind}
