@@ -322,7 +322,8 @@ __device__ __forceinline__ void store_half_chunk(uint8_t* ps, int c, int hh, int
 // (d g^2) (or, in terms of the normalised row x_hat = c x, kappa = (x_hat .
 // v) / (d g^2) with x_hat in place of x).  Columns [col, col + 16 P) of this
 // warp's 32 lanes, 16 at a time; xw(step, x8) gives the 8 packed bf16 words
-// of x for columns col + 16 step ..; staging and stores as drain_warp.
+// of x for columns col + 16 step ..; staging and stores as drain_warp, the
+// plain (not reduce-add) stores marked evict-first in L2.
 template <int P, typename XW>
 __device__ __forceinline__ void drain_warp_norm(uint32_t trow, uint32_t col, uint8_t* stage,
                                                 const CUtensorMap* map, int x0, int y0, float* dst,
@@ -372,8 +373,9 @@ __device__ __forceinline__ void drain_warp_norm(uint32_t trow, uint32_t col, uin
             if (lane == 0) {
                 if (atomic)
                     tma_reduce_add_2d(map, buf, x0 + pass * 16, y0 + row0);
-                else
-                    tma_store_2d(map, buf, x0 + pass * 16, y0 + row0);
+                else   // (evict-first: 6.28 -> 6.10 ms for this kernel's backward,
+                       // where the same hint slows the plain kernels' stores)
+                    tma_store_2d_hint(map, buf, x0 + pass * 16, y0 + row0, policy_evict_first());
                 bulk_commit();
             }
         } else if (row0 + lane < nrows) {

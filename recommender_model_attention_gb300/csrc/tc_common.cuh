@@ -185,6 +185,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
         : "memory");
 }
 
+// Same with an L2 eviction-priority hint for the written lines.
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* map, const void* src,
+                                                  int32_t x, int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+        " [%0, {%1, %2}], [%3], %4;" ::"l"(map),
+        "r"(x), "r"(y), "r"(smem_u32(src)), "l"(policy)
+        : "memory");
+}
+
 // Same, adding into global memory element-wise (f32 add, atomic per element).
 __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src,
                                                   int32_t x, int32_t y) {
