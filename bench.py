@@ -44,8 +44,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # reported null.
 TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
-    "gdpa_fwd": ("2db4b4c8e0ddc353", 0.9602),
-    "gdpa_bwd": ("d0bd78d7bbd86bc2", 1.0461),
+    "gdpa_fwd": ("2451a965b2c28742", 0.9602),
+    "gdpa_bwd": ("addd61b03d5a9dab", 1.0459),
 }
 KERNEL_SOURCES = {
     "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh", "f2.cuh"),
