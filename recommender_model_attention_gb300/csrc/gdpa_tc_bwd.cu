@@ -555,6 +555,16 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
                 drow = d_next;
                 if (m + 1 < u.m1) row_stats(m + 1, lse_next, d_next);
             }
+            // fused RMSNorm: the keys are normalised; this row's scale c,
+            // from the tile's raw Q, joins alpha (x = alpha c q . k_hat);
+            // computed while S and dP are on the tensor core (their Q is in)
+            float ci = 1.0f;
+            if constexpr (NORM) {
+                if (!wg_wait(&bars[C::kQFull + (i & 1)], (i >> 1) & 1, ab, 42)) return;
+                ci = row_scale<D>(smem + C::kOffQ + (i & 1) * C::kTileBytes, r, prm.qk_gain,
+                                  prm.qk_eps);
+                ksc = act_scale<ACT>(prm.alpha * ci);
+            }
             if (!wg_wait(&bars[C::kSDFull], i & 1, ab, 43)) return;
             // the previous tile's dQ bulk stores have long been issued: once
             // they have read their staging, its Q stage goes back to the
@@ -570,16 +580,7 @@ __device__ void bwd_compute(const BwdParams& prm, const CUtensorMap* tmDQ, const
             if (m == u.m0 && nu > 0 && !wg_wait(&bars[C::kPSFree], (nu - 1) & 1, ab, 47)) return;
             if (!wg_wait(&bars[C::kPVDone], (i & 1) ^ 1, ab, 44)) return;
             tc_fence_after();
-            // fused RMSNorm: the keys are normalised; this row's scale c,
-            // from the tile's raw Q, joins alpha (x = alpha c q . k_hat)
-            float ci = 1.0f;
             uint64_t gdot2 = f2_make(0.0f, 0.0f);   // sum_j dS_j s_j over this warpgroup's keys
-            if constexpr (NORM) {
-                if (!wg_wait(&bars[C::kQFull + (i & 1)], (i >> 1) & 1, ab, 42)) return;
-                ci = row_scale<D>(smem + C::kOffQ + (i & 1) * C::kTileBytes, r, prm.qk_gain,
-                                  prm.qk_eps);
-                ksc = act_scale<ACT>(prm.alpha * ci);
-            }
             uint32_t pp[4][8];
             if (warp_rows) {
 #pragma unroll
