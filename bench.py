@@ -45,7 +45,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 TRAFFIC_WORKLOAD = "training_cross_fwd_bwd"
 TRAFFIC_RATIO = {
     "gdpa_fwd": ("2451a965b2c28742", 0.9602),
-    "gdpa_bwd": ("addd61b03d5a9dab", 1.0459),
+    "gdpa_bwd": ("583aee4f29bf51c3", 1.0463),
 }
 KERNEL_SOURCES = {
     "gdpa_fwd": ("gdpa_tc_fwd.cu", "tc_common.cuh", "tc_drain.cuh", "act.cuh", "f2.cuh"),
