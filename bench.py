@@ -62,6 +62,17 @@ def kernel_source_hash(kernel):
     return h.hexdigest()[:16]
 
 
+def dram_traffic(kernel, algorithmic_bytes, workload, key_split, softmax, qk_norm):
+    """DRAM bytes of one launch of `kernel` from its captured ratio, or None
+    where the capture does not apply (other kernel sources, another
+    workload, the key-split, softmax or fused-RMSNorm kernels)."""
+    src_hash, ratio = TRAFFIC_RATIO[kernel]
+    if (kernel_source_hash(kernel) != src_hash or workload != TRAFFIC_WORKLOAD or key_split
+            or softmax or qk_norm):
+        return None
+    return ratio * algorithmic_bytes
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -530,10 +541,7 @@ def main():
     else:
         dom, dom_ms, dom_bytes = "gdpa_fwd", fwd_ms, fwd_bytes
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    src_hash, ratio = TRAFFIC_RATIO[dom]
-    traffic = (ratio * dom_bytes if kernel_source_hash(dom) == src_hash and
-               w.name == TRAFFIC_WORKLOAD and not key_split and not softmax and
-               not args.qk_norm > 0 else None)
+    traffic = dram_traffic(dom, dom_bytes, w.name, key_split, softmax, args.qk_norm > 0)
     roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                 "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
                 "algorithmic_bytes": dom_bytes, "peak_kind": pk_kind}
