@@ -3,9 +3,11 @@
 Same tolerances as the main parity file (bf16 inputs: 1e-2 of max|ref| for
 O, dQ, dK, dV separately).  Cases: a batch of zero samples, a batch whose
 lengths are all zero, lengths on and next to the 128-row tile boundaries,
-many heads, d = 64 with the causal window in the backward pass, the
-round-robin dealing policy, fewer persistent CTAs than SMs, and a launch on
-a side stream.
+many heads, d = 64 with the causal window in the backward pass, key blocks
+on and next to 64 keys (the forward's score product and P V run in halves
+of 64 keys, the second skipped for a block of at most 64), the round-robin
+dealing policy, fewer persistent CTAs than SMs, and a launch on a side
+stream.
 """
 
 import numpy as np
@@ -81,6 +83,14 @@ def test_tile_boundary_lengths_window(gd):
     lens = [127, 128, 129, 255, 256, 257, 511, 512, 513]
     x = _case(lens, lens, 2, 128, 3)
     _assert(compare_full(gd, x, 2, 128, 128 ** -0.5, "gelu_tanh", "bf16", "causal_window", 128))
+
+
+@pytest.mark.parametrize("act,mask,window", [("gelu_erf", "none", 0), ("silu", "causal_window", 100)])
+def test_key_half_boundary_lengths(gd, act, mask, window):
+    lkv = [63, 64, 65, 66, 79, 80, 191, 192, 193, 200]
+    lq = lkv if mask == "causal_window" else [70, 130, 64, 65, 200, 1, 129, 300, 64, 190]
+    x = _case(lq, lkv, 2, 128, 11)
+    _assert(compare_full(gd, x, 2, 128, 128 ** -0.5, act, "bf16", mask, window))
 
 
 def test_many_heads(gd):

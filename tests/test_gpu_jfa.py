@@ -149,6 +149,17 @@ def test_softmax_backward_bf16(gd, kernel, d):
     assert lse_err <= 1e-3
 
 
+def test_softmax_key_half_boundary_lengths(gd):
+    # key blocks on and next to 64 keys: the forward's score product and
+    # P V run in halves of 64 keys, the second skipped for at most 64
+    lkv = [63, 64, 65, 66, 79, 80, 191, 192, 193, 200]
+    lq = [70, 130, 64, 65, 200, 1, 129, 300, 64, 190]
+    x = _case(lq, lkv, 2, 128, 95)
+    errs, lse_err = _softmax_fwd_bwd(gd, x, 2, 128, 128 ** -0.5, seed=95)
+    _assert(errs, TOL["bf16"])
+    assert lse_err <= 1e-3
+
+
 @pytest.mark.parametrize("kernel", ["simt", "auto"])
 @pytest.mark.parametrize("window", [1, 77])
 def test_softmax_backward_window_bf16(gd, kernel, window):
